@@ -1,0 +1,463 @@
+"""Benchmark of the paged-attention hot path on one GB300 (or N independent replicas).
+
+One step = one pass of the whole hot path over one batch: slot mapping, the
+copy-on-write block copies (when the batch has any), the KV write of the step's
+new tokens, and paged attention over the block tables (CUDA-core decode items,
+tensor-core items, the split-KV combine). Inputs are resident in HBM when the
+timed region starts; the KV pools (several GB) are larger than L2, so no flush
+is needed between steps. The default workload is the decode-only batch with
+the OPT-13B attention shape (256 sequences, one query token each, Hq=Hkv=40,
+D=128, block size 16, contexts uniform in [128, 2048]).
+
+Prints ONE JSON line (rank 0). ``--impl reference`` times the fp64 CPU oracle on
+the host cores instead (a deliberately plain program, the baseline arm).
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "paged attn tokens/s and achieved HBM GB/s / TC util vs roofline (1×GB300)"
+UNIT = "tokens/s"
+PROFILE_TRAFFIC = os.path.join(ROOT, "profiles", "traffic.json")
+KERNEL_SOURCES = ["pa_dec.cu", "pa_ptx.cuh", "pa_internal.h"]
+
+
+def log(*a):
+    print(*a, file=sys.stderr, flush=True)
+
+
+def kernel_source_hash() -> str:
+    h = hashlib.sha256()
+    for f in KERNEL_SOURCES:
+        with open(os.path.join(ROOT, "paged_kv_cache_02_gb300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def measured_peaks() -> dict:
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        d["_source"] = "measured"
+        return d
+    return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0,
+            "_source": "fallback"}
+
+
+# ------------------------------------------------------------------ clocks
+
+class ClockSampler:
+    """nvidia-smi samples every 200 ms while running (read-only query)."""
+
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.idx = gpu_index
+        self.samples = []
+        self.proc = None
+        self.thread = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.idx), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.samples.append((time.perf_counter(), line.strip()))
+
+    def stop(self):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+        if self.thread is not None:
+            self.thread.join(timeout=5)
+
+    def summary(self, t0: float, t1: float) -> dict:
+        rows = [s for t, s in self.samples if t0 <= t <= t1] or [s for _, s in self.samples]
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for r in rows:
+            parts = [p.strip() for p in r.split(",")]
+            if len(parts) < 8:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                mx.append(float(parts[1]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[4:8]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        sm.sort()
+        return {"sm_mhz": sm[len(sm) // 2], "sm_max_mhz": max(mx), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# ------------------------------------------------------------------ distributed plumbing
+
+def dist_setup(n_gpus: int):
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        import torch
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        if backend == "nccl":
+            torch.cuda.set_device(local)
+        dist.init_process_group(backend)
+    return rank, local, world
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(x: float, world: int) -> float:
+    if world <= 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    dev = "cuda" if torch.cuda.is_available() else "cpu"
+    t = torch.tensor([x], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+# ------------------------------------------------------------------ oracle (CPU) arm
+
+def oracle_step_sample(w, orc, host, n_threads, budget_s=10.0, max_passes=30):
+    """Times the oracle on bounded passes over the same workload: slot mapping, copies,
+    KV write and attention for a contiguous block of query rows. Returns (rows/s, sample)."""
+    import numpy as np
+    from tests.oracle_checks import u16
+    T = w.total_q
+    rows_per_pass = T
+    # estimated cost per row (visible keys * heads) to bound one pass to ~budget/3
+    pref = np.concatenate([[0], np.cumsum(w.query_lens)])
+    seq_of_row = np.repeat(np.arange(w.num_seqs), w.query_lens)
+    pos = w.context_lens[seq_of_row] - w.query_lens[seq_of_row] + (np.arange(T) - pref[seq_of_row])
+    cost = (pos + 1).astype(np.float64) * w.Hq * w.D * 2  # MACs per row
+    t_probe = time.perf_counter()
+    probe_rows = np.arange(min(T, 8), dtype=np.int64)
+    orc.attention(host["q"], host["k_pool"], host["v_pool"], w.block_table, w.context_lens,
+                  w.query_lens, rows=probe_rows, n_threads=n_threads)
+    dt_probe = max(1e-6, time.perf_counter() - t_probe)
+    macs_per_s = max(1e6, cost[:len(probe_rows)].sum() / dt_probe)
+    cum = np.cumsum(cost)
+    limit = macs_per_s * budget_s / 3.0
+    rows_per_pass = int(max(1, min(T, np.searchsorted(cum, limit) + 1)))
+    rows = np.arange(rows_per_pass, dtype=np.int64)
+    kp, vp = host["k_pool"].copy(), host["v_pool"].copy()
+    done_rows = 0
+    passes = 0
+    t0 = time.perf_counter()
+    while True:
+        slots = orc.slot_mapping(w.block_table, w.num_blocks, w.block_size, w.new_seq, w.new_pos)
+        if len(w.cow_src):
+            orc.copy_blocks(kp, vp, w.cow_src, w.cow_dst)
+        orc.write_kv(host["k_new"], host["v_new"], slots, kp, vp)
+        orc.attention(host["q"], kp, vp, w.block_table, w.context_lens, w.query_lens,
+                      rows=None if rows_per_pass == T else rows, n_threads=n_threads)
+        done_rows += rows_per_pass
+        passes += 1
+        el = time.perf_counter() - t0
+        if el >= budget_s or passes >= max_passes:
+            break
+    sample = (f"{passes} pass(es) of slot mapping + KV write of all {len(w.new_seq)} new tokens "
+              f"+ attention of query rows [0, {rows_per_pass}) of {T} ({w.name}), "
+              f"{el:.1f} s on {n_threads} threads")
+    return done_rows / el, sample, el
+
+
+def run_reference(args, w, cfg_name):
+    import numpy as np
+    import oracle
+    from tests.oracle_checks import u16
+    orc = oracle.default()
+    host = {"q": u16(w.q), "k_pool": u16(w.k_pool), "v_pool": u16(w.v_pool),
+            "k_new": u16(w.k_new), "v_new": u16(w.v_new)}
+    n_threads = os.cpu_count() or 1
+    budget = max(1.0, min(20.0, 150.0 / max(1, args.steps + args.warmup)))
+    for _ in range(args.warmup):
+        oracle_step_sample(w, orc, host, n_threads, budget_s=min(budget, 2.0), max_passes=1)
+    vals, samples, total = [], [], 0.0
+    for _ in range(args.steps):
+        v, s, el = oracle_step_sample(w, orc, host, n_threads, budget_s=budget)
+        vals.append(v)
+        samples.append(s)
+        total += el
+    value = float(np.median(vals))
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": 1,
+        "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": 1000.0 * w.total_q / value, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": cfg_name,
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": n_threads, "kind": "oracle",
+                         "sample": samples[0]},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+        "gpu_launches": 0,
+    }
+    print(json.dumps(line), flush=True)
+
+
+# ------------------------------------------------------------------ GPU arm
+
+def run_gpu(args, w, cfg_name, rank, local, world):
+    import numpy as np
+    import torch
+    import paged_kv_cache_02_gb300 as pa
+
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    stream = torch.cuda.current_stream(dev)
+    # ---- device-resident inputs
+    bt = torch.from_numpy(w.block_table).to(dev)
+    cl = torch.from_numpy(w.context_lens).to(dev)
+    ql = torch.from_numpy(w.query_lens).to(dev)
+    sid = torch.from_numpy(w.new_seq).to(dev)
+    pos = torch.from_numpy(w.new_pos).to(dev)
+    src = torch.from_numpy(w.cow_src).to(dev)
+    dst = torch.from_numpy(w.cow_dst).to(dev)
+    q, kn, vn = w.q.to(dev), w.k_new.to(dev), w.v_new.to(dev)
+    kp, vp = w.k_pool.to(dev), w.v_pool.to(dev)
+    slots = torch.empty(len(w.new_seq), dtype=torch.int64, device=dev)
+    out = torch.empty(q.shape, dtype=torch.float32, device=dev)
+    plan = pa.Plan(w.context_lens, w.query_lens, w.Hq, w.Hkv, w.D, w.block_size, w.max_blocks)
+    st = plan.stats()
+    ws = plan.workspace(dev)
+    n_pairs = len(w.cow_src)
+
+    ev = {k: [torch.cuda.Event(enable_timing=True) for _ in range(args.steps + 1)]
+          for k in ("a", "b", "c", "d", "e")}
+
+    def step(i=None):
+        if i is not None:
+            ev["a"][i].record(stream)
+        pa.pa_slot_mapping(bt, w.num_blocks, w.block_size, sid, pos, out=slots)
+        if i is not None:
+            ev["b"][i].record(stream)
+        if n_pairs:
+            pa.pa_copy_blocks(kp, vp, src, dst)
+        if i is not None:
+            ev["c"][i].record(stream)
+        pa.pa_write_kv(kn, vn, slots, kp, vp)
+        if i is not None:
+            ev["d"][i].record(stream)
+        pa.pa_attention(plan, q, kp, vp, bt, cl, ql, out=out, workspace=ws)
+        if i is not None:
+            ev["e"][i].record(stream)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize(dev)
+    err = pa.pa_get_device_error(reset=True)
+    if err:
+        raise RuntimeError(f"device error {pa.DEVERR.get(err, err)} during warm-up")
+
+    clocks = ClockSampler(local)
+    clocks.start()
+    time.sleep(0.5)  # the sampler's first line
+    barrier(world)
+    torch.cuda.synchronize(dev)
+    start_ev = torch.cuda.Event(enable_timing=True)
+    end_ev = torch.cuda.Event(enable_timing=True)
+    h0 = time.perf_counter()
+    start_ev.record(stream)
+    for i in range(args.steps):
+        step(i)
+    end_ev.record(stream)
+    torch.cuda.synchronize(dev)
+    h1 = time.perf_counter()
+    barrier(world)
+    clocks.stop()
+    elapsed_ms = start_ev.elapsed_time(end_ev)
+    elapsed_ms = max_over_ranks(elapsed_ms, world)
+    per = {k: float(np.mean([ev[a][i].elapsed_time(ev[b][i]) for i in range(args.steps)]))
+           for k, (a, b) in {"slot_mapping": ("a", "b"), "copy_blocks": ("b", "c"),
+                             "write_kv": ("c", "d"), "attention": ("d", "e")}.items()}
+    err = pa.pa_get_device_error(reset=True)
+    if err:
+        raise RuntimeError(f"device error {pa.DEVERR.get(err, err)} in the timed region")
+
+    T = w.total_q
+    value = T * args.steps * world / (elapsed_ms / 1000.0)
+    launches_per_step = 1 + (1 if n_pairs else 0) + 1 + (1 if st["n_dec_items"] else 0) + \
+        (1 if st["n_tc_items"] else 0) + (1 if st["n_split_groups"] else 0)
+
+    # ---- roofline of the dominant kernel (paged attention)
+    peaks = measured_peaks()
+    kv_b, q_b, o_b = w.kv_bytes(), w.q_bytes(), T * w.Hq * w.D * 4
+    flops = w.flops()
+    attn_s = per["attention"] / 1000.0
+    hbm_peak = float(peaks["hbm_gbs"])
+    tc_peak = float(peaks.get("bf16_tflops", 1900.0))
+    t_hbm = (kv_b + q_b) / (hbm_peak * 1e9)
+    t_tc = flops / (tc_peak * 1e12)
+    bound = "hbm" if t_hbm >= t_tc else "tensor"
+    traffic = None
+    if os.path.exists(PROFILE_TRAFFIC):
+        with open(PROFILE_TRAFFIC) as f:
+            prof = json.load(f)
+        entry = prof.get(args.config_key)
+        if entry and entry.get("kernel_hash") == kernel_source_hash():
+            traffic = entry.get("dram_bytes_per_launch")
+    if bound == "hbm":
+        achieved = (kv_b + q_b) / attn_s / 1e9
+        roof = {"bound": "hbm", "achieved": achieved, "peak": hbm_peak, "unit": "GB/s",
+                "frac": achieved / hbm_peak, "traffic": traffic,
+                "peak_source": f"{peaks['_source']} hbm_gbs"}
+    else:
+        achieved = flops / attn_s / 1e12
+        roof = {"bound": "tensor", "achieved": achieved, "peak": tc_peak, "unit": "TFLOP/s",
+                "frac": achieved / tc_peak, "traffic": traffic,
+                "peak_source": f"{peaks['_source']} bf16_tflops"}
+
+    # ---- end to end through the public API, host buffers in pinned memory
+    pin = lambda t: t.cpu().pin_memory()
+    h_q, h_kn, h_vn = pin(w.q), pin(w.k_new), pin(w.v_new)
+    h_bt, h_cl, h_ql = pin(bt), pin(cl), pin(ql)
+    h_sid, h_pos, h_src, h_dst = pin(sid), pin(pos), pin(src), pin(dst)
+    h_out = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+    h2d = sum(t.numel() * t.element_size() for t in
+              (h_q, h_kn, h_vn, h_bt, h_cl, h_ql, h_sid, h_pos, h_src, h_dst))
+    d2h = h_out.numel() * h_out.element_size()
+    d_bufs = [torch.empty_like(t, device=dev) for t in
+              (h_q, h_kn, h_vn, h_bt, h_cl, h_ql, h_sid, h_pos, h_src, h_dst)]
+
+    def e2e_step():
+        for hb, db in zip((h_q, h_kn, h_vn, h_bt, h_cl, h_ql, h_sid, h_pos, h_src, h_dst), d_bufs):
+            db.copy_(hb, non_blocking=True)
+        dq, dkn, dvn, dbt, dcl, dql, dsid, dpos, dsrc, ddst = d_bufs
+        p2 = pa.Plan(w.context_lens, w.query_lens, w.Hq, w.Hkv, w.D, w.block_size, w.max_blocks)
+        pa.pa_slot_mapping(dbt, w.num_blocks, w.block_size, dsid, dpos, out=slots)
+        if n_pairs:
+            pa.pa_copy_blocks(kp, vp, dsrc, ddst)
+        pa.pa_write_kv(dkn, dvn, slots, kp, vp)
+        pa.pa_attention(p2, dq, kp, vp, dbt, dcl, dql, out=out, workspace=ws)
+        h_out.copy_(out, non_blocking=True)
+        torch.cuda.current_stream(dev).synchronize()
+        p2.close()
+
+    for _ in range(min(3, args.warmup)):
+        e2e_step()
+    e2e_steps = max(3, min(args.steps, 200))
+    barrier(world)
+    torch.cuda.synchronize(dev)
+    t0 = time.perf_counter()
+    for _ in range(e2e_steps):
+        e2e_step()
+    torch.cuda.synchronize(dev)
+    e2e_s = max_over_ranks(time.perf_counter() - t0, world)
+    e2e_value = T * e2e_steps * world / e2e_s
+
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": elapsed_ms / args.steps, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": cfg_name,
+        "roofline": roof,
+        "hbm_gbs_attention": (kv_b + q_b) / attn_s / 1e9,
+        "tc_tflops_attention": flops / attn_s / 1e12,
+        "per_call_ms": per,
+        "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": int(h2d),
+                "d2h_bytes_per_step": int(d2h), "steps": e2e_steps,
+                "includes": "H2D of the step's inputs from pinned memory, host plan build, "
+                            "slot mapping, copies, KV write, attention, D2H of the output"},
+        "gpu_launches": launches_per_step * args.steps,
+        "clocks": clocks.summary(h0, h1),
+        "plan": {k: st[k] for k in ("n_dec_items", "n_tc_items", "n_split_groups", "chunk_tokens")},
+        "bytes": {"kv": kv_b, "q": q_b, "o_write": o_b}, "flops": flops,
+    }
+    if rank == 0:
+        line["cpu_baseline"] = cpu_baseline(args, w)
+        print(json.dumps(line), flush=True)
+
+
+def cpu_baseline(args, w):
+    if args.no_cpu_baseline:
+        return None
+    import oracle
+    from tests.oracle_checks import u16
+    orc = oracle.default()
+    host = {"q": u16(w.q), "k_pool": u16(w.k_pool), "v_pool": u16(w.v_pool),
+            "k_new": u16(w.k_new), "v_new": u16(w.v_new)}
+    n = os.cpu_count() or 1
+    v, sample, _ = oracle_step_sample(w, orc, host, n, budget_s=args.cpu_budget)
+    return {"value": v, "unit": UNIT, "cores": n, "kind": "oracle", "sample": sample}
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=1000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", choices=["gb300", "reference"], default="gb300")
+    ap.add_argument("--config", default="2", help="workload: 1..5 or 5cow (default 2)")
+    ap.add_argument("--cpu-budget", type=float, default=12.0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    args.warmup = max(3, args.warmup)
+    args.config_key = f"cfg{args.config}"
+    rank, local, world = dist_setup(args.gpus)
+
+    import workloads
+    cfg = args.config if args.config == "5cow" else int(args.config)
+
+    if args.impl == "reference":
+        if rank != 0:
+            return
+        w = workloads.make(cfg, device="cpu" if cfg == 1 else "cuda")
+        run_reference(args, w, cfg_dict(w, cfg))
+        return
+
+    import torch
+    torch.cuda.set_device(local)
+    w = workloads.make(cfg, device=f"cuda:{local}")
+    run_gpu(args, w, cfg_dict(w, cfg), rank, local, world)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+def cfg_dict(w, cfg):
+    return {"workload": f"config {cfg}: {w.name}", "num_seqs": w.num_seqs, "total_q": w.total_q,
+            "kv_tokens": int(w.context_lens.sum()), "Hq": w.Hq, "Hkv": w.Hkv, "D": w.D,
+            "block_size": w.block_size, "num_blocks": w.num_blocks,
+            "cow_pairs": int(len(w.cow_src)), "new_tokens": int(len(w.new_seq)),
+            "l2": "no flush: the K/V pools read each step are larger than the 129 MB L2",
+            "parallelism": "replicas only (one independent batch per GPU)"}
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,199 @@
+/*
+ * pa.h -- C ABI of libpa: paged multi-token attention over a block-table KV cache.
+ *
+ * The operations follow the problem as the pages state it:
+ *   - vLLM post (devpress), "1. overall architecture": the KV cache is cut
+ *     into fixed-size physical blocks of block_size tokens; a sequence's
+ *     logical block j lives in physical block block_table[j], so token
+ *     position p sits in slot block_table[p / B] * B + p % B.
+ *   - vLLM wiki note, "kernel layer": fused reshape + block write, fused
+ *     block read + attention, batched block copy.
+ *   - vLLM post, "2.1 parallel sampling": copy-on-write copies one whole block.
+ *   - "PagedAttention" wiki page, "mathematical formulation": exact causal
+ *     softmax attention with scale 1/sqrt(d), token form and block form.
+ *   - Pensieve summary, "multi-token attention for non-contiguous cache" and
+ *     "unified prefill and generation": every sequence contributes any number
+ *     of query tokens, which are the LAST query_len tokens of its context;
+ *     decode is query_len == 1; a context split into disjoint segments is
+ *     passed as sub-requests (extra rows whose block-table rows repeat the same
+ *     physical block ids) without copying.
+ *
+ * Layouts (row-major, C order):
+ *   K pool, V pool   [num_blocks, block_size, Hkv, D]   bf16
+ *   q                [total_q, Hq, D]                    bf16, sequences in order;
+ *                    sequence s owns rows sum_{s'<s} query_lens[s'] ...
+ *   out              [total_q, Hq, D]                    fp32 (PA_F32) or bf16
+ *   block_table      [num_seqs, max_blocks_per_seq]      int32 physical block ids
+ *   context_lens, query_lens [num_seqs]                  int32; context_len
+ *                    counts the step's new tokens (write first, then attend)
+ *   query head h reads KV head h / (Hq / Hkv).
+ *
+ * Conventions:
+ *   - Every pointer argument named d_* or documented "device" is a device
+ *     pointer owned by the caller; the library never frees or keeps it.
+ *     Pointers documented "host" are read during the call only.
+ *   - The stream argument is a cudaStream_t passed as void* (NULL = legacy
+ *     default stream). Calls are asynchronous on that stream unless stated.
+ *   - Argument errors are detected on the host and returned synchronously;
+ *     nothing is launched then. Device-side problems (a block id or slot
+ *     out of range, a device length that disagrees with the plan, a bounded
+ *     wait that ran out) never trap: the kernel skips the access and records
+ *     a code in the library's device error word, read by pa_get_device_error.
+ *   - No entry point allocates device memory; scratch comes from the
+ *     caller's workspace. pa_plan_create allocates host memory only.
+ *   - Thread-compatible: distinct plans may be used from distinct threads.
+ */
+#ifndef PA_H_
+#define PA_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  PA_OK = 0,
+  PA_ERR_INVALID_ARG = 1,  /* a null pointer, negative size, inconsistent lengths */
+  PA_ERR_SHAPE = 2,        /* sizes that do not fit together */
+  PA_ERR_RANGE = 3,        /* a block id, slot or length outside its range */
+  PA_ERR_UNSUPPORTED = 4,  /* valid but not built: head dim, alignment, dtype, device */
+  PA_ERR_CUDA = 5,         /* a CUDA runtime call failed */
+  PA_ERR_TIMEOUT = 6       /* a bounded device wait ran out */
+} pa_status;
+
+typedef enum { PA_F32 = 0, PA_BF16 = 1 } pa_dtype;
+
+/* Device error codes stored in the error word (first error wins). */
+#define PA_DEVERR_NONE 0
+#define PA_DEVERR_SLOT_RANGE 1    /* pa_write_kv: slot >= num_blocks * block_size */
+#define PA_DEVERR_BLOCK_RANGE 2   /* a block id outside [0, num_blocks) */
+#define PA_DEVERR_TABLE_RANGE 3   /* a position beyond max_blocks_per_seq * block_size */
+#define PA_DEVERR_LENS 4          /* device lengths disagree with the plan */
+#define PA_DEVERR_TIMEOUT 5       /* a bounded mbarrier wait ran out */
+
+/* Short English text for a status. Never NULL. */
+const char* pa_status_string(pa_status s);
+
+/* Library version string, e.g. "pa 0.1 sm_103a". */
+const char* pa_version(void);
+
+/* Reads the device error word of the current device after synchronizing
+ * `stream`; writes the PA_DEVERR_* code to *code and, when reset != 0,
+ * clears it. Returns PA_OK, or PA_ERR_CUDA if the sync or read failed. */
+pa_status pa_get_device_error(int32_t* code, int32_t reset, void* stream);
+
+/* Slot of each listed token (vLLM post, "1. overall architecture", worked
+ * example): slots[t] = block_table[seq_ids[t]][positions[t] / B] * B
+ *                      + positions[t] % B;  positions[t] < 0 gives -1.
+ * d_block_table [num_seqs, max_blocks_per_seq] int32, d_seq_ids and
+ * d_positions int32 [n], d_slots int64 [n], all device. Out-of-range entries
+ * give slot -1 and set the device error word. */
+pa_status pa_slot_mapping(const int32_t* d_block_table, int32_t num_seqs,
+                          int32_t max_blocks_per_seq, int32_t block_size, int32_t num_blocks,
+                          const int32_t* d_seq_ids, const int32_t* d_positions, int64_t n,
+                          int64_t* d_slots, void* stream);
+
+/* Scatter the step's new tokens into the cache (vLLM wiki note, "kernel
+ * layer": fused reshape + block write; Pensieve: new KV-tokens are stored in
+ * their allocated slots before attention). For each t < n_new with
+ * slot = d_slot_mapping[t] >= 0: row `slot` of each pool (viewed as
+ * [num_blocks * block_size, Hkv, D]) receives token t of d_k_new / d_v_new
+ * ([n_new, Hkv, D] bf16). Slot -1 is skipped; a slot past the pool is skipped
+ * and recorded (PA_DEVERR_SLOT_RANGE). Slots must be distinct (duplicates
+ * race; the result is then one of the writers). Bit-exact copy.
+ * Requires D % 8 == 0 and 16-byte aligned pointers (else PA_ERR_UNSUPPORTED). */
+pa_status pa_write_kv(const void* d_k_new, const void* d_v_new, const int64_t* d_slot_mapping,
+                      int64_t n_new, void* d_k_pool, void* d_v_pool, int32_t num_blocks,
+                      int32_t block_size, int32_t Hkv, int32_t D, void* stream);
+
+/* Copy-on-write block copy (vLLM post, "2.1 parallel sampling"): for each
+ * pair i < n_pairs, physical block d_src[i] is copied onto d_dst[i] in both
+ * pools. d_src, d_dst int32 [n_pairs], device. Destinations must be distinct
+ * and disjoint from the sources (else the copies race). Ids outside
+ * [0, num_blocks) are skipped and recorded (PA_DEVERR_BLOCK_RANGE).
+ * n_pairs == 0 launches nothing. Bit-exact copy. */
+pa_status pa_copy_blocks(void* d_k_pool, void* d_v_pool, const int32_t* d_src,
+                         const int32_t* d_dst, int32_t n_pairs, int32_t num_blocks,
+                         int32_t block_size, int32_t Hkv, int32_t D, void* stream);
+
+/* ---------------------------------------------------------------- plan
+ * The plan is the host-side auxiliary data of one batch (Pensieve summary,
+ * kernel microbenchmark: the aux data is computed on the CPU). It splits the
+ * batch into work items: (sequence, KV head, a range of query rows, a range
+ * of keys), picks the CUDA-core decode kernel or the tensor-core tile kernel
+ * for each, and splits long key ranges (split-KV) so the GPU fills. A plan
+ * depends only on the host lengths and the shapes, so one plan serves every
+ * layer of a step. */
+typedef struct pa_plan_s* pa_plan_t;
+
+typedef struct {
+  int32_t max_chunk_tokens;  /* 0: automatic split-KV; >0: split key ranges into chunks of at
+                                most this many tokens (rounded up to 64) */
+  int32_t tc_min_rows;       /* 0: default; >0: items with at least this many rows (query
+                                tokens x packed heads) use the tensor-core kernel; <0: never */
+  int32_t num_sms;           /* 0: query the current device */
+  int32_t reserved[5];       /* must be zero */
+} pa_plan_options;
+
+typedef struct {
+  int64_t total_q;           /* sum of query_lens */
+  int32_t num_seqs;
+  int32_t n_dec_items;       /* CUDA-core items */
+  int32_t n_tc_items;        /* tensor-core items */
+  int32_t n_split_groups;    /* row groups whose keys were split (need the combine pass) */
+  int32_t n_partials;        /* partial results the split items write */
+  int32_t chunk_tokens;      /* split chunk length used (0 = no split) */
+  int64_t kv_tokens;         /* sum of context_lens (keys read once per KV head) */
+  int64_t workspace_bytes;
+} pa_plan_stats;
+
+/* Build a plan from HOST copies of the lengths. Validates 0 <= query_len <=
+ * context_len, ceil(context_len / block_size) <= max_blocks_per_seq,
+ * Hq % Hkv == 0, D in {64, 128}, block_size a power of two in [1, 256].
+ * On success *out receives the plan and *workspace_bytes the size of the
+ * device workspace pa_attention needs (at least 256). opts may be NULL. */
+pa_status pa_plan_create(const int32_t* h_context_lens, const int32_t* h_query_lens,
+                         int32_t num_seqs, int32_t Hq, int32_t Hkv, int32_t D,
+                         int32_t block_size, int32_t max_blocks_per_seq,
+                         const pa_plan_options* opts, pa_plan_t* out, size_t* workspace_bytes);
+
+/* Frees a plan (NULL is ignored). Safe once no pa_attention that uses it is
+ * still being enqueued; kernels already enqueued do not read the plan. */
+pa_status pa_plan_destroy(pa_plan_t plan);
+
+pa_status pa_plan_get_stats(pa_plan_t plan, pa_plan_stats* out);
+
+/* Copies the plan's work items to host memory, 9 int32 per item:
+ * (path, seq, kv_head, row_begin, row_count, kv_begin, kv_end, part, q_row0),
+ * path 0 = CUDA-core kernel, 1 = tensor-core kernel; packed row rho of a
+ * (seq, kv_head) pair is query token rho / g and query head kv_head * g + rho % g;
+ * part = first partial-result row (-1 = written straight to out); q_row0 = row
+ * of the sequence's first query in q. Writes at most max_items items and the
+ * total count to *n_items. For inspection and tests; host only. */
+pa_status pa_plan_export(pa_plan_t plan, int32_t* h_items, int32_t max_items, int32_t* n_items);
+
+/* Paged multi-token causal attention (PagedAttention wiki page, token and
+ * block forms; Pensieve multi-token kernel with the causal mask fused).
+ * For every sequence s, query row i < query_lens[s] (absolute position
+ * p = context_lens[s] - query_lens[s] + i) and query head h:
+ *   out[r, h, :] = sum_{j <= p} softmax_j(scale * q[r,h,:] . k_j) v_j,
+ * k_j, v_j read from the pools through d_block_table row s, KV head h/(Hq/Hkv).
+ * scale <= 0 selects 1/sqrt(D). The plan must come from the same lengths
+ * (device lengths that disagree are recorded as PA_DEVERR_LENS).
+ * d_workspace: device buffer of at least the plan's workspace_bytes, 256-byte
+ * aligned; its contents need no initialisation and are overwritten.
+ * Calls sharing one workspace must not overlap on the GPU.
+ * Keys past context_len in a sequence's last block are never used, whatever
+ * bits they hold. */
+pa_status pa_attention(pa_plan_t plan, void* d_out, pa_dtype out_dtype, const void* d_q,
+                       const void* d_k_pool, const void* d_v_pool, const int32_t* d_block_table,
+                       const int32_t* d_context_lens, const int32_t* d_query_lens,
+                       int32_t num_blocks, float scale, void* d_workspace,
+                       size_t workspace_bytes, void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* PA_H_ */

@@ -1,0 +1,248 @@
+"""ctypes binding of libpa (include/pa.h): argument marshalling only.
+
+Every function takes torch tensors, checks dtype / device / contiguity, and
+passes raw pointers, sizes and the current CUDA stream to the C ABI. No step of
+the computation happens here: if ``libpa.so`` is missing the calls raise.
+"""
+from __future__ import annotations
+
+import ctypes as C
+import os
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libpa.so")
+
+PA_OK = 0
+PA_F32, PA_BF16 = 0, 1
+DEVERR = {0: "none", 1: "slot out of range", 2: "block id out of range",
+          3: "position beyond the block table", 4: "device lengths disagree with the plan",
+          5: "bounded wait ran out"}
+
+
+class PagedAttentionError(RuntimeError):
+    def __init__(self, status: int, what: str):
+        self.status = status
+        super().__init__(f"{what}: {_lib().pa_status_string(status).decode()} (status {status})")
+
+
+class _Options(C.Structure):
+    _fields_ = [("max_chunk_tokens", C.c_int32), ("tc_min_rows", C.c_int32),
+                ("num_sms", C.c_int32), ("reserved", C.c_int32 * 5)]
+
+
+class _Stats(C.Structure):
+    _fields_ = [("total_q", C.c_int64), ("num_seqs", C.c_int32), ("n_dec_items", C.c_int32),
+                ("n_tc_items", C.c_int32), ("n_split_groups", C.c_int32),
+                ("n_partials", C.c_int32), ("chunk_tokens", C.c_int32),
+                ("kv_tokens", C.c_int64), ("workspace_bytes", C.c_int64)]
+
+
+_LIB = None
+_P, _I32, _I64 = C.c_void_p, C.c_int32, C.c_int64
+
+
+def _lib() -> C.CDLL:
+    global _LIB
+    if _LIB is None:
+        if not os.path.exists(LIB_PATH):
+            raise RuntimeError(f"libpa.so is not built ({LIB_PATH}); run "
+                               "paged_kv_cache_02_gb300._build.build() first")
+        lib = C.CDLL(LIB_PATH)
+        lib.pa_status_string.restype = C.c_char_p
+        lib.pa_status_string.argtypes = [C.c_int]
+        lib.pa_version.restype = C.c_char_p
+        lib.pa_get_device_error.argtypes = [C.POINTER(C.c_int32), _I32, _P]
+        lib.pa_slot_mapping.argtypes = [_P, _I32, _I32, _I32, _I32, _P, _P, _I64, _P, _P]
+        lib.pa_write_kv.argtypes = [_P, _P, _P, _I64, _P, _P, _I32, _I32, _I32, _I32, _P]
+        lib.pa_copy_blocks.argtypes = [_P, _P, _P, _P, _I32, _I32, _I32, _I32, _I32, _P]
+        lib.pa_plan_create.argtypes = [_P, _P, _I32, _I32, _I32, _I32, _I32, _I32,
+                                       C.POINTER(_Options), C.POINTER(_P), C.POINTER(C.c_size_t)]
+        lib.pa_plan_destroy.argtypes = [_P]
+        lib.pa_plan_get_stats.argtypes = [_P, C.POINTER(_Stats)]
+        lib.pa_plan_export.argtypes = [_P, _P, _I32, C.POINTER(C.c_int32)]
+        lib.pa_attention.argtypes = [_P, _P, C.c_int, _P, _P, _P, _P, _P, _P, _I32, C.c_float, _P,
+                                     C.c_size_t, _P]
+        for f in ("pa_get_device_error", "pa_slot_mapping", "pa_write_kv", "pa_copy_blocks",
+                  "pa_plan_create", "pa_plan_destroy", "pa_plan_get_stats", "pa_plan_export",
+                  "pa_attention"):
+            getattr(lib, f).restype = C.c_int
+        _LIB = lib
+    return _LIB
+
+
+def library() -> C.CDLL:
+    """The loaded libpa handle (raises if the library is not built)."""
+    return _lib()
+
+
+def _check(status: int, what: str):
+    if status != PA_OK:
+        raise PagedAttentionError(status, what)
+
+
+def _stream(t: torch.Tensor | None = None):
+    dev = t.device if t is not None else torch.device("cuda", torch.cuda.current_device())
+    return C.c_void_p(torch.cuda.current_stream(dev).cuda_stream)
+
+
+def _dev(t: torch.Tensor, dtype, name: str, ndim: int | None = None) -> int:
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch.Tensor")
+    if not t.is_cuda:
+        raise ValueError(f"{name} must live on a CUDA device")
+    if t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if ndim is not None and t.dim() != ndim:
+        raise ValueError(f"{name} must have {ndim} dimensions, got {t.dim()}")
+    return t.data_ptr()
+
+
+def version() -> str:
+    return _lib().pa_version().decode()
+
+
+def pa_get_device_error(reset: bool = True) -> int:
+    """PA_DEVERR_* code recorded by kernels on the current device (syncs the stream)."""
+    code = C.c_int32(0)
+    _check(_lib().pa_get_device_error(C.byref(code), int(reset), _stream()), "pa_get_device_error")
+    return code.value
+
+
+def pa_slot_mapping(block_table: torch.Tensor, num_blocks: int, block_size: int,
+                    seq_ids: torch.Tensor, positions: torch.Tensor,
+                    out: torch.Tensor | None = None) -> torch.Tensor:
+    bt = _dev(block_table, torch.int32, "block_table", 2)
+    n = seq_ids.numel()
+    if out is None:
+        out = torch.empty(n, dtype=torch.int64, device=block_table.device)
+    _check(_lib().pa_slot_mapping(bt, block_table.shape[0], block_table.shape[1], block_size,
+                                  num_blocks, _dev(seq_ids, torch.int32, "seq_ids", 1),
+                                  _dev(positions, torch.int32, "positions", 1), n,
+                                  _dev(out, torch.int64, "out", 1), _stream(block_table)),
+           "pa_slot_mapping")
+    return out
+
+
+def pa_write_kv(k_new: torch.Tensor, v_new: torch.Tensor, slot_mapping: torch.Tensor,
+                k_pool: torch.Tensor, v_pool: torch.Tensor) -> None:
+    nb, B, Hkv, D = k_pool.shape
+    if v_pool.shape != k_pool.shape or k_new.shape != v_new.shape:
+        raise ValueError("pool / new-token shapes differ")
+    if k_new.shape[1:] != (Hkv, D) or slot_mapping.numel() != k_new.shape[0]:
+        raise ValueError("new tokens must be [n_new, Hkv, D] with one slot each")
+    _check(_lib().pa_write_kv(_dev(k_new, torch.bfloat16, "k_new", 3),
+                              _dev(v_new, torch.bfloat16, "v_new", 3),
+                              _dev(slot_mapping, torch.int64, "slot_mapping", 1), k_new.shape[0],
+                              _dev(k_pool, torch.bfloat16, "k_pool", 4),
+                              _dev(v_pool, torch.bfloat16, "v_pool", 4), nb, B, Hkv, D,
+                              _stream(k_pool)), "pa_write_kv")
+
+
+def pa_copy_blocks(k_pool: torch.Tensor, v_pool: torch.Tensor, src: torch.Tensor,
+                   dst: torch.Tensor) -> None:
+    nb, B, Hkv, D = k_pool.shape
+    if src.numel() != dst.numel():
+        raise ValueError("src and dst need the same length")
+    _check(_lib().pa_copy_blocks(_dev(k_pool, torch.bfloat16, "k_pool", 4),
+                                 _dev(v_pool, torch.bfloat16, "v_pool", 4),
+                                 _dev(src, torch.int32, "src", 1), _dev(dst, torch.int32, "dst", 1),
+                                 src.numel(), nb, B, Hkv, D, _stream(k_pool)), "pa_copy_blocks")
+
+
+class Plan:
+    """Host plan of one batch (pa_plan_create). Reusable across layers; close() frees it."""
+
+    def __init__(self, context_lens, query_lens, Hq: int, Hkv: int, D: int, block_size: int,
+                 max_blocks_per_seq: int, max_chunk_tokens: int = 0, tc_min_rows: int = 0,
+                 num_sms: int = 0):
+        import numpy as np
+        self._cl = np.ascontiguousarray(np.asarray(context_lens, dtype=np.int32))
+        self._ql = np.ascontiguousarray(np.asarray(query_lens, dtype=np.int32))
+        if self._cl.shape != self._ql.shape or self._cl.ndim != 1:
+            raise ValueError("context_lens and query_lens must be 1-D of equal length")
+        opts = _Options(max_chunk_tokens, tc_min_rows, num_sms)
+        handle = C.c_void_p()
+        ws = C.c_size_t(0)
+        self._h = None
+        _check(_lib().pa_plan_create(self._cl.ctypes.data, self._ql.ctypes.data, len(self._cl), Hq,
+                                     Hkv, D, block_size, max_blocks_per_seq, C.byref(opts),
+                                     C.byref(handle), C.byref(ws)), "pa_plan_create")
+        self._h = handle
+        self.workspace_bytes = int(ws.value)
+        self.Hq, self.Hkv, self.D, self.block_size = Hq, Hkv, D, block_size
+        self.max_blocks_per_seq = max_blocks_per_seq
+        self.total_q = int(self._ql.astype("int64").sum())
+
+    def stats(self) -> dict:
+        st = _Stats()
+        _check(_lib().pa_plan_get_stats(self._h, C.byref(st)), "pa_plan_get_stats")
+        return {k: getattr(st, k) for k, _ in _Stats._fields_}
+
+    def items(self):
+        """Work items as an int32 array [n, 9]: (path, seq, kv_head, row_begin, row_count,
+        kv_begin, kv_end, part, q_row0)."""
+        import numpy as np
+        n = C.c_int32(0)
+        _check(_lib().pa_plan_export(self._h, None, 0, C.byref(n)), "pa_plan_export")
+        arr = np.zeros((n.value, 9), dtype=np.int32)
+        _check(_lib().pa_plan_export(self._h, arr.ctypes.data, n.value, C.byref(n)),
+               "pa_plan_export")
+        return arr
+
+    def close(self):
+        if self._h is not None and _LIB is not None:
+            _LIB.pa_plan_destroy(self._h)
+        self._h = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+    def workspace(self, device) -> torch.Tensor:
+        """A fresh device workspace of the size this plan needs (uint8, 256-byte aligned)."""
+        return torch.empty(self.workspace_bytes, dtype=torch.uint8, device=device)
+
+
+def pa_plan_create(context_lens, query_lens, Hq, Hkv, D, block_size, max_blocks_per_seq,
+                   **options) -> Plan:
+    return Plan(context_lens, query_lens, Hq, Hkv, D, block_size, max_blocks_per_seq, **options)
+
+
+def pa_attention(plan: Plan, q: torch.Tensor, k_pool: torch.Tensor, v_pool: torch.Tensor,
+                 block_table: torch.Tensor, context_lens: torch.Tensor, query_lens: torch.Tensor,
+                 out: torch.Tensor | None = None, out_dtype=torch.float32, scale: float = 0.0,
+                 workspace: torch.Tensor | None = None) -> torch.Tensor:
+    nb, B, Hkv, D = k_pool.shape
+    if (Hkv, D, B) != (plan.Hkv, plan.D, plan.block_size):
+        raise ValueError("pool shape does not match the plan")
+    if q.dim() != 3 or q.shape[1:] != (plan.Hq, D) or q.shape[0] != plan.total_q:
+        raise ValueError("q must be [total_q, Hq, D] as planned")
+    if block_table.dim() != 2 or block_table.shape[1] != plan.max_blocks_per_seq:
+        raise ValueError("block_table must be [num_seqs, max_blocks_per_seq] as planned")
+    if out is None:
+        out = torch.empty(q.shape, dtype=out_dtype, device=q.device)
+    dt = {torch.float32: PA_F32, torch.bfloat16: PA_BF16}.get(out.dtype)
+    if dt is None:
+        raise TypeError("out must be float32 or bfloat16")
+    if out.shape != q.shape:
+        raise ValueError("out must be shaped like q")
+    if workspace is None:
+        workspace = plan.workspace(q.device)
+    if workspace.data_ptr() % 256:
+        raise ValueError("workspace must be 256-byte aligned")
+    _check(_lib().pa_attention(plan._h, _dev(out, out.dtype, "out", 3), dt,
+                               _dev(q, torch.bfloat16, "q", 3),
+                               _dev(k_pool, torch.bfloat16, "k_pool", 4),
+                               _dev(v_pool, torch.bfloat16, "v_pool", 4),
+                               _dev(block_table, torch.int32, "block_table", 2),
+                               _dev(context_lens, torch.int32, "context_lens", 1),
+                               _dev(query_lens, torch.int32, "query_lens", 1), nb, float(scale),
+                               workspace.data_ptr(), workspace.numel(), _stream(q)),
+           "pa_attention")
+    return out

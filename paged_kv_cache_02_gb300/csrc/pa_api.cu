@@ -1,0 +1,451 @@
+// pa_api.cu -- the C ABI: argument checks, the host plan, tensor maps, launches.
+//
+// The plan is the auxiliary data Pensieve computes on the CPU (Pensieve summary,
+// kernel microbenchmark): the batch's (sequence, KV head) pairs cut into work
+// items, each item a range of packed rows (query tokens x the query heads of one
+// KV head) against a range of keys. Items with many rows go to the tensor-core
+// kernel, the rest to the CUDA-core kernel; long key ranges are split so that
+// every SM has work (split-KV), and the split rows are merged by a combine pass.
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <cudaTypedefs.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+
+#include <algorithm>
+#include <cmath>
+#include <mutex>
+#include <new>
+#include <vector>
+
+#include "pa_internal.h"
+
+namespace pa {
+
+// ------------------------------------------------------------------ error word
+// One word per device (plus spare room), written by kernels with atomicCAS.
+__device__ int g_error_word[4];
+
+int* device_error_word() {
+  static std::mutex mu;
+  static int* cache[64] = {nullptr};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
+  std::lock_guard<std::mutex> lock(mu);
+  if (!cache[dev]) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_error_word) != cudaSuccess) return nullptr;
+    cache[dev] = static_cast<int*>(p);
+  }
+  return cache[dev];
+}
+
+// ------------------------------------------------------------------ tensor maps
+namespace {
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  });
+  return fn;
+}
+}  // namespace
+
+pa_status make_pool_map(CUtensorMap* map, const void* pool, int64_t num_blocks, int block_size,
+                        int Hkv, int D, int box_d, int box_t, bool swizzle128) {
+  auto fn = encode_fn();
+  if (!fn) return PA_ERR_CUDA;
+  cuuint64_t dims[3] = {(cuuint64_t)D, (cuuint64_t)Hkv, (cuuint64_t)(num_blocks * block_size)};
+  cuuint64_t strides[2] = {(cuuint64_t)D * 2, (cuuint64_t)Hkv * D * 2};
+  cuuint32_t box[3] = {(cuuint32_t)box_d, 1u, (cuuint32_t)box_t};
+  cuuint32_t estr[3] = {1u, 1u, 1u};
+  CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(pool), dims, strides,
+                  box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                  swizzle128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? PA_OK : PA_ERR_CUDA;
+}
+
+}  // namespace pa
+
+// ====================================================================== plan
+
+struct pa_plan_s {
+  int32_t num_seqs, Hq, Hkv, D, block_size, max_blocks, g;
+  int64_t total_q;
+  int32_t n_dec, n_tc, n_groups;
+  int32_t dec_rows_max;
+  int64_t n_part_rows;
+  int32_t chunk;
+  int64_t kv_tokens;
+  // workspace layout (byte offsets)
+  size_t off_dec, off_tc, off_groups, off_acc, off_ml, ws_bytes;
+  size_t table_bytes;       // bytes of the item / group tables (copied each call)
+  void* host_tables;        // table image: [dec items][tc items][groups] at their offsets
+  bool host_pinned;
+};
+
+namespace {
+
+using pa::Item;
+using pa::SplitGroup;
+
+bool is_pow2(int x) { return x > 0 && (x & (x - 1)) == 0; }
+size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+int device_sms() {
+  int dev = 0, sms = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) { cudaGetLastError(); return 0; }
+  if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) {
+    cudaGetLastError();
+    return 0;
+  }
+  return sms;
+}
+
+struct Unit {
+  int32_t seq, kvh, row_begin, row_count, keys, q_row0;
+  bool tc;
+};
+
+}  // namespace
+
+extern "C" {
+
+const char* pa_status_string(pa_status s) {
+  switch (s) {
+    case PA_OK: return "ok";
+    case PA_ERR_INVALID_ARG: return "invalid argument";
+    case PA_ERR_SHAPE: return "inconsistent shapes";
+    case PA_ERR_RANGE: return "value out of range";
+    case PA_ERR_UNSUPPORTED: return "unsupported configuration";
+    case PA_ERR_CUDA: return "CUDA runtime error";
+    case PA_ERR_TIMEOUT: return "bounded device wait ran out";
+  }
+  return "unknown status";
+}
+
+const char* pa_version(void) { return "pa 0.1 sm_103a"; }
+
+pa_status pa_get_device_error(int32_t* code, int32_t reset, void* stream) {
+  if (!code) return PA_ERR_INVALID_ARG;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (cudaStreamSynchronize(s) != cudaSuccess) return PA_ERR_CUDA;
+  int v = 0;
+  if (cudaMemcpyFromSymbol(&v, pa::g_error_word, sizeof(int)) != cudaSuccess) return PA_ERR_CUDA;
+  *code = v;
+  if (reset) {
+    const int zero = 0;
+    if (cudaMemcpyToSymbol(pa::g_error_word, &zero, sizeof(int)) != cudaSuccess)
+      return PA_ERR_CUDA;
+  }
+  return PA_OK;
+}
+
+pa_status pa_slot_mapping(const int32_t* d_block_table, int32_t num_seqs,
+                          int32_t max_blocks_per_seq, int32_t block_size, int32_t num_blocks,
+                          const int32_t* d_seq_ids, const int32_t* d_positions, int64_t n,
+                          int64_t* d_slots, void* stream) {
+  if (n < 0 || num_seqs < 0 || max_blocks_per_seq <= 0 || block_size <= 0 || num_blocks <= 0)
+    return PA_ERR_INVALID_ARG;
+  if (n == 0) return PA_OK;
+  if (!d_block_table || !d_seq_ids || !d_positions || !d_slots) return PA_ERR_INVALID_ARG;
+  int* err = pa::device_error_word();
+  if (!err) return PA_ERR_CUDA;
+  cudaError_t e = pa::launch_slot_mapping(d_block_table, num_seqs, max_blocks_per_seq, block_size,
+                                          num_blocks, d_seq_ids, d_positions, n, d_slots, err,
+                                          static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? PA_OK : PA_ERR_CUDA;
+}
+
+pa_status pa_write_kv(const void* d_k_new, const void* d_v_new, const int64_t* d_slot_mapping,
+                      int64_t n_new, void* d_k_pool, void* d_v_pool, int32_t num_blocks,
+                      int32_t block_size, int32_t Hkv, int32_t D, void* stream) {
+  if (n_new < 0 || num_blocks <= 0 || block_size <= 0 || Hkv <= 0 || D <= 0)
+    return PA_ERR_INVALID_ARG;
+  if (n_new == 0) return PA_OK;
+  if (!d_k_new || !d_v_new || !d_slot_mapping || !d_k_pool || !d_v_pool) return PA_ERR_INVALID_ARG;
+  if (D % 8) return PA_ERR_UNSUPPORTED;
+  for (const void* p : {d_k_new, d_v_new, (const void*)d_k_pool, (const void*)d_v_pool})
+    if (reinterpret_cast<uintptr_t>(p) % 16) return PA_ERR_UNSUPPORTED;
+  int* err = pa::device_error_word();
+  if (!err) return PA_ERR_CUDA;
+  const int64_t row_bytes = (int64_t)Hkv * D * 2;
+  cudaError_t e = pa::launch_write_kv(d_k_new, d_v_new, d_slot_mapping, n_new, d_k_pool, d_v_pool,
+                                      (int64_t)num_blocks * block_size, row_bytes, err,
+                                      static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? PA_OK : PA_ERR_CUDA;
+}
+
+pa_status pa_copy_blocks(void* d_k_pool, void* d_v_pool, const int32_t* d_src,
+                         const int32_t* d_dst, int32_t n_pairs, int32_t num_blocks,
+                         int32_t block_size, int32_t Hkv, int32_t D, void* stream) {
+  if (n_pairs < 0 || num_blocks <= 0 || block_size <= 0 || Hkv <= 0 || D <= 0)
+    return PA_ERR_INVALID_ARG;
+  if (n_pairs == 0) return PA_OK;
+  if (!d_k_pool || !d_v_pool || !d_src || !d_dst) return PA_ERR_INVALID_ARG;
+  if (D % 8) return PA_ERR_UNSUPPORTED;
+  if (reinterpret_cast<uintptr_t>(d_k_pool) % 16 || reinterpret_cast<uintptr_t>(d_v_pool) % 16)
+    return PA_ERR_UNSUPPORTED;
+  int* err = pa::device_error_word();
+  if (!err) return PA_ERR_CUDA;
+  const int64_t block_bytes = (int64_t)block_size * Hkv * D * 2;
+  cudaError_t e = pa::launch_copy_blocks(d_k_pool, d_v_pool, d_src, d_dst, n_pairs, num_blocks,
+                                         block_bytes, err, static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? PA_OK : PA_ERR_CUDA;
+}
+
+pa_status pa_plan_create(const int32_t* h_context_lens, const int32_t* h_query_lens,
+                         int32_t num_seqs, int32_t Hq, int32_t Hkv, int32_t D,
+                         int32_t block_size, int32_t max_blocks_per_seq,
+                         const pa_plan_options* opts, pa_plan_t* out, size_t* workspace_bytes) {
+  if (!out || !workspace_bytes) return PA_ERR_INVALID_ARG;
+  *out = nullptr;
+  if (num_seqs < 0 || Hq <= 0 || Hkv <= 0 || max_blocks_per_seq <= 0) return PA_ERR_INVALID_ARG;
+  if (num_seqs > 0 && (!h_context_lens || !h_query_lens)) return PA_ERR_INVALID_ARG;
+  if (Hq % Hkv) return PA_ERR_SHAPE;
+  if (D != 64 && D != 128) return PA_ERR_UNSUPPORTED;
+  if (!is_pow2(block_size) || block_size > 256) return PA_ERR_UNSUPPORTED;
+  pa_plan_options o;
+  memset(&o, 0, sizeof o);
+  if (opts) {
+    o = *opts;
+    for (int i = 0; i < 5; ++i)
+      if (o.reserved[i]) return PA_ERR_INVALID_ARG;
+  }
+  const int g = Hq / Hkv;
+  int64_t total_q = 0, kv_tokens = 0;
+  for (int32_t s = 0; s < num_seqs; ++s) {
+    const int32_t L = h_context_lens[s], q = h_query_lens[s];
+    if (L < 0 || q < 0 || q > L) return PA_ERR_RANGE;
+    if ((int64_t)(L + block_size - 1) / block_size > max_blocks_per_seq) return PA_ERR_RANGE;
+    total_q += q;
+    kv_tokens += L;
+  }
+  if (total_q * Hq > INT32_MAX || (int64_t)Hq * g > INT32_MAX) return PA_ERR_UNSUPPORTED;
+
+  int sms = o.num_sms > 0 ? o.num_sms : device_sms();
+  if (sms <= 0) sms = 152;
+  // Tensor-core items are not built yet: every item runs on the CUDA-core path.
+  const bool tc_enabled = false;
+
+  // ---- units: (sequence, KV head, row tile)
+  std::vector<Unit> units;
+  int64_t total_keys = 0;
+  int64_t q_row0 = 0;
+  for (int32_t s = 0; s < num_seqs; ++s) {
+    const int32_t L = h_context_lens[s], q = h_query_lens[s];
+    if (q > 0) {
+      const int64_t rows = (int64_t)q * g;
+      const bool tc = tc_enabled && o.tc_min_rows >= 0 && rows >= o.tc_min_rows && D == 128;
+      const int rt = tc ? pa::kTcRows : pa::kDecRows;
+      for (int32_t kvh = 0; kvh < Hkv; ++kvh) {
+        for (int64_t rb = 0; rb < rows; rb += rt) {
+          const int32_t rc = (int32_t)std::min<int64_t>(rt, rows - rb);
+          const int32_t t_last = (int32_t)((rb + rc - 1) / g);
+          const int32_t keys = L - q + t_last + 1;
+          units.push_back({s, kvh, (int32_t)rb, rc, keys, (int32_t)q_row0, tc});
+          total_keys += keys;
+        }
+      }
+    }
+    q_row0 += q;
+  }
+  // ---- split-KV chunk length
+  int64_t chunk;
+  if (o.max_chunk_tokens > 0) {
+    chunk = align_up((size_t)o.max_chunk_tokens, pa::kChunkAlign);
+  } else {
+    // about three items per SM over the whole batch, never below 256 keys
+    chunk = std::max<int64_t>(256, align_up((size_t)(total_keys / (3 * (int64_t)sms) + 1),
+                                            pa::kChunkAlign));
+  }
+  std::vector<Item> dec, tc;
+  std::vector<SplitGroup> groups;
+  int64_t part_rows = 0;
+  int32_t dec_rows_max = 1;
+  bool any_split = false;
+  for (const Unit& u : units) {
+    const int64_t n_chunks = (u.keys + chunk - 1) / chunk;
+    std::vector<Item>& dst = u.tc ? tc : dec;
+    if (!u.tc) dec_rows_max = std::max(dec_rows_max, u.row_count);
+    if (n_chunks <= 1) {
+      dst.push_back({u.seq, u.kvh, u.row_begin, u.row_count, 0, u.keys, -1, u.q_row0});
+    } else {
+      any_split = true;
+      if (part_rows + n_chunks * u.row_count > INT32_MAX) return PA_ERR_UNSUPPORTED;
+      groups.push_back({u.seq, u.kvh, u.row_begin, u.row_count, (int32_t)part_rows,
+                        (int32_t)n_chunks, u.q_row0, 0});
+      for (int64_t c = 0; c < n_chunks; ++c) {
+        const int32_t kb = (int32_t)(c * chunk);
+        const int32_t ke = (int32_t)std::min<int64_t>((c + 1) * chunk, u.keys);
+        dst.push_back({u.seq, u.kvh, u.row_begin, u.row_count, kb, ke,
+                       (int32_t)(part_rows + c * u.row_count), u.q_row0});
+      }
+      part_rows += n_chunks * u.row_count;
+    }
+  }
+  // longest key range first: with the round-robin walk of the persistent
+  // kernel this balances the SMs (longest-processing-time order)
+  auto longer = [](const Item& x, const Item& y) {
+    return (x.kv_end - x.kv_begin) > (y.kv_end - y.kv_begin);
+  };
+  std::stable_sort(dec.begin(), dec.end(), longer);
+  std::stable_sort(tc.begin(), tc.end(), longer);
+
+  pa_plan_s* p = new (std::nothrow) pa_plan_s();
+  if (!p) return PA_ERR_INVALID_ARG;
+  p->num_seqs = num_seqs; p->Hq = Hq; p->Hkv = Hkv; p->D = D; p->block_size = block_size;
+  p->max_blocks = max_blocks_per_seq; p->g = g; p->total_q = total_q;
+  p->n_dec = (int32_t)dec.size(); p->n_tc = (int32_t)tc.size(); p->n_groups = (int32_t)groups.size();
+  p->dec_rows_max = dec_rows_max; p->n_part_rows = part_rows;
+  p->chunk = any_split ? (int32_t)chunk : 0; p->kv_tokens = kv_tokens;
+  size_t off = 0;
+  p->off_dec = off; off = align_up(off + dec.size() * sizeof(Item), 256);
+  p->off_tc = off; off = align_up(off + tc.size() * sizeof(Item), 256);
+  p->off_groups = off; off = align_up(off + groups.size() * sizeof(SplitGroup), 256);
+  p->table_bytes = off;
+  p->off_acc = off; off = align_up(off + (size_t)part_rows * D * sizeof(float), 256);
+  p->off_ml = off; off = align_up(off + (size_t)part_rows * 2 * sizeof(float), 256);
+  p->ws_bytes = std::max<size_t>(off, 256);
+  p->host_tables = nullptr;
+  p->host_pinned = false;
+  if (p->table_bytes > 0) {
+    if (cudaMallocHost(&p->host_tables, p->table_bytes) == cudaSuccess) {
+      p->host_pinned = true;
+    } else {
+      cudaGetLastError();
+      p->host_tables = malloc(p->table_bytes);
+      if (!p->host_tables) { delete p; return PA_ERR_INVALID_ARG; }
+    }
+    uint8_t* h = static_cast<uint8_t*>(p->host_tables);
+    memset(h, 0, p->table_bytes);
+    if (!dec.empty()) memcpy(h + p->off_dec, dec.data(), dec.size() * sizeof(Item));
+    if (!tc.empty()) memcpy(h + p->off_tc, tc.data(), tc.size() * sizeof(Item));
+    if (!groups.empty())
+      memcpy(h + p->off_groups, groups.data(), groups.size() * sizeof(SplitGroup));
+  }
+  *out = p;
+  *workspace_bytes = p->ws_bytes;
+  return PA_OK;
+}
+
+pa_status pa_plan_destroy(pa_plan_t p) {
+  if (!p) return PA_OK;
+  if (p->host_tables) {
+    if (p->host_pinned)
+      cudaFreeHost(p->host_tables);
+    else
+      free(p->host_tables);
+  }
+  delete p;
+  return PA_OK;
+}
+
+pa_status pa_plan_get_stats(pa_plan_t p, pa_plan_stats* out) {
+  if (!p || !out) return PA_ERR_INVALID_ARG;
+  out->total_q = p->total_q;
+  out->num_seqs = p->num_seqs;
+  out->n_dec_items = p->n_dec;
+  out->n_tc_items = p->n_tc;
+  out->n_split_groups = p->n_groups;
+  out->n_partials = (int32_t)p->n_part_rows;
+  out->chunk_tokens = p->chunk;
+  out->kv_tokens = p->kv_tokens;
+  out->workspace_bytes = (int64_t)p->ws_bytes;
+  return PA_OK;
+}
+
+pa_status pa_plan_export(pa_plan_t p, int32_t* h_items, int32_t max_items, int32_t* n_items) {
+  if (!p || !n_items || max_items < 0 || (max_items > 0 && !h_items)) return PA_ERR_INVALID_ARG;
+  *n_items = p->n_dec + p->n_tc;
+  const uint8_t* h = static_cast<const uint8_t*>(p->host_tables);
+  int32_t k = 0;
+  for (int path = 0; path < 2; ++path) {
+    const int32_t n = path == 0 ? p->n_dec : p->n_tc;
+    const Item* it = reinterpret_cast<const Item*>(h + (path == 0 ? p->off_dec : p->off_tc));
+    for (int32_t i = 0; i < n && k < max_items; ++i, ++k) {
+      int32_t* r = h_items + (int64_t)k * 9;
+      r[0] = path; r[1] = it[i].seq; r[2] = it[i].kv_head; r[3] = it[i].row_begin;
+      r[4] = it[i].row_count; r[5] = it[i].kv_begin; r[6] = it[i].kv_end; r[7] = it[i].part;
+      r[8] = it[i].q_row0;
+    }
+  }
+  return PA_OK;
+}
+
+pa_status pa_attention(pa_plan_t p, void* d_out, pa_dtype out_dtype, const void* d_q,
+                       const void* d_k_pool, const void* d_v_pool, const int32_t* d_block_table,
+                       const int32_t* d_context_lens, const int32_t* d_query_lens,
+                       int32_t num_blocks, float scale, void* d_workspace,
+                       size_t workspace_bytes, void* stream) {
+  if (!p) return PA_ERR_INVALID_ARG;
+  if (out_dtype != PA_F32 && out_dtype != PA_BF16) return PA_ERR_INVALID_ARG;
+  if (num_blocks <= 0) return PA_ERR_INVALID_ARG;
+  if ((int64_t)num_blocks * p->block_size > INT32_MAX) return PA_ERR_UNSUPPORTED;
+  if (p->total_q == 0) return PA_OK;
+  if (!d_out || !d_q || !d_k_pool || !d_v_pool || !d_block_table || !d_context_lens ||
+      !d_query_lens || !d_workspace)
+    return PA_ERR_INVALID_ARG;
+  if (workspace_bytes < p->ws_bytes) return PA_ERR_SHAPE;
+  if (reinterpret_cast<uintptr_t>(d_workspace) % 256) return PA_ERR_UNSUPPORTED;
+  for (const void* ptr : {d_q, d_k_pool, d_v_pool, (const void*)d_out})
+    if (reinterpret_cast<uintptr_t>(ptr) % 16) return PA_ERR_UNSUPPORTED;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  int* err = pa::device_error_word();
+  if (!err) return PA_ERR_CUDA;
+  uint8_t* ws = static_cast<uint8_t*>(d_workspace);
+  if (p->table_bytes &&
+      cudaMemcpyAsync(ws, p->host_tables, p->table_bytes, cudaMemcpyHostToDevice, s) !=
+          cudaSuccess)
+    return PA_ERR_CUDA;
+
+  pa::AttnArgs a;
+  a.q = static_cast<const uint16_t*>(d_q);
+  a.out = d_out;
+  a.out_bf16 = out_dtype == PA_BF16;
+  a.block_table = d_block_table;
+  a.context_lens = d_context_lens;
+  a.query_lens = d_query_lens;
+  a.max_blocks = p->max_blocks;
+  a.num_blocks = num_blocks;
+  a.block_size = p->block_size;
+  a.Hq = p->Hq; a.Hkv = p->Hkv; a.g = p->g;
+  const float sc = scale > 0.f ? scale : 1.0f / sqrtf((float)p->D);
+  a.scale_log2 = sc * 1.4426950408889634f;
+  a.part_acc = reinterpret_cast<float*>(ws + p->off_acc);
+  a.part_ml = reinterpret_cast<float*>(ws + p->off_ml);
+  a.err = err;
+
+  if (p->n_dec > 0) {
+    const int box_t = std::min(p->block_size, pa::kKeyTile);
+    CUtensorMap kmap, vmap;
+    pa_status st = pa::make_pool_map(&kmap, d_k_pool, num_blocks, p->block_size, p->Hkv, p->D,
+                                     p->D, box_t, false);
+    if (st != PA_OK) return st;
+    st = pa::make_pool_map(&vmap, d_v_pool, num_blocks, p->block_size, p->Hkv, p->D, p->D, box_t,
+                           false);
+    if (st != PA_OK) return st;
+    int sms = device_sms();
+    if (sms <= 0) return PA_ERR_CUDA;
+    const int grid = std::min(p->n_dec, sms);
+    cudaError_t e = pa::launch_decode(a, kmap, vmap, reinterpret_cast<const Item*>(ws + p->off_dec),
+                                      p->n_dec, p->D, p->dec_rows_max, box_t, grid, s);
+    if (e != cudaSuccess) return PA_ERR_CUDA;
+  }
+  if (p->n_groups > 0) {
+    cudaError_t e = pa::launch_combine(
+        a, reinterpret_cast<const SplitGroup*>(ws + p->off_groups), p->n_groups, p->D, s);
+    if (e != cudaSuccess) return PA_ERR_CUDA;
+  }
+  return PA_OK;
+}
+
+}  // extern "C"

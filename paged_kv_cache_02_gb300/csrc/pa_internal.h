@@ -1,0 +1,88 @@
+// pa_internal.h -- host-side declarations shared by the library's translation units.
+#pragma once
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "../../include/pa.h"
+
+namespace pa {
+
+// One unit of attention work: a range of rows of one (sequence, KV head) pair
+// against a range of keys. Row rho of the pair is query token rho / g and query
+// head kv_head * g + rho % g, g = Hq / Hkv (query heads packed per KV head).
+struct Item {
+  int32_t seq;
+  int32_t kv_head;
+  int32_t row_begin;  // first packed row
+  int32_t row_count;  // rows in this item
+  int32_t kv_begin;   // first key (a multiple of the key tile)
+  int32_t kv_end;     // one past the last key any row of the item may see
+  int32_t part;       // first partial-result row of this item, -1 = write the output directly
+  int32_t q_row0;     // row of the sequence's first query in q / out
+};
+static_assert(sizeof(Item) == 32, "Item is 32 bytes");
+
+// Rows whose keys were split: merged by the combine kernel.
+struct SplitGroup {
+  int32_t seq;
+  int32_t kv_head;
+  int32_t row_begin;
+  int32_t row_count;
+  int32_t part_begin;  // chunk c, row r of the group is partial row part_begin + c * row_count + r
+  int32_t n_parts;     // key chunks
+  int32_t q_row0;
+  int32_t pad;
+};
+static_assert(sizeof(SplitGroup) == 32, "SplitGroup is 32 bytes");
+
+constexpr int kDecRows = 8;     // rows a CUDA-core item holds at most
+constexpr int kTcRows = 128;    // rows of a tensor-core item (one M tile)
+constexpr int kKeyTile = 64;    // keys per pipeline stage of the decode kernel
+constexpr int kChunkAlign = 64;   // split-KV chunk boundaries are multiples of this
+
+// Common launch arguments of the attention kernels.
+struct AttnArgs {
+  const uint16_t* q;          // bf16 [total_q, Hq, D]
+  void* out;                  // fp32 or bf16 [total_q, Hq, D]
+  int32_t out_bf16;
+  const int32_t* block_table;
+  const int32_t* context_lens;
+  const int32_t* query_lens;
+  int32_t max_blocks;
+  int32_t num_blocks;
+  int32_t block_size;
+  int32_t Hq, Hkv, g;
+  float scale_log2;           // scale * log2(e)
+  float* part_acc;            // [n_partial_rows, D]: unnormalised sum of p * v
+  float* part_ml;             // [n_partial_rows, 2]: running max (log2 domain) and sum of p
+  int* err;                   // device error word
+};
+
+// Device address of the error word of the current device (set up once per device).
+int* device_error_word();
+
+// Builds a 3-D tiled tensor map over a pool viewed as [num_blocks * B][Hkv][D] bf16.
+// box = (box_d, 1, box_t); swizzle128 selects the 128-byte swizzle.
+pa_status make_pool_map(CUtensorMap* map, const void* pool, int64_t num_blocks, int block_size,
+                        int Hkv, int D, int box_d, int box_t, bool swizzle128);
+
+// Launchers (return cudaGetLastError of the launch).
+cudaError_t launch_slot_mapping(const int32_t* bt, int32_t num_seqs, int32_t max_blocks,
+                                int32_t block_size, int32_t num_blocks, const int32_t* seq_ids,
+                                const int32_t* positions, int64_t n, int64_t* slots, int* err,
+                                cudaStream_t s);
+cudaError_t launch_write_kv(const void* k_new, const void* v_new, const int64_t* slots,
+                            int64_t n_new, void* k_pool, void* v_pool, int64_t n_slots,
+                            int64_t row_bytes, int* err, cudaStream_t s);
+cudaError_t launch_copy_blocks(void* k_pool, void* v_pool, const int32_t* src, const int32_t* dst,
+                               int32_t n_pairs, int32_t num_blocks, int64_t block_bytes, int* err,
+                               cudaStream_t s);
+cudaError_t launch_decode(const AttnArgs& a, const CUtensorMap& kmap, const CUtensorMap& vmap,
+                          const Item* items, int32_t n_items, int D, int rows_max, int box_t,
+                          int grid, cudaStream_t s);
+cudaError_t launch_combine(const AttnArgs& a, const SplitGroup* groups, int32_t n_groups, int D,
+                           cudaStream_t s);
+int decode_smem_bytes(int D, int rows_max);
+
+}  // namespace pa

@@ -1,0 +1,154 @@
+"""CPU-side checks of the C-ABI library: it builds, loads, exports every symbol the
+header declares, and its host logic (argument checks, the plan) behaves. No kernel runs."""
+import ctypes as C
+import os
+import re
+
+import numpy as np
+import pytest
+
+import workloads
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def pa():
+    from paged_kv_cache_02_gb300 import _build
+    _build.build()
+    import paged_kv_cache_02_gb300 as pa
+    return pa
+
+
+def declared_entry_points():
+    names = []
+    for h in sorted(os.listdir(os.path.join(ROOT, "include"))):
+        if h.endswith(".h"):
+            src = open(os.path.join(ROOT, "include", h)).read()
+            src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+            names += re.findall(r"^\s*(?:const\s+)?[A-Za-z_][A-Za-z0-9_]*\s*\*?\s*(pa_[a-z0-9_]+)\s*\(",
+                                src, flags=re.M)
+    return sorted(set(names))
+
+
+def test_header_declares_the_boundary():
+    names = declared_entry_points()
+    for must in ("pa_write_kv", "pa_copy_blocks", "pa_attention", "pa_plan_create",
+                 "pa_plan_destroy", "pa_status_string", "pa_slot_mapping"):
+        assert must in names, names
+
+
+def test_library_exports_every_declared_symbol(pa):
+    lib = pa.library()
+    for name in declared_entry_points():
+        assert hasattr(lib, name), f"libpa.so does not export {name}"
+
+
+def test_status_strings_and_version(pa):
+    lib = pa.library()
+    for s in range(7):
+        assert lib.pa_status_string(s)
+    assert lib.pa_status_string(99) == b"unknown status"
+    assert "sm_103a" in pa.version()
+
+
+def plan(pa, L, q, Hq=4, Hkv=4, D=64, B=16, **kw):
+    mb = max(1, max((-(-l // B) for l in L), default=1))
+    return pa.Plan(L, q, Hq, Hkv, D, B, mb, **kw)
+
+
+@pytest.mark.parametrize("bad,status", [
+    (dict(L=[5], q=[6]), 3),                      # query longer than context
+    (dict(L=[5], q=[-1]), 3),
+    (dict(Hq=6, Hkv=4), 2),                        # heads not a multiple
+    (dict(D=96), 4),                               # head dim not built
+    (dict(B=12), 4),                               # block size not a power of two
+])
+def test_plan_rejects(pa, bad, status):
+    args = dict(L=[5, 9], q=[1, 2], Hq=4, Hkv=4, D=64, B=16)
+    args.update(bad)
+    L, q = args.pop("L"), args.pop("q")
+    if len(L) != len(q):
+        L = L[:len(q)]
+    with pytest.raises(pa.PagedAttentionError) as e:
+        plan(pa, L, q, **args)
+    assert e.value.status == status
+
+
+def test_plan_rejects_short_table(pa):
+    with pytest.raises(pa.PagedAttentionError) as e:
+        pa.Plan([40], [1], 4, 4, 64, 16, 2)
+    assert e.value.status == 3
+
+
+def _coverage(items, L, q, g, Hkv):
+    """Every (seq, kv head, row) covered by exactly one row range; for each the key
+    chunks partition [0, last visible key] without overlap."""
+    seen = {}
+    for path, s, kvh, rb, rc, kb, ke, part, q0 in items:
+        for r in range(rb, rb + rc):
+            seen.setdefault((s, kvh, r), []).append((kb, ke, part))
+    for s in range(len(L)):
+        for kvh in range(Hkv):
+            for r in range(q[s] * g):
+                assert (s, kvh, r) in seen, (s, kvh, r)
+                ranges = sorted(seen[(s, kvh, r)])
+                assert ranges[0][0] == 0
+                for (a0, a1, _), (b0, b1, _) in zip(ranges, ranges[1:]):
+                    assert a1 == b0
+                t = r // g
+                assert ranges[-1][1] >= L[s] - q[s] + t + 1
+                assert ranges[-1][1] <= L[s]
+                if len(ranges) == 1:
+                    assert ranges[0][2] == -1
+                else:
+                    assert all(p >= 0 for _, _, p in ranges)
+    assert len(seen) == sum(qq * g * Hkv for qq in q)
+
+
+@pytest.mark.parametrize("chunk", [0, 128, 256])
+def test_plan_covers_every_row_and_key(pa, chunk):
+    L = [7, 33, 64, 100, 0, 513, 2048]
+    q = [1, 1, 7, 17, 0, 40, 1]
+    for Hq, Hkv in ((4, 4), (8, 2), (16, 1)):
+        p = plan(pa, L, q, Hq=Hq, Hkv=Hkv, max_chunk_tokens=chunk)
+        items = p.items()
+        _coverage(items, L, q, Hq // Hkv, Hkv)
+        st = p.stats()
+        assert st["total_q"] == sum(q) and st["kv_tokens"] == sum(L)
+        assert st["n_dec_items"] + st["n_tc_items"] == len(items)
+        assert st["workspace_bytes"] >= 256
+        if chunk:
+            assert st["chunk_tokens"] == chunk
+            assert all(ke - kb <= chunk for *_, kb, ke, _, _ in items)
+        # partial rows are distinct
+        parts = [(pt + i) for (_, _, _, _, rc, _, _, pt, _) in items if pt >= 0 for i in range(rc)]
+        assert len(parts) == len(set(parts)) == st["n_partials"]
+        # q_row0 = prefix sum of query lens
+        pref = np.concatenate([[0], np.cumsum(q)])
+        for it in items:
+            assert it[8] == pref[it[1]]
+
+
+def test_plan_orders_longest_first(pa):
+    L = list(range(100, 2100, 50))
+    p = plan(pa, L, [1] * len(L))
+    lens = [ke - kb for *_, kb, ke, _, _ in p.items()]
+    assert lens == sorted(lens, reverse=True)
+
+
+def test_plan_auto_split_fills_the_gpu(pa):
+    # one very long decode: 8 KV heads x 100k keys must be split into many chunks
+    p = pa.Plan([100_000], [1], 8, 8, 128, 16, 100_000 // 16 + 1, num_sms=152)
+    st = p.stats()
+    assert st["n_split_groups"] == 8
+    assert st["n_dec_items"] >= 152
+    # a large decode batch needs no split
+    L = [1000 + 3 * i for i in range(256)]
+    p2 = pa.Plan(L, [1] * 256, 40, 40, 128, 16, 200, num_sms=152)
+    assert p2.stats()["n_split_groups"] == 0
+
+
+def test_empty_batch(pa):
+    p = pa.Plan([0, 0], [0, 0], 4, 4, 64, 16, 1)
+    assert p.stats()["total_q"] == 0 and len(p.items()) == 0

@@ -1,0 +1,202 @@
+"""GPU parity of the hot path (through the C ABI) against the fp64 oracle.
+
+Writes, copies and slot mappings must be bit-exact; attention must be within
+max abs 5e-3 and mean abs 5e-4 of the oracle (bf16 inputs, fp32 accumulation).
+"""
+import numpy as np
+import pytest
+import torch
+
+import workloads
+from tests import gpu_util as gu
+from tests.oracle_checks import f64, u16
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def pa():
+    assert torch.cuda.is_available(), "GPU tests need a CUDA device"
+    return gu.lib()
+
+
+def full_check(pa, w, **plan_kw):
+    got = gu.gpu_step(pa, w, **plan_kw)
+    ref = gu.oracle_step(w)
+    assert got["err"] == 0, f"device error {pa.DEVERR.get(got['err'])}"
+    assert np.array_equal(got["slots"], ref["slots"]), "slot mapping differs"
+    assert gu.pools_equal(got["k_pool"], ref["k_pool"]), "K pool differs after write/copy"
+    assert gu.pools_equal(got["v_pool"], ref["v_pool"]), "V pool differs after write/copy"
+    want = gu.oracle_rows(w, ref)
+    out = got["out"].float().cpu().numpy()
+    return gu.assert_attention_close(out, want, w.name), got, want
+
+
+def test_config1_tiny_mixed(pa):
+    full_check(pa, workloads.make(1))
+
+
+@pytest.mark.parametrize("chunk", [64, 128])
+def test_config1_forced_split(pa, chunk):
+    w = workloads.make(1) if chunk == 64 else workloads.make_custom(
+        [7, 130, 300, 1000], [1, 20, 3, 1], Hq=8, Hkv=2, D=128, block_size=16, seed=chunk)
+    (_, _), got, want = full_check(pa, w, max_chunk_tokens=chunk)
+    assert got["plan"].stats()["n_split_groups"] > 0
+    base = gu.gpu_step(pa, w)["out"]
+    assert torch.allclose(got["out"], base, atol=2e-5, rtol=0)
+
+
+CASES = []
+for B in (8, 16, 32):
+    for D in (64, 128):
+        for Hq, Hkv in ((4, 4), (8, 2), (8, 1)):
+            CASES.append((B, D, Hq, Hkv))
+
+
+@pytest.mark.parametrize("B,D,Hq,Hkv", CASES)
+def test_ragged_fuzz(pa, B, D, Hq, Hkv):
+    rng = np.random.default_rng(B * 1000 + D * 10 + Hq + Hkv)
+    n = 7
+    L = rng.integers(0, 300, size=n)
+    L[0] = 0
+    L[1] = 1
+    q = np.array([rng.integers(0, min(l, 40) + 1) for l in L])
+    q[2] = min(L[2], 1)
+    w = workloads.make_custom(L, q, Hq=Hq, Hkv=Hkv, D=D, block_size=B, seed=int(rng.integers(1e6)))
+    full_check(pa, w)
+    full_check(pa, w, max_chunk_tokens=64)
+
+
+@pytest.mark.parametrize("B", [1, 4, 64, 128, 256])
+def test_block_size_extremes(pa, B):
+    w = workloads.make_custom([3, 200, 517, 64], [3, 1, 9, 64], Hq=8, Hkv=2, D=128, block_size=B,
+                              seed=B)
+    full_check(pa, w)
+
+
+def test_long_context_split(pa):
+    w = workloads.make_custom([40000, 1], [1, 1], Hq=8, Hkv=8, D=128, block_size=16, seed=77)
+    got = gu.gpu_step(pa, w)
+    assert got["plan"].stats()["n_split_groups"] > 0
+    ref = gu.oracle_step(w)
+    gu.assert_attention_close(got["out"].cpu().numpy(), gu.oracle_rows(w, ref), "40k context")
+
+
+def test_unused_slots_hold_nan(pa):
+    """Slots past each context (tail of the last block, unused blocks) hold NaN: no effect."""
+    w = workloads.make_custom([9, 20, 3, 130], [2, 3, 3, 1], Hq=4, Hkv=2, D=128, block_size=16,
+                              seed=5)
+    used = np.zeros((w.num_blocks, w.block_size), bool)
+    for s in range(w.num_seqs):
+        for t in range(int(w.context_lens[s])):
+            used[w.block_table[s, t // 16], t % 16] = True
+    nan = torch.tensor(float("nan"), dtype=torch.bfloat16)
+    mask = torch.from_numpy(~used)
+    w.k_pool[mask] = nan
+    w.v_pool[mask] = nan
+    (_, _), got, _ = full_check(pa, w)
+    assert torch.isfinite(got["out"]).all()
+
+
+def test_permuted_physical_ids_bit_identical(pa):
+    w = workloads.make_custom([77, 300, 5], [5, 1, 5], Hq=8, Hkv=2, D=128, block_size=16, seed=8)
+    a = gu.gpu_step(pa, w)["out"]
+    perm = np.random.default_rng(1).permutation(w.num_blocks)
+    inv = torch.from_numpy(np.argsort(perm))
+    w.k_pool = w.k_pool[inv].contiguous()
+    w.v_pool = w.v_pool[inv].contiguous()
+    w.block_table = np.where(w.block_table >= 0, perm[np.maximum(w.block_table, 0)], -1).astype(np.int32)
+    b = gu.gpu_step(pa, w)["out"]
+    assert torch.equal(a, b)
+
+
+def test_subrequests_match_single_request(pa):
+    """Pensieve Fig. 8: sub-requests A (leading tokens on themselves) and B (new prompt on
+    the whole context) reproduce the matching rows of one full causal request."""
+    L, r, qn = 300, 64, 45
+    full = workloads.make_custom([L], [L], Hq=8, Hkv=8, D=128, block_size=32, seed=12,
+                                 write_new=False)
+    one = gu.gpu_step(pa, full)["out"]
+    two_w = workloads.make_custom([r, L], [r, qn], Hq=8, Hkv=8, D=128, block_size=32, seed=12,
+                                  write_new=False)
+    two_w.block_table = np.concatenate([full.block_table, full.block_table])
+    two_w.k_pool, two_w.v_pool, two_w.num_blocks = full.k_pool, full.v_pool, full.num_blocks
+    two_w.q = torch.cat([full.q[:r], full.q[L - qn:]])
+    two = gu.gpu_step(pa, two_w)["out"]
+    assert torch.allclose(two[:r], one[:r], atol=1e-5, rtol=0)
+    assert torch.allclose(two[r:], one[L - qn:], atol=1e-5, rtol=0)
+
+
+def test_bf16_output(pa):
+    w = workloads.make(1)
+    got = gu.gpu_step(pa, w, out_dtype=torch.bfloat16)
+    want = gu.oracle_rows(w, gu.oracle_step(w))
+    out = got["out"].float().cpu().numpy()
+    # within one bf16 rounding of the oracle plus the attention tolerance
+    assert np.all(np.abs(out - want) <= np.abs(want) * 2.0 ** -8 + gu.ATOL_MAX)
+
+
+def test_empty_batch_and_zero_queries(pa):
+    w = workloads.make_custom([0, 5, 0], [0, 0, 0], Hq=4, Hkv=4, D=64, block_size=16, seed=1)
+    got = gu.gpu_step(pa, w)
+    assert got["out"].numel() == 0 and got["err"] == 0
+
+
+def test_bad_block_id_is_reported_not_faulted(pa):
+    """A block id past the pool is skipped by the kernel and reported in the error word."""
+    w = workloads.make_custom([40, 40], [1, 1], Hq=4, Hkv=4, D=64, block_size=16, seed=3,
+                              write_new=False)
+    good = w.block_table.copy()
+    w.block_table[1, 1] = w.num_blocks + 5
+    got = gu.gpu_step(pa, w)
+    assert got["err"] == 2
+    # the healthy sequence is still right
+    w.block_table = good
+    want = gu.oracle_rows(w, gu.oracle_step(w), rows=np.array([0]))
+    gu.assert_attention_close(got["out"].cpu().numpy()[:1], want, "healthy row")
+
+
+def test_write_kv_skip_and_range(pa):
+    dev = "cuda"
+    kp = torch.zeros(4, 2, 1, 8, dtype=torch.bfloat16, device=dev)
+    vp = kp.clone()
+    kn = torch.ones(3, 1, 8, dtype=torch.bfloat16, device=dev)
+    vn = kn * 2
+    slots = torch.tensor([-1, 5, 99], dtype=torch.int64, device=dev)
+    pa.pa_write_kv(kn, vn, slots, kp, vp)
+    assert pa.pa_get_device_error(reset=True) == 1
+    flat = kp.view(8, 8).float().cpu()
+    assert flat[5].eq(1).all() and flat.sum() == 8
+    assert vp.view(8, 8)[5].float().eq(2).all()
+
+
+def test_cow_config_copies_bit_exact(pa):
+    w = workloads.make("5cow", device="cuda")
+    got = gu.gpu_step(pa, w)
+    ref = gu.oracle_step(w)
+    assert got["err"] == 0
+    assert np.array_equal(got["slots"], ref["slots"])
+    assert gu.pools_equal(got["k_pool"], ref["k_pool"])
+    assert gu.pools_equal(got["v_pool"], ref["v_pool"])
+    rows = gu.sample_rows(w, 48, seed=5)
+    gu.assert_attention_close(got["out"].cpu().numpy()[rows], gu.oracle_rows(w, ref, rows), w.name)
+
+
+@pytest.mark.parametrize("config", [2, 3, 4, 5])
+def test_full_size_configs(pa, config):
+    """The bench's workloads at full size: bit-exact pools, sampled attention rows."""
+    w = workloads.make(config, device="cuda")
+    got = gu.gpu_step(pa, w)
+    assert got["err"] == 0
+    ref = gu.oracle_step(w)
+    assert np.array_equal(got["slots"], ref["slots"])
+    assert gu.pools_equal(got["k_pool"], ref["k_pool"])
+    assert gu.pools_equal(got["v_pool"], ref["v_pool"])
+    rows = gu.sample_rows(w, 64, seed=config)
+    for name, seqs in w.groups.items():
+        pref = np.concatenate([[0], np.cumsum(w.query_lens)])
+        extra = [int(pref[s]) for s in seqs[:4]] + [int(pref[s + 1] - 1) for s in seqs[-4:]]
+        rows = np.unique(np.concatenate([rows, np.array(extra, np.int64)]))
+    out = got["out"].cpu().numpy()[rows]
+    gu.assert_attention_close(out, gu.oracle_rows(w, ref, rows), w.name)
+    assert torch.isfinite(got["out"]).all()
