@@ -193,6 +193,39 @@ pa_status pa_attention(pa_plan_t plan, void* d_out, pa_dtype out_dtype, const vo
                        int32_t num_blocks, float scale, void* d_workspace,
                        size_t workspace_bytes, void* stream);
 
+/* ---------------------------------------------------------------- no-alloc variant
+ * The pages have no counterpart to this entry point; it exists for callers
+ * that cannot allocate device memory for a workspace. A serving engine
+ * typically reserves nearly all HBM for its KV-cache pool at start-up, so a
+ * later cudaMalloc for scratch can fail, and cudaMalloc also synchronizes the
+ * device, which stalls a pipelined decode loop; plain C callers without an
+ * allocator of their own are in the same position.
+ *
+ * pa_attention_static computes exactly what pa_attention computes, but its
+ * scratch (the plan's work-item tables and split-KV partial results) lives in
+ * a fixed array of PA_STATIC_WORKSPACE_BYTES inside the library's device
+ * image, which every GPU that loads the library keeps until the process exits.
+ * It allocates nothing and calls no allocating routine. The caller still owns
+ * q, out, the pools, block_table and the length arrays.
+ *   - A plan whose workspace_bytes exceeds PA_STATIC_WORKSPACE_BYTES is
+ *     rejected with PA_ERR_SHAPE before anything is enqueued; use
+ *     pa_attention with a caller-provided workspace for such batches.
+ *   - The first call on each device looks up the array's device address
+ *     (cudaGetSymbolAddress) with that device current and caches it; make
+ *     that first call before any stream capture.
+ *   - All calls on a device share the one array and it keeps the last call's
+ *     contents (nothing in it needs to start at zero: every call writes the
+ *     tables and partials it reads). Calls that overlap on the GPU -- on
+ *     different streams, or from different threads -- race on it; serialize
+ *     them on one stream. */
+#define PA_STATIC_WORKSPACE_BYTES (8u << 20)
+
+pa_status pa_attention_static(pa_plan_t plan, void* d_out, pa_dtype out_dtype, const void* d_q,
+                              const void* d_k_pool, const void* d_v_pool,
+                              const int32_t* d_block_table, const int32_t* d_context_lens,
+                              const int32_t* d_query_lens, int32_t num_blocks, float scale,
+                              void* stream);
+
 #ifdef __cplusplus
 }
 #endif

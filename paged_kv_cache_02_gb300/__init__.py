@@ -4,10 +4,11 @@ The computation lives in ``libpa.so`` (hand-written CUDA kernels behind the C
 ABI of ``include/pa.h``); this package is its thin Python binding. See
 ``_binding`` for the functions, which carry the C entry points' names.
 """
-from ._binding import (DEVERR, LIB_PATH, PagedAttentionError, Plan, library, pa_attention,
-                       pa_copy_blocks, pa_get_device_error, pa_plan_create, pa_slot_mapping,
-                       pa_write_kv, version)
+from ._binding import (DEVERR, LIB_PATH, STATIC_WORKSPACE_BYTES, PagedAttentionError, Plan,
+                       library, pa_attention, pa_attention_static, pa_copy_blocks,
+                       pa_get_device_error, pa_plan_create, pa_slot_mapping, pa_write_kv, version)
 
-__all__ = ["DEVERR", "LIB_PATH", "PagedAttentionError", "Plan", "library", "pa_attention",
+__all__ = ["DEVERR", "LIB_PATH", "STATIC_WORKSPACE_BYTES", "PagedAttentionError", "Plan",
+           "library", "pa_attention", "pa_attention_static",
            "pa_copy_blocks", "pa_get_device_error", "pa_plan_create", "pa_slot_mapping",
            "pa_write_kv", "version"]

@@ -64,9 +64,11 @@ def _lib() -> C.CDLL:
         lib.pa_plan_export.argtypes = [_P, _P, _I32, C.POINTER(C.c_int32)]
         lib.pa_attention.argtypes = [_P, _P, C.c_int, _P, _P, _P, _P, _P, _P, _I32, C.c_float, _P,
                                      C.c_size_t, _P]
+        lib.pa_attention_static.argtypes = [_P, _P, C.c_int, _P, _P, _P, _P, _P, _P, _I32,
+                                            C.c_float, _P]
         for f in ("pa_get_device_error", "pa_slot_mapping", "pa_write_kv", "pa_copy_blocks",
                   "pa_plan_create", "pa_plan_destroy", "pa_plan_get_stats", "pa_plan_export",
-                  "pa_attention"):
+                  "pa_attention", "pa_attention_static"):
             getattr(lib, f).restype = C.c_int
         _LIB = lib
     return _LIB
@@ -245,4 +247,41 @@ def pa_attention(plan: Plan, q: torch.Tensor, k_pool: torch.Tensor, v_pool: torc
                                _dev(query_lens, torch.int32, "query_lens", 1), nb, float(scale),
                                workspace.data_ptr(), workspace.numel(), _stream(q)),
            "pa_attention")
+    return out
+
+
+STATIC_WORKSPACE_BYTES = 8 << 20   # PA_STATIC_WORKSPACE_BYTES in include/pa.h
+
+
+def pa_attention_static(plan: Plan, q: torch.Tensor, k_pool: torch.Tensor, v_pool: torch.Tensor,
+                        block_table: torch.Tensor, context_lens: torch.Tensor,
+                        query_lens: torch.Tensor, out: torch.Tensor | None = None,
+                        out_dtype=torch.float32, scale: float = 0.0) -> torch.Tensor:
+    """pa_attention without a caller workspace: the library's fixed device scratch array
+    (PA_STATIC_WORKSPACE_BYTES) holds the plan tables and split partials, so nothing is
+    allocated beyond ``out`` (and only when ``out`` is not given). For callers that cannot
+    allocate scratch; calls that overlap on the GPU share that array and race."""
+    nb, B, Hkv, D = k_pool.shape
+    if (Hkv, D, B) != (plan.Hkv, plan.D, plan.block_size):
+        raise ValueError("pool shape does not match the plan")
+    if q.dim() != 3 or q.shape[1:] != (plan.Hq, D) or q.shape[0] != plan.total_q:
+        raise ValueError("q must be [total_q, Hq, D] as planned")
+    if block_table.dim() != 2 or block_table.shape[1] != plan.max_blocks_per_seq:
+        raise ValueError("block_table must be [num_seqs, max_blocks_per_seq] as planned")
+    if out is None:
+        out = torch.empty(q.shape, dtype=out_dtype, device=q.device)
+    dt = {torch.float32: PA_F32, torch.bfloat16: PA_BF16}.get(out.dtype)
+    if dt is None:
+        raise TypeError("out must be float32 or bfloat16")
+    if out.shape != q.shape:
+        raise ValueError("out must be shaped like q")
+    _check(_lib().pa_attention_static(plan._h, _dev(out, out.dtype, "out", 3), dt,
+                                      _dev(q, torch.bfloat16, "q", 3),
+                                      _dev(k_pool, torch.bfloat16, "k_pool", 4),
+                                      _dev(v_pool, torch.bfloat16, "v_pool", 4),
+                                      _dev(block_table, torch.int32, "block_table", 2),
+                                      _dev(context_lens, torch.int32, "context_lens", 1),
+                                      _dev(query_lens, torch.int32, "query_lens", 1), nb,
+                                      float(scale), _stream(q)),
+           "pa_attention_static")
     return out

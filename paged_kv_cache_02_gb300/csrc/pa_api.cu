@@ -449,3 +449,46 @@ pa_status pa_attention(pa_plan_t p, void* d_out, pa_dtype out_dtype, const void*
 }
 
 }  // extern "C"
+
+// ====================================================================== no-alloc variant
+// Scratch for pa_attention_static: a fixed device array instead of a caller
+// workspace, for callers that cannot allocate device memory (see pa.h). Its
+// name is only a host-side stand-in; kernels get the device address that
+// cudaGetSymbolAddress returns for the current device.
+static __device__ __align__(256) uint8_t g_static_workspace[PA_STATIC_WORKSPACE_BYTES];
+
+namespace {
+// Device address of g_static_workspace on the current device, looked up on the
+// first call per device with that device current, then cached.
+pa_status static_workspace(void** out) {
+  static std::mutex mu;
+  static void* cache[64] = {nullptr};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return PA_ERR_CUDA;
+  std::lock_guard<std::mutex> lock(mu);
+  if (!cache[dev]) {
+    void* ptr = nullptr;
+    if (cudaGetSymbolAddress(&ptr, g_static_workspace) != cudaSuccess || !ptr)
+      return PA_ERR_CUDA;
+    cache[dev] = ptr;
+  }
+  *out = cache[dev];
+  return PA_OK;
+}
+}  // namespace
+
+extern "C" pa_status pa_attention_static(pa_plan_t plan, void* d_out, pa_dtype out_dtype,
+                                         const void* d_q, const void* d_k_pool,
+                                         const void* d_v_pool, const int32_t* d_block_table,
+                                         const int32_t* d_context_lens,
+                                         const int32_t* d_query_lens, int32_t num_blocks,
+                                         float scale, void* stream) {
+  if (!plan) return PA_ERR_INVALID_ARG;
+  if (plan->ws_bytes > (size_t)PA_STATIC_WORKSPACE_BYTES) return PA_ERR_SHAPE;
+  void* ws = nullptr;
+  const pa_status st = static_workspace(&ws);
+  if (st != PA_OK) return st;
+  return pa_attention(plan, d_out, out_dtype, d_q, d_k_pool, d_v_pool, d_block_table,
+                      d_context_lens, d_query_lens, num_blocks, scale, ws,
+                      (size_t)PA_STATIC_WORKSPACE_BYTES, stream);
+}
