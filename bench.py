@@ -426,6 +426,8 @@ def main():
     ap.add_argument("--config", default="2", help="workload: 1..5 or 5cow (default 2)")
     ap.add_argument("--cpu-budget", type=float, default=12.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--max-seqs", type=int, default=None,
+                    help="keep only the first N sequences (profiler captures of config 2)")
     args = ap.parse_args()
     args.warmup = max(3, args.warmup)
     args.config_key = f"cfg{args.config}"
@@ -443,7 +445,7 @@ def main():
 
     import torch
     torch.cuda.set_device(local)
-    w = workloads.make(cfg, device=f"cuda:{local}")
+    w = workloads.make(cfg, device=f"cuda:{local}", max_seqs=args.max_seqs)
     run_gpu(args, w, cfg_dict(w, cfg), rank, local, world)
     if world > 1:
         import torch.distributed as dist

@@ -10,17 +10,18 @@
 // (Pensieve summary, multi-token attention with the causal mask fused).
 //
 // How (GB300): one persistent CTA per SM walks a static round-robin list of
-// items. Warp 8 is a producer: for every 64-key stage it reads the block ids
-// and issues one 3-D TMA copy per (block piece, K or V) into a 4-stage
-// shared-memory ring guarded by mbarriers, running ahead across item
-// boundaries. Warps 0-7 consume: QK^T with each 16-byte K chunk loaded once and
-// reused for every row, scores reduced across the lanes of a token with a
-// reduce-scatter of shuffles, an online softmax in the log2 domain (one warp
-// per row), then P.V with the rescale folded in. Memory traffic is the
-// algorithmic minimum: every K/V byte of an item's key range is read once.
-// Long key ranges are split by the plan; split items write (m, l, acc) partials
-// that combine_kernel merges exactly (the normaliser of the softmax rewritten
-// as a sum over chunks).
+// items. Warp 8 is the producer: for every 64-key stage it issues one 3-D TMA
+// copy per (block piece, K or V) into a shared-memory ring guarded by
+// mbarriers, and on an item's first stage also the item's query rows (1-D bulk
+// copies). Block ids are read one stage ahead, so their latency hides behind
+// the ring. Warps 0-7 consume, each on its own 8-key slice of every stage and
+// with its own online softmax (an exact split of the keys inside the CTA): no
+// CTA-wide barrier is needed per stage. QK^T loads every 16-byte K chunk once
+// and uses it for all rows; the per-key sums are reduce-scattered with
+// shuffles; P.V folds the rescale in. At the end of an item the eight warp
+// partials (m, l, acc) are merged with the log-sum-exp rule. Every K/V byte of
+// an item's key range is read from HBM once. Long key ranges are split by the
+// plan; split items write (m, l, acc) partials that combine_kernel merges.
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
@@ -33,27 +34,38 @@
 namespace pa {
 namespace {
 
-constexpr int kStages = 4;
 constexpr int kCWarps = 8;                       // consumer warps
 constexpr int kCThreads = kCWarps * 32;          // consumer threads
 constexpr int kThreads = kCThreads + 32;         // + one producer warp
-constexpr int kSPad = kKeyTile + 4;              // score row stride (bank spread)
+constexpr int kSlice = kKeyTile / kCWarps;       // keys per warp per stage (8)
 constexpr int kConsumerBar = 1;                  // named barrier id of the consumers
+
+// Pipeline depth from the shared-memory budget (stages of 64 keys).
+template <int D, int RM>
+constexpr int dec_stages() {
+  return D == 64 ? 8 : (RM <= 2 ? 6 : 5);
+}
 
 template <int D, int RM>
 struct DecSmem {
-  uint16_t k[kStages][kKeyTile][D];
-  uint16_t v[kStages][kKeyTile][D];
-  float s[RM][kSPad];           // scores of the stage, log2 domain
-  float p[kKeyTile][RM];        // probabilities, key-major
-  float red[kCWarps][RM][D];    // end-of-item reduction of the P.V partial sums
-  float alpha[RM];
-  float m[RM];
-  float l[RM];
-  uint64_t full[kStages];
-  uint64_t empty[kStages];
-  int issued[kStages];    // TMA phases issued per stage (producer)
-  int consumed[kStages];  // phases the consumers have waited for
+  static constexpr int S = dec_stages<D, RM>();
+  uint16_t k[S][kKeyTile][D];
+  uint16_t v[S][kKeyTile][D];
+  uint16_t q[S][RM][D];              // the item's query rows, carried by its first stage
+  float s[kCWarps][RM][kSlice];      // per-warp scores of the slice (log2 domain)
+  float p[kCWarps][kSlice][RM];      // per-warp probabilities, key-major
+  float alpha[kCWarps][RM];          // per-warp rescale factors of the stage
+  float red[kCWarps][RM][D];         // end-of-item partial sums of the warps
+  float red_m[kCWarps][RM];
+  float red_l[kCWarps][RM];
+  float wgt[kCWarps][RM];            // merge weights 2^(m_w - m)
+  float inv_l[RM];
+  float m_fin[RM];
+  float l_fin[RM];
+  uint64_t full[S];
+  uint64_t empty[S];
+  int issued[S];    // copy phases issued per stage (producer)
+  int consumed[S];  // phases the consumers have waited for
   int abort_flag;
 };
 
@@ -61,7 +73,7 @@ __device__ __forceinline__ uint8_t* align1024(uint8_t* p) {
   return reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(p) + 1023) & ~uintptr_t(1023));
 }
 
-// Sum across the CH lanes of a token group, scattering rows: afterwards lane
+// Sum across the CH lanes of a key group, scattering rows: afterwards the lane
 // holds the full score of row `row` (RM <= CH).
 template <int N, int OFF, int RM>
 struct ReduceScatter {
@@ -86,31 +98,6 @@ struct ReduceScatter {
   }
 };
 
-__device__ __forceinline__ float warp_max(float x) {
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) x = fmaxf(x, __shfl_xor_sync(0xffffffffu, x, o));
-  return x;
-}
-__device__ __forceinline__ float warp_sum(float x) {
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) x += __shfl_xor_sync(0xffffffffu, x, o);
-  return x;
-}
-
-// All consumer threads agree on `ok` (AND) at a named barrier.
-__device__ __forceinline__ bool consumers_all(bool ok) {
-  uint32_t r;
-  asm volatile(
-      "{\n\t.reg .pred p, q;\n\t"
-      "setp.ne.u32 p, %1, 0;\n\t"
-      "bar.red.and.pred q, %2, %3, p;\n\t"
-      "selp.u32 %0, 1, 0, q;\n\t}"
-      : "=r"(r)
-      : "r"((uint32_t)ok), "n"(kConsumerBar), "n"(kCThreads)
-      : "memory");
-  return r != 0;
-}
-
 __device__ __forceinline__ void unpack8(const uint4& w, float (&f)[8]) {
   f[0] = bf16lo(w.x); f[1] = bf16hi(w.x);
   f[2] = bf16lo(w.y); f[3] = bf16hi(w.y);
@@ -118,24 +105,41 @@ __device__ __forceinline__ void unpack8(const uint4& w, float (&f)[8]) {
   f[6] = bf16lo(w.w); f[7] = bf16hi(w.w);
 }
 
+// 1-D bulk copy global -> shared, completing on `bar` (16-byte aligned, size % 16 == 0).
+__device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t bytes,
+                                          uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::
+          "r"(smem_addr(dst)),
+      "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes), "r"(smem_addr(bar))
+      : "memory");
+}
+
+// Block ids of the (at most two) pieces a producer lane loads for one stage:
+// -1 = no piece, -2 = block-table index out of range.
+struct Lookahead {
+  int phys0, phys1;
+};
+
 template <int D, int RM>
 __global__ void __launch_bounds__(kThreads, 1)
     decode_kernel(const __grid_constant__ AttnArgs a, const __grid_constant__ CUtensorMap kmap,
                   const __grid_constant__ CUtensorMap vmap, const Item* __restrict__ items,
                   int n_items, int box_t) {
+  using Smem = DecSmem<D, RM>;
+  constexpr int S = Smem::S;
   constexpr int CH = D / 8;                     // 16-byte chunks per key row
   constexpr int TPW = 32 / CH;                  // keys per warp step
-  constexpr int QK_STEPS = kKeyTile / (kCWarps * TPW);
-  constexpr int PV_STEPS = kKeyTile / (kCWarps * TPW);
+  constexpr int STEPS = kSlice / TPW;           // warp steps per slice
   static_assert(RM <= CH, "rows per item must not exceed the lanes of a key");
-  static_assert(QK_STEPS * kCWarps * TPW == kKeyTile, "tile split");
+  static_assert(STEPS * TPW == kSlice, "slice split");
 
   extern __shared__ uint8_t smem_raw[];
-  DecSmem<D, RM>& sm = *reinterpret_cast<DecSmem<D, RM>*>(align1024(smem_raw));
+  Smem& sm = *reinterpret_cast<Smem*>(align1024(smem_raw));
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
   if (threadIdx.x == 0) {
-    for (int s = 0; s < kStages; ++s) {
+    for (int s = 0; s < S; ++s) {
       mbar_init(&sm.full[s], 1);
       mbar_init(&sm.empty[s], kCWarps);
       sm.issued[s] = 0;
@@ -152,57 +156,103 @@ __global__ void __launch_bounds__(kThreads, 1)
       prefetch_tensormap(&kmap);
       prefetch_tensormap(&vmap);
     }
-    const int pieces = kKeyTile / box_t;
+    const int pieces = kKeyTile / box_t;           // <= 64
     const uint32_t piece_bytes = (uint32_t)box_t * D * 2u;
+    auto lookup = [&](const Item& item, int t0) -> Lookahead {
+      Lookahead r{-1, -1};
+      const int32_t* bt = a.block_table + (int64_t)item.seq * a.max_blocks;
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        const int pc = lane + 32 * h;
+        int ph = -1;
+        if (pc < pieces) {
+          const int j0 = t0 + pc * box_t;
+          if (j0 < item.kv_end) {
+            const int lb = j0 / a.block_size;
+            ph = (lb < a.max_blocks) ? __ldg(bt + lb) : -2;
+          }
+        }
+        if (h == 0) r.phys0 = ph; else r.phys1 = ph;
+      }
+      return r;
+    };
     int stage = 0;
     uint32_t phase = 0;
     bool ok = true;
-    for (int it = blockIdx.x; it < n_items && ok; it += gridDim.x) {
-      const Item item = items[it];
-      const int L = __ldg(a.context_lens + item.seq);
-      const int kv_end = min(item.kv_end, L);
-      const int32_t* bt = a.block_table + (int64_t)item.seq * a.max_blocks;
-      for (int t0 = item.kv_begin; t0 < kv_end; t0 += kKeyTile) {
+    int it = blockIdx.x;
+    if (it < n_items) {
+      Item cur = items[it];
+      Item nxt = cur;
+      if (it + (int)gridDim.x < n_items) nxt = items[it + gridDim.x];
+      int t0 = cur.kv_begin;
+      Lookahead la = lookup(cur, t0);
+      while (true) {
+        // position and block ids of the stage after this one (loads in flight meanwhile)
+        int nit = it, nt0 = t0 + kKeyTile;
+        bool next_is_new = false;
+        if (nt0 >= cur.kv_end) {
+          nit = it + gridDim.x;
+          nt0 = nxt.kv_begin;
+          next_is_new = true;
+        }
+        Lookahead nla{-1, -1};
+        if (nit < n_items) nla = lookup(next_is_new ? nxt : cur, nt0);
+
         ok = mbar_wait(&sm.empty[stage], phase ^ 1u, a.err);
         if (!ok || *(volatile int*)&sm.abort_flag) { ok = false; break; }
-        // pieces lane and lane + 32 of this stage (a stage has at most 64 pieces)
-        auto locate = [&](int pc, int& tok) -> bool {
-          if (pc >= pieces) return false;
+        int tok0 = 0, tok1 = 0;
+        auto valid_piece = [&](int ph, int pc, int& tok) -> bool {
+          if (ph == -1) return false;
+          if (ph == -2) { record_error(a.err, PA_DEVERR_TABLE_RANGE); return false; }
+          if (ph < 0 || ph >= a.num_blocks) { record_error(a.err, PA_DEVERR_BLOCK_RANGE); return false; }
           const int j0 = t0 + pc * box_t;
-          if (j0 >= kv_end) return false;
-          const int lb = j0 / a.block_size;
-          if (lb >= a.max_blocks) {
-            record_error(a.err, PA_DEVERR_TABLE_RANGE);
-            return false;
-          }
-          const int phys = __ldg(bt + lb);
-          if (phys < 0 || phys >= a.num_blocks) {
-            record_error(a.err, PA_DEVERR_BLOCK_RANGE);
-            return false;
-          }
-          tok = phys * a.block_size + (j0 - lb * a.block_size);
+          tok = ph * a.block_size + (j0 - (j0 / a.block_size) * a.block_size);
           return true;
         };
-        int tok0 = 0, tok1 = 0;
-        const bool v0 = locate(lane, tok0);
-        const bool v1 = locate(lane + 32, tok1);
-        const uint32_t n_pieces = __popc(__ballot_sync(0xffffffffu, v0)) +
-                                  __popc(__ballot_sync(0xffffffffu, v1));
-        // one arrive carrying every byte of the stage, before any copy is issued
-        if (lane == 0) mbar_arrive_expect_tx(&sm.full[stage], n_pieces * piece_bytes * 2u);
+        const bool v0 = valid_piece(la.phys0, lane, tok0);
+        const bool v1 = valid_piece(la.phys1, lane + 32, tok1);
+        uint32_t bytes = (__popc(__ballot_sync(0xffffffffu, v0)) +
+                          __popc(__ballot_sync(0xffffffffu, v1))) * piece_bytes * 2u;
+        // the item's query rows ride on its first stage: one copy per query token
+        const bool first = (t0 == cur.kv_begin);
+        int qt_first = 0, n_qtok = 0;
+        if (first) {
+          qt_first = cur.row_begin / a.g;
+          n_qtok = (cur.row_begin + cur.row_count - 1) / a.g - qt_first + 1;
+          bytes += (uint32_t)cur.row_count * D * 2u;
+        }
+        if (lane == 0) mbar_arrive_expect_tx(&sm.full[stage], bytes);
         __syncwarp();
         if (v0) {
-          tma_load_3d(&sm.k[stage][lane * box_t][0], &kmap, &sm.full[stage], 0, item.kv_head, tok0);
-          tma_load_3d(&sm.v[stage][lane * box_t][0], &vmap, &sm.full[stage], 0, item.kv_head, tok0);
+          tma_load_3d(&sm.k[stage][lane * box_t][0], &kmap, &sm.full[stage], 0, cur.kv_head, tok0);
+          tma_load_3d(&sm.v[stage][lane * box_t][0], &vmap, &sm.full[stage], 0, cur.kv_head, tok0);
         }
         if (v1) {
           tma_load_3d(&sm.k[stage][(lane + 32) * box_t][0], &kmap, &sm.full[stage], 0,
-                      item.kv_head, tok1);
+                      cur.kv_head, tok1);
           tma_load_3d(&sm.v[stage][(lane + 32) * box_t][0], &vmap, &sm.full[stage], 0,
-                      item.kv_head, tok1);
+                      cur.kv_head, tok1);
+        }
+        if (first && lane < n_qtok) {
+          const int t = qt_first + lane;
+          const int h_lo = max(cur.row_begin, t * a.g) - t * a.g;
+          const int h_hi = min(cur.row_begin + cur.row_count, (t + 1) * a.g) - t * a.g;
+          const uint16_t* src =
+              a.q + ((int64_t)(cur.q_row0 + t) * a.Hq + (int64_t)cur.kv_head * a.g + h_lo) * D;
+          bulk_load(&sm.q[stage][t * a.g + h_lo - cur.row_begin][0], src,
+                    (uint32_t)(h_hi - h_lo) * D * 2u, &sm.full[stage]);
         }
         if (lane == 0) sm.issued[stage] += 1;
-        if (++stage == kStages) { stage = 0; phase ^= 1u; }
+        if (++stage == S) { stage = 0; phase ^= 1u; }
+        // advance to the stage looked up above
+        if (next_is_new) {
+          it = nit;
+          if (it >= n_items) break;
+          cur = nxt;
+          if (it + (int)gridDim.x < n_items) nxt = items[it + gridDim.x];
+        }
+        t0 = nt0;
+        la = nla;
       }
     }
     if (!ok) sm.abort_flag = 1;
@@ -210,42 +260,42 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ------------------------------------------------------------ consumers
     const int c = lane % CH;   // 16-byte chunk of the key row this lane owns
     const int tl = lane / CH;  // key within the warp step
+    // softmax lanes: (row, key) pairs of the warp's slice
+    constexpr int PPL = (RM * kSlice + 31) / 32;   // pairs per lane (1 or 2)
+    constexpr int LPR = kSlice / PPL;              // lanes per row
+    const int sm_row = lane / LPR;                 // row this lane runs the softmax for
+    const int sm_key = (lane % LPR) * PPL;         // first slice key of its pair(s)
     int stage = 0;
     uint32_t phase = 0;
     bool alive = true;
-    for (int it = blockIdx.x; it < n_items && alive; it += gridDim.x) {
-      const Item item = items[it];
-      const int L = __ldg(a.context_lens + item.seq);
-      const int ql = __ldg(a.query_lens + item.seq);
-      const int kv_end = min(item.kv_end, L);
+    const int G = gridDim.x;
+    // items and their sequences' lengths are fetched one item ahead
+    Item item{}, nitem{};
+    int L = 0, ql = 0;
+    if ((int)blockIdx.x < n_items) {
+      item = items[blockIdx.x];
+      L = __ldg(a.context_lens + item.seq);
+      ql = __ldg(a.query_lens + item.seq);
+    }
+    if ((int)blockIdx.x + G < n_items) nitem = items[blockIdx.x + G];
+    for (int it = blockIdx.x; it < n_items && alive; it += G) {
+      Item nn{};
+      int nL = 0, nql = 0;
+      if (it + 2 * G < n_items) nn = items[it + 2 * G];
+      if (it + G < n_items) {
+        nL = __ldg(a.context_lens + nitem.seq);
+        nql = __ldg(a.query_lens + nitem.seq);
+      }
+      const int kv_end = item.kv_end;
       const int nrows = item.row_count;
-      if (threadIdx.x == 0 && item.row_begin + nrows > ql * a.g)
-        record_error(a.err, PA_DEVERR_LENS);
-
-      // this lane's chunk of every row's query, pre-scaled into the log2 domain
+      int lim = -1;   // last key the softmax row of this lane may see
+      if (sm_row < RM && sm_row < nrows) {
+        const int t = (item.row_begin + sm_row) / a.g;
+        lim = min(kv_end - 1, L - ql + t);
+        if (warp == 0 && lane == 0 && (item.kv_end > L || item.row_begin + nrows > ql * a.g))
+          record_error(a.err, PA_DEVERR_LENS);
+      }
       float qv[RM][8];
-#pragma unroll
-      for (int r = 0; r < RM; ++r) {
-        if (r < nrows) {
-          const int rho = item.row_begin + r;
-          const int t = rho / a.g;
-          const int h = item.kv_head * a.g + (rho - t * a.g);
-          const uint4 w = __ldg(reinterpret_cast<const uint4*>(
-                                    a.q + ((int64_t)(item.q_row0 + t) * a.Hq + h) * D) + c);
-          unpack8(w, qv[r]);
-#pragma unroll
-          for (int e = 0; e < 8; ++e) qv[r][e] *= a.scale_log2;
-        } else {
-#pragma unroll
-          for (int e = 0; e < 8; ++e) qv[r][e] = 0.f;
-        }
-      }
-      // causal limit of the row this warp runs the softmax for
-      int my_lim = -1;
-      if (warp < RM && warp < nrows) {
-        const int t = (item.row_begin + warp) / a.g;
-        my_lim = min(kv_end - 1, L - ql + t);
-      }
       float m_run = -INFINITY, l_run = 0.f;
       float acc[RM][8];
 #pragma unroll
@@ -255,60 +305,92 @@ __global__ void __launch_bounds__(kThreads, 1)
 
       for (int t0 = item.kv_begin; t0 < kv_end; t0 += kKeyTile) {
         const bool got = mbar_wait(&sm.full[stage], phase, a.err);
-        // ---- S = Q K^T for the stage's 64 keys
-        const uint16_t* Ks = &sm.k[stage][0][0];
+        if (!got) { alive = false; break; }
+        if (warp == 0 && lane == 0) sm.consumed[stage] += 1;
+        if (t0 == item.kv_begin) {
+          // query rows of the item (arrived with this stage), pre-scaled to the log2 domain
 #pragma unroll
-        for (int i = 0; i < QK_STEPS; ++i) {
-          const int tok = warp * (kKeyTile / kCWarps) + i * TPW + tl;
+          for (int r = 0; r < RM; ++r) {
+            if (r < nrows) {
+              unpack8(*reinterpret_cast<const uint4*>(&sm.q[stage][r][c * 8]), qv[r]);
+#pragma unroll
+              for (int e = 0; e < 8; ++e) qv[r][e] *= a.scale_log2;
+            } else {
+#pragma unroll
+              for (int e = 0; e < 8; ++e) qv[r][e] = 0.f;
+            }
+          }
+        }
+        // ---- S = Q K^T on this warp's 8 keys
+        const uint16_t* Ks = &sm.k[stage][warp * kSlice][0];
+#pragma unroll
+        for (int i = 0; i < STEPS; ++i) {
+          const int key = i * TPW + tl;
           float kf[8];
-          unpack8(*reinterpret_cast<const uint4*>(Ks + tok * D + c * 8), kf);
+          unpack8(*reinterpret_cast<const uint4*>(Ks + key * D + c * 8), kf);
           float part[RM];
 #pragma unroll
           for (int r = 0; r < RM; ++r) {
-            float x = 0.f;
-#pragma unroll
-            for (int e = 0; e < 8; ++e) x = fmaf(qv[r][e], kf[e], x);
-            part[r] = x;
+            float x0 = qv[r][0] * kf[0], x1 = qv[r][1] * kf[1];
+            x0 = fmaf(qv[r][2], kf[2], x0); x1 = fmaf(qv[r][3], kf[3], x1);
+            x0 = fmaf(qv[r][4], kf[4], x0); x1 = fmaf(qv[r][5], kf[5], x1);
+            x0 = fmaf(qv[r][6], kf[6], x0); x1 = fmaf(qv[r][7], kf[7], x1);
+            part[r] = x0 + x1;
           }
           int row = 0;
           ReduceScatter<RM, CH / 2, RM>::run(part, lane, row);
-          if ((c & (CH / RM - 1)) == 0) sm.s[row][tok] = part[0];
+          if ((c & (CH / RM - 1)) == 0) sm.s[warp][row][key] = part[0];
         }
-        if (!consumers_all(got)) { alive = false; break; }
-        if (threadIdx.x == 0) sm.consumed[stage] += 1;
-        // ---- online softmax, one warp per row
-        if (warp < RM) {
-          const int j0 = t0 + lane, j1 = t0 + lane + 32;
-          const float s0 = (j0 <= my_lim) ? sm.s[warp][lane] : -INFINITY;
-          const float s1 = (j1 <= my_lim) ? sm.s[warp][lane + 32] : -INFINITY;
-          const float m_new = fmaxf(m_run, warp_max(fmaxf(s0, s1)));
+        __syncwarp();
+        // ---- online softmax of the warp's slice: lanes own (row, key) pairs
+        {
+          const int kbase = t0 + warp * kSlice + sm_key;
+          float sv[PPL], pv[PPL];
+          float mx = -INFINITY;
+#pragma unroll
+          for (int u = 0; u < PPL; ++u) {
+            const bool ok_key = (sm_row < RM) && (kbase + u <= lim);
+            sv[u] = ok_key ? sm.s[warp][sm_row][sm_key + u] : -INFINITY;
+            mx = fmaxf(mx, sv[u]);
+          }
+#pragma unroll
+          for (int o = LPR / 2; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+          const float m_new = fmaxf(m_run, mx);
           const float alpha = (m_run == -INFINITY) ? 0.f : fast_exp2(m_run - m_new);
-          const float p0 = (j0 <= my_lim) ? fast_exp2(s0 - m_new) : 0.f;
-          const float p1 = (j1 <= my_lim) ? fast_exp2(s1 - m_new) : 0.f;
-          l_run = l_run * alpha + warp_sum(p0 + p1);
+          float sum = 0.f;
+#pragma unroll
+          for (int u = 0; u < PPL; ++u) {
+            pv[u] = (sv[u] == -INFINITY) ? 0.f : fast_exp2(sv[u] - m_new);
+            sum += pv[u];
+          }
+#pragma unroll
+          for (int o = LPR / 2; o > 0; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
+          l_run = l_run * alpha + sum;
           m_run = m_new;
-          sm.p[lane][warp] = p0;
-          sm.p[lane + 32][warp] = p1;
-          if (lane == 0) sm.alpha[warp] = alpha;
+          if (sm_row < RM) {
+#pragma unroll
+            for (int u = 0; u < PPL; ++u) sm.p[warp][sm_key + u][sm_row] = pv[u];
+            if (lane % LPR == 0) sm.alpha[warp][sm_row] = alpha;
+          }
         }
-        named_bar_sync(kConsumerBar, kCThreads);
-        // ---- O = alpha * O + P V
+        __syncwarp();
+        // ---- acc = alpha * acc + P V on the warp's 8 keys
 #pragma unroll
         for (int r = 0; r < RM; ++r) {
-          const float al = sm.alpha[r];
+          const float al = sm.alpha[warp][r];
 #pragma unroll
           for (int e = 0; e < 8; ++e) acc[r][e] *= al;
         }
-        const uint16_t* Vs = &sm.v[stage][0][0];
+        const uint16_t* Vs = &sm.v[stage][warp * kSlice][0];
 #pragma unroll
-        for (int i = 0; i < PV_STEPS; ++i) {
-          const int tok = i * (kCWarps * TPW) + warp * TPW + tl;
-          if (t0 + tok < kv_end) {
+        for (int i = 0; i < STEPS; ++i) {
+          const int key = i * TPW + tl;
+          if (t0 + warp * kSlice + key < kv_end) {
             float vf[8];
-            unpack8(*reinterpret_cast<const uint4*>(Vs + tok * D + c * 8), vf);
+            unpack8(*reinterpret_cast<const uint4*>(Vs + key * D + c * 8), vf);
             float pr[RM];
 #pragma unroll
-            for (int r = 0; r < RM; ++r) pr[r] = sm.p[tok][r];
+            for (int r = 0; r < RM; ++r) pr[r] = sm.p[warp][key][r];
 #pragma unroll
             for (int r = 0; r < RM; ++r)
 #pragma unroll
@@ -317,11 +399,23 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         __syncwarp();
         if (lane == 0) mbar_arrive(&sm.empty[stage]);
-        if (++stage == kStages) { stage = 0; phase ^= 1u; }
+        if (++stage == S) { stage = 0; phase ^= 1u; }
       }
-      if (!alive) break;
+      // the whole consumer group agrees before touching the shared merge buffers
+      {
+        uint32_t all_ok;
+        asm volatile(
+            "{\n\t.reg .pred p, q;\n\t"
+            "setp.ne.u32 p, %1, 0;\n\t"
+            "bar.red.and.pred q, %2, %3, p;\n\t"
+            "selp.u32 %0, 1, 0, q;\n\t}"
+            : "=r"(all_ok)
+            : "r"((uint32_t)alive), "n"(kConsumerBar), "n"(kCThreads)
+            : "memory");
+        if (!all_ok) { alive = false; break; }
+      }
 
-      // ---- epilogue: sum the P.V partials of all keys of the warp, then of all warps
+      // ---- merge: keys of the warp (lanes of a chunk), then the eight warps
 #pragma unroll
       for (int off = CH; off < 32; off <<= 1)
 #pragma unroll
@@ -336,23 +430,40 @@ __global__ void __launch_bounds__(kThreads, 1)
           dst[1] = make_float4(acc[r][4], acc[r][5], acc[r][6], acc[r][7]);
         }
       }
-      if (warp < RM && lane == 0) {
-        sm.m[warp] = m_run;
-        sm.l[warp] = l_run;
+      if (sm_row < RM && lane % LPR == 0) {
+        sm.red_m[warp][sm_row] = m_run;
+        sm.red_l[warp][sm_row] = l_run;
+      }
+      named_bar_sync(kConsumerBar, kCThreads);
+      if (threadIdx.x < RM) {
+        const int r = threadIdx.x;
+        float m = -INFINITY;
+#pragma unroll
+        for (int w = 0; w < kCWarps; ++w) m = fmaxf(m, sm.red_m[w][r]);
+        float l = 0.f;
+#pragma unroll
+        for (int w = 0; w < kCWarps; ++w) {
+          const float mw = sm.red_m[w][r];
+          const float wg = (mw == -INFINITY) ? 0.f : fast_exp2(mw - m);
+          sm.wgt[w][r] = wg;
+          l += wg * sm.red_l[w][r];
+        }
+        sm.m_fin[r] = m;
+        sm.l_fin[r] = l;
+        sm.inv_l[r] = (l > 0.f) ? 1.f / l : 0.f;
       }
       named_bar_sync(kConsumerBar, kCThreads);
       for (int idx = threadIdx.x; idx < nrows * D; idx += kCThreads) {
         const int r = idx / D, d = idx - r * D;
         float o = 0.f;
 #pragma unroll
-        for (int w = 0; w < kCWarps; ++w) o += sm.red[w][r][d];
+        for (int w = 0; w < kCWarps; ++w) o = fmaf(sm.wgt[w][r], sm.red[w][r][d], o);
         if (item.part < 0) {
           const int rho = item.row_begin + r;
           const int t = rho / a.g;
           const int h = item.kv_head * a.g + (rho - t * a.g);
           const int64_t off = ((int64_t)(item.q_row0 + t) * a.Hq + h) * D + d;
-          const float l = sm.l[r];
-          o = (l > 0.f) ? o / l : 0.f;
+          o *= sm.inv_l[r];
           if (a.out_bf16)
             reinterpret_cast<__nv_bfloat16*>(a.out)[off] = __float2bfloat16_rn(o);
           else
@@ -361,12 +472,16 @@ __global__ void __launch_bounds__(kThreads, 1)
           const int64_t prow = (int64_t)item.part + r;
           a.part_acc[prow * D + d] = o;
           if (d == 0) {
-            a.part_ml[prow * 2 + 0] = sm.m[r];
-            a.part_ml[prow * 2 + 1] = sm.l[r];
+            a.part_ml[prow * 2 + 0] = sm.m_fin[r];
+            a.part_ml[prow * 2 + 1] = sm.l_fin[r];
           }
         }
       }
       named_bar_sync(kConsumerBar, kCThreads);
+      item = nitem;
+      L = nL;
+      ql = nql;
+      nitem = nn;
     }
     if (!alive && threadIdx.x == 0) sm.abort_flag = 1;
   }
@@ -374,7 +489,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   // After an abort, give copies still in flight a bounded time to land
   // before the CTA's shared memory is released.
   if (sm.abort_flag && threadIdx.x == 0) {
-    for (int s = 0; s < kStages; ++s) {
+    for (int s = 0; s < S; ++s) {
       if (sm.issued[s] > sm.consumed[s]) {
         const uint32_t parity = (uint32_t)(sm.issued[s] - 1) & 1u;
         const uint64_t t0 = global_timer_ns();

@@ -197,11 +197,13 @@ def _cfg1(device):
     return _finish(CONFIG_NAMES[1], seed, 4, 4, 64, B, nb, L, ql, bt, seqs, pos, device)
 
 
-def _cfg2(device):
+def _cfg2(device, max_seqs=None):
     seed = 1002
     g = torch.Generator().manual_seed(seed)
     N, B, H, D = 256, 16, 40, 128
     L = _randint(g, 128, 2048, N)
+    if max_seqs is not None:
+        N, L = min(N, max_seqs), L[:max_seqs]
     ql = np.ones(N, np.int64)
     need = [_cdiv(int(l), B) for l in L]
     nb = int(math.ceil(1.2 * sum(need)))
@@ -354,12 +356,16 @@ def _cfg5(device, cow: bool):
                    cow=(np.array(src, np.int32), np.array(dst, np.int32)))
 
 
-def make(config, device="cpu") -> Workload:
-    """Workload for config 1..5 or "5cow", values drawn on ``device``."""
+def make(config, device="cpu", max_seqs=None) -> Workload:
+    """Workload for config 1..5 or "5cow", values drawn on ``device``.
+
+    ``max_seqs`` keeps only the first sequences of the decode-only batch (config 2): the
+    same draw, smaller, for profiler captures that must stay small.
+    """
     if config in (1, "1"):
         return _cfg1(device)
     if config in (2, "2"):
-        return _cfg2(device)
+        return _cfg2(device, max_seqs)
     if config in (3, "3"):
         return _cfg3(device)
     if config in (4, "4"):
