@@ -233,8 +233,9 @@ pa_status pa_plan_create(const int32_t* h_context_lens, const int32_t* h_query_l
 
   int sms = o.num_sms > 0 ? o.num_sms : device_sms();
   if (sms <= 0) sms = 152;
-  // Tensor-core items are not built yet: every item runs on the CUDA-core path.
-  const bool tc_enabled = false;
+  // Tensor-core tiles: D = 128 and blocks of at least 8 tokens (one swizzle atom per piece).
+  const bool tc_enabled = (D == 128) && (block_size >= 8) && o.tc_min_rows >= 0;
+  const int tc_min_rows = o.tc_min_rows > 0 ? o.tc_min_rows : pa::kTcMinRowsDefault;
 
   // ---- units: (sequence, KV head, row tile)
   std::vector<Unit> units;
@@ -244,7 +245,7 @@ pa_status pa_plan_create(const int32_t* h_context_lens, const int32_t* h_query_l
     const int32_t L = h_context_lens[s], q = h_query_lens[s];
     if (q > 0) {
       const int64_t rows = (int64_t)q * g;
-      const bool tc = tc_enabled && o.tc_min_rows >= 0 && rows >= o.tc_min_rows && D == 128;
+      const bool tc = tc_enabled && rows >= tc_min_rows;
       const int rt = tc ? pa::kTcRows : pa::kDecRows;
       for (int32_t kvh = 0; kvh < Hkv; ++kvh) {
         for (int64_t rb = 0; rb < rows; rb += rt) {
@@ -438,6 +439,22 @@ pa_status pa_attention(pa_plan_t p, void* d_out, pa_dtype out_dtype, const void*
     const int grid = std::min(p->n_dec, sms);
     cudaError_t e = pa::launch_decode(a, kmap, vmap, reinterpret_cast<const Item*>(ws + p->off_dec),
                                       p->n_dec, p->D, p->dec_rows_max, box_t, grid, s);
+    if (e != cudaSuccess) return PA_ERR_CUDA;
+  }
+  if (p->n_tc > 0) {
+    const int box_t = std::min(p->block_size, 64);
+    CUtensorMap kmap, vmap;
+    pa_status st = pa::make_pool_map(&kmap, d_k_pool, num_blocks, p->block_size, p->Hkv, p->D,
+                                     64, box_t, true);
+    if (st != PA_OK) return st;
+    st = pa::make_pool_map(&vmap, d_v_pool, num_blocks, p->block_size, p->Hkv, p->D, 64, box_t,
+                           true);
+    if (st != PA_OK) return st;
+    int sms = device_sms();
+    if (sms <= 0) return PA_ERR_CUDA;
+    const int grid = std::min(p->n_tc, sms);
+    cudaError_t e = pa::launch_tc(a, kmap, vmap, reinterpret_cast<const Item*>(ws + p->off_tc),
+                                  p->n_tc, box_t, grid, s);
     if (e != cudaSuccess) return PA_ERR_CUDA;
   }
   if (p->n_groups > 0) {

@@ -84,5 +84,9 @@ cudaError_t launch_decode(const AttnArgs& a, const CUtensorMap& kmap, const CUte
 cudaError_t launch_combine(const AttnArgs& a, const SplitGroup* groups, int32_t n_groups, int D,
                            cudaStream_t s);
 int decode_smem_bytes(int D, int rows_max);
+cudaError_t launch_tc(const AttnArgs& a, const CUtensorMap& kmap, const CUtensorMap& vmap,
+                      const Item* items, int32_t n_items, int box_t, int grid, cudaStream_t s);
+int tc_smem_bytes();
+constexpr int kTcMinRowsDefault = 16;  // items with at least this many rows use tensor cores
 
 }  // namespace pa
