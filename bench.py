@@ -253,7 +253,9 @@ def run_gpu(args, w, cfg_name, rank, local, world):
     kp, vp = w.k_pool.to(dev), w.v_pool.to(dev)
     slots = torch.empty(len(w.new_seq), dtype=torch.int64, device=dev)
     out = torch.empty(q.shape, dtype=torch.float32, device=dev)
-    plan = pa.Plan(w.context_lens, w.query_lens, w.Hq, w.Hkv, w.D, w.block_size, w.max_blocks)
+    plan_kw = dict(tc_min_rows=args.tc_min_rows, max_chunk_tokens=args.max_chunk)
+    plan = pa.Plan(w.context_lens, w.query_lens, w.Hq, w.Hkv, w.D, w.block_size, w.max_blocks,
+                   **plan_kw)
     st = plan.stats()
     ws = plan.workspace(dev)
     n_pairs = len(w.cow_src)
@@ -359,7 +361,8 @@ def run_gpu(args, w, cfg_name, rank, local, world):
         for hb, db in zip((h_q, h_kn, h_vn, h_bt, h_cl, h_ql, h_sid, h_pos, h_src, h_dst), d_bufs):
             db.copy_(hb, non_blocking=True)
         dq, dkn, dvn, dbt, dcl, dql, dsid, dpos, dsrc, ddst = d_bufs
-        p2 = pa.Plan(w.context_lens, w.query_lens, w.Hq, w.Hkv, w.D, w.block_size, w.max_blocks)
+        p2 = pa.Plan(w.context_lens, w.query_lens, w.Hq, w.Hkv, w.D, w.block_size, w.max_blocks,
+                     **plan_kw)
         pa.pa_slot_mapping(dbt, w.num_blocks, w.block_size, dsid, dpos, out=slots)
         if n_pairs:
             pa.pa_copy_blocks(kp, vp, dsrc, ddst)
@@ -426,6 +429,12 @@ def main():
     ap.add_argument("--config", default="2", help="workload: 1..5 or 5cow (default 2)")
     ap.add_argument("--cpu-budget", type=float, default=12.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--tc-min-rows", type=int, default=0,
+                    help="plan option: rows from which items use the tensor cores (0 = default)")
+    ap.add_argument("--max-chunk", type=int, default=0,
+                    help="plan option: split-KV chunk length (0 = automatic)")
+    ap.add_argument("--subset", choices=["prefill", "decode"], default=None,
+                    help="run only the prefill or decode sequences of a mixed batch (3, 4)")
     ap.add_argument("--max-seqs", type=int, default=None,
                     help="keep only the first N sequences (profiler captures of config 2)")
     args = ap.parse_args()
@@ -446,14 +455,18 @@ def main():
     import torch
     torch.cuda.set_device(local)
     w = workloads.make(cfg, device=f"cuda:{local}", max_seqs=args.max_seqs)
-    run_gpu(args, w, cfg_dict(w, cfg), rank, local, world)
+    if args.subset:
+        w = w.subset(w.groups[f"{args.subset}_seqs"])
+        args.config_key += f"_{args.subset}"
+    run_gpu(args, w, cfg_dict(w, cfg, args.subset), rank, local, world)
     if world > 1:
         import torch.distributed as dist
         dist.destroy_process_group()
 
 
-def cfg_dict(w, cfg):
-    return {"workload": f"config {cfg}: {w.name}", "num_seqs": w.num_seqs, "total_q": w.total_q,
+def cfg_dict(w, cfg, subset=None):
+    tag = f" ({subset} sequences only)" if subset else ""
+    return {"workload": f"config {cfg}: {w.name}{tag}", "num_seqs": w.num_seqs, "total_q": w.total_q,
             "kv_tokens": int(w.context_lens.sum()), "Hq": w.Hq, "Hkv": w.Hkv, "D": w.D,
             "block_size": w.block_size, "num_blocks": w.num_blocks,
             "cow_pairs": int(len(w.cow_src)), "new_tokens": int(len(w.new_seq)),

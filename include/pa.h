@@ -131,9 +131,10 @@ typedef struct pa_plan_s* pa_plan_t;
 typedef struct {
   int32_t max_chunk_tokens;  /* 0: automatic split-KV; >0: split key ranges into chunks of at
                                 most this many tokens (rounded up to 64) */
-  int32_t tc_min_rows;       /* 0: default (16); >0: items with at least this many rows (query
+  int32_t tc_min_rows;       /* 0: default (4); >0: items with at least this many rows (query
                                 tokens x packed heads) use the tensor-core kernel; <0: never.
-                                Tensor-core items need D = 128 and block_size >= 8. */
+                                Tensor-core items need D = 128, block_size >= 8 and
+                                Hq / Hkv dividing 128. */
   int32_t num_sms;           /* 0: query the current device */
   int32_t reserved[5];       /* must be zero */
 } pa_plan_options;

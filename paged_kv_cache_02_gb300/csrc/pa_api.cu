@@ -73,6 +73,19 @@ pa_status make_pool_map(CUtensorMap* map, const void* pool, int64_t num_blocks, 
   return r == CUDA_SUCCESS ? PA_OK : PA_ERR_CUDA;
 }
 
+pa_status make_q_map(CUtensorMap* map, const void* q, int64_t total_q, int Hq, int D, int g) {
+  auto fn = encode_fn();
+  if (!fn) return PA_ERR_CUDA;
+  cuuint64_t dims[3] = {(cuuint64_t)D, (cuuint64_t)Hq, (cuuint64_t)total_q};
+  cuuint64_t strides[2] = {(cuuint64_t)D * 2, (cuuint64_t)Hq * D * 2};
+  cuuint32_t box[3] = {64u, (cuuint32_t)g, (cuuint32_t)(kTcRows / g)};
+  cuuint32_t estr[3] = {1u, 1u, 1u};
+  CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(q), dims, strides,
+                  box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? PA_OK : PA_ERR_CUDA;
+}
+
 }  // namespace pa
 
 // ====================================================================== plan
@@ -233,8 +246,10 @@ pa_status pa_plan_create(const int32_t* h_context_lens, const int32_t* h_query_l
 
   int sms = o.num_sms > 0 ? o.num_sms : device_sms();
   if (sms <= 0) sms = 152;
-  // Tensor-core tiles: D = 128 and blocks of at least 8 tokens (one swizzle atom per piece).
-  const bool tc_enabled = (D == 128) && (block_size >= 8) && o.tc_min_rows >= 0;
+  // Tensor-core tiles: D = 128, blocks of at least 8 tokens (one swizzle atom per piece) and
+  // g dividing the 128-row tile (a tile is whole tokens x the g heads of one KV head).
+  const bool tc_enabled = (D == 128) && (block_size >= 8) && (pa::kTcRows % g == 0) &&
+                          o.tc_min_rows >= 0;
   const int tc_min_rows = o.tc_min_rows > 0 ? o.tc_min_rows : pa::kTcMinRowsDefault;
 
   // ---- units: (sequence, KV head, row tile)
@@ -450,11 +465,15 @@ pa_status pa_attention(pa_plan_t p, void* d_out, pa_dtype out_dtype, const void*
     st = pa::make_pool_map(&vmap, d_v_pool, num_blocks, p->block_size, p->Hkv, p->D, 64, box_t,
                            true);
     if (st != PA_OK) return st;
+    CUtensorMap qmap;
+    st = pa::make_q_map(&qmap, d_q, p->total_q, p->Hq, p->D, p->g);
+    if (st != PA_OK) return st;
     int sms = device_sms();
     if (sms <= 0) return PA_ERR_CUDA;
     const int grid = std::min(p->n_tc, sms);
-    cudaError_t e = pa::launch_tc(a, kmap, vmap, reinterpret_cast<const Item*>(ws + p->off_tc),
-                                  p->n_tc, box_t, grid, s);
+    cudaError_t e = pa::launch_tc(a, kmap, vmap, qmap,
+                                  reinterpret_cast<const Item*>(ws + p->off_tc), p->n_tc, box_t,
+                                  grid, s);
     if (e != cudaSuccess) return PA_ERR_CUDA;
   }
   if (p->n_groups > 0) {

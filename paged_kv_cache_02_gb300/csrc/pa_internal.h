@@ -85,8 +85,12 @@ cudaError_t launch_combine(const AttnArgs& a, const SplitGroup* groups, int32_t 
                            cudaStream_t s);
 int decode_smem_bytes(int D, int rows_max);
 cudaError_t launch_tc(const AttnArgs& a, const CUtensorMap& kmap, const CUtensorMap& vmap,
-                      const Item* items, int32_t n_items, int box_t, int grid, cudaStream_t s);
+                      const CUtensorMap& qmap, const Item* items, int32_t n_items, int box_t,
+                      int grid, cudaStream_t s);
+// 3-D tiled map over q viewed as [total_q][Hq][D] bf16 with box (64, g, 128 / g), 128-byte
+// swizzle: one box is the 128 packed rows (tokens x the g heads of a KV head) of one D half.
+pa_status make_q_map(CUtensorMap* map, const void* q, int64_t total_q, int Hq, int D, int g);
 int tc_smem_bytes();
-constexpr int kTcMinRowsDefault = 16;  // items with at least this many rows use tensor cores
+constexpr int kTcMinRowsDefault = 4;   // items with at least this many rows use tensor cores
 
 }  // namespace pa

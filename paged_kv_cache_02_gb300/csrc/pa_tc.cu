@@ -9,18 +9,20 @@
 // that the score matrix is never written to memory.
 //
 // How (GB300): one persistent CTA per SM, warp-specialised.
-//   warp 0     TMA producer: per 128-key tile, one 3-D TMA copy per (block
-//              piece, D half, K or V) straight from the physical blocks named by
-//              the block table, 128-byte swizzled, into a 2-stage ring.
+//   warp 0     TMA producer: the item's 128 Q rows (one 3-D box per D half,
+//              double-buffered across items) and, per 64-key tile, one 3-D
+//              TMA copy per (block piece, D half, K or V) straight from the
+//              physical blocks named by the block table, 128-byte swizzled,
+//              into a 3-stage ring.
 //   warp 1     allocates TMEM and issues tcgen05.mma from one thread:
 //              S(j+1) = Q K_{j+1}^T is issued before O += P_j V_j so the tensor
 //              core computes the next scores while the softmax runs.
-//   warps 2-5  one thread per row (its TMEM lane): load the Q rows into
-//              shared memory, read S from TMEM, mask (causal, bottom-right
-//              aligned), online softmax in the log2 domain, write P (bf16,
-//              swizzled) for the next MMA, rescale O in TMEM only when the
-//              running maximum grows by more than 2^8, and write the output.
-// TMEM columns: S double buffer [0,256), O [256,384). Every wait is bounded.
+//   warps 2-5  one thread per row (its TMEM lane): read S from TMEM, mask
+//              (causal, bottom-right aligned), online softmax in the log2
+//              domain, write P (bf16, swizzled, double-buffered) for the next
+//              MMA, rescale O in TMEM only when the running maximum grows by
+//              more than 2^8, and write the output.
+// TMEM columns: S double buffer [0,128), O [128,256). Every wait is bounded.
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
@@ -34,29 +36,36 @@
 namespace pa {
 namespace {
 
-constexpr int kRows = kTcRows;        // 128 rows per tile (M)
-constexpr int kKeys = 128;            // keys per tile (N of S, K of P V)
-constexpr int kD = 128;               // head dim of this kernel
-constexpr int kStagesTc = 2;
+constexpr int kRows = kTcRows;          // 128 rows per tile (M)
+constexpr int kKeys = 64;               // keys per tile (N of S, K of P V)
+constexpr int kD = 128;                 // head dim of this kernel
+constexpr int kStagesTc = 3;
 constexpr int kThreadsTc = 192;
-constexpr int kHalf = kRows * 128;    // bytes of one 128-row x 64-element swizzled sub-tile
-constexpr float kRescaleLog2 = 8.f;   // O is rescaled once the max grows by > 2^8
-constexpr uint32_t kTmemCols = 512;
+constexpr int kQHalf = kRows * 128;     // 128 rows x 64 elements, swizzled (16 KB)
+constexpr int kKVHalf = kKeys * 128;    // 64 keys x 64 elements, swizzled (8 KB)
+constexpr float kRescaleLog2 = 8.f;     // O is rescaled once the max grows by > 2^8
+constexpr uint32_t kTmemCols = 256;
+constexpr uint32_t kTmemO = 2 * kKeys;  // first column of O
 
 constexpr uint32_t kIdescS = tc::idesc_bf16_f32(kRows, kKeys, false);  // Q K^T, both K-major
 constexpr uint32_t kIdescO = tc::idesc_bf16_f32(kRows, kD, true);      // P V, V is MN-major
 
 struct TcSmem {
-  uint8_t q[2][kHalf];                  // Q rows, D halves
-  uint8_t k[kStagesTc][2][kHalf];       // K tile, D halves
-  uint8_t v[kStagesTc][2][kHalf];       // V tile, D halves (rows = keys)
-  uint8_t p[2][kHalf];                  // P tile, key halves
+  uint8_t q[2][2][kQHalf];              // [buffer][D half]
+  uint8_t k[kStagesTc][2][kKVHalf];     // [stage][D half]
+  uint8_t v[kStagesTc][2][kKVHalf];     // [stage][D half], rows = keys
+  uint8_t p[2][kQHalf];                 // [buffer]: 128 rows x 64 keys
   uint64_t kv_full[kStagesTc];
   uint64_t kv_empty[kStagesTc];
-  uint64_t q_full, s_full[2], s_free[2], p_full, o_done, o_free, drain;
+  uint64_t q_full[2], q_free[2];
+  uint64_t s_full[2], s_free[2];
+  uint64_t p_full[2], o_done[2];
+  uint64_t o_free, drain;
   uint32_t tmem_base;
   int issued[kStagesTc];
   int consumed[kStagesTc];
+  int q_issued[2];
+  int q_consumed[2];
   int abort_flag;
 };
 
@@ -69,10 +78,12 @@ __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
   return *reinterpret_cast<uint32_t*>(&h);
 }
 
+__device__ __forceinline__ uint32_t ph(int n, int ring) { return (uint32_t)(n / ring) & 1u; }
+
 __global__ void __launch_bounds__(kThreadsTc, 1)
     tc_kernel(const __grid_constant__ AttnArgs a, const __grid_constant__ CUtensorMap kmap,
-              const __grid_constant__ CUtensorMap vmap, const Item* __restrict__ items,
-              int n_items, int box_t) {
+              const __grid_constant__ CUtensorMap vmap, const __grid_constant__ CUtensorMap qmap,
+              const Item* __restrict__ items, int n_items, int box_t) {
   extern __shared__ uint8_t smem_raw[];
   TcSmem& sm = *reinterpret_cast<TcSmem*>(align1024(smem_raw));
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -85,13 +96,16 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
       sm.issued[s] = 0;
       sm.consumed[s] = 0;
     }
-    mbar_init(&sm.q_full, kRows);
     for (int b = 0; b < 2; ++b) {
+      mbar_init(&sm.q_full[b], 1);
+      mbar_init(&sm.q_free[b], 1);
       mbar_init(&sm.s_full[b], 1);
       mbar_init(&sm.s_free[b], kRows);
+      mbar_init(&sm.p_full[b], kRows);
+      mbar_init(&sm.o_done[b], 1);
+      sm.q_issued[b] = 0;
+      sm.q_consumed[b] = 0;
     }
-    mbar_init(&sm.p_full, kRows);
-    mbar_init(&sm.o_done, 1);
     mbar_init(&sm.o_free, kRows);
     mbar_init(&sm.drain, 1);
     sm.abort_flag = 0;
@@ -111,18 +125,32 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
     if (lane == 0) {
       prefetch_tensormap(&kmap);
       prefetch_tensormap(&vmap);
+      prefetch_tensormap(&qmap);
     }
-    const int pieces = kKeys / box_t;                  // <= 16
+    const int pieces = kKeys / box_t;                     // <= 8
     const uint32_t piece_bytes = (uint32_t)box_t * 128u;  // one D half of one piece
-    int n = 0;                                         // global tile counter
+    int n = 0, k = 0;                                     // global tile / item counters
     bool ok = true;
-    for (int it = blockIdx.x; it < n_items && ok; it += G) {
+    for (int it = blockIdx.x; it < n_items && ok; it += G, ++k) {
       const Item item = items[it];
+      // the item's 128 Q rows: tokens x the g heads of its KV head, one box per D half
+      {
+        const int qb = k & 1;
+        ok = mbar_wait(&sm.q_free[qb], ph(k, 2) ^ 1u, a.err);
+        if (!ok || *(volatile int*)&sm.abort_flag) { ok = false; break; }
+        if (lane == 0) {
+          mbar_arrive_expect_tx(&sm.q_full[qb], 2u * kQHalf);
+          const int tok = item.q_row0 + item.row_begin / a.g;
+          tma_load_3d(&sm.q[qb][0][0], &qmap, &sm.q_full[qb], 0, item.kv_head * a.g, tok);
+          tma_load_3d(&sm.q[qb][1][0], &qmap, &sm.q_full[qb], 64, item.kv_head * a.g, tok);
+          sm.q_issued[qb] += 1;
+        }
+        __syncwarp();
+      }
       const int32_t* bt = a.block_table + (int64_t)item.seq * a.max_blocks;
       for (int t0 = item.kv_begin; t0 < item.kv_end; t0 += kKeys, ++n) {
-        const int st = n & 1;
-        const uint32_t ph = (uint32_t)(n >> 1) & 1u;
-        ok = mbar_wait(&sm.kv_empty[st], ph ^ 1u, a.err);
+        const int st = n % kStagesTc;
+        ok = mbar_wait(&sm.kv_empty[st], ph(n, kStagesTc) ^ 1u, a.err);
         if (!ok || *(volatile int*)&sm.abort_flag) { ok = false; break; }
         bool valid = false;
         int tok = 0;
@@ -160,55 +188,62 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0) {
-      const uint32_t q_addr = smem_addr(&sm.q[0][0]);
-      const uint32_t p_addr = smem_addr(&sm.p[0][0]);
-      int nS = 0, nP = 0, item_idx = 0;
+      int nS = 0, nP = 0, k = 0;
       bool ok = true;
+      uint32_t q_addr = 0;
       // S(tile nS) = Q K^T into TMEM buffer nS % 2
       auto issue_s = [&]() -> bool {
-        const int st = nS & 1;
-        if (!mbar_wait(&sm.kv_full[st], (uint32_t)(nS >> 1) & 1u, a.err)) return false;
+        const int st = nS % kStagesTc;
+        const int sb = nS & 1;
+        if (!mbar_wait(&sm.kv_full[st], ph(nS, kStagesTc), a.err)) return false;
         sm.consumed[st] += 1;
-        if (!mbar_wait(&sm.s_free[st], ((uint32_t)(nS >> 1) & 1u) ^ 1u, a.err)) return false;
+        if (!mbar_wait(&sm.s_free[sb], ph(nS, 2) ^ 1u, a.err)) return false;
         tc::fence_after_sync();
         const uint32_t k_addr = smem_addr(&sm.k[st][0][0]);
-        const uint32_t d_tmem = tmem + (uint32_t)st * kKeys;
 #pragma unroll
         for (int kk = 0; kk < kD / 16; ++kk) {
-          const uint32_t off = (uint32_t)(kk >> 2) * kHalf + (uint32_t)(kk & 3) * 32u;
-          tc::mma_bf16(d_tmem, tc::smem_desc_sw128(q_addr + off, 16, 1024),
-                       tc::smem_desc_sw128(k_addr + off, 16, 1024), kIdescS, kk > 0);
+          const uint32_t qo = (uint32_t)(kk >> 2) * kQHalf + (uint32_t)(kk & 3) * 32u;
+          const uint32_t ko = (uint32_t)(kk >> 2) * kKVHalf + (uint32_t)(kk & 3) * 32u;
+          tc::mma_bf16(tmem + (uint32_t)sb * kKeys, tc::smem_desc_sw128(q_addr + qo, 16, 1024),
+                       tc::smem_desc_sw128(k_addr + ko, 16, 1024), kIdescS, kk > 0);
         }
-        tc::commit(&sm.s_full[st]);
+        tc::commit(&sm.s_full[sb]);
         ++nS;
         return true;
       };
-      for (int it = blockIdx.x; it < n_items && ok; it += G, ++item_idx) {
+      for (int it = blockIdx.x; it < n_items && ok; it += G, ++k) {
         const Item item = items[it];
         const int nt = (item.kv_end - item.kv_begin + kKeys - 1) / kKeys;
-        if (!mbar_wait(&sm.q_full, (uint32_t)item_idx & 1u, a.err)) { ok = false; break; }
+        const int qb = k & 1;
+        if (!mbar_wait(&sm.q_full[qb], ph(k, 2), a.err)) { ok = false; break; }
+        sm.q_consumed[qb] += 1;
         tc::fence_after_sync();
+        q_addr = smem_addr(&sm.q[qb][0][0]);
         if (!issue_s()) { ok = false; break; }
+        if (nt == 1) tc::commit(&sm.q_free[qb]);
         for (int j = 0; j < nt; ++j) {
-          if (j + 1 < nt && !issue_s()) { ok = false; break; }
+          if (j + 1 < nt) {
+            if (!issue_s()) { ok = false; break; }
+            if (j + 2 == nt) tc::commit(&sm.q_free[qb]);  // last S of the item issued
+          }
           // O += P_j V_j
-          if (!mbar_wait(&sm.p_full, (uint32_t)nP & 1u, a.err)) { ok = false; break; }
-          if (j == 0 && !mbar_wait(&sm.o_free, ((uint32_t)item_idx & 1u) ^ 1u, a.err)) {
+          const int pb = nP & 1;
+          if (!mbar_wait(&sm.p_full[pb], ph(nP, 2), a.err)) { ok = false; break; }
+          if (j == 0 && !mbar_wait(&sm.o_free, ((uint32_t)k & 1u) ^ 1u, a.err)) {
             ok = false;
             break;
           }
           tc::fence_after_sync();
-          const int st = nP & 1;
+          const int st = nP % kStagesTc;
+          const uint32_t p_addr = smem_addr(&sm.p[pb][0]);
           const uint32_t v_addr = smem_addr(&sm.v[st][0][0]);
 #pragma unroll
           for (int kk = 0; kk < kKeys / 16; ++kk) {
-            const uint32_t a_off = (uint32_t)(kk >> 2) * kHalf + (uint32_t)(kk & 3) * 32u;
-            const uint32_t b_off = (uint32_t)kk * 16u * 128u;
-            tc::mma_bf16(tmem + 2u * kKeys, tc::smem_desc_sw128(p_addr + a_off, 16, 1024),
-                         tc::smem_desc_sw128(v_addr + b_off, kHalf, 1024), kIdescO,
-                         (j > 0) || (kk > 0));
+            tc::mma_bf16(tmem + kTmemO, tc::smem_desc_sw128(p_addr + (uint32_t)kk * 32u, 16, 1024),
+                         tc::smem_desc_sw128(v_addr + (uint32_t)kk * 16u * 128u, kKVHalf, 1024),
+                         kIdescO, (j > 0) || (kk > 0));
           }
-          tc::commit(&sm.o_done);
+          tc::commit(&sm.o_done[pb]);
           tc::commit(&sm.kv_empty[st]);
           ++nP;
         }
@@ -224,9 +259,9 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
     const int quad = warp & 3;                    // TMEM lane quadrant of this warp
     const int row = quad * 32 + lane;             // tile row = TMEM lane
     const uint32_t t_lane = tmem + ((uint32_t)(quad * 32) << 16);
-    int n = 0, item_idx = 0;
+    int n = 0;
     bool ok = true;
-    for (int it = blockIdx.x; it < n_items && ok; it += G, ++item_idx) {
+    for (int it = blockIdx.x; it < n_items && ok; it += G) {
       const Item item = items[it];
       const int nt = (item.kv_end - item.kv_begin + kKeys - 1) / kKeys;
       const bool live = row < item.row_count;
@@ -241,90 +276,84 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
         if (item.kv_end > L || item.row_begin + item.row_count > ql * a.g)
           record_error(a.err, PA_DEVERR_LENS);
       }
-      // ---- this row of Q into the swizzled Q tile (zeros for rows past the item)
-      {
-        const uint4* src = reinterpret_cast<const uint4*>(
-            a.q + ((int64_t)(item.q_row0 + t) * a.Hq + h) * kD);
-        uint4 vals[16];
-#pragma unroll
-        for (int j = 0; j < 16; ++j) vals[j] = live ? __ldg(src + j) : make_uint4(0, 0, 0, 0);
-#pragma unroll
-        for (int j = 0; j < 16; ++j)
-          *reinterpret_cast<uint4*>(&sm.q[j >> 3][tc::sw128_offset(row, j & 7)]) = vals[j];
-        tc::fence_async_shared();
-        mbar_arrive(&sm.q_full);
-      }
       float m_used = -INFINITY, l = 0.f;
       for (int j = 0; j < nt; ++j, ++n) {
-        const int b = n & 1;
-        if (!mbar_wait(&sm.s_full[b], (uint32_t)(n >> 1) & 1u, a.err)) { ok = false; break; }
+        const int sb = n & 1;
+        if (!mbar_wait(&sm.s_full[sb], ph(n, 2), a.err)) { ok = false; break; }
         tc::fence_after_sync();
         float s[kKeys];
-#pragma unroll
-        for (int c4 = 0; c4 < kKeys / 32; ++c4) {
-          float tmp[32];
-          tc::tmem_ld32(t_lane + (uint32_t)b * kKeys + (uint32_t)c4 * 32u, tmp);
-#pragma unroll
-          for (int i = 0; i < 32; ++i) s[c4 * 32 + i] = tmp[i];
-        }
+        tc::tmem_ld64(t_lane + (uint32_t)sb * kKeys, s);
         tc::fence_before_sync();
-        mbar_arrive(&sm.s_free[b]);
-        // mask and scale; running max
+        mbar_arrive(&sm.s_free[sb]);
+        // running max of the raw scores (the scale is positive, so it commutes with max);
+        // only a tile that crosses this row's causal limit needs the mask
         const int key0 = item.kv_begin + j * kKeys;
-        float mx = -INFINITY;
+        if (key0 + kKeys - 1 > lim) {
 #pragma unroll
-        for (int c = 0; c < kKeys; ++c) {
-          s[c] = (key0 + c <= lim) ? s[c] * a.scale_log2 : -INFINITY;
-          mx = fmaxf(mx, s[c]);
+          for (int c = 0; c < kKeys; ++c) s[c] = (key0 + c <= lim) ? s[c] : -INFINITY;
         }
-        const float m_new = fmaxf(m_used, mx);
-        if (j > 0) {
-          // P V of the previous tile must be done before O or P are touched
-          if (!mbar_wait(&sm.o_done, (uint32_t)(n - 1) & 1u, a.err)) { ok = false; break; }
-          tc::fence_after_sync();
-        }
+        float mx8[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) mx8[i] = s[i];
+#pragma unroll
+        for (int c = 8; c < kKeys; ++c) mx8[c & 7] = fmaxf(mx8[c & 7], s[c]);
+        const float mx = fmaxf(fmaxf(fmaxf(mx8[0], mx8[1]), fmaxf(mx8[2], mx8[3])),
+                               fmaxf(fmaxf(mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7])));
+        const float m_new = fmaxf(m_used, mx * a.scale_log2);
         if (m_used == -INFINITY) {
           m_used = m_new;  // nothing accumulated yet: O holds only zero rows
         } else if (m_new > m_used + kRescaleLog2) {
+          // the previous P V must be done before O is touched
+          if (!mbar_wait(&sm.o_done[(n - 1) & 1], ph(n - 1, 2), a.err)) { ok = false; break; }
+          tc::fence_after_sync();
           const float alpha = fast_exp2(m_used - m_new);
 #pragma unroll
-          for (int c4 = 0; c4 < kD / 32; ++c4) {
-            float o[32];
-            const uint32_t addr = t_lane + 2u * kKeys + (uint32_t)c4 * 32u;
-            tc::tmem_ld32(addr, o);
+          for (int c2 = 0; c2 < kD / 64; ++c2) {
+            float o[64];
+            const uint32_t addr = t_lane + kTmemO + (uint32_t)c2 * 64u;
+            tc::tmem_ld64(addr, o);
+            float o0[32], o1[32];
 #pragma unroll
-            for (int i = 0; i < 32; ++i) o[i] *= alpha;
-            tc::tmem_st32(addr, o);
+            for (int i = 0; i < 32; ++i) {
+              o0[i] = o[i] * alpha;
+              o1[i] = o[32 + i] * alpha;
+            }
+            tc::tmem_st32(addr, o0);
+            tc::tmem_st32(addr + 32u, o1);
           }
           tc::tmem_wait_st();
           l *= alpha;
           m_used = m_new;
         }
-        // P = 2^(s - m) in bf16, written as the swizzled A operand of the next MMA
-        float sum = 0.f;
+        // P buffer sb was last read by P V two tiles ago
+        if (j >= 2) {
+          if (!mbar_wait(&sm.o_done[sb], ph(n - 2, 2), a.err)) { ok = false; break; }
+        }
+        // P = 2^(scale * s - m) in bf16, written as the swizzled A operand of the next MMA.
+        // A masked score is -inf and gives exactly 0; with no visible key yet every
+        // score is -inf and the offset is irrelevant.
+        const float neg_m = (m_used == -INFINITY) ? 0.f : -m_used;
+        float sum8[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
 #pragma unroll
         for (int c8 = 0; c8 < kKeys / 8; ++c8) {
           float p[8];
 #pragma unroll
           for (int i = 0; i < 8; ++i) {
-            const float x = s[c8 * 8 + i];
-            p[i] = (x == -INFINITY) ? 0.f : fast_exp2(x - m_used);
+            p[i] = fast_exp2(fmaf(s[c8 * 8 + i], a.scale_log2, neg_m));
+            sum8[i] += p[i];
           }
           uint4 w;
           w.x = pack_bf16(p[0], p[1]);
           w.y = pack_bf16(p[2], p[3]);
           w.z = pack_bf16(p[4], p[5]);
           w.w = pack_bf16(p[6], p[7]);
-          // the normaliser sums the rounded weights the tensor core multiplies
-          sum += bf16lo(w.x) + bf16hi(w.x) + bf16lo(w.y) + bf16hi(w.y) + bf16lo(w.z) +
-                 bf16hi(w.z) + bf16lo(w.w) + bf16hi(w.w);
-          *reinterpret_cast<uint4*>(&sm.p[c8 >> 3][tc::sw128_offset(row, c8 & 7)]) = w;
+          *reinterpret_cast<uint4*>(&sm.p[sb][tc::sw128_offset(row, c8)]) = w;
         }
-        l += sum;
+        l += ((sum8[0] + sum8[1]) + (sum8[2] + sum8[3])) + ((sum8[4] + sum8[5]) + (sum8[6] + sum8[7]));
         // keys past the item's range hold whatever the block tail holds: zero those
         // V rows so that 0 * (non-finite) never reaches the accumulator
-        if (key0 + row >= item.kv_end) {
-          const int st = n & 1;
+        if (row < kKeys && key0 + row >= item.kv_end) {
+          const int st = n % kStagesTc;
           uint4* v0 = reinterpret_cast<uint4*>(&sm.v[st][0][row * 128]);
           uint4* v1 = reinterpret_cast<uint4*>(&sm.v[st][1][row * 128]);
 #pragma unroll
@@ -335,19 +364,22 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
         }
         tc::fence_async_shared();
         tc::fence_before_sync();
-        mbar_arrive(&sm.p_full);
+        mbar_arrive(&sm.p_full[sb]);
       }
       if (!ok) break;
       // ---- epilogue: O / l
-      if (!mbar_wait(&sm.o_done, (uint32_t)(n - 1) & 1u, a.err)) { ok = false; break; }
+      if (!mbar_wait(&sm.o_done[(n - 1) & 1], ph(n - 1, 2), a.err)) { ok = false; break; }
       tc::fence_after_sync();
       float o[kD];
+      {
+        float o0[64], o1[64];
+        tc::tmem_ld64(t_lane + kTmemO, o0);
+        tc::tmem_ld64(t_lane + kTmemO + 64u, o1);
 #pragma unroll
-      for (int c4 = 0; c4 < kD / 32; ++c4) {
-        float tmp[32];
-        tc::tmem_ld32(t_lane + 2u * kKeys + (uint32_t)c4 * 32u, tmp);
-#pragma unroll
-        for (int i = 0; i < 32; ++i) o[c4 * 32 + i] = tmp[i];
+        for (int i = 0; i < 64; ++i) {
+          o[i] = o0[i];
+          o[64 + i] = o1[i];
+        }
       }
       tc::fence_before_sync();
       mbar_arrive(&sm.o_free);
@@ -391,11 +423,18 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
   __syncthreads();
   // After an abort, give copies still in flight a bounded time to land.
   if (sm.abort_flag && threadIdx.x == 0) {
+    const uint64_t t0 = global_timer_ns();
     for (int s = 0; s < kStagesTc; ++s) {
       if (sm.issued[s] > sm.consumed[s]) {
         const uint32_t parity = (uint32_t)(sm.issued[s] - 1) & 1u;
-        const uint64_t t0 = global_timer_ns();
         while (!mbar_try_wait(smem_addr(&sm.kv_full[s]), parity))
+          if (global_timer_ns() - t0 > kWaitLimitNs) break;
+      }
+    }
+    for (int b = 0; b < 2; ++b) {
+      if (sm.q_issued[b] > sm.q_consumed[b]) {
+        const uint32_t parity = (uint32_t)(sm.q_issued[b] - 1) & 1u;
+        while (!mbar_try_wait(smem_addr(&sm.q_full[b]), parity))
           if (global_timer_ns() - t0 > kWaitLimitNs) break;
       }
     }
@@ -411,13 +450,14 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
 int tc_smem_bytes() { return (int)sizeof(TcSmem) + 1024; }
 
 cudaError_t launch_tc(const AttnArgs& a, const CUtensorMap& kmap, const CUtensorMap& vmap,
-                      const Item* items, int32_t n_items, int box_t, int grid, cudaStream_t s) {
+                      const CUtensorMap& qmap, const Item* items, int32_t n_items, int box_t,
+                      int grid, cudaStream_t s) {
   if (n_items <= 0) return cudaSuccess;
   const int smem = tc_smem_bytes();
   cudaError_t e =
       cudaFuncSetAttribute(tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
-  tc_kernel<<<grid, kThreadsTc, smem, s>>>(a, kmap, vmap, items, n_items, box_t);
+  tc_kernel<<<grid, kThreadsTc, smem, s>>>(a, kmap, vmap, qmap, items, n_items, box_t);
   return cudaGetLastError();
 }
 

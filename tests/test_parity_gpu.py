@@ -51,6 +51,7 @@ for B in (8, 16, 32):
     for D in (64, 128):
         for Hq, Hkv in ((4, 4), (8, 2), (8, 1)):
             CASES.append((B, D, Hq, Hkv))
+CASES += [(16, 128, 12, 4), (32, 128, 64, 4), (16, 64, 12, 4)]
 
 
 @pytest.mark.parametrize("B,D,Hq,Hkv", CASES)

@@ -69,6 +69,26 @@ class Workload:
     def max_blocks(self) -> int:
         return int(self.block_table.shape[1])
 
+    def subset(self, seqs) -> "Workload":
+        """The sub-batch of the listed sequences (same pools, same values, same blocks)."""
+        seqs = np.asarray(sorted(int(x) for x in seqs), dtype=np.int64)
+        pref = np.concatenate([[0], np.cumsum(self.query_lens.astype(np.int64))])
+        rows = np.concatenate([np.arange(pref[s], pref[s + 1]) for s in seqs]) if len(seqs) else \
+            np.zeros(0, np.int64)
+        remap = {int(s): i for i, s in enumerate(seqs)}
+        keep = np.array([int(s) in remap for s in self.new_seq], dtype=bool)
+        idx = torch.from_numpy(np.nonzero(keep)[0])
+        return Workload(name=self.name, Hq=self.Hq, Hkv=self.Hkv, D=self.D,
+                        block_size=self.block_size, num_blocks=self.num_blocks,
+                        context_lens=self.context_lens[seqs], query_lens=self.query_lens[seqs],
+                        block_table=self.block_table[seqs],
+                        new_seq=np.array([remap[int(s)] for s in self.new_seq[keep]], np.int32),
+                        new_pos=self.new_pos[keep], cow_src=self.cow_src, cow_dst=self.cow_dst,
+                        q=self.q[torch.from_numpy(rows).to(self.q.device)],
+                        k_pool=self.k_pool, v_pool=self.v_pool,
+                        k_new=self.k_new[idx.to(self.k_new.device)],
+                        v_new=self.v_new[idx.to(self.v_new.device)], seed=self.seed, groups={})
+
     def kv_bytes(self) -> int:
         """K and V bytes one attention pass reads: sum over sequences of L * 2 * Hkv * D * 2."""
         return int(self.context_lens.astype(np.int64).sum()) * 2 * self.Hkv * self.D * 2
