@@ -30,16 +30,17 @@ sys.path.insert(0, ROOT)
 METRIC = "paged attn tokens/s and achieved HBM GB/s / TC util vs roofline (1×GB300)"
 UNIT = "tokens/s"
 PROFILE_TRAFFIC = os.path.join(ROOT, "profiles", "traffic.json")
-KERNEL_SOURCES = ["pa_dec.cu", "pa_ptx.cuh", "pa_internal.h"]
+KERNEL_SOURCES = {"decode": ["pa_dec.cu", "pa_ptx.cuh", "pa_internal.h"],
+                  "tc": ["pa_tc.cu", "pa_tc.cuh", "pa_ptx.cuh", "pa_internal.h"]}
 
 
 def log(*a):
     print(*a, file=sys.stderr, flush=True)
 
 
-def kernel_source_hash() -> str:
+def kernel_source_hash(kernel: str) -> str:
     h = hashlib.sha256()
-    for f in KERNEL_SOURCES:
+    for f in KERNEL_SOURCES[kernel]:
         with open(os.path.join(ROOT, "paged_kv_cache_02_gb300", "csrc", f), "rb") as fh:
             h.update(fh.read())
     return h.hexdigest()[:16]
@@ -327,12 +328,19 @@ def run_gpu(args, w, cfg_name, rank, local, world):
     t_hbm = (kv_b + q_b) / (hbm_peak * 1e9)
     t_tc = flops / (tc_peak * 1e12)
     bound = "hbm" if t_hbm >= t_tc else "tensor"
+    # the attention call runs one kernel when the plan holds one kind of item; its
+    # committed DRAM counters apply while that kernel's sources are unchanged
+    kernel = None
+    if st["n_dec_items"] and not st["n_tc_items"]:
+        kernel = "decode"
+    elif st["n_tc_items"] and not st["n_dec_items"]:
+        kernel = "tc"
     traffic = None
-    if os.path.exists(PROFILE_TRAFFIC):
+    if kernel and os.path.exists(PROFILE_TRAFFIC):
         with open(PROFILE_TRAFFIC) as f:
             prof = json.load(f)
         entry = prof.get(args.config_key)
-        if entry and entry.get("kernel_hash") == kernel_source_hash():
+        if entry and entry.get("kernel_hash") == kernel_source_hash(kernel):
             traffic = entry.get("dram_bytes_per_launch")
     if bound == "hbm":
         achieved = (kv_b + q_b) / attn_s / 1e9
