@@ -13,8 +13,9 @@
 // items. Warp 8 is the producer: for every 64-key stage it issues one 3-D TMA
 // copy per (block piece, K or V) into a shared-memory ring guarded by
 // mbarriers, and on an item's first stage also the item's query rows (1-D bulk
-// copies). Block ids are read one stage ahead, so their latency hides behind
-// the ring. Warps 0-7 consume, each on its own 8-key slice of every stage and
+// copies). An item's block ids are loaded while the previous item is being
+// issued and kept in shared memory, so no global load sits between a free
+// stage and its copies. Warps 0-7 consume, each on its own 8-key slice of every stage and
 // with its own online softmax (an exact split of the keys inside the CTA): no
 // CTA-wide barrier is needed per stage. QK^T loads every 16-byte K chunk once
 // and uses it for all rows; the per-key sums are reduce-scattered with
@@ -64,6 +65,7 @@ struct DecSmem {
   float l_fin[RM];
   uint64_t full[S];
   uint64_t empty[S];
+  int bt_cache[2][kBtCache];  // block ids of the producer's current and next item
   int issued[S];    // copy phases issued per stage (producer)
   int consumed[S];  // phases the consumers have waited for
   int abort_flag;
@@ -115,12 +117,6 @@ __device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t b
       : "memory");
 }
 
-// Block ids of the (at most two) pieces a producer lane loads for one stage:
-// -1 = no piece, -2 = block-table index out of range.
-struct Lookahead {
-  int phys0, phys1;
-};
-
 template <int D, int RM>
 __global__ void __launch_bounds__(kThreads, 1)
     decode_kernel(const __grid_constant__ AttnArgs a, const __grid_constant__ CUtensorMap kmap,
@@ -158,59 +154,52 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     const int pieces = kKeyTile / box_t;           // <= 64
     const uint32_t piece_bytes = (uint32_t)box_t * D * 2u;
-    auto lookup = [&](const Item& item, int t0) -> Lookahead {
-      Lookahead r{-1, -1};
-      const int32_t* bt = a.block_table + (int64_t)item.seq * a.max_blocks;
-#pragma unroll
-      for (int h = 0; h < 2; ++h) {
-        const int pc = lane + 32 * h;
-        int ph = -1;
-        if (pc < pieces) {
-          const int j0 = t0 + pc * box_t;
-          if (j0 < item.kv_end) {
-            const int lb = j0 / a.block_size;
-            ph = (lb < a.max_blocks) ? __ldg(bt + lb) : -2;
-          }
-        }
-        if (h == 0) r.phys0 = ph; else r.phys1 = ph;
-      }
-      return r;
-    };
+    const int G = gridDim.x;
     int stage = 0;
     uint32_t phase = 0;
     bool ok = true;
-    int it = blockIdx.x;
-    if (it < n_items) {
-      Item cur = items[it];
-      Item nxt = cur;
-      if (it + (int)gridDim.x < n_items) nxt = items[it + gridDim.x];
-      int t0 = cur.kv_begin;
-      Lookahead la = lookup(cur, t0);
-      while (true) {
-        // position and block ids of the stage after this one (loads in flight meanwhile)
-        int nit = it, nt0 = t0 + kKeyTile;
-        bool next_is_new = false;
-        if (nt0 >= cur.kv_end) {
-          nit = it + gridDim.x;
-          nt0 = nxt.kv_begin;
-          next_is_new = true;
-        }
-        Lookahead nla{-1, -1};
-        if (nit < n_items) nla = lookup(next_is_new ? nxt : cur, nt0);
-
+    // block ids are staged one item ahead: registers -> shared cache at the switch
+    int nb[kBtPerLane];
+    Item item_next{};
+    if ((int)blockIdx.x < n_items) {
+      const Item f = items[blockIdx.x];
+      bt_prefetch(a.block_table + (int64_t)f.seq * a.max_blocks, a.max_blocks,
+                  bt_window(f.kv_begin, f.kv_end, a.block_size), lane, nb);
+      bt_store(sm.bt_cache[0], nb, lane);
+      if ((int)blockIdx.x + G < n_items) item_next = items[blockIdx.x + G];
+    }
+    __syncwarp();
+    int k = 0;
+    for (int it = blockIdx.x; it < n_items && ok; it += G, ++k) {
+      const Item cur = items[it];
+      const BtWindow win = bt_window(cur.kv_begin, cur.kv_end, a.block_size);
+      const int* cache = sm.bt_cache[k & 1];
+      const int32_t* bt = a.block_table + (int64_t)cur.seq * a.max_blocks;
+      const bool has_next = it + G < n_items;
+      Item item_after{};
+      if (has_next) {
+        bt_prefetch(a.block_table + (int64_t)item_next.seq * a.max_blocks, a.max_blocks,
+                    bt_window(item_next.kv_begin, item_next.kv_end, a.block_size), lane, nb);
+        if (it + 2 * G < n_items) item_after = items[it + 2 * G];
+      }
+      for (int t0 = cur.kv_begin; t0 < cur.kv_end; t0 += kKeyTile) {
         ok = mbar_wait(&sm.empty[stage], phase ^ 1u, a.err);
         if (!ok || *(volatile int*)&sm.abort_flag) { ok = false; break; }
-        int tok0 = 0, tok1 = 0;
-        auto valid_piece = [&](int ph, int pc, int& tok) -> bool {
-          if (ph == -1) return false;
+        // pieces lane and lane + 32 of this stage (a stage has at most 64 pieces)
+        auto locate = [&](int pc, int& tok) -> bool {
+          if (pc >= pieces) return false;
+          const int j0 = t0 + pc * box_t;
+          if (j0 >= cur.kv_end) return false;
+          const int lb = j0 / a.block_size;
+          const int ph = bt_lookup(cache, win, bt, a.max_blocks, lb);
           if (ph == -2) { record_error(a.err, PA_DEVERR_TABLE_RANGE); return false; }
           if (ph < 0 || ph >= a.num_blocks) { record_error(a.err, PA_DEVERR_BLOCK_RANGE); return false; }
-          const int j0 = t0 + pc * box_t;
-          tok = ph * a.block_size + (j0 - (j0 / a.block_size) * a.block_size);
+          tok = ph * a.block_size + (j0 - lb * a.block_size);
           return true;
         };
-        const bool v0 = valid_piece(la.phys0, lane, tok0);
-        const bool v1 = valid_piece(la.phys1, lane + 32, tok1);
+        int tok0 = 0, tok1 = 0;
+        const bool v0 = locate(lane, tok0);
+        const bool v1 = locate(lane + 32, tok1);
         uint32_t bytes = (__popc(__ballot_sync(0xffffffffu, v0)) +
                           __popc(__ballot_sync(0xffffffffu, v1))) * piece_bytes * 2u;
         // the item's query rows ride on its first stage: one copy per query token
@@ -221,6 +210,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           n_qtok = (cur.row_begin + cur.row_count - 1) / a.g - qt_first + 1;
           bytes += (uint32_t)cur.row_count * D * 2u;
         }
+        // one arrive carrying every byte of the stage, before any copy is issued
         if (lane == 0) mbar_arrive_expect_tx(&sm.full[stage], bytes);
         __syncwarp();
         if (v0) {
@@ -244,16 +234,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         if (lane == 0) sm.issued[stage] += 1;
         if (++stage == S) { stage = 0; phase ^= 1u; }
-        // advance to the stage looked up above
-        if (next_is_new) {
-          it = nit;
-          if (it >= n_items) break;
-          cur = nxt;
-          if (it + (int)gridDim.x < n_items) nxt = items[it + gridDim.x];
-        }
-        t0 = nt0;
-        la = nla;
       }
+      if (has_next) {
+        bt_store(sm.bt_cache[(k + 1) & 1], nb, lane);
+        item_next = item_after;
+      }
+      __syncwarp();
     }
     if (!ok) sm.abort_flag = 1;
   } else {

@@ -90,6 +90,52 @@ __device__ __forceinline__ void named_bar_sync(int id, int count) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
 }
 
+// ---- block-table cache of a producer warp.
+// An item's block ids (logical blocks first .. first + count - 1 of its row) are
+// loaded into registers one item ahead (16 per lane, 512 per item) and stored to
+// shared memory when the producer reaches that item, so that issuing a tile only
+// reads shared memory. Ids past the cached 512 are read from global memory.
+constexpr int kBtCache = 512;
+constexpr int kBtPerLane = kBtCache / 32;
+
+struct BtWindow {
+  int first;  // first logical block held
+  int count;  // number of logical blocks the item needs
+};
+
+__device__ __forceinline__ BtWindow bt_window(int kv_begin, int kv_end, int block_size) {
+  BtWindow w;
+  w.first = kv_begin / block_size;
+  w.count = (kv_end - 1) / block_size - w.first + 1;
+  return w;
+}
+
+// Loads (into registers) the cached part of an item's block ids; -2 marks an index
+// past the table row, -3 an unused slot.
+__device__ __forceinline__ void bt_prefetch(const int32_t* bt_row, int max_blocks, BtWindow w,
+                                            int lane, int (&r)[kBtPerLane]) {
+#pragma unroll
+  for (int i = 0; i < kBtPerLane; ++i) {
+    const int idx = lane + 32 * i;
+    const int lb = w.first + idx;
+    r[i] = (idx >= w.count) ? -3 : (lb < max_blocks ? __ldg(bt_row + lb) : -2);
+  }
+}
+
+__device__ __forceinline__ void bt_store(int* cache, const int (&r)[kBtPerLane], int lane) {
+#pragma unroll
+  for (int i = 0; i < kBtPerLane; ++i) cache[lane + 32 * i] = r[i];
+}
+
+// Block id of logical block lb of the item (cache first, global memory beyond it);
+// -2 if lb is past the table row.
+__device__ __forceinline__ int bt_lookup(const int* cache, BtWindow w, const int32_t* bt_row,
+                                         int max_blocks, int lb) {
+  const int idx = lb - w.first;
+  if (idx < kBtCache) return cache[idx];
+  return lb < max_blocks ? __ldg(bt_row + lb) : -2;
+}
+
 __device__ __forceinline__ float bf16lo(uint32_t w) { return __uint_as_float(w << 16); }
 __device__ __forceinline__ float bf16hi(uint32_t w) { return __uint_as_float(w & 0xffff0000u); }
 

@@ -8,21 +8,25 @@
 // context that lives in non-contiguous blocks, with the causal mask fused so
 // that the score matrix is never written to memory.
 //
-// How (GB300): one persistent CTA per SM, warp-specialised.
+// How (GB300): one persistent CTA per SM, warp-specialised, 10 warps.
 //   warp 0     TMA producer: the item's 128 Q rows (one 3-D box per D half,
 //              double-buffered across items) and, per 64-key tile, one 3-D
 //              TMA copy per (block piece, D half, K or V) straight from the
 //              physical blocks named by the block table, 128-byte swizzled,
 //              into a 3-stage ring.
-//   warp 1     allocates TMEM and issues tcgen05.mma from one thread:
-//              S(j+1) = Q K_{j+1}^T is issued before O += P_j V_j so the tensor
-//              core computes the next scores while the softmax runs.
-//   warps 2-5  one thread per row (its TMEM lane): read S from TMEM, mask
-//              (causal, bottom-right aligned), online softmax in the log2
-//              domain, write P (bf16, swizzled, double-buffered) for the next
-//              MMA, rescale O in TMEM only when the running maximum grows by
-//              more than 2^8, and write the output.
-// TMEM columns: S double buffer [0,128), O [128,256). Every wait is bounded.
+//   warp 1     allocates TMEM and issues tcgen05.mma from one thread. Tile j
+//              of an item belongs to softmax group j % 2; S(j+2) = Q K^T is
+//              issued right after O_g += P_j V_j, so the tensor core always has
+//              the next scores of both groups queued.
+//   warps 2-5  softmax group 0, warps 6-9 softmax group 1: one thread per row
+//              (its TMEM lane). Each group runs an online softmax over its
+//              own tiles (an exact split of the keys): mask (causal,
+//              bottom-right aligned), log2-domain exp, bf16 P written swizzled
+//              as the next MMA's A operand, O rescaled in TMEM only when the
+//              group's running maximum grows by more than 2^8. At the end of an
+//              item group 0 merges both groups' (m, l, O) and writes the output.
+// TMEM (512 columns): S double buffer of group g at [128 g, 128 g + 128),
+// O of group g at [256 + 128 g, 384 + 128 g). Every wait is bounded.
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
@@ -40,26 +44,32 @@ constexpr int kRows = kTcRows;          // 128 rows per tile (M)
 constexpr int kKeys = 64;               // keys per tile (N of S, K of P V)
 constexpr int kD = 128;                 // head dim of this kernel
 constexpr int kStagesTc = 3;
-constexpr int kThreadsTc = 192;
+constexpr int kThreadsTc = 320;
 constexpr int kQHalf = kRows * 128;     // 128 rows x 64 elements, swizzled (16 KB)
 constexpr int kKVHalf = kKeys * 128;    // 64 keys x 64 elements, swizzled (8 KB)
 constexpr float kRescaleLog2 = 8.f;     // O is rescaled once the max grows by > 2^8
-constexpr uint32_t kTmemCols = 256;
-constexpr uint32_t kTmemO = 2 * kKeys;  // first column of O
+constexpr uint32_t kTmemCols = 512;
+constexpr int kGroupBar = 1;            // named barrier of the two softmax groups
+constexpr int kGroupThreads = 256;
 
 constexpr uint32_t kIdescS = tc::idesc_bf16_f32(kRows, kKeys, false);  // Q K^T, both K-major
 constexpr uint32_t kIdescO = tc::idesc_bf16_f32(kRows, kD, true);      // P V, V is MN-major
+
+__host__ __device__ constexpr uint32_t s_col(int g, int b) { return (uint32_t)(g * 2 + b) * kKeys; }
+__host__ __device__ constexpr uint32_t o_col(int g) { return 256u + (uint32_t)g * kD; }
 
 struct TcSmem {
   uint8_t q[2][2][kQHalf];              // [buffer][D half]
   uint8_t k[kStagesTc][2][kKVHalf];     // [stage][D half]
   uint8_t v[kStagesTc][2][kKVHalf];     // [stage][D half], rows = keys
-  uint8_t p[2][kQHalf];                 // [buffer]: 128 rows x 64 keys
+  uint8_t p[2][kQHalf];                 // [softmax group]: 128 rows x 64 keys
+  float ml1[2][kRows];                  // group 1's running max and sum per row
+  int bt_cache[2][kBtCache];            // block ids of the current and the next item
   uint64_t kv_full[kStagesTc];
   uint64_t kv_empty[kStagesTc];
   uint64_t q_full[2], q_free[2];
-  uint64_t s_full[2], s_free[2];
-  uint64_t p_full[2], o_done[2];
+  uint64_t s_full[2][2], s_free[2][2];  // [group][buffer]
+  uint64_t p_full[2], o_done[2];        // [group]
   uint64_t o_free, drain;
   uint32_t tmem_base;
   int issued[kStagesTc];
@@ -80,6 +90,20 @@ __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
 
 __device__ __forceinline__ uint32_t ph(int n, int ring) { return (uint32_t)(n / ring) & 1u; }
 
+// The two softmax groups agree on `ok` (AND) at their named barrier.
+__device__ __forceinline__ bool groups_all(bool ok) {
+  uint32_t r;
+  asm volatile(
+      "{\n\t.reg .pred p, q;\n\t"
+      "setp.ne.u32 p, %1, 0;\n\t"
+      "bar.red.and.pred q, %2, %3, p;\n\t"
+      "selp.u32 %0, 1, 0, q;\n\t}"
+      : "=r"(r)
+      : "r"((uint32_t)ok), "n"(kGroupBar), "n"(kGroupThreads)
+      : "memory");
+  return r != 0;
+}
+
 __global__ void __launch_bounds__(kThreadsTc, 1)
     tc_kernel(const __grid_constant__ AttnArgs a, const __grid_constant__ CUtensorMap kmap,
               const __grid_constant__ CUtensorMap vmap, const __grid_constant__ CUtensorMap qmap,
@@ -99,10 +123,12 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
     for (int b = 0; b < 2; ++b) {
       mbar_init(&sm.q_full[b], 1);
       mbar_init(&sm.q_free[b], 1);
-      mbar_init(&sm.s_full[b], 1);
-      mbar_init(&sm.s_free[b], kRows);
       mbar_init(&sm.p_full[b], kRows);
       mbar_init(&sm.o_done[b], 1);
+      for (int c = 0; c < 2; ++c) {
+        mbar_init(&sm.s_full[b][c], 1);
+        mbar_init(&sm.s_free[b][c], kRows);
+      }
       sm.q_issued[b] = 0;
       sm.q_consumed[b] = 0;
     }
@@ -131,8 +157,28 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
     const uint32_t piece_bytes = (uint32_t)box_t * 128u;  // one D half of one piece
     int n = 0, k = 0;                                     // global tile / item counters
     bool ok = true;
+    // block ids are staged one item ahead: registers -> shared cache at the switch
+    int nb[kBtPerLane];
+    Item item_next{};
+    if ((int)blockIdx.x < n_items) {
+      const Item f = items[blockIdx.x];
+      bt_prefetch(a.block_table + (int64_t)f.seq * a.max_blocks, a.max_blocks,
+                  bt_window(f.kv_begin, f.kv_end, a.block_size), lane, nb);
+      bt_store(sm.bt_cache[0], nb, lane);
+      if ((int)blockIdx.x + G < n_items) item_next = items[blockIdx.x + G];
+    }
+    __syncwarp();
     for (int it = blockIdx.x; it < n_items && ok; it += G, ++k) {
       const Item item = items[it];
+      const BtWindow win = bt_window(item.kv_begin, item.kv_end, a.block_size);
+      const int* cache = sm.bt_cache[k & 1];
+      const bool has_next = it + G < n_items;
+      Item item_after{};
+      if (has_next) {
+        bt_prefetch(a.block_table + (int64_t)item_next.seq * a.max_blocks, a.max_blocks,
+                    bt_window(item_next.kv_begin, item_next.kv_end, a.block_size), lane, nb);
+        if (it + 2 * G < n_items) item_after = items[it + 2 * G];
+      }
       // the item's 128 Q rows: tokens x the g heads of its KV head, one box per D half
       {
         const int qb = k & 1;
@@ -158,16 +204,14 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
           const int j0 = t0 + lane * box_t;
           if (j0 < item.kv_end) {
             const int lb = j0 / a.block_size;
-            if (lb >= a.max_blocks) {
+            const int phys = bt_lookup(cache, win, bt, a.max_blocks, lb);
+            if (phys == -2) {
               record_error(a.err, PA_DEVERR_TABLE_RANGE);
+            } else if (phys < 0 || phys >= a.num_blocks) {
+              record_error(a.err, PA_DEVERR_BLOCK_RANGE);
             } else {
-              const int phys = __ldg(bt + lb);
-              if (phys < 0 || phys >= a.num_blocks) {
-                record_error(a.err, PA_DEVERR_BLOCK_RANGE);
-              } else {
-                valid = true;
-                tok = phys * a.block_size + (j0 - lb * a.block_size);
-              }
+              valid = true;
+              tok = phys * a.block_size + (j0 - lb * a.block_size);
             }
           }
         }
@@ -183,69 +227,79 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
         }
         if (lane == 0) sm.issued[st] += 1;
       }
+      if (has_next) {
+        bt_store(sm.bt_cache[(k + 1) & 1], nb, lane);
+        item_next = item_after;
+      }
+      __syncwarp();
     }
     if (!ok) sm.abort_flag = 1;
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0) {
-      int nS = 0, nP = 0, k = 0;
+      int nS = 0, nP = 0, k = 0;       // global tiles whose S / P V were issued; items
+      int cS[2] = {0, 0}, cP[2] = {0, 0};  // per softmax group
       bool ok = true;
       uint32_t q_addr = 0;
-      // S(tile nS) = Q K^T into TMEM buffer nS % 2
+      int js = 0, nt = 0;              // next tile of the item whose S is due; tiles of the item
+      // S(tile js) = Q K^T into the S buffer of group js % 2
       auto issue_s = [&]() -> bool {
         const int st = nS % kStagesTc;
-        const int sb = nS & 1;
+        const int g = js & 1;
+        const int b = cS[g] & 1;
         if (!mbar_wait(&sm.kv_full[st], ph(nS, kStagesTc), a.err)) return false;
         sm.consumed[st] += 1;
-        if (!mbar_wait(&sm.s_free[sb], ph(nS, 2) ^ 1u, a.err)) return false;
+        if (!mbar_wait(&sm.s_free[g][b], ph(cS[g], 2) ^ 1u, a.err)) return false;
         tc::fence_after_sync();
         const uint32_t k_addr = smem_addr(&sm.k[st][0][0]);
 #pragma unroll
         for (int kk = 0; kk < kD / 16; ++kk) {
           const uint32_t qo = (uint32_t)(kk >> 2) * kQHalf + (uint32_t)(kk & 3) * 32u;
           const uint32_t ko = (uint32_t)(kk >> 2) * kKVHalf + (uint32_t)(kk & 3) * 32u;
-          tc::mma_bf16(tmem + (uint32_t)sb * kKeys, tc::smem_desc_sw128(q_addr + qo, 16, 1024),
+          tc::mma_bf16(tmem + s_col(g, b), tc::smem_desc_sw128(q_addr + qo, 16, 1024),
                        tc::smem_desc_sw128(k_addr + ko, 16, 1024), kIdescS, kk > 0);
         }
-        tc::commit(&sm.s_full[sb]);
+        tc::commit(&sm.s_full[g][b]);
+        ++cS[g];
         ++nS;
+        ++js;
+        if (js == nt) tc::commit(&sm.q_free[k & 1]);  // the item's last S: Q may be reloaded
         return true;
       };
       for (int it = blockIdx.x; it < n_items && ok; it += G, ++k) {
         const Item item = items[it];
-        const int nt = (item.kv_end - item.kv_begin + kKeys - 1) / kKeys;
+        nt = (item.kv_end - item.kv_begin + kKeys - 1) / kKeys;
+        js = 0;
         const int qb = k & 1;
         if (!mbar_wait(&sm.q_full[qb], ph(k, 2), a.err)) { ok = false; break; }
         sm.q_consumed[qb] += 1;
         tc::fence_after_sync();
         q_addr = smem_addr(&sm.q[qb][0][0]);
         if (!issue_s()) { ok = false; break; }
-        if (nt == 1) tc::commit(&sm.q_free[qb]);
+        if (js < nt && !issue_s()) { ok = false; break; }
         for (int j = 0; j < nt; ++j) {
-          if (j + 1 < nt) {
-            if (!issue_s()) { ok = false; break; }
-            if (j + 2 == nt) tc::commit(&sm.q_free[qb]);  // last S of the item issued
-          }
-          // O += P_j V_j
-          const int pb = nP & 1;
-          if (!mbar_wait(&sm.p_full[pb], ph(nP, 2), a.err)) { ok = false; break; }
+          // O_g += P_j V_j, g = j % 2
+          const int g = j & 1;
+          if (!mbar_wait(&sm.p_full[g], (uint32_t)cP[g] & 1u, a.err)) { ok = false; break; }
           if (j == 0 && !mbar_wait(&sm.o_free, ((uint32_t)k & 1u) ^ 1u, a.err)) {
             ok = false;
             break;
           }
           tc::fence_after_sync();
           const int st = nP % kStagesTc;
-          const uint32_t p_addr = smem_addr(&sm.p[pb][0]);
+          const uint32_t p_addr = smem_addr(&sm.p[g][0]);
           const uint32_t v_addr = smem_addr(&sm.v[st][0][0]);
 #pragma unroll
           for (int kk = 0; kk < kKeys / 16; ++kk) {
-            tc::mma_bf16(tmem + kTmemO, tc::smem_desc_sw128(p_addr + (uint32_t)kk * 32u, 16, 1024),
+            tc::mma_bf16(tmem + o_col(g), tc::smem_desc_sw128(p_addr + (uint32_t)kk * 32u, 16, 1024),
                          tc::smem_desc_sw128(v_addr + (uint32_t)kk * 16u * 128u, kKVHalf, 1024),
-                         kIdescO, (j > 0) || (kk > 0));
+                         kIdescO, (j >= 2) || (kk > 0));
           }
-          tc::commit(&sm.o_done[pb]);
+          tc::commit(&sm.o_done[g]);
           tc::commit(&sm.kv_empty[st]);
+          ++cP[g];
           ++nP;
+          if (js < nt && !issue_s()) { ok = false; break; }
         }
       }
       if (!ok) sm.abort_flag = 1;
@@ -255,13 +309,15 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
     }
     __syncwarp();
   } else {
-    // ------------------------------------------------------------ softmax / epilogue
+    // ------------------------------------------------------------ softmax groups
+    const int g = (warp - 2) >> 2;                // softmax group 0 or 1
     const int quad = warp & 3;                    // TMEM lane quadrant of this warp
     const int row = quad * 32 + lane;             // tile row = TMEM lane
     const uint32_t t_lane = tmem + ((uint32_t)(quad * 32) << 16);
-    int n = 0;
+    int cnt = 0;                                  // tiles this group has processed
+    int n_base = 0;                               // global index of the item's first tile
     bool ok = true;
-    for (int it = blockIdx.x; it < n_items && ok; it += G) {
+    for (int it = blockIdx.x; it < n_items; it += G) {
       const Item item = items[it];
       const int nt = (item.kv_end - item.kv_begin + kKeys - 1) / kKeys;
       const bool live = row < item.row_count;
@@ -273,18 +329,19 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
         const int L = __ldg(a.context_lens + item.seq);
         const int ql = __ldg(a.query_lens + item.seq);
         lim = min(item.kv_end - 1, L - ql + t);
-        if (item.kv_end > L || item.row_begin + item.row_count > ql * a.g)
+        if (g == 0 && (item.kv_end > L || item.row_begin + item.row_count > ql * a.g))
           record_error(a.err, PA_DEVERR_LENS);
       }
       float m_used = -INFINITY, l = 0.f;
-      for (int j = 0; j < nt; ++j, ++n) {
-        const int sb = n & 1;
-        if (!mbar_wait(&sm.s_full[sb], ph(n, 2), a.err)) { ok = false; break; }
+      bool first = true;
+      for (int j = g; j < nt && ok; j += 2) {
+        const int b = cnt & 1;
+        if (!mbar_wait(&sm.s_full[g][b], ph(cnt, 2), a.err)) { ok = false; break; }
         tc::fence_after_sync();
         float s[kKeys];
-        tc::tmem_ld64(t_lane + (uint32_t)sb * kKeys, s);
+        tc::tmem_ld64(t_lane + s_col(g, b), s);
         tc::fence_before_sync();
-        mbar_arrive(&sm.s_free[sb]);
+        mbar_arrive(&sm.s_free[g][b]);
         // running max of the raw scores (the scale is positive, so it commutes with max);
         // only a tile that crosses this row's causal limit needs the mask
         const int key0 = item.kv_begin + j * kKeys;
@@ -300,34 +357,27 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
         const float mx = fmaxf(fmaxf(fmaxf(mx8[0], mx8[1]), fmaxf(mx8[2], mx8[3])),
                                fmaxf(fmaxf(mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7])));
         const float m_new = fmaxf(m_used, mx * a.scale_log2);
+        // this group's previous P V must be done before its O or P are touched
+        if (!first) {
+          if (!mbar_wait(&sm.o_done[g], (uint32_t)(cnt - 1) & 1u, a.err)) { ok = false; break; }
+          tc::fence_after_sync();
+        }
         if (m_used == -INFINITY) {
           m_used = m_new;  // nothing accumulated yet: O holds only zero rows
         } else if (m_new > m_used + kRescaleLog2) {
-          // the previous P V must be done before O is touched
-          if (!mbar_wait(&sm.o_done[(n - 1) & 1], ph(n - 1, 2), a.err)) { ok = false; break; }
-          tc::fence_after_sync();
           const float alpha = fast_exp2(m_used - m_new);
+#pragma unroll 1
+          for (int c4 = 0; c4 < kD / 32; ++c4) {
+            float o[32];
+            const uint32_t addr = t_lane + o_col(g) + (uint32_t)c4 * 32u;
+            tc::tmem_ld32(addr, o);
 #pragma unroll
-          for (int c2 = 0; c2 < kD / 64; ++c2) {
-            float o[64];
-            const uint32_t addr = t_lane + kTmemO + (uint32_t)c2 * 64u;
-            tc::tmem_ld64(addr, o);
-            float o0[32], o1[32];
-#pragma unroll
-            for (int i = 0; i < 32; ++i) {
-              o0[i] = o[i] * alpha;
-              o1[i] = o[32 + i] * alpha;
-            }
-            tc::tmem_st32(addr, o0);
-            tc::tmem_st32(addr + 32u, o1);
+            for (int i = 0; i < 32; ++i) o[i] *= alpha;
+            tc::tmem_st32(addr, o);
           }
           tc::tmem_wait_st();
           l *= alpha;
           m_used = m_new;
-        }
-        // P buffer sb was last read by P V two tiles ago
-        if (j >= 2) {
-          if (!mbar_wait(&sm.o_done[sb], ph(n - 2, 2), a.err)) { ok = false; break; }
         }
         // P = 2^(scale * s - m) in bf16, written as the swizzled A operand of the next MMA.
         // A masked score is -inf and gives exactly 0; with no visible key yet every
@@ -347,13 +397,13 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
           w.y = pack_bf16(p[2], p[3]);
           w.z = pack_bf16(p[4], p[5]);
           w.w = pack_bf16(p[6], p[7]);
-          *reinterpret_cast<uint4*>(&sm.p[sb][tc::sw128_offset(row, c8)]) = w;
+          *reinterpret_cast<uint4*>(&sm.p[g][tc::sw128_offset(row, c8)]) = w;
         }
         l += ((sum8[0] + sum8[1]) + (sum8[2] + sum8[3])) + ((sum8[4] + sum8[5]) + (sum8[6] + sum8[7]));
         // keys past the item's range hold whatever the block tail holds: zero those
         // V rows so that 0 * (non-finite) never reaches the accumulator
         if (row < kKeys && key0 + row >= item.kv_end) {
-          const int st = n % kStagesTc;
+          const int st = (n_base + j) % kStagesTc;
           uint4* v0 = reinterpret_cast<uint4*>(&sm.v[st][0][row * 128]);
           uint4* v1 = reinterpret_cast<uint4*>(&sm.v[st][1][row * 128]);
 #pragma unroll
@@ -364,57 +414,82 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
         }
         tc::fence_async_shared();
         tc::fence_before_sync();
-        mbar_arrive(&sm.p_full[sb]);
+        mbar_arrive(&sm.p_full[g]);
+        ++cnt;
+        first = false;
       }
-      if (!ok) break;
-      // ---- epilogue: O / l
-      if (!mbar_wait(&sm.o_done[(n - 1) & 1], ph(n - 1, 2), a.err)) { ok = false; break; }
-      tc::fence_after_sync();
-      float o[kD];
-      {
-        float o0[64], o1[64];
-        tc::tmem_ld64(t_lane + kTmemO, o0);
-        tc::tmem_ld64(t_lane + kTmemO + 64u, o1);
+      // ---- end of the item: this group's last P V, then merge the two groups
+      if (ok && !first) {
+        ok = mbar_wait(&sm.o_done[g], (uint32_t)(cnt - 1) & 1u, a.err);
+        tc::fence_after_sync();
+      }
+      // group 1 owns tiles 1, 3, ...: it publishes (m, l) only for items where it has some,
+      // so it can never overwrite values group 0 has not read yet (its next write needs
+      // a P V that waits for group 0's o_free)
+      const bool has1 = nt > 1;
+      if (g == 1 && has1) {
+        sm.ml1[0][row] = m_used;
+        sm.ml1[1][row] = l;
+      }
+      if (!groups_all(ok)) { ok = false; break; }
+      n_base += nt;
+      if (g == 1) continue;
+      const float m1 = has1 ? sm.ml1[0][row] : -INFINITY;
+      const float l1 = has1 ? sm.ml1[1][row] : 0.f;
+      const float M = fmaxf(m_used, m1);
+      const float a0 = (M == -INFINITY) ? 0.f : fast_exp2(m_used - M);
+      const float a1 = (!has1 || M == -INFINITY || m1 == -INFINITY) ? 0.f : fast_exp2(m1 - M);
+      const float Lsum = a0 * l + a1 * l1;
+      const float inv = (item.part < 0 && Lsum > 0.f) ? 1.f / Lsum : 1.f;
+      const float w0 = a0 * inv, w1 = a1 * inv;
+      float* out_f = nullptr;
+      __nv_bfloat16* out_h = nullptr;
+      if (live) {
+        if (item.part < 0) {
+          const int64_t off = ((int64_t)(item.q_row0 + t) * a.Hq + h) * kD;
+          if (a.out_bf16)
+            out_h = reinterpret_cast<__nv_bfloat16*>(a.out) + off;
+          else
+            out_f = reinterpret_cast<float*>(a.out) + off;
+        } else {
+          const int64_t prow = (int64_t)item.part + row;
+          out_f = a.part_acc + prow * kD;
+          a.part_ml[prow * 2 + 0] = M;
+          a.part_ml[prow * 2 + 1] = Lsum;
+        }
+      }
+#pragma unroll 1
+      for (int c4 = 0; c4 < kD / 32; ++c4) {
+        float o[32];
+        tc::tmem_ld32(t_lane + o_col(0) + (uint32_t)c4 * 32u, o);
 #pragma unroll
-        for (int i = 0; i < 64; ++i) {
-          o[i] = o0[i];
-          o[64 + i] = o1[i];
+        for (int i = 0; i < 32; ++i) o[i] *= w0;
+        if (has1) {
+          float o1[32];
+          tc::tmem_ld32(t_lane + o_col(1) + (uint32_t)c4 * 32u, o1);
+#pragma unroll
+          for (int i = 0; i < 32; ++i) o[i] = fmaf(w1, o1[i], o[i]);
+        }
+        if (out_f) {
+          float4* dst = reinterpret_cast<float4*>(out_f + c4 * 32);
+#pragma unroll
+          for (int i = 0; i < 8; ++i)
+            dst[i] = make_float4(o[4 * i], o[4 * i + 1], o[4 * i + 2], o[4 * i + 3]);
+        } else if (out_h) {
+          uint4* dst = reinterpret_cast<uint4*>(out_h + c4 * 32);
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            uint4 w;
+            w.x = pack_bf16(o[8 * i + 0], o[8 * i + 1]);
+            w.y = pack_bf16(o[8 * i + 2], o[8 * i + 3]);
+            w.z = pack_bf16(o[8 * i + 4], o[8 * i + 5]);
+            w.w = pack_bf16(o[8 * i + 6], o[8 * i + 7]);
+            dst[i] = w;
+          }
         }
       }
       tc::fence_before_sync();
       mbar_arrive(&sm.o_free);
-      if (live) {
-        if (item.part < 0) {
-          const float inv = (l > 0.f) ? 1.f / l : 0.f;
-          const int64_t off = ((int64_t)(item.q_row0 + t) * a.Hq + h) * kD;
-          if (a.out_bf16) {
-            uint4* dst = reinterpret_cast<uint4*>(reinterpret_cast<__nv_bfloat16*>(a.out) + off);
-#pragma unroll
-            for (int c8 = 0; c8 < kD / 8; ++c8) {
-              uint4 w;
-              w.x = pack_bf16(o[c8 * 8 + 0] * inv, o[c8 * 8 + 1] * inv);
-              w.y = pack_bf16(o[c8 * 8 + 2] * inv, o[c8 * 8 + 3] * inv);
-              w.z = pack_bf16(o[c8 * 8 + 4] * inv, o[c8 * 8 + 5] * inv);
-              w.w = pack_bf16(o[c8 * 8 + 6] * inv, o[c8 * 8 + 7] * inv);
-              dst[c8] = w;
-            }
-          } else {
-            float4* dst = reinterpret_cast<float4*>(reinterpret_cast<float*>(a.out) + off);
-#pragma unroll
-            for (int c4 = 0; c4 < kD / 4; ++c4)
-              dst[c4] = make_float4(o[c4 * 4] * inv, o[c4 * 4 + 1] * inv, o[c4 * 4 + 2] * inv,
-                                    o[c4 * 4 + 3] * inv);
-          }
-        } else {
-          const int64_t prow = (int64_t)item.part + row;
-          float4* dst = reinterpret_cast<float4*>(a.part_acc + prow * kD);
-#pragma unroll
-          for (int c4 = 0; c4 < kD / 4; ++c4)
-            dst[c4] = make_float4(o[c4 * 4], o[c4 * 4 + 1], o[c4 * 4 + 2], o[c4 * 4 + 3]);
-          a.part_ml[prow * 2 + 0] = m_used;
-          a.part_ml[prow * 2 + 1] = l;
-        }
-      }
     }
     if (!ok) sm.abort_flag = 1;
   }
