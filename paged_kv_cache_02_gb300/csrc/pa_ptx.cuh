@@ -71,6 +71,13 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, int* e
   }
 }
 
+// mbar_wait executed by every lane of a warp, with one verdict for the whole warp:
+// warp-collective instructions that follow (shuffles, ballots, tcgen05.ld / st)
+// then never see a warp split by a wait that ran out in some lanes only.
+__device__ __forceinline__ bool mbar_wait_warp(uint64_t* bar, uint32_t parity, int* err) {
+  return __all_sync(0xffffffffu, mbar_wait(bar, parity, err));
+}
+
 // 3-D tiled TMA load into shared memory, completing on `bar` (tx bytes).
 __device__ __forceinline__ void tma_load_3d(void* dst, const CUtensorMap* map, uint64_t* bar,
                                             int c0, int c1, int c2) {

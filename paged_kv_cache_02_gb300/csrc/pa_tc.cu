@@ -8,25 +8,25 @@
 // context that lives in non-contiguous blocks, with the causal mask fused so
 // that the score matrix is never written to memory.
 //
-// How (GB300): one persistent CTA per SM, warp-specialised, 10 warps.
+// How (GB300): one persistent CTA per SM, warp-specialised, 7 warps.
 //   warp 0     TMA producer: the item's 128 Q rows (one 3-D box per D half,
-//              double-buffered across items) and, per 64-key tile, one 3-D
+//              double-buffered across items) and, per 128-key tile, one 3-D
 //              TMA copy per (block piece, D half, K or V) straight from the
 //              physical blocks named by the block table, 128-byte swizzled,
-//              into a 3-stage ring.
-//   warp 1     allocates TMEM and issues tcgen05.mma from one thread. Tile j
-//              of an item belongs to softmax group j % 2; S(j+2) = Q K^T is
-//              issued right after O_g += P_j V_j, so the tensor core always has
-//              the next scores of both groups queued.
-//   warps 2-5  softmax group 0, warps 6-9 softmax group 1: one thread per row
-//              (its TMEM lane). Each group runs an online softmax over its
-//              own tiles (an exact split of the keys): mask (causal,
-//              bottom-right aligned), log2-domain exp, bf16 P written swizzled
-//              as the next MMA's A operand, O rescaled in TMEM only when the
-//              group's running maximum grows by more than 2^8. At the end of an
-//              item group 0 merges both groups' (m, l, O) and writes the output.
-// TMEM (512 columns): S double buffer of group g at [128 g, 128 g + 128),
-// O of group g at [256 + 128 g, 384 + 128 g). Every wait is bounded.
+//              into a 2-stage ring. Block ids come from a shared-memory cache
+//              filled one item ahead.
+//   warp 1     issues S_j = Q K_j^T (tcgen05.mma, both operands in shared
+//              memory, M = N = 128) into TMEM buffer j % 2.
+//   warp 2     issues O += P_j V_j with P_j read from TMEM (the softmax writes
+//              it over S_j as bf16) and V_j from shared memory. Two issuing
+//              warps keep the tensor core fed: one thread alone cannot issue
+//              these instructions as fast as they execute.
+//   warps 3-6  one thread per row (its TMEM lane): mask (causal, bottom-right
+//              aligned), online softmax in the log2 domain, P to TMEM,
+//              O rescaled in TMEM only when the running maximum grows by more
+//              than 2^8, output O / l. Warps whose rows all lie past the item's
+//              rows skip the arithmetic.
+// TMEM columns: S/P double buffer [0, 256), O [256, 384). Every wait is bounded.
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
@@ -41,36 +41,30 @@ namespace pa {
 namespace {
 
 constexpr int kRows = kTcRows;          // 128 rows per tile (M)
-constexpr int kKeys = 64;               // keys per tile (N of S, K of P V)
+constexpr int kKeys = 128;              // keys per tile (N of S, K of P V)
 constexpr int kD = 128;                 // head dim of this kernel
-constexpr int kStagesTc = 3;
-constexpr int kThreadsTc = 320;
-constexpr int kQHalf = kRows * 128;     // 128 rows x 64 elements, swizzled (16 KB)
-constexpr int kKVHalf = kKeys * 128;    // 64 keys x 64 elements, swizzled (8 KB)
+constexpr int kStagesTc = 2;
+constexpr int kThreadsTc = 224;
+constexpr int kHalf = 128 * 128;        // 128 rows x 64 elements, swizzled (16 KB)
 constexpr float kRescaleLog2 = 8.f;     // O is rescaled once the max grows by > 2^8
 constexpr uint32_t kTmemCols = 512;
-constexpr int kGroupBar = 1;            // named barrier of the two softmax groups
-constexpr int kGroupThreads = 256;
+constexpr uint32_t kTmemO = 256;        // first column of O
 
 constexpr uint32_t kIdescS = tc::idesc_bf16_f32(kRows, kKeys, false);  // Q K^T, both K-major
 constexpr uint32_t kIdescO = tc::idesc_bf16_f32(kRows, kD, true);      // P V, V is MN-major
 
-__host__ __device__ constexpr uint32_t s_col(int g, int b) { return (uint32_t)(g * 2 + b) * kKeys; }
-__host__ __device__ constexpr uint32_t o_col(int g) { return 256u + (uint32_t)g * kD; }
-
 struct TcSmem {
-  uint8_t q[2][2][kQHalf];              // [buffer][D half]
-  uint8_t k[kStagesTc][2][kKVHalf];     // [stage][D half]
-  uint8_t v[kStagesTc][2][kKVHalf];     // [stage][D half], rows = keys
-  uint8_t p[2][kQHalf];                 // [softmax group]: 128 rows x 64 keys
-  float ml1[2][kRows];                  // group 1's running max and sum per row
+  uint8_t q[2][2][kHalf];               // [buffer][D half]
+  uint8_t k[kStagesTc][2][kHalf];       // [stage][D half], rows = keys
+  uint8_t v[kStagesTc][2][kHalf];       // [stage][D half], rows = keys
   int bt_cache[2][kBtCache];            // block ids of the current and the next item
   uint64_t kv_full[kStagesTc];
   uint64_t kv_empty[kStagesTc];
   uint64_t q_full[2], q_free[2];
-  uint64_t s_full[2][2], s_free[2][2];  // [group][buffer]
-  uint64_t p_full[2], o_done[2];        // [group]
-  uint64_t o_free, drain;
+  uint64_t s_full[2], s_free[2], p_full[2];
+  uint64_t o_done[2];                   // P V of tiles with this parity done (one barrier per
+                                        // parity, so a waiter is never two phases behind)
+  uint64_t o_free, drain[2];
   uint32_t tmem_base;
   int issued[kStagesTc];
   int consumed[kStagesTc];
@@ -90,18 +84,8 @@ __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
 
 __device__ __forceinline__ uint32_t ph(int n, int ring) { return (uint32_t)(n / ring) & 1u; }
 
-// The two softmax groups agree on `ok` (AND) at their named barrier.
-__device__ __forceinline__ bool groups_all(bool ok) {
-  uint32_t r;
-  asm volatile(
-      "{\n\t.reg .pred p, q;\n\t"
-      "setp.ne.u32 p, %1, 0;\n\t"
-      "bar.red.and.pred q, %2, %3, p;\n\t"
-      "selp.u32 %0, 1, 0, q;\n\t}"
-      : "=r"(r)
-      : "r"((uint32_t)ok), "n"(kGroupBar), "n"(kGroupThreads)
-      : "memory");
-  return r != 0;
+__device__ __forceinline__ int tiles_of(const Item& x) {
+  return (x.kv_end - x.kv_begin + kKeys - 1) / kKeys;
 }
 
 __global__ void __launch_bounds__(kThreadsTc, 1)
@@ -123,17 +107,16 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
     for (int b = 0; b < 2; ++b) {
       mbar_init(&sm.q_full[b], 1);
       mbar_init(&sm.q_free[b], 1);
+      mbar_init(&sm.s_full[b], 1);
+      mbar_init(&sm.s_free[b], 1);
       mbar_init(&sm.p_full[b], kRows);
-      mbar_init(&sm.o_done[b], 1);
-      for (int c = 0; c < 2; ++c) {
-        mbar_init(&sm.s_full[b][c], 1);
-        mbar_init(&sm.s_free[b][c], kRows);
-      }
+      mbar_init(&sm.drain[b], 1);
       sm.q_issued[b] = 0;
       sm.q_consumed[b] = 0;
     }
+    mbar_init(&sm.o_done[0], 1);
+    mbar_init(&sm.o_done[1], 1);
     mbar_init(&sm.o_free, kRows);
-    mbar_init(&sm.drain, 1);
     sm.abort_flag = 0;
     fence_barrier_init();
   }
@@ -153,7 +136,7 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
       prefetch_tensormap(&vmap);
       prefetch_tensormap(&qmap);
     }
-    const int pieces = kKeys / box_t;                     // <= 8
+    const int pieces = kKeys / box_t;                     // <= 16
     const uint32_t piece_bytes = (uint32_t)box_t * 128u;  // one D half of one piece
     int n = 0, k = 0;                                     // global tile / item counters
     bool ok = true;
@@ -182,10 +165,10 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
       // the item's 128 Q rows: tokens x the g heads of its KV head, one box per D half
       {
         const int qb = k & 1;
-        ok = mbar_wait(&sm.q_free[qb], ph(k, 2) ^ 1u, a.err);
+        ok = mbar_wait_warp(&sm.q_free[qb], ph(k, 2) ^ 1u, a.err);
         if (!ok || *(volatile int*)&sm.abort_flag) { ok = false; break; }
         if (lane == 0) {
-          mbar_arrive_expect_tx(&sm.q_full[qb], 2u * kQHalf);
+          mbar_arrive_expect_tx(&sm.q_full[qb], 2u * kHalf);
           const int tok = item.q_row0 + item.row_begin / a.g;
           tma_load_3d(&sm.q[qb][0][0], &qmap, &sm.q_full[qb], 0, item.kv_head * a.g, tok);
           tma_load_3d(&sm.q[qb][1][0], &qmap, &sm.q_full[qb], 64, item.kv_head * a.g, tok);
@@ -196,7 +179,7 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
       const int32_t* bt = a.block_table + (int64_t)item.seq * a.max_blocks;
       for (int t0 = item.kv_begin; t0 < item.kv_end; t0 += kKeys, ++n) {
         const int st = n % kStagesTc;
-        ok = mbar_wait(&sm.kv_empty[st], ph(n, kStagesTc) ^ 1u, a.err);
+        ok = mbar_wait_warp(&sm.kv_empty[st], ph(n, kStagesTc) ^ 1u, a.err);
         if (!ok || *(volatile int*)&sm.abort_flag) { ok = false; break; }
         bool valid = false;
         int tok = 0;
@@ -235,92 +218,85 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
     }
     if (!ok) sm.abort_flag = 1;
   } else if (warp == 1) {
-    // ------------------------------------------------------------ MMA issuer
+    // ------------------------------------------------------------ S issuer
     if (lane == 0) {
-      int nS = 0, nP = 0, k = 0;       // global tiles whose S / P V were issued; items
-      int cS[2] = {0, 0}, cP[2] = {0, 0};  // per softmax group
+      int n = 0, k = 0;
       bool ok = true;
-      uint32_t q_addr = 0;
-      int js = 0, nt = 0;              // next tile of the item whose S is due; tiles of the item
-      // S(tile js) = Q K^T into the S buffer of group js % 2
-      auto issue_s = [&]() -> bool {
-        const int st = nS % kStagesTc;
-        const int g = js & 1;
-        const int b = cS[g] & 1;
-        if (!mbar_wait(&sm.kv_full[st], ph(nS, kStagesTc), a.err)) return false;
-        sm.consumed[st] += 1;
-        if (!mbar_wait(&sm.s_free[g][b], ph(cS[g], 2) ^ 1u, a.err)) return false;
-        tc::fence_after_sync();
-        const uint32_t k_addr = smem_addr(&sm.k[st][0][0]);
-#pragma unroll
-        for (int kk = 0; kk < kD / 16; ++kk) {
-          const uint32_t qo = (uint32_t)(kk >> 2) * kQHalf + (uint32_t)(kk & 3) * 32u;
-          const uint32_t ko = (uint32_t)(kk >> 2) * kKVHalf + (uint32_t)(kk & 3) * 32u;
-          tc::mma_bf16(tmem + s_col(g, b), tc::smem_desc_sw128(q_addr + qo, 16, 1024),
-                       tc::smem_desc_sw128(k_addr + ko, 16, 1024), kIdescS, kk > 0);
-        }
-        tc::commit(&sm.s_full[g][b]);
-        ++cS[g];
-        ++nS;
-        ++js;
-        if (js == nt) tc::commit(&sm.q_free[k & 1]);  // the item's last S: Q may be reloaded
-        return true;
-      };
       for (int it = blockIdx.x; it < n_items && ok; it += G, ++k) {
-        const Item item = items[it];
-        nt = (item.kv_end - item.kv_begin + kKeys - 1) / kKeys;
-        js = 0;
+        const int nt = tiles_of(items[it]);
         const int qb = k & 1;
         if (!mbar_wait(&sm.q_full[qb], ph(k, 2), a.err)) { ok = false; break; }
         sm.q_consumed[qb] += 1;
         tc::fence_after_sync();
-        q_addr = smem_addr(&sm.q[qb][0][0]);
-        if (!issue_s()) { ok = false; break; }
-        if (js < nt && !issue_s()) { ok = false; break; }
-        for (int j = 0; j < nt; ++j) {
-          // O_g += P_j V_j, g = j % 2
-          const int g = j & 1;
-          if (!mbar_wait(&sm.p_full[g], (uint32_t)cP[g] & 1u, a.err)) { ok = false; break; }
+        const uint32_t q_addr = smem_addr(&sm.q[qb][0][0]);
+        for (int j = 0; j < nt; ++j, ++n) {
+          const int st = n % kStagesTc;
+          const int b = n & 1;
+          if (!mbar_wait(&sm.kv_full[st], ph(n, kStagesTc), a.err)) { ok = false; break; }
+          sm.consumed[st] += 1;
+          if (!mbar_wait(&sm.s_free[b], ph(n, 2) ^ 1u, a.err)) { ok = false; break; }
+          tc::fence_after_sync();
+          const uint32_t k_addr = smem_addr(&sm.k[st][0][0]);
+#pragma unroll
+          for (int kk = 0; kk < kD / 16; ++kk) {
+            const uint32_t off = (uint32_t)(kk >> 2) * kHalf + (uint32_t)(kk & 3) * 32u;
+            tc::mma_bf16(tmem + (uint32_t)b * kKeys, tc::smem_desc_sw128(q_addr + off, 16, 1024),
+                         tc::smem_desc_sw128(k_addr + off, 16, 1024), kIdescS, kk > 0);
+          }
+          tc::commit(&sm.s_full[b]);
+        }
+        if (ok) tc::commit(&sm.q_free[qb]);  // the item's last S issued: Q may be reloaded
+      }
+      if (!ok) sm.abort_flag = 1;
+      tc::commit(&sm.drain[0]);
+      mbar_wait(&sm.drain[0], 0, a.err);
+    }
+    __syncwarp();
+  } else if (warp == 2) {
+    // ------------------------------------------------------------ P V issuer
+    if (lane == 0) {
+      int n = 0, k = 0;
+      bool ok = true;
+      for (int it = blockIdx.x; it < n_items && ok; it += G, ++k) {
+        const int nt = tiles_of(items[it]);
+        for (int j = 0; j < nt; ++j, ++n) {
+          const int st = n % kStagesTc;
+          const int b = n & 1;
+          if (!mbar_wait(&sm.p_full[b], ph(n, 2), a.err)) { ok = false; break; }
           if (j == 0 && !mbar_wait(&sm.o_free, ((uint32_t)k & 1u) ^ 1u, a.err)) {
             ok = false;
             break;
           }
           tc::fence_after_sync();
-          const int st = nP % kStagesTc;
-          const uint32_t p_addr = smem_addr(&sm.p[g][0]);
           const uint32_t v_addr = smem_addr(&sm.v[st][0][0]);
 #pragma unroll
           for (int kk = 0; kk < kKeys / 16; ++kk) {
-            tc::mma_bf16(tmem + o_col(g), tc::smem_desc_sw128(p_addr + (uint32_t)kk * 32u, 16, 1024),
-                         tc::smem_desc_sw128(v_addr + (uint32_t)kk * 16u * 128u, kKVHalf, 1024),
-                         kIdescO, (j >= 2) || (kk > 0));
+            tc::mma_bf16_ts(tmem + kTmemO, tmem + (uint32_t)b * kKeys + (uint32_t)kk * 8u,
+                            tc::smem_desc_sw128(v_addr + (uint32_t)kk * 16u * 128u, kHalf, 1024),
+                            kIdescO, (j > 0) || (kk > 0));
           }
-          tc::commit(&sm.o_done[g]);
+          tc::commit(&sm.o_done[b]);
           tc::commit(&sm.kv_empty[st]);
-          ++cP[g];
-          ++nP;
-          if (js < nt && !issue_s()) { ok = false; break; }
+          tc::commit(&sm.s_free[b]);
         }
       }
       if (!ok) sm.abort_flag = 1;
-      // every MMA this thread issued has finished before the CTA moves on
-      tc::commit(&sm.drain);
-      mbar_wait(&sm.drain, 0, a.err);
+      tc::commit(&sm.drain[1]);
+      mbar_wait(&sm.drain[1], 0, a.err);
     }
     __syncwarp();
   } else {
-    // ------------------------------------------------------------ softmax groups
-    const int g = (warp - 2) >> 2;                // softmax group 0 or 1
+    // ------------------------------------------------------------ softmax / epilogue
     const int quad = warp & 3;                    // TMEM lane quadrant of this warp
     const int row = quad * 32 + lane;             // tile row = TMEM lane
     const uint32_t t_lane = tmem + ((uint32_t)(quad * 32) << 16);
-    int cnt = 0;                                  // tiles this group has processed
-    int n_base = 0;                               // global index of the item's first tile
+    int n = 0;
     bool ok = true;
-    for (int it = blockIdx.x; it < n_items; it += G) {
+    for (int it = blockIdx.x; it < n_items && ok; it += G) {
       const Item item = items[it];
-      const int nt = (item.kv_end - item.kv_begin + kKeys - 1) / kKeys;
+      const int nt = tiles_of(item);
       const bool live = row < item.row_count;
+      const bool warp_live = quad * 32 < item.row_count;
       int t = 0, h = 0, lim = -1;
       if (live) {
         const int rho = item.row_begin + row;
@@ -329,81 +305,97 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
         const int L = __ldg(a.context_lens + item.seq);
         const int ql = __ldg(a.query_lens + item.seq);
         lim = min(item.kv_end - 1, L - ql + t);
-        if (g == 0 && (item.kv_end > L || item.row_begin + item.row_count > ql * a.g))
+        if (item.kv_end > L || item.row_begin + item.row_count > ql * a.g)
           record_error(a.err, PA_DEVERR_LENS);
       }
       float m_used = -INFINITY, l = 0.f;
-      bool first = true;
-      for (int j = g; j < nt && ok; j += 2) {
-        const int b = cnt & 1;
-        if (!mbar_wait(&sm.s_full[g][b], ph(cnt, 2), a.err)) { ok = false; break; }
+      for (int j = 0; j < nt; ++j, ++n) {
+        const int b = n & 1;
+        if (!mbar_wait_warp(&sm.s_full[b], ph(n, 2), a.err)) { ok = false; break; }
         tc::fence_after_sync();
-        float s[kKeys];
-        tc::tmem_ld64(t_lane + s_col(g, b), s);
-        tc::fence_before_sync();
-        mbar_arrive(&sm.s_free[g][b]);
-        // running max of the raw scores (the scale is positive, so it commutes with max);
-        // only a tile that crosses this row's causal limit needs the mask
         const int key0 = item.kv_begin + j * kKeys;
-        if (key0 + kKeys - 1 > lim) {
+        if (warp_live) {
+          float s[kKeys];
+          {
+            float s0[64], s1[64];
+            tc::tmem_ld64(t_lane + (uint32_t)b * kKeys, s0);
+            tc::tmem_ld64(t_lane + (uint32_t)b * kKeys + 64u, s1);
 #pragma unroll
-          for (int c = 0; c < kKeys; ++c) s[c] = (key0 + c <= lim) ? s[c] : -INFINITY;
-        }
-        float mx8[8];
+            for (int i = 0; i < 64; ++i) {
+              s[i] = s0[i];
+              s[64 + i] = s1[i];
+            }
+          }
+          // running max of the raw scores (the scale is positive, so it commutes with
+          // max); only a tile that crosses this row's causal limit needs the mask
+          if (key0 + kKeys - 1 > lim) {
 #pragma unroll
-        for (int i = 0; i < 8; ++i) mx8[i] = s[i];
+            for (int c = 0; c < kKeys; ++c) s[c] = (key0 + c <= lim) ? s[c] : -INFINITY;
+          }
+          float mx8[8];
 #pragma unroll
-        for (int c = 8; c < kKeys; ++c) mx8[c & 7] = fmaxf(mx8[c & 7], s[c]);
-        const float mx = fmaxf(fmaxf(fmaxf(mx8[0], mx8[1]), fmaxf(mx8[2], mx8[3])),
-                               fmaxf(fmaxf(mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7])));
-        const float m_new = fmaxf(m_used, mx * a.scale_log2);
-        // this group's previous P V must be done before its O or P are touched
-        if (!first) {
-          if (!mbar_wait(&sm.o_done[g], (uint32_t)(cnt - 1) & 1u, a.err)) { ok = false; break; }
-          tc::fence_after_sync();
-        }
-        if (m_used == -INFINITY) {
-          m_used = m_new;  // nothing accumulated yet: O holds only zero rows
-        } else if (m_new > m_used + kRescaleLog2) {
-          const float alpha = fast_exp2(m_used - m_new);
+          for (int i = 0; i < 8; ++i) mx8[i] = s[i];
+#pragma unroll
+          for (int c = 8; c < kKeys; ++c) mx8[c & 7] = fmaxf(mx8[c & 7], s[c]);
+          const float mx = fmaxf(fmaxf(fmaxf(mx8[0], mx8[1]), fmaxf(mx8[2], mx8[3])),
+                                 fmaxf(fmaxf(mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7])));
+          const float m_new = fmaxf(m_used, mx * a.scale_log2);
+          // nothing accumulated yet: O holds only zero rows, adopt the new maximum
+          if (m_used == -INFINITY) m_used = m_new;
+          // tcgen05.ld / st are warp-collective: the whole warp rescales when any of
+          // its rows needs it, the others with factor 1
+          const bool need = m_new > m_used + kRescaleLog2;
+          if (__any_sync(0xffffffffu, need)) {
+            // the previous P V must be done before O is rescaled
+            if (!mbar_wait_warp(&sm.o_done[(n - 1) & 1], ph(n - 1, 2), a.err)) { ok = false; break; }
+            tc::fence_after_sync();
+            const float alpha = need ? fast_exp2(m_used - m_new) : 1.f;
 #pragma unroll 1
-          for (int c4 = 0; c4 < kD / 32; ++c4) {
-            float o[32];
-            const uint32_t addr = t_lane + o_col(g) + (uint32_t)c4 * 32u;
-            tc::tmem_ld32(addr, o);
+            for (int c4 = 0; c4 < kD / 32; ++c4) {
+              float o[32];
+              const uint32_t addr = t_lane + kTmemO + (uint32_t)c4 * 32u;
+              tc::tmem_ld32(addr, o);
 #pragma unroll
-            for (int i = 0; i < 32; ++i) o[i] *= alpha;
-            tc::tmem_st32(addr, o);
+              for (int i = 0; i < 32; ++i) o[i] *= alpha;
+              tc::tmem_st32(addr, o);
+            }
+            if (need) {
+              l *= alpha;
+              m_used = m_new;
+            }
+          }
+          // P = 2^(scale * s - m) as bf16 pairs over the S columns: the A operand of P V.
+          // A masked score is -inf and gives exactly 0.
+          const float neg_m = (m_used == -INFINITY) ? 0.f : -m_used;
+          float sum8[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+          for (int h2 = 0; h2 < 2; ++h2) {
+            float pk[32];
+#pragma unroll
+            for (int c = 0; c < 32; ++c) {
+              const float p0 = fast_exp2(fmaf(s[h2 * 64 + 2 * c], a.scale_log2, neg_m));
+              const float p1 = fast_exp2(fmaf(s[h2 * 64 + 2 * c + 1], a.scale_log2, neg_m));
+              sum8[c & 7] += p0 + p1;
+              pk[c] = __uint_as_float(pack_bf16(p0, p1));
+            }
+            tc::tmem_st32(t_lane + (uint32_t)b * kKeys + (uint32_t)h2 * 32u, pk);
           }
           tc::tmem_wait_st();
-          l *= alpha;
-          m_used = m_new;
-        }
-        // P = 2^(scale * s - m) in bf16, written as the swizzled A operand of the next MMA.
-        // A masked score is -inf and gives exactly 0; with no visible key yet every
-        // score is -inf and the offset is irrelevant.
-        const float neg_m = (m_used == -INFINITY) ? 0.f : -m_used;
-        float sum8[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+          l += ((sum8[0] + sum8[1]) + (sum8[2] + sum8[3])) +
+               ((sum8[4] + sum8[5]) + (sum8[6] + sum8[7]));
+        } else {
+          // rows past the item: zero P, so that no stale bits reach the tensor core
+          float z[32];
 #pragma unroll
-        for (int c8 = 0; c8 < kKeys / 8; ++c8) {
-          float p[8];
-#pragma unroll
-          for (int i = 0; i < 8; ++i) {
-            p[i] = fast_exp2(fmaf(s[c8 * 8 + i], a.scale_log2, neg_m));
-            sum8[i] += p[i];
-          }
-          uint4 w;
-          w.x = pack_bf16(p[0], p[1]);
-          w.y = pack_bf16(p[2], p[3]);
-          w.z = pack_bf16(p[4], p[5]);
-          w.w = pack_bf16(p[6], p[7]);
-          *reinterpret_cast<uint4*>(&sm.p[g][tc::sw128_offset(row, c8)]) = w;
+          for (int c = 0; c < 32; ++c) z[c] = 0.f;
+          tc::tmem_st32(t_lane + (uint32_t)b * kKeys, z);
+          tc::tmem_st32(t_lane + (uint32_t)b * kKeys + 32u, z);
+          tc::tmem_wait_st();
         }
-        l += ((sum8[0] + sum8[1]) + (sum8[2] + sum8[3])) + ((sum8[4] + sum8[5]) + (sum8[6] + sum8[7]));
         // keys past the item's range hold whatever the block tail holds: zero those
         // V rows so that 0 * (non-finite) never reaches the accumulator
-        if (row < kKeys && key0 + row >= item.kv_end) {
-          const int st = (n_base + j) % kStagesTc;
+        if (key0 + row >= item.kv_end) {
+          const int st = n % kStagesTc;
           uint4* v0 = reinterpret_cast<uint4*>(&sm.v[st][0][row * 128]);
           uint4* v1 = reinterpret_cast<uint4*>(&sm.v[st][1][row * 128]);
 #pragma unroll
@@ -411,80 +403,57 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
             v0[i] = make_uint4(0, 0, 0, 0);
             v1[i] = make_uint4(0, 0, 0, 0);
           }
+          tc::fence_async_shared();
         }
-        tc::fence_async_shared();
         tc::fence_before_sync();
-        mbar_arrive(&sm.p_full[g]);
-        ++cnt;
-        first = false;
+        mbar_arrive(&sm.p_full[b]);
       }
-      // ---- end of the item: this group's last P V, then merge the two groups
-      if (ok && !first) {
-        ok = mbar_wait(&sm.o_done[g], (uint32_t)(cnt - 1) & 1u, a.err);
-        tc::fence_after_sync();
-      }
-      // group 1 owns tiles 1, 3, ...: it publishes (m, l) only for items where it has some,
-      // so it can never overwrite values group 0 has not read yet (its next write needs
-      // a P V that waits for group 0's o_free)
-      const bool has1 = nt > 1;
-      if (g == 1 && has1) {
-        sm.ml1[0][row] = m_used;
-        sm.ml1[1][row] = l;
-      }
-      if (!groups_all(ok)) { ok = false; break; }
-      n_base += nt;
-      if (g == 1) continue;
-      const float m1 = has1 ? sm.ml1[0][row] : -INFINITY;
-      const float l1 = has1 ? sm.ml1[1][row] : 0.f;
-      const float M = fmaxf(m_used, m1);
-      const float a0 = (M == -INFINITY) ? 0.f : fast_exp2(m_used - M);
-      const float a1 = (!has1 || M == -INFINITY || m1 == -INFINITY) ? 0.f : fast_exp2(m1 - M);
-      const float Lsum = a0 * l + a1 * l1;
-      const float inv = (item.part < 0 && Lsum > 0.f) ? 1.f / Lsum : 1.f;
-      const float w0 = a0 * inv, w1 = a1 * inv;
-      float* out_f = nullptr;
-      __nv_bfloat16* out_h = nullptr;
-      if (live) {
-        if (item.part < 0) {
-          const int64_t off = ((int64_t)(item.q_row0 + t) * a.Hq + h) * kD;
-          if (a.out_bf16)
-            out_h = reinterpret_cast<__nv_bfloat16*>(a.out) + off;
-          else
-            out_f = reinterpret_cast<float*>(a.out) + off;
-        } else {
-          const int64_t prow = (int64_t)item.part + row;
-          out_f = a.part_acc + prow * kD;
-          a.part_ml[prow * 2 + 0] = M;
-          a.part_ml[prow * 2 + 1] = Lsum;
+      if (!ok) break;
+      // ---- epilogue: O / l
+      if (!mbar_wait_warp(&sm.o_done[(n - 1) & 1], ph(n - 1, 2), a.err)) { ok = false; break; }
+      tc::fence_after_sync();
+      // tcgen05.ld is warp-collective: every lane of a live warp reads its row of O,
+      // only rows of the item are stored
+      if (warp_live) {
+        float* out_f = nullptr;
+        __nv_bfloat16* out_h = nullptr;
+        float inv = 1.f;
+        if (live) {
+          if (item.part < 0) {
+            inv = (l > 0.f) ? 1.f / l : 0.f;
+            const int64_t off = ((int64_t)(item.q_row0 + t) * a.Hq + h) * kD;
+            if (a.out_bf16)
+              out_h = reinterpret_cast<__nv_bfloat16*>(a.out) + off;
+            else
+              out_f = reinterpret_cast<float*>(a.out) + off;
+          } else {
+            const int64_t prow = (int64_t)item.part + row;
+            out_f = a.part_acc + prow * kD;
+            a.part_ml[prow * 2 + 0] = m_used;
+            a.part_ml[prow * 2 + 1] = l;
+          }
         }
-      }
 #pragma unroll 1
-      for (int c4 = 0; c4 < kD / 32; ++c4) {
-        float o[32];
-        tc::tmem_ld32(t_lane + o_col(0) + (uint32_t)c4 * 32u, o);
+        for (int c4 = 0; c4 < kD / 32; ++c4) {
+          float o[32];
+          tc::tmem_ld32(t_lane + kTmemO + (uint32_t)c4 * 32u, o);
+          if (out_f) {
+            float4* dst = reinterpret_cast<float4*>(out_f + c4 * 32);
 #pragma unroll
-        for (int i = 0; i < 32; ++i) o[i] *= w0;
-        if (has1) {
-          float o1[32];
-          tc::tmem_ld32(t_lane + o_col(1) + (uint32_t)c4 * 32u, o1);
+            for (int i = 0; i < 8; ++i)
+              dst[i] = make_float4(o[4 * i] * inv, o[4 * i + 1] * inv, o[4 * i + 2] * inv,
+                                   o[4 * i + 3] * inv);
+          } else if (out_h) {
+            uint4* dst = reinterpret_cast<uint4*>(out_h + c4 * 32);
 #pragma unroll
-          for (int i = 0; i < 32; ++i) o[i] = fmaf(w1, o1[i], o[i]);
-        }
-        if (out_f) {
-          float4* dst = reinterpret_cast<float4*>(out_f + c4 * 32);
-#pragma unroll
-          for (int i = 0; i < 8; ++i)
-            dst[i] = make_float4(o[4 * i], o[4 * i + 1], o[4 * i + 2], o[4 * i + 3]);
-        } else if (out_h) {
-          uint4* dst = reinterpret_cast<uint4*>(out_h + c4 * 32);
-#pragma unroll
-          for (int i = 0; i < 4; ++i) {
-            uint4 w;
-            w.x = pack_bf16(o[8 * i + 0], o[8 * i + 1]);
-            w.y = pack_bf16(o[8 * i + 2], o[8 * i + 3]);
-            w.z = pack_bf16(o[8 * i + 4], o[8 * i + 5]);
-            w.w = pack_bf16(o[8 * i + 6], o[8 * i + 7]);
-            dst[i] = w;
+            for (int i = 0; i < 4; ++i) {
+              uint4 w;
+              w.x = pack_bf16(o[8 * i + 0] * inv, o[8 * i + 1] * inv);
+              w.y = pack_bf16(o[8 * i + 2] * inv, o[8 * i + 3] * inv);
+              w.z = pack_bf16(o[8 * i + 4] * inv, o[8 * i + 5] * inv);
+              w.w = pack_bf16(o[8 * i + 6] * inv, o[8 * i + 7] * inv);
+              dst[i] = w;
+            }
           }
         }
       }
