@@ -253,8 +253,10 @@ def run_gpu(args, w, cfg_name, rank, local, world):
     q, kn, vn = w.q.to(dev), w.k_new.to(dev), w.v_new.to(dev)
     kp, vp = w.k_pool.to(dev), w.v_pool.to(dev)
     slots = torch.empty(len(w.new_seq), dtype=torch.int64, device=dev)
-    out = torch.empty(q.shape, dtype=torch.float32, device=dev)
-    plan_kw = dict(tc_min_rows=args.tc_min_rows, max_chunk_tokens=args.max_chunk)
+    out_dtype = torch.bfloat16 if args.out == "bf16" else torch.float32
+    out = torch.empty(q.shape, dtype=out_dtype, device=dev)
+    plan_kw = dict(tc_min_rows=args.tc_min_rows, max_chunk_tokens=args.max_chunk,
+                   tc_pair=args.tc_pair)
     plan = pa.Plan(w.context_lens, w.query_lens, w.Hq, w.Hkv, w.D, w.block_size, w.max_blocks,
                    **plan_kw)
     st = plan.stats()
@@ -315,12 +317,14 @@ def run_gpu(args, w, cfg_name, rank, local, world):
 
     T = w.total_q
     value = T * args.steps * world / (elapsed_ms / 1000.0)
+    n_tc1 = st["n_tc_items"] - st["n_tc_pair_items"]
     launches_per_step = 1 + (1 if n_pairs else 0) + 1 + (1 if st["n_dec_items"] else 0) + \
-        (1 if st["n_tc_items"] else 0) + (1 if st["n_split_groups"] else 0)
+        (1 if n_tc1 else 0) + (1 if st["n_tc_pair_items"] else 0) + \
+        (1 if st["n_split_groups"] else 0)
 
     # ---- roofline of the dominant kernel (paged attention)
     peaks = measured_peaks()
-    kv_b, q_b, o_b = w.kv_bytes(), w.q_bytes(), T * w.Hq * w.D * 4
+    kv_b, q_b, o_b = w.kv_bytes(), w.q_bytes(), T * w.Hq * w.D * out.element_size()
     flops = w.flops()
     attn_s = per["attention"] / 1000.0
     hbm_peak = float(peaks["hbm_gbs"])
@@ -439,6 +443,10 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--tc-min-rows", type=int, default=0,
                     help="plan option: rows from which items use the tensor cores (0 = default)")
+    ap.add_argument("--out", choices=["f32", "bf16"], default="f32",
+                    help="attention output dtype")
+    ap.add_argument("--tc-pair", type=int, default=0,
+                    help="plan option: 0 = 256-row tensor-core items (default), -1 = 128-row only")
     ap.add_argument("--max-chunk", type=int, default=0,
                     help="plan option: split-KV chunk length (0 = automatic)")
     ap.add_argument("--subset", choices=["prefill", "decode"], default=None,
@@ -466,7 +474,9 @@ def main():
     if args.subset:
         w = w.subset(w.groups[f"{args.subset}_seqs"])
         args.config_key += f"_{args.subset}"
-    run_gpu(args, w, cfg_dict(w, cfg, args.subset), rank, local, world)
+    cd = cfg_dict(w, cfg, args.subset)
+    cd["out_dtype"] = args.out
+    run_gpu(args, w, cd, rank, local, world)
     if world > 1:
         import torch.distributed as dist
         dist.destroy_process_group()

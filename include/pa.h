@@ -136,19 +136,24 @@ typedef struct {
                                 Tensor-core items need D = 128, block_size >= 8 and
                                 Hq / Hkv dividing 128. */
   int32_t num_sms;           /* 0: query the current device */
-  int32_t reserved[5];       /* must be zero */
+  int32_t tc_pair;           /* 0: default (on): tensor-core rows go in 256-row items (two
+                                128-row tiles per CTA sharing every K/V tile) while more than
+                                128 rows remain; <0: 128-row items only */
+  int32_t reserved[4];       /* must be zero */
 } pa_plan_options;
 
 typedef struct {
   int64_t total_q;           /* sum of query_lens */
   int32_t num_seqs;
   int32_t n_dec_items;       /* CUDA-core items */
-  int32_t n_tc_items;        /* tensor-core items */
+  int32_t n_tc_items;        /* tensor-core items (both kinds) */
   int32_t n_split_groups;    /* row groups whose keys were split (need the combine pass) */
   int32_t n_partials;        /* partial results the split items write */
   int32_t chunk_tokens;      /* split chunk length used (0 = no split) */
   int64_t kv_tokens;         /* sum of context_lens (keys read once per KV head) */
   int64_t workspace_bytes;
+  int32_t n_tc_pair_items;   /* of which 256-row (two-tile) items */
+  int32_t pad;
 } pa_plan_stats;
 
 /* Build a plan from HOST copies of the lengths. Validates 0 <= query_len <=
@@ -169,7 +174,8 @@ pa_status pa_plan_get_stats(pa_plan_t plan, pa_plan_stats* out);
 
 /* Copies the plan's work items to host memory, 9 int32 per item:
  * (path, seq, kv_head, row_begin, row_count, kv_begin, kv_end, part, q_row0),
- * path 0 = CUDA-core kernel, 1 = tensor-core kernel; packed row rho of a
+ * path 0 = CUDA-core kernel, 1 = tensor-core kernel (128-row tile), 2 = tensor-core
+ * kernel with two 128-row tiles per item; packed row rho of a
  * (seq, kv_head) pair is query token rho / g and query head kv_head * g + rho % g;
  * part = first partial-result row (-1 = written straight to out); q_row0 = row
  * of the sequence's first query in q. Writes at most max_items items and the

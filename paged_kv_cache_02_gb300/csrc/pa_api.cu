@@ -93,15 +93,15 @@ pa_status make_q_map(CUtensorMap* map, const void* q, int64_t total_q, int Hq, i
 struct pa_plan_s {
   int32_t num_seqs, Hq, Hkv, D, block_size, max_blocks, g;
   int64_t total_q;
-  int32_t n_dec, n_tc, n_groups;
+  int32_t n_dec, n_tc, n_tc2, n_groups;
   int32_t dec_rows_max;
   int64_t n_part_rows;
   int32_t chunk;
   int64_t kv_tokens;
   // workspace layout (byte offsets)
-  size_t off_dec, off_tc, off_groups, off_acc, off_ml, ws_bytes;
+  size_t off_dec, off_tc, off_tc2, off_groups, off_acc, off_ml, ws_bytes;
   size_t table_bytes;       // bytes of the item / group tables (copied each call)
-  void* host_tables;        // table image: [dec items][tc items][groups] at their offsets
+  void* host_tables;        // table image: [dec][tc][tc pair items][groups] at their offsets
   bool host_pinned;
 };
 
@@ -123,9 +123,12 @@ int device_sms() {
   return sms;
 }
 
+// Kernel a work item runs on (the path number pa_plan_export reports).
+enum Path : int { kPathDec = 0, kPathTc = 1, kPathTcPair = 2 };
+
 struct Unit {
   int32_t seq, kvh, row_begin, row_count, keys, q_row0;
-  bool tc;
+  int path;
 };
 
 }  // namespace
@@ -230,7 +233,7 @@ pa_status pa_plan_create(const int32_t* h_context_lens, const int32_t* h_query_l
   memset(&o, 0, sizeof o);
   if (opts) {
     o = *opts;
-    for (int i = 0; i < 5; ++i)
+    for (int i = 0; i < 4; ++i)
       if (o.reserved[i]) return PA_ERR_INVALID_ARG;
   }
   const int g = Hq / Hkv;
@@ -251,8 +254,11 @@ pa_status pa_plan_create(const int32_t* h_context_lens, const int32_t* h_query_l
   const bool tc_enabled = (D == 128) && (block_size >= 8) && (pa::kTcRows % g == 0) &&
                           o.tc_min_rows >= 0;
   const int tc_min_rows = o.tc_min_rows > 0 ? o.tc_min_rows : pa::kTcMinRowsDefault;
+  const bool pair_enabled = tc_enabled && o.tc_pair >= 0;
 
-  // ---- units: (sequence, KV head, row tile)
+  // ---- units: (sequence, KV head, row tile). Tensor-core rows go in tiles of 256
+  // (two 128-row halves sharing every K/V tile) while more than 128 rows remain,
+  // the rest in one 128-row tile.
   std::vector<Unit> units;
   int64_t total_keys = 0;
   int64_t q_row0 = 0;
@@ -261,14 +267,23 @@ pa_status pa_plan_create(const int32_t* h_context_lens, const int32_t* h_query_l
     if (q > 0) {
       const int64_t rows = (int64_t)q * g;
       const bool tc = tc_enabled && rows >= tc_min_rows;
-      const int rt = tc ? pa::kTcRows : pa::kDecRows;
       for (int32_t kvh = 0; kvh < Hkv; ++kvh) {
-        for (int64_t rb = 0; rb < rows; rb += rt) {
-          const int32_t rc = (int32_t)std::min<int64_t>(rt, rows - rb);
+        for (int64_t rb = 0; rb < rows;) {
+          const int64_t left = rows - rb;
+          int path, rt;
+          if (!tc) {
+            path = kPathDec; rt = pa::kDecRows;
+          } else if (pair_enabled && left > pa::kTcRows) {
+            path = kPathTcPair; rt = 2 * pa::kTcRows;
+          } else {
+            path = kPathTc; rt = pa::kTcRows;
+          }
+          const int32_t rc = (int32_t)std::min<int64_t>(rt, left);
           const int32_t t_last = (int32_t)((rb + rc - 1) / g);
           const int32_t keys = L - q + t_last + 1;
-          units.push_back({s, kvh, (int32_t)rb, rc, keys, (int32_t)q_row0, tc});
+          units.push_back({s, kvh, (int32_t)rb, rc, keys, (int32_t)q_row0, path});
           total_keys += keys;
+          rb += rc;
         }
       }
     }
@@ -283,15 +298,15 @@ pa_status pa_plan_create(const int32_t* h_context_lens, const int32_t* h_query_l
     chunk = std::max<int64_t>(256, align_up((size_t)(total_keys / (3 * (int64_t)sms) + 1),
                                             pa::kChunkAlign));
   }
-  std::vector<Item> dec, tc;
+  std::vector<Item> dec, tc, tc2;
   std::vector<SplitGroup> groups;
   int64_t part_rows = 0;
   int32_t dec_rows_max = 1;
   bool any_split = false;
   for (const Unit& u : units) {
     const int64_t n_chunks = (u.keys + chunk - 1) / chunk;
-    std::vector<Item>& dst = u.tc ? tc : dec;
-    if (!u.tc) dec_rows_max = std::max(dec_rows_max, u.row_count);
+    std::vector<Item>& dst = u.path == kPathDec ? dec : (u.path == kPathTc ? tc : tc2);
+    if (u.path == kPathDec) dec_rows_max = std::max(dec_rows_max, u.row_count);
     if (n_chunks <= 1) {
       dst.push_back({u.seq, u.kvh, u.row_begin, u.row_count, 0, u.keys, -1, u.q_row0});
     } else {
@@ -315,17 +330,20 @@ pa_status pa_plan_create(const int32_t* h_context_lens, const int32_t* h_query_l
   };
   std::stable_sort(dec.begin(), dec.end(), longer);
   std::stable_sort(tc.begin(), tc.end(), longer);
+  std::stable_sort(tc2.begin(), tc2.end(), longer);
 
   pa_plan_s* p = new (std::nothrow) pa_plan_s();
   if (!p) return PA_ERR_INVALID_ARG;
   p->num_seqs = num_seqs; p->Hq = Hq; p->Hkv = Hkv; p->D = D; p->block_size = block_size;
   p->max_blocks = max_blocks_per_seq; p->g = g; p->total_q = total_q;
-  p->n_dec = (int32_t)dec.size(); p->n_tc = (int32_t)tc.size(); p->n_groups = (int32_t)groups.size();
+  p->n_dec = (int32_t)dec.size(); p->n_tc = (int32_t)tc.size(); p->n_tc2 = (int32_t)tc2.size();
+  p->n_groups = (int32_t)groups.size();
   p->dec_rows_max = dec_rows_max; p->n_part_rows = part_rows;
   p->chunk = any_split ? (int32_t)chunk : 0; p->kv_tokens = kv_tokens;
   size_t off = 0;
   p->off_dec = off; off = align_up(off + dec.size() * sizeof(Item), 256);
   p->off_tc = off; off = align_up(off + tc.size() * sizeof(Item), 256);
+  p->off_tc2 = off; off = align_up(off + tc2.size() * sizeof(Item), 256);
   p->off_groups = off; off = align_up(off + groups.size() * sizeof(SplitGroup), 256);
   p->table_bytes = off;
   p->off_acc = off; off = align_up(off + (size_t)part_rows * D * sizeof(float), 256);
@@ -345,6 +363,7 @@ pa_status pa_plan_create(const int32_t* h_context_lens, const int32_t* h_query_l
     memset(h, 0, p->table_bytes);
     if (!dec.empty()) memcpy(h + p->off_dec, dec.data(), dec.size() * sizeof(Item));
     if (!tc.empty()) memcpy(h + p->off_tc, tc.data(), tc.size() * sizeof(Item));
+    if (!tc2.empty()) memcpy(h + p->off_tc2, tc2.data(), tc2.size() * sizeof(Item));
     if (!groups.empty())
       memcpy(h + p->off_groups, groups.data(), groups.size() * sizeof(SplitGroup));
   }
@@ -370,7 +389,9 @@ pa_status pa_plan_get_stats(pa_plan_t p, pa_plan_stats* out) {
   out->total_q = p->total_q;
   out->num_seqs = p->num_seqs;
   out->n_dec_items = p->n_dec;
-  out->n_tc_items = p->n_tc;
+  out->n_tc_items = p->n_tc + p->n_tc2;
+  out->n_tc_pair_items = p->n_tc2;
+  out->pad = 0;
   out->n_split_groups = p->n_groups;
   out->n_partials = (int32_t)p->n_part_rows;
   out->chunk_tokens = p->chunk;
@@ -381,12 +402,13 @@ pa_status pa_plan_get_stats(pa_plan_t p, pa_plan_stats* out) {
 
 pa_status pa_plan_export(pa_plan_t p, int32_t* h_items, int32_t max_items, int32_t* n_items) {
   if (!p || !n_items || max_items < 0 || (max_items > 0 && !h_items)) return PA_ERR_INVALID_ARG;
-  *n_items = p->n_dec + p->n_tc;
+  *n_items = p->n_dec + p->n_tc + p->n_tc2;
   const uint8_t* h = static_cast<const uint8_t*>(p->host_tables);
   int32_t k = 0;
-  for (int path = 0; path < 2; ++path) {
-    const int32_t n = path == 0 ? p->n_dec : p->n_tc;
-    const Item* it = reinterpret_cast<const Item*>(h + (path == 0 ? p->off_dec : p->off_tc));
+  for (int path = 0; path < 3; ++path) {
+    const int32_t n = path == kPathDec ? p->n_dec : (path == kPathTc ? p->n_tc : p->n_tc2);
+    const size_t off = path == kPathDec ? p->off_dec : (path == kPathTc ? p->off_tc : p->off_tc2);
+    const Item* it = reinterpret_cast<const Item*>(h + off);
     for (int32_t i = 0; i < n && k < max_items; ++i, ++k) {
       int32_t* r = h_items + (int64_t)k * 9;
       r[0] = path; r[1] = it[i].seq; r[2] = it[i].kv_head; r[3] = it[i].row_begin;
@@ -456,7 +478,7 @@ pa_status pa_attention(pa_plan_t p, void* d_out, pa_dtype out_dtype, const void*
                                       p->n_dec, p->D, p->dec_rows_max, box_t, grid, s);
     if (e != cudaSuccess) return PA_ERR_CUDA;
   }
-  if (p->n_tc > 0) {
+  if (p->n_tc + p->n_tc2 > 0) {
     const int box_t = std::min(p->block_size, 64);
     CUtensorMap kmap, vmap;
     pa_status st = pa::make_pool_map(&kmap, d_k_pool, num_blocks, p->block_size, p->Hkv, p->D,
@@ -470,11 +492,20 @@ pa_status pa_attention(pa_plan_t p, void* d_out, pa_dtype out_dtype, const void*
     if (st != PA_OK) return st;
     int sms = device_sms();
     if (sms <= 0) return PA_ERR_CUDA;
-    const int grid = std::min(p->n_tc, sms);
-    cudaError_t e = pa::launch_tc(a, kmap, vmap, qmap,
-                                  reinterpret_cast<const Item*>(ws + p->off_tc), p->n_tc, box_t,
-                                  grid, s);
-    if (e != cudaSuccess) return PA_ERR_CUDA;
+    if (p->n_tc2 > 0) {
+      const int grid = std::min(p->n_tc2, sms);
+      cudaError_t e = pa::launch_tc2(a, kmap, vmap, qmap,
+                                     reinterpret_cast<const Item*>(ws + p->off_tc2), p->n_tc2,
+                                     box_t, grid, s);
+      if (e != cudaSuccess) return PA_ERR_CUDA;
+    }
+    if (p->n_tc > 0) {
+      const int grid = std::min(p->n_tc, sms);
+      cudaError_t e = pa::launch_tc(a, kmap, vmap, qmap,
+                                    reinterpret_cast<const Item*>(ws + p->off_tc), p->n_tc, box_t,
+                                    grid, s);
+      if (e != cudaSuccess) return PA_ERR_CUDA;
+    }
   }
   if (p->n_groups > 0) {
     cudaError_t e = pa::launch_combine(

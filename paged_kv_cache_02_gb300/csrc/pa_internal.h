@@ -91,6 +91,11 @@ cudaError_t launch_tc(const AttnArgs& a, const CUtensorMap& kmap, const CUtensor
 // swizzle: one box is the 128 packed rows (tokens x the g heads of a KV head) of one D half.
 pa_status make_q_map(CUtensorMap* map, const void* q, int64_t total_q, int Hq, int D, int g);
 int tc_smem_bytes();
+// Items of 129..256 rows: two 128-row tiles per CTA that share every K/V tile.
+cudaError_t launch_tc2(const AttnArgs& a, const CUtensorMap& kmap, const CUtensorMap& vmap,
+                       const CUtensorMap& qmap, const Item* items, int32_t n_items, int box_t,
+                       int grid, cudaStream_t s);
+int tc2_smem_bytes();
 constexpr int kTcMinRowsDefault = 4;   // items with at least this many rows use tensor cores
 
 }  // namespace pa

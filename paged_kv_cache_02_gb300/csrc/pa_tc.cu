@@ -228,7 +228,7 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
         if (!mbar_wait(&sm.q_full[qb], ph(k, 2), a.err)) { ok = false; break; }
         sm.q_consumed[qb] += 1;
         tc::fence_after_sync();
-        const uint32_t q_addr = smem_addr(&sm.q[qb][0][0]);
+        const uint64_t qd = tc::smem_desc_sw128(smem_addr(&sm.q[qb][0][0]), 16, 1024);
         for (int j = 0; j < nt; ++j, ++n) {
           const int st = n % kStagesTc;
           const int b = n & 1;
@@ -236,12 +236,14 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
           sm.consumed[st] += 1;
           if (!mbar_wait(&sm.s_free[b], ph(n, 2) ^ 1u, a.err)) { ok = false; break; }
           tc::fence_after_sync();
-          const uint32_t k_addr = smem_addr(&sm.k[st][0][0]);
+          // S = Q K^T: 8 steps of 16 dims; step kk starts (kk / 4) D halves and
+          // (kk % 4) 32-byte chunks into both operands
+          const uint64_t kd = tc::smem_desc_sw128(smem_addr(&sm.k[st][0][0]), 16, 1024);
+          tc::mma_bf16_c<false>(tmem + (uint32_t)b * kKeys, qd, kd, kIdescS);
 #pragma unroll
-          for (int kk = 0; kk < kD / 16; ++kk) {
-            const uint32_t off = (uint32_t)(kk >> 2) * kHalf + (uint32_t)(kk & 3) * 32u;
-            tc::mma_bf16(tmem + (uint32_t)b * kKeys, tc::smem_desc_sw128(q_addr + off, 16, 1024),
-                         tc::smem_desc_sw128(k_addr + off, 16, 1024), kIdescS, kk > 0);
+          for (int kk = 1; kk < kD / 16; ++kk) {
+            const uint64_t off = (uint64_t)(((kk >> 2) * kHalf + (kk & 3) * 32) >> 4);
+            tc::mma_bf16_c<true>(tmem + (uint32_t)b * kKeys, qd + off, kd + off, kIdescS);
           }
           tc::commit(&sm.s_full[b]);
         }
@@ -268,12 +270,18 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
             break;
           }
           tc::fence_after_sync();
-          const uint32_t v_addr = smem_addr(&sm.v[st][0][0]);
+          // V as the MN-major B operand: step kk covers keys 16 kk .. 16 kk + 15 (rows
+          // of 128 bytes), the two D halves are kHalf apart
+          const uint64_t vd = tc::smem_desc_sw128(smem_addr(&sm.v[st][0][0]), kHalf, 1024);
+          const uint32_t pa = tmem + (uint32_t)b * kKeys;
+          if (j > 0)
+            tc::mma_bf16_ts_c<true>(tmem + kTmemO, pa, vd, kIdescO);
+          else
+            tc::mma_bf16_ts_c<false>(tmem + kTmemO, pa, vd, kIdescO);
 #pragma unroll
-          for (int kk = 0; kk < kKeys / 16; ++kk) {
-            tc::mma_bf16_ts(tmem + kTmemO, tmem + (uint32_t)b * kKeys + (uint32_t)kk * 8u,
-                            tc::smem_desc_sw128(v_addr + (uint32_t)kk * 16u * 128u, kHalf, 1024),
-                            kIdescO, (j > 0) || (kk > 0));
+          for (int kk = 1; kk < kKeys / 16; ++kk) {
+            tc::mma_bf16_ts_c<true>(tmem + kTmemO, pa + (uint32_t)kk * 8u,
+                                    vd + (uint64_t)((kk * 16 * 128) >> 4), kIdescO);
           }
           tc::commit(&sm.o_done[b]);
           tc::commit(&sm.kv_empty[st]);

@@ -1,0 +1,605 @@
+// pa_tc2.cu -- paged multi-token attention, two 128-row query tiles per CTA (tcgen05).
+//
+// Same computation as pa_tc.cu ("PagedAttention" wiki page, "mathematical
+// formulation"; Pensieve summary, multi-token attention with the causal mask
+// fused), for items of 129..256 packed rows: two 128-row tiles A and B of the
+// same (sequence, KV head) that read the same keys. Every K/V tile that lands in
+// shared memory feeds both tiles, so a FLOP costs half the K/V traffic of a
+// single tile, and the two tiles form two independent chains
+//     S_t(j) = Q_t K_j^T  ->  softmax_t(j)  ->  O_t += P_t(j) V_j
+// that keep the tensor core busy while the other chain's softmax runs.
+//
+// Warps (11, one persistent CTA per SM):
+//   0        TMA producer: both tiles' Q rows once per item (single buffer);
+//            K and V tiles of 128 keys gathered per block piece into two
+//            2-stage rings with their own barriers, so that K_{j+2} is loaded
+//            as soon as both chains have multiplied by K_j.
+//   1, 2     MMA issuer of chain A / B: S_t(j); then P_t(j) V_j once the
+//            softmax wrote P_t(j) over S_t(j) in TMEM; then waits for that
+//            P V before the next S_t (P and S share the TMEM columns).
+//   3-10     softmax of both chains, a tile of chain A then the same tile of
+//            chain B: warp w owns TMEM lane quadrant w % 4 (32 rows) and half
+//            the key columns; the two warps of a quadrant exchange row maxima
+//            and row sums. P is written back over S as bf16 pairs, O is
+//            rescaled in TMEM only when the running maximum grows by more than
+//            2^8. The epilogue stages O through shared memory so that every
+//            global store writes whole 64-byte row pieces.
+// TMEM: S/P of A [0,128), of B [128,256); O of A [256,384), of B [384,512).
+// TMEM loads/stores and whole-warp waits are always warp-uniform; every wait is
+// bounded.
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <math.h>
+#include <stdint.h>
+
+#include "pa_internal.h"
+#include "pa_ptx.cuh"
+#include "pa_tc.cuh"
+
+namespace pa {
+namespace {
+
+constexpr int kKeys = 128;              // keys per tile
+constexpr int kD = 128;
+constexpr int kStages = 2;
+constexpr int kThreads2 = 352;          // 11 warps
+constexpr int kHalf = 128 * 128;        // 128 rows x 64 elements, swizzled (16 KB)
+constexpr int kSoftmaxWarps = 8;
+constexpr int kStageCols = 16;          // epilogue staging: 32 rows x 16 fp32 per warp
+constexpr float kRescaleLog2 = 8.f;
+constexpr uint32_t kTmemCols = 512;
+
+constexpr uint32_t kIdescS = tc::idesc_bf16_f32(128, kKeys, false);
+constexpr uint32_t kIdescO = tc::idesc_bf16_f32(128, kD, true);
+
+__host__ __device__ constexpr uint32_t s_col(int t) { return (uint32_t)t * 128u; }
+__host__ __device__ constexpr uint32_t o_col(int t) { return 256u + (uint32_t)t * 128u; }
+
+struct Tc2Smem {
+  uint8_t q[2][2][kHalf];               // [tile A/B][D half]
+  uint8_t k[kStages][2][kHalf];         // [stage][D half], rows = keys
+  uint8_t v[kStages][2][kHalf];
+  float stage[kSoftmaxWarps][32 * kStageCols];
+  float xmax[2][2][128];                // [chain][key half][row]: partial row maxima
+  float xsum[2][2][128];                // [chain][D half][row]: partial row sums
+  int bt_cache[2][kBtCache];
+  uint64_t k_full[kStages], k_empty[kStages];
+  uint64_t v_full[kStages], v_empty[kStages];
+  uint64_t q_full, q_free;
+  uint64_t s_full[2], o_done[2], o_free[2];
+  uint64_t p_full[2][2];                // [chain][key half]: P of keys 64 h .. 64 h + 63 written
+  uint64_t drain[2];
+  uint64_t xbar[4];                     // per TMEM lane quadrant: its two softmax warps met
+  uint32_t tmem_base;
+  int k_issued[kStages], k_consumed[kStages];
+  int v_issued[kStages], v_consumed[kStages];
+  int q_issued, q_consumed;
+  int abort_flag;
+};
+
+__device__ __forceinline__ uint8_t* align1024(uint8_t* p) {
+  return reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(p) + 1023) & ~uintptr_t(1023));
+}
+
+__device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
+  __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
+  return *reinterpret_cast<uint32_t*>(&h);
+}
+
+__device__ __forceinline__ uint32_t ph(int n, int ring) { return (uint32_t)(n / ring) & 1u; }
+
+__device__ __forceinline__ int tiles_of(const Item& x) {
+  return (x.kv_end - x.kv_begin + kKeys - 1) / kKeys;
+}
+
+__global__ void __launch_bounds__(kThreads2, 1)
+    tc2_kernel(const __grid_constant__ AttnArgs a, const __grid_constant__ CUtensorMap kmap,
+               const __grid_constant__ CUtensorMap vmap, const __grid_constant__ CUtensorMap qmap,
+               const Item* __restrict__ items, int n_items, int box_t) {
+  extern __shared__ uint8_t smem_raw[];
+  Tc2Smem& sm = *reinterpret_cast<Tc2Smem*>(align1024(smem_raw));
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int G = gridDim.x;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kStages; ++s) {
+      mbar_init(&sm.k_full[s], 1);
+      mbar_init(&sm.k_empty[s], 2);    // both chains' S
+      mbar_init(&sm.v_full[s], 1);
+      mbar_init(&sm.v_empty[s], 2);    // both chains' P V
+      sm.k_issued[s] = sm.k_consumed[s] = 0;
+      sm.v_issued[s] = sm.v_consumed[s] = 0;
+    }
+    mbar_init(&sm.q_full, 1);
+    mbar_init(&sm.q_free, 2);          // both chains' last S of the item
+    for (int t = 0; t < 2; ++t) {
+      mbar_init(&sm.s_full[t], 1);
+      mbar_init(&sm.p_full[t][0], 128);
+      mbar_init(&sm.p_full[t][1], 128);
+      mbar_init(&sm.o_done[t], 1);
+      mbar_init(&sm.o_free[t], 256);   // all 8 softmax warps
+      mbar_init(&sm.drain[t], 1);
+    }
+    for (int q = 0; q < 4; ++q) mbar_init(&sm.xbar[q], 64);
+    sm.q_issued = 0;
+    sm.q_consumed = 0;
+    sm.abort_flag = 0;
+    fence_barrier_init();
+  }
+  if (warp == 1) {
+    tc::tmem_alloc(&sm.tmem_base, kTmemCols);
+    tc::tmem_relinquish();
+  }
+  tc::fence_before_sync();
+  __syncthreads();
+  tc::fence_after_sync();
+  const uint32_t tmem = sm.tmem_base;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ TMA producer
+    if (lane == 0) {
+      prefetch_tensormap(&kmap);
+      prefetch_tensormap(&vmap);
+      prefetch_tensormap(&qmap);
+    }
+    const int pieces = kKeys / box_t;
+    const uint32_t piece_bytes = (uint32_t)box_t * 128u;
+    int n = 0, k = 0;
+    bool ok = true;
+    int nb[kBtPerLane];
+    Item item_next{};
+    if ((int)blockIdx.x < n_items) {
+      const Item f = items[blockIdx.x];
+      bt_prefetch(a.block_table + (int64_t)f.seq * a.max_blocks, a.max_blocks,
+                  bt_window(f.kv_begin, f.kv_end, a.block_size), lane, nb);
+      bt_store(sm.bt_cache[0], nb, lane);
+      if ((int)blockIdx.x + G < n_items) item_next = items[blockIdx.x + G];
+    }
+    __syncwarp();
+    for (int it = blockIdx.x; it < n_items && ok; it += G, ++k) {
+      const Item item = items[it];
+      const BtWindow win = bt_window(item.kv_begin, item.kv_end, a.block_size);
+      const int* cache = sm.bt_cache[k & 1];
+      const bool has_next = it + G < n_items;
+      Item item_after{};
+      if (has_next) {
+        bt_prefetch(a.block_table + (int64_t)item_next.seq * a.max_blocks, a.max_blocks,
+                    bt_window(item_next.kv_begin, item_next.kv_end, a.block_size), lane, nb);
+        if (it + 2 * G < n_items) item_after = items[it + 2 * G];
+      }
+      // both tiles' Q rows. The buffer is free once both chains issued the item's last
+      // S: q_free then completed phase k - 1. It cannot be further ahead, since phase k
+      // needs the Q load below.
+      if (k > 0) {
+        ok = mbar_wait_warp(&sm.q_free, (uint32_t)(k - 1) & 1u, a.err);
+        if (!ok || *(volatile int*)&sm.abort_flag) { ok = false; break; }
+      }
+      if (lane == 0) {
+        mbar_arrive_expect_tx(&sm.q_full, 4u * kHalf);
+#pragma unroll
+        for (int t = 0; t < 2; ++t) {
+          const int tok = item.q_row0 + (item.row_begin + 128 * t) / a.g;
+          tma_load_3d(&sm.q[t][0][0], &qmap, &sm.q_full, 0, item.kv_head * a.g, tok);
+          tma_load_3d(&sm.q[t][1][0], &qmap, &sm.q_full, 64, item.kv_head * a.g, tok);
+        }
+        sm.q_issued += 1;
+      }
+      __syncwarp();
+      const int32_t* bt = a.block_table + (int64_t)item.seq * a.max_blocks;
+      for (int t0 = item.kv_begin; t0 < item.kv_end; t0 += kKeys, ++n) {
+        const int st = n % kStages;
+        bool valid = false;
+        int tok = 0;
+        if (lane < pieces) {
+          const int j0 = t0 + lane * box_t;
+          if (j0 < item.kv_end) {
+            const int lb = j0 / a.block_size;
+            const int phys = bt_lookup(cache, win, bt, a.max_blocks, lb);
+            if (phys == -2) {
+              record_error(a.err, PA_DEVERR_TABLE_RANGE);
+            } else if (phys < 0 || phys >= a.num_blocks) {
+              record_error(a.err, PA_DEVERR_BLOCK_RANGE);
+            } else {
+              valid = true;
+              tok = phys * a.block_size + (j0 - lb * a.block_size);
+            }
+          }
+        }
+        const uint32_t tile_bytes = __popc(__ballot_sync(0xffffffffu, valid)) * piece_bytes * 2u;
+        const uint32_t row_off = (uint32_t)lane * box_t * 128u;
+        // K_n: its stage is free once both chains' S of tile n - 2 completed
+        ok = mbar_wait_warp(&sm.k_empty[st], ph(n, kStages) ^ 1u, a.err);
+        if (!ok || *(volatile int*)&sm.abort_flag) { ok = false; break; }
+        if (lane == 0) mbar_arrive_expect_tx(&sm.k_full[st], tile_bytes);
+        __syncwarp();
+        if (valid) {
+          tma_load_3d(&sm.k[st][0][row_off], &kmap, &sm.k_full[st], 0, item.kv_head, tok);
+          tma_load_3d(&sm.k[st][1][row_off], &kmap, &sm.k_full[st], 64, item.kv_head, tok);
+        }
+        if (lane == 0) sm.k_issued[st] += 1;
+        // V_n: free once both chains' P V of tile n - 2 completed
+        ok = mbar_wait_warp(&sm.v_empty[st], ph(n, kStages) ^ 1u, a.err);
+        if (!ok || *(volatile int*)&sm.abort_flag) { ok = false; break; }
+        if (lane == 0) mbar_arrive_expect_tx(&sm.v_full[st], tile_bytes);
+        __syncwarp();
+        if (valid) {
+          tma_load_3d(&sm.v[st][0][row_off], &vmap, &sm.v_full[st], 0, item.kv_head, tok);
+          tma_load_3d(&sm.v[st][1][row_off], &vmap, &sm.v_full[st], 64, item.kv_head, tok);
+        }
+        if (lane == 0) sm.v_issued[st] += 1;
+      }
+      if (has_next) {
+        bt_store(sm.bt_cache[(k + 1) & 1], nb, lane);
+        item_next = item_after;
+      }
+      __syncwarp();
+    }
+    if (!ok) sm.abort_flag = 1;
+  } else if (warp == 1 || warp == 2) {
+    // ------------------------------------------------------------ MMA issuer of chain t
+    // Phase bounds: every barrier this thread waits on is at most one phase ahead of
+    // the wait. k_full / v_full of tile n + 2 need both chains' S / P V of tile n;
+    // p_full(n + 1) needs s_full(n + 1), which this thread commits after the wait
+    // for p_full(n); o_free of item k + 1 needs the P V of item k + 1.
+    const int t = warp - 1;
+    if (lane == 0) {
+      int n = 0, k = 0;   // tile, item of the CTA (each chain sees every tile)
+      bool ok = true;
+      // tile counts are read one item ahead, off the critical path
+      int nt_next = (int)blockIdx.x < n_items ? tiles_of(items[blockIdx.x]) : 0;
+      for (int it = blockIdx.x; it < n_items && ok; it += G, ++k) {
+        const int nt = nt_next;
+        if (it + G < n_items) nt_next = tiles_of(items[it + G]);
+        if (!mbar_wait(&sm.q_full, (uint32_t)k & 1u, a.err)) { ok = false; break; }
+        if (t == 0) sm.q_consumed += 1;
+        tc::fence_after_sync();
+        const uint64_t qd = tc::smem_desc_sw128(smem_addr(&sm.q[t][0][0]), 16, 1024);
+        for (int j = 0; j < nt; ++j, ++n) {
+          const int st = n % kStages;
+          if (!mbar_wait(&sm.k_full[st], ph(n, kStages), a.err)) { ok = false; break; }
+          if (t == 0) sm.k_consumed[st] += 1;
+          tc::fence_after_sync();
+          // S_t = Q_t K^T: 8 steps of 16 dims; step kk starts (kk / 4) D halves and
+          // (kk % 4) 32-byte chunks into both operands
+          const uint64_t kd = tc::smem_desc_sw128(smem_addr(&sm.k[st][0][0]), 16, 1024);
+          tc::mma_bf16_c<false>(tmem + s_col(t), qd, kd, kIdescS);
+#pragma unroll
+          for (int kk = 1; kk < kD / 16; ++kk) {
+            const uint64_t off = (uint64_t)(((kk >> 2) * kHalf + (kk & 3) * 32) >> 4);
+            tc::mma_bf16_c<true>(tmem + s_col(t), qd + off, kd + off, kIdescS);
+          }
+          tc::commit(&sm.s_full[t]);
+          tc::commit(&sm.k_empty[st]);
+          if (j + 1 == nt) tc::commit(&sm.q_free);  // this chain's last S of the item
+          // at an item's first tile, O_t must have been read out by the previous
+          // item's epilogue
+          if (j == 0 && !mbar_wait(&sm.o_free[t], ((uint32_t)k & 1u) ^ 1u, a.err)) {
+            ok = false;
+            break;
+          }
+          if (!mbar_wait(&sm.v_full[st], ph(n, kStages), a.err)) { ok = false; break; }
+          if (t == 0) sm.v_consumed[st] += 1;
+          // V as the MN-major B operand: step kk covers keys 16 kk .. 16 kk + 15 (rows
+          // of 128 bytes), the two D halves are kHalf apart
+          const uint64_t vd = tc::smem_desc_sw128(smem_addr(&sm.v[st][0][0]), kHalf, 1024);
+          // P_t(j) is written over S_t(j) by the softmax in two key halves; the P V of
+          // the first half runs while the second half is computed
+#pragma unroll
+          for (int hk = 0; hk < 2; ++hk) {
+            if (!mbar_wait(&sm.p_full[t][hk], (uint32_t)n & 1u, a.err)) { ok = false; break; }
+            tc::fence_after_sync();
+#pragma unroll
+            for (int kk = 4 * hk; kk < 4 * hk + 4; ++kk) {
+              const uint32_t pa = tmem + s_col(t) + (uint32_t)kk * 8u;
+              const uint64_t vk = vd + (uint64_t)((kk * 16 * 128) >> 4);
+              if (kk > 0)
+                tc::mma_bf16_ts_c<true>(tmem + o_col(t), pa, vk, kIdescO);
+              else if (j > 0)
+                tc::mma_bf16_ts_c<true>(tmem + o_col(t), pa, vk, kIdescO);
+              else
+                tc::mma_bf16_ts_c<false>(tmem + o_col(t), pa, vk, kIdescO);
+            }
+          }
+          if (!ok) break;
+          tc::commit(&sm.o_done[t]);
+          tc::commit(&sm.v_empty[st]);
+          // the next S_t overwrites the columns this P V reads
+          if (!mbar_wait(&sm.o_done[t], (uint32_t)n & 1u, a.err)) { ok = false; break; }
+        }
+      }
+      if (!ok) sm.abort_flag = 1;
+      tc::commit(&sm.drain[t]);
+      mbar_wait(&sm.drain[t], 0, a.err);
+    }
+    __syncwarp();
+  } else {
+    // ------------------------------------------------------------ softmax (both chains)
+    // All 8 warps take every tile of chain A, then the same tile of chain B. Warp w
+    // reads TMEM lane quadrant w % 4 (32 rows) and key columns 64 hf .. 64 hf + 63 of
+    // S, hf = (w - 3) / 4; the two warps of a quadrant exchange their row maxima (and,
+    // at the end of an item, their row sums) through shared memory and meet on an
+    // mbarrier of 64 arrivals (a bounded wait, unlike a named barrier). The meeting
+    // also orders both warps' reads of S before either writes P over it. Both warps
+    // meet the same number of times in the same order (x counts the meetings), so the
+    // barrier is never two phases ahead of a wait.
+    // Phase bounds: s_full[t](n + 1) needs p_full[t](n), which these threads arrive
+    // on; o_done[t](n + 1) needs p_full[t](n + 1); v_full of tile n + 2 needs both
+    // chains' P V of tile n. So no barrier is ever two phases ahead of a wait here.
+    const int quad = warp & 3;
+    const int hf = (warp - 3) >> 2;               // key half of S (and D half of O)
+    const int row = quad * 32 + lane;             // row within a tile = TMEM lane
+    const uint32_t t_lane = tmem + ((uint32_t)(quad * 32) << 16);
+    uint64_t* xbar = &sm.xbar[quad];
+    uint32_t x = 0;                               // meetings so far
+    float* stg = sm.stage[warp - 3];
+    int n = 0;                                    // tile of the CTA
+    bool ok = true;
+    // the next item and its lengths are read one item ahead, off the critical path
+    Item item_next{};
+    int L_next = 0, ql_next = 0;
+    if ((int)blockIdx.x < n_items) {
+      item_next = items[blockIdx.x];
+      L_next = __ldg(a.context_lens + item_next.seq);
+      ql_next = __ldg(a.query_lens + item_next.seq);
+    }
+    for (int it = blockIdx.x; it < n_items && ok; it += G) {
+      const Item item = item_next;
+      const int L = L_next, ql = ql_next;
+      if (it + G < n_items) {
+        item_next = items[it + G];
+        L_next = __ldg(a.context_lens + item_next.seq);
+        ql_next = __ldg(a.query_lens + item_next.seq);
+      }
+      if (item.kv_end > L || item.row_begin + item.row_count > ql * a.g)
+        record_error(a.err, PA_DEVERR_LENS);
+      const int nt = tiles_of(item);
+      // this thread's row in each chain: causal limit (-1: not a row of the item)
+      int lim[2];
+      float m_used[2], l[2];
+#pragma unroll
+      for (int t = 0; t < 2; ++t) {
+        const int trow = t * 128 + row;
+        lim[t] = -1;
+        if (trow < item.row_count) {
+          const int qt = (item.row_begin + trow) / a.g;
+          lim[t] = min(item.kv_end - 1, L - ql + qt);
+        }
+        m_used[t] = -INFINITY;
+        l[t] = 0.f;
+      }
+      for (int j = 0; j < nt; ++j, ++n) {
+        const int key0 = item.kv_begin + j * kKeys;
+        const int st = n % kStages;
+#pragma unroll
+        for (int t = 0; t < 2; ++t) {
+          const bool warp_live = t * 128 + quad * 32 < item.row_count;
+          if (!mbar_wait_warp(&sm.s_full[t], (uint32_t)n & 1u, a.err)) { ok = false; break; }
+          tc::fence_after_sync();
+          // The item's last tile may hold keys past its range, and those V rows hold
+          // whatever the block tail holds: zero them (after V_n landed, before either
+          // chain's P V of the tile) so that 0 * (non-finite) never reaches O.
+          if (t == 0 && key0 + kKeys > item.kv_end) {
+            if (!mbar_wait_warp(&sm.v_full[st], ph(n, kStages), a.err)) { ok = false; break; }
+            if (key0 + row >= item.kv_end) {
+              uint4* v = reinterpret_cast<uint4*>(&sm.v[st][hf][row * 128]);
+#pragma unroll
+              for (int i = 0; i < 8; ++i) v[i] = make_uint4(0, 0, 0, 0);
+              tc::fence_async_shared();
+            }
+          }
+          const int k0 = key0 + hf * 64;           // first key of this warp's columns
+          const bool masked = k0 + 63 > lim[t];
+          float s[64];
+          if (warp_live) {
+            tc::tmem_ld64(t_lane + s_col(t) + (uint32_t)hf * 64u, s);
+            if (masked) {
+#pragma unroll
+              for (int i = 0; i < 64; ++i)
+                if (k0 + i > lim[t]) s[i] = -INFINITY;
+            }
+            float m4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+#pragma unroll
+            for (int i = 0; i < 32; ++i) m4[i & 3] = fmax3(m4[i & 3], s[2 * i], s[2 * i + 1]);
+            sm.xmax[t][hf][row] = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3]));
+          }
+          tc::fence_before_sync();
+          mbar_arrive(xbar);
+          if (!mbar_wait_warp(xbar, x++ & 1u, a.err)) { ok = false; break; }
+          tc::fence_after_sync();
+          if (warp_live) {
+            // running maximum of the raw scores (the scale is positive)
+            const float mx = fmaxf(sm.xmax[t][0][row], sm.xmax[t][1][row]);
+            const float m_new = fmaxf(m_used[t], mx * a.scale_log2);
+            if (m_used[t] == -INFINITY) m_used[t] = m_new;
+            // O_t is idle: its issuer waited for the previous P V before this S. Both
+            // warps of the quadrant take the same decision per row; each rescales its
+            // own D half (tcgen05.ld / st are warp-collective: the warp goes together)
+            const bool need = m_new > m_used[t] + kRescaleLog2;
+            if (__any_sync(0xffffffffu, need)) {
+              const float alpha = need ? fast_exp2(m_used[t] - m_new) : 1.f;
+#pragma unroll 1
+              for (int c4 = 0; c4 < 2; ++c4) {
+                float o[32];
+                const uint32_t addr = t_lane + o_col(t) + (uint32_t)(hf * 64 + c4 * 32);
+                tc::tmem_ld32(addr, o);
+#pragma unroll
+                for (int i = 0; i < 32; ++i) o[i] *= alpha;
+                tc::tmem_st32(addr, o);
+              }
+              if (need) {
+                l[t] *= alpha;
+                m_used[t] = m_new;
+              }
+            }
+            // P = 2^(scale * s - m) as bf16 pairs; keys 64 hf .. 64 hf + 63 go to
+            // columns 32 hf .. 32 hf + 31 (the pair barrier ordered the reads of S),
+            // written 16 columns at a time
+            const float neg_m = (m_used[t] == -INFINITY) ? 0.f : -m_used[t];
+            const uint64_t sc2 = f2_pack(a.scale_log2, a.scale_log2);
+            const uint64_t nm2 = f2_pack(neg_m, neg_m);
+            uint64_t sum2[4] = {0ull, 0ull, 0ull, 0ull};
+#pragma unroll
+            for (int c = 0; c < 2; ++c) {
+              float pk[16];
+#pragma unroll
+              for (int i2 = 0; i2 < 16; ++i2) {
+                const int i = c * 16 + i2;
+                float x0, x1;
+                f2_unpack(f2_fma(f2_pack(s[2 * i], s[2 * i + 1]), sc2, nm2), x0, x1);
+                if (masked) {
+                  if (k0 + 2 * i > lim[t]) x0 = -INFINITY;
+                  if (k0 + 2 * i + 1 > lim[t]) x1 = -INFINITY;
+                }
+                const float p0 = fast_exp2(x0), p1 = fast_exp2(x1);
+                sum2[i & 3] = f2_add(sum2[i & 3], f2_pack(p0, p1));
+                pk[i2] = __uint_as_float(pack_bf16(p0, p1));
+              }
+              tc::tmem_st16(t_lane + s_col(t) + (uint32_t)(hf * 32 + c * 16), pk);
+            }
+            float sa, sb;
+            f2_unpack(f2_add(f2_add(sum2[0], sum2[1]), f2_add(sum2[2], sum2[3])), sa, sb);
+            l[t] += sa + sb;
+          } else {
+            // rows past the item: zero P, so that no stale bits reach the tensor core
+            float z[16];
+#pragma unroll
+            for (int i = 0; i < 16; ++i) z[i] = 0.f;
+            tc::tmem_st16(t_lane + s_col(t) + (uint32_t)hf * 32u, z);
+            tc::tmem_st16(t_lane + s_col(t) + (uint32_t)hf * 32u + 16u, z);
+          }
+          tc::tmem_wait_st();
+          tc::fence_before_sync();
+          mbar_arrive(&sm.p_full[t][hf]);
+        }
+        if (!ok) break;
+      }
+      if (!ok) break;
+      // ---- epilogue of each chain: its last P V (the issuer waited for the one
+      // before, so o_done is at most one phase ahead); O / l for this warp's D half
+#pragma unroll
+      for (int t = 0; t < 2; ++t) {
+        const bool warp_live = t * 128 + quad * 32 < item.row_count;
+        if (!mbar_wait_warp(&sm.o_done[t], (uint32_t)(n - 1) & 1u, a.err)) { ok = false; break; }
+        tc::fence_after_sync();
+        sm.xsum[t][hf][row] = l[t];
+        mbar_arrive(xbar);
+        if (!mbar_wait_warp(xbar, x++ & 1u, a.err)) { ok = false; break; }
+        const float l_tot = sm.xsum[t][0][row] + sm.xsum[t][1][row];
+        const int trow = t * 128 + row;
+        if (warp_live) {
+          // destination of this lane's row piece (nullptr: not a row of the item)
+          char* dst_row = nullptr;
+          float inv = 1.f;
+          if (trow < item.row_count) {
+            if (item.part < 0) {
+              inv = (l_tot > 0.f) ? 1.f / l_tot : 0.f;
+              const int rho = item.row_begin + trow;
+              const int qt = rho / a.g;
+              const int h = item.kv_head * a.g + (rho - qt * a.g);
+              const int64_t off = ((int64_t)(item.q_row0 + qt) * a.Hq + h) * kD + hf * 64;
+              dst_row = reinterpret_cast<char*>(a.out) + off * (a.out_bf16 ? 2 : 4);
+            } else {
+              const int64_t prow = (int64_t)item.part + trow;
+              dst_row = reinterpret_cast<char*>(a.part_acc + prow * kD + hf * 64);
+              if (hf == 0) {
+                a.part_ml[prow * 2 + 0] = m_used[t];
+                a.part_ml[prow * 2 + 1] = l_tot;
+              }
+            }
+          }
+          const bool bf = a.out_bf16 && item.part < 0;
+#pragma unroll 1
+          for (int c4 = 0; c4 < 2; ++c4) {
+            float o[32];
+            tc::tmem_ld32(t_lane + o_col(t) + (uint32_t)(hf * 64 + c4 * 32), o);
+#pragma unroll
+            for (int hh = 0; hh < 2; ++hh) {
+              // this lane's 16 values -> staging row `lane`; 16-byte chunk cj sits at
+              // position cj ^ ((row / 2) % 4), which keeps both the row-wise writes
+              // and the column-wise reads below free of bank conflicts
+#pragma unroll
+              for (int cj = 0; cj < 4; ++cj) {
+                const int pos = cj ^ ((lane >> 1) & 3);
+                reinterpret_cast<float4*>(stg + lane * kStageCols)[pos] =
+                    make_float4(o[hh * 16 + 4 * cj] * inv, o[hh * 16 + 4 * cj + 1] * inv,
+                                o[hh * 16 + 4 * cj + 2] * inv, o[hh * 16 + 4 * cj + 3] * inv);
+              }
+              __syncwarp();
+              // 8 rows x 64 bytes per store instruction: lane -> row 8 qq + lane / 4,
+              // 16-byte chunk lane % 4
+              const int col0 = c4 * 32 + hh * 16 + (lane & 3) * 4;
+#pragma unroll
+              for (int qq = 0; qq < 4; ++qq) {
+                const int r = qq * 8 + (lane >> 2);
+                char* d = reinterpret_cast<char*>(__shfl_sync(
+                    0xffffffffu, reinterpret_cast<unsigned long long>(dst_row), r));
+                const float4 v = reinterpret_cast<const float4*>(
+                    stg + r * kStageCols)[(lane & 3) ^ ((r >> 1) & 3)];
+                if (d) {
+                  if (bf) {
+                    uint2 w;
+                    w.x = pack_bf16(v.x, v.y);
+                    w.y = pack_bf16(v.z, v.w);
+                    *reinterpret_cast<uint2*>(d + col0 * 2) = w;
+                  } else {
+                    *reinterpret_cast<float4*>(d + col0 * 4) = v;
+                  }
+                }
+              }
+              __syncwarp();
+            }
+          }
+        }
+        tc::fence_before_sync();
+        mbar_arrive(&sm.o_free[t]);
+      }
+    }
+    if (!ok) sm.abort_flag = 1;
+  }
+  tc::fence_before_sync();
+  __syncthreads();
+  // After an abort, give copies still in flight a bounded time to land.
+  if (sm.abort_flag && threadIdx.x == 0) {
+    const uint64_t t0 = global_timer_ns();
+    for (int s = 0; s < kStages; ++s) {
+      if (sm.k_issued[s] > sm.k_consumed[s]) {
+        const uint32_t parity = (uint32_t)(sm.k_issued[s] - 1) & 1u;
+        while (!mbar_try_wait(smem_addr(&sm.k_full[s]), parity))
+          if (global_timer_ns() - t0 > kWaitLimitNs) break;
+      }
+      if (sm.v_issued[s] > sm.v_consumed[s]) {
+        const uint32_t parity = (uint32_t)(sm.v_issued[s] - 1) & 1u;
+        while (!mbar_try_wait(smem_addr(&sm.v_full[s]), parity))
+          if (global_timer_ns() - t0 > kWaitLimitNs) break;
+      }
+    }
+    if (sm.q_issued > sm.q_consumed) {
+      const uint32_t parity = (uint32_t)(sm.q_issued - 1) & 1u;
+      while (!mbar_try_wait(smem_addr(&sm.q_full), parity))
+        if (global_timer_ns() - t0 > kWaitLimitNs) break;
+    }
+  }
+  if (warp == 1) {
+    tc::fence_after_sync();
+    tc::tmem_dealloc(tmem, kTmemCols);
+  }
+}
+
+}  // namespace
+
+int tc2_smem_bytes() { return (int)sizeof(Tc2Smem) + 1024; }
+
+cudaError_t launch_tc2(const AttnArgs& a, const CUtensorMap& kmap, const CUtensorMap& vmap,
+                       const CUtensorMap& qmap, const Item* items, int32_t n_items, int box_t,
+                       int grid, cudaStream_t s) {
+  if (n_items <= 0) return cudaSuccess;
+  const int smem = tc2_smem_bytes();
+  cudaError_t e =
+      cudaFuncSetAttribute(tc2_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  if (e != cudaSuccess) return e;
+  tc2_kernel<<<grid, kThreads2, smem, s>>>(a, kmap, vmap, qmap, items, n_items, box_t);
+  return cudaGetLastError();
+}
+
+}  // namespace pa

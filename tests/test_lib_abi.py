@@ -130,6 +130,30 @@ def test_plan_covers_every_row_and_key(pa, chunk):
             assert it[8] == pref[it[1]]
 
 
+def test_plan_pair_tiles(pa):
+    """Tensor-core rows go in 256-row items (two 128-row tiles) while more than 128 rows
+    remain, the rest in one 128-row item; tc_pair=-1 keeps 128-row items only."""
+    L = [300, 1000, 700, 129, 2000]
+    q = [300, 40, 33, 129, 1]
+    g, Hkv = 8, 2
+    p = plan(pa, L, q, Hq=g * Hkv, Hkv=Hkv, D=128, max_chunk_tokens=256)
+    items = p.items()
+    _coverage(items, L, q, g, Hkv)
+    rows_by_path = {}
+    for path, s, kvh, rb, rc, *_ in items:
+        rows_by_path.setdefault(int(path), []).append((int(s), int(rc)))
+    assert all(rc <= 128 for _, rc in rows_by_path.get(1, []))
+    assert all(128 < rc <= 256 for _, rc in rows_by_path[2])
+    assert p.stats()["n_tc_pair_items"] == len(rows_by_path[2])
+    # 300 tokens x 8 heads = 2400 rows = 9 x 256 + 96
+    assert sorted(rc for s, rc in set((s, rc) for s, rc in rows_by_path[2] if s == 0)) == [256]
+    p1 = plan(pa, L, q, Hq=g * Hkv, Hkv=Hkv, D=128, max_chunk_tokens=256, tc_pair=-1)
+    items1 = p1.items()
+    _coverage(items1, L, q, g, Hkv)
+    assert 2 not in set(items1[:, 0].tolist())
+    assert p1.stats()["n_tc_pair_items"] == 0
+
+
 def test_plan_orders_longest_first(pa):
     L = list(range(100, 2100, 50))
     p = plan(pa, L, [1] * len(L))

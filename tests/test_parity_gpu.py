@@ -103,6 +103,35 @@ def test_tensor_core_tiny_first(pa):
     assert got["plan"].stats()["n_tc_items"] > 0
 
 
+PAIR_CASES = [
+    # (g, block_size, chunk): ragged row counts around the 128 / 256 tile edges
+    (1, 16, 0), (1, 32, 128), (8, 32, 0), (8, 8, 256), (4, 256, 0), (16, 64, 192),
+]
+
+
+@pytest.mark.parametrize("g,B,chunk", PAIR_CASES)
+def test_tensor_core_pair_tiles(pa, g, B, chunk):
+    """Items of 129..256 rows run as two 128-row tiles sharing every K/V tile; the result
+    matches the oracle and the one-tile kernel."""
+    rows = [129, 200, 256, 257, 384, 511, 64]
+    q = [max(1, -(-r // g)) for r in rows]
+    L = [qq + extra for qq, extra in zip(q, [0, 37, 300, 5, 900, 128, 700])]
+    w = workloads.make_custom(L, q, Hq=2 * g, Hkv=2, D=128, block_size=B, seed=300 + g + B)
+    kw = dict(max_chunk_tokens=chunk) if chunk else {}
+    (_, _), pair_run, want = full_check(pa, w, **kw)
+    assert pair_run["plan"].stats()["n_tc_pair_items"] > 0
+    (_, _), one_run, _ = full_check(pa, w, tc_pair=-1, **kw)
+    assert one_run["plan"].stats()["n_tc_pair_items"] == 0
+    assert torch.allclose(pair_run["out"], one_run["out"], atol=gu.ATOL_MAX, rtol=0)
+
+
+def test_tensor_core_pair_tiny_first(pa):
+    """Smallest two-tile case: 129 rows, one key tile."""
+    w = workloads.make_custom([129], [129], Hq=1, Hkv=1, D=128, block_size=16, seed=11)
+    (_, _), got, _ = full_check(pa, w)
+    assert got["plan"].stats()["n_tc_pair_items"] == 1
+
+
 def test_unused_slots_hold_nan(pa):
     """Slots past each context (tail of the last block, unused blocks) hold NaN: no effect."""
     w = workloads.make_custom([9, 20, 3, 130], [2, 3, 3, 1], Hq=4, Hkv=2, D=128, block_size=16,
@@ -137,22 +166,26 @@ def test_subrequests_match_single_request(pa):
     L, r, qn = 300, 64, 45
     full = workloads.make_custom([L], [L], Hq=8, Hkv=8, D=128, block_size=32, seed=12,
                                  write_new=False)
-    one = gu.gpu_step(pa, full)["out"]
     two_w = workloads.make_custom([r, L], [r, qn], Hq=8, Hkv=8, D=128, block_size=32, seed=12,
                                   write_new=False)
     two_w.block_table = np.concatenate([full.block_table, full.block_table])
     two_w.k_pool, two_w.v_pool, two_w.num_blocks = full.k_pool, full.v_pool, full.num_blocks
     two_w.q = torch.cat([full.q[:r], full.q[L - qn:]])
-    two = gu.gpu_step(pa, two_w)["out"]
-    # the rows land in different tiles (and so different tensor-core work items) in the
-    # two batches: equal up to float rounding, and each equal to the oracle
     want = gu.oracle_rows(full, gu.oracle_step(full))
-    gu.assert_attention_close(one.cpu().numpy(), want, "one request")
-    gu.assert_attention_close(two[:r].cpu().numpy(), want[:r], "sub-request A")
-    gu.assert_attention_close(two[r:].cpu().numpy(), want[L - qn:], "sub-request B")
+    for kw in ({}, {"tc_pair": -1}):
+        one = gu.gpu_step(pa, full, **kw)["out"]
+        two = gu.gpu_step(pa, two_w, **kw)["out"]
+        gu.assert_attention_close(one.cpu().numpy(), want, "one request")
+        gu.assert_attention_close(two[:r].cpu().numpy(), want[:r], "sub-request A")
+        gu.assert_attention_close(two[r:].cpu().numpy(), want[L - qn:], "sub-request B")
+    # With 128-row tiles only, every row takes the same arithmetic in both batches (the
+    # same key tiles, the same exponentials); the rows only land in different work
+    # items, so the two agree far inside the oracle tolerance. (With 256-row items the
+    # full request's rows take the polynomial exponentials for part of the keys, and
+    # then only the oracle comparison above applies.)
     d_a = float((two[:r] - one[:r]).abs().max())
     d_b = float((two[r:] - one[L - qn:]).abs().max())
-    assert d_a <= 1e-4 and d_b <= 1e-4, (d_a, d_b)
+    assert d_a <= 2e-4 and d_b <= 2e-4, (d_a, d_b)
 
 
 def test_bf16_output(pa):
