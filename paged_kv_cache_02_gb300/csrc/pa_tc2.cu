@@ -17,13 +17,12 @@
 //   1, 2     MMA issuer of chain A / B: S_t(j); then P_t(j) V_j once the
 //            softmax wrote P_t(j) over S_t(j) in TMEM; then waits for that
 //            P V before the next S_t (P and S share the TMEM columns).
-//   3-10     softmax of both chains, a tile of chain A then the same tile of
-//            chain B: warp w owns TMEM lane quadrant w % 4 (32 rows) and half
-//            the key columns; the two warps of a quadrant exchange row maxima
-//            and row sums. P is written back over S as bf16 pairs, O is
-//            rescaled in TMEM only when the running maximum grows by more than
-//            2^8. The epilogue stages O through shared memory so that every
-//            global store writes whole 64-byte row pieces.
+//   3-6      softmax of chain A, 7-10 softmax of chain B: one thread per row
+//            (its TMEM lane) reads its whole 128-key score row with one TMEM
+//            load; P is written back over S as bf16 pairs, O is rescaled in
+//            TMEM only when the running maximum grows by more than 2^8. The
+//            epilogue stages O through shared memory so that every global
+//            store writes whole 64-byte row pieces.
 // TMEM: S/P of A [0,128), of B [128,256); O of A [256,384), of B [384,512).
 // TMEM loads/stores and whole-warp waits are always warp-uniform; every wait is
 // bounded.
@@ -61,16 +60,15 @@ struct Tc2Smem {
   uint8_t k[kStages][2][kHalf];         // [stage][D half], rows = keys
   uint8_t v[kStages][2][kHalf];
   float stage[kSoftmaxWarps][32 * kStageCols];
-  float xmax[2][2][128];                // [chain][key half][row]: partial row maxima
-  float xsum[2][2][128];                // [chain][D half][row]: partial row sums
   int bt_cache[2][kBtCache];
+  Item info[3];                         // item k and its lengths, by k % 3 (written by the
+  int info_L[3], info_ql[3];            // producer before item k's Q load)
   uint64_t k_full[kStages], k_empty[kStages];
   uint64_t v_full[kStages], v_empty[kStages];
   uint64_t q_full, q_free;
   uint64_t s_full[2], o_done[2], o_free[2];
   uint64_t p_full[2][2];                // [chain][key half]: P of keys 64 h .. 64 h + 63 written
   uint64_t drain[2];
-  uint64_t xbar[4];                     // per TMEM lane quadrant: its two softmax warps met
   uint32_t tmem_base;
   int k_issued[kStages], k_consumed[kStages];
   int v_issued[kStages], v_consumed[kStages];
@@ -93,6 +91,23 @@ __device__ __forceinline__ int tiles_of(const Item& x) {
   return (x.kv_end - x.kv_begin + kKeys - 1) / kKeys;
 }
 
+// The work items of a CTA: items c + i G, i < cnt (c = blockIdx.x, G = gridDim.x), a
+// round-robin walk of the longest-first list. CTAs then work on items of similar
+// length at the same time, and the row tiles of one (sequence, KV head) -- which read
+// the same keys -- sit next to each other in that list: their K/V reads meet in L2.
+struct ItemWalk {
+  int c, G, cnt;
+  __device__ __forceinline__ int at(int s) const { return c + s * G; }
+};
+
+__device__ __forceinline__ ItemWalk item_walk(int n_items) {
+  ItemWalk w;
+  w.c = blockIdx.x;
+  w.G = gridDim.x;
+  w.cnt = w.c < n_items ? (n_items - w.c + w.G - 1) / w.G : 0;
+  return w;
+}
+
 __global__ void __launch_bounds__(kThreads2, 1)
     tc2_kernel(const __grid_constant__ AttnArgs a, const __grid_constant__ CUtensorMap kmap,
                const __grid_constant__ CUtensorMap vmap, const __grid_constant__ CUtensorMap qmap,
@@ -100,7 +115,7 @@ __global__ void __launch_bounds__(kThreads2, 1)
   extern __shared__ uint8_t smem_raw[];
   Tc2Smem& sm = *reinterpret_cast<Tc2Smem*>(align1024(smem_raw));
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int G = gridDim.x;
+  const ItemWalk W = item_walk(n_items);
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < kStages; ++s) {
@@ -118,10 +133,9 @@ __global__ void __launch_bounds__(kThreads2, 1)
       mbar_init(&sm.p_full[t][0], 128);
       mbar_init(&sm.p_full[t][1], 128);
       mbar_init(&sm.o_done[t], 1);
-      mbar_init(&sm.o_free[t], 256);   // all 8 softmax warps
+      mbar_init(&sm.o_free[t], 128);
       mbar_init(&sm.drain[t], 1);
     }
-    for (int q = 0; q < 4; ++q) mbar_init(&sm.xbar[q], 64);
     sm.q_issued = 0;
     sm.q_consumed = 0;
     sm.abort_flag = 0;
@@ -149,24 +163,24 @@ __global__ void __launch_bounds__(kThreads2, 1)
     bool ok = true;
     int nb[kBtPerLane];
     Item item_next{};
-    if ((int)blockIdx.x < n_items) {
-      const Item f = items[blockIdx.x];
+    if (W.cnt > 0) {
+      const Item f = items[W.at(0)];
       bt_prefetch(a.block_table + (int64_t)f.seq * a.max_blocks, a.max_blocks,
                   bt_window(f.kv_begin, f.kv_end, a.block_size), lane, nb);
       bt_store(sm.bt_cache[0], nb, lane);
-      if ((int)blockIdx.x + G < n_items) item_next = items[blockIdx.x + G];
+      if (W.cnt > 1) item_next = items[W.at(1)];
     }
     __syncwarp();
-    for (int it = blockIdx.x; it < n_items && ok; it += G, ++k) {
-      const Item item = items[it];
+    for (int sidx = 0; sidx < W.cnt && ok; ++sidx, ++k) {
+      const Item item = items[W.at(sidx)];
       const BtWindow win = bt_window(item.kv_begin, item.kv_end, a.block_size);
       const int* cache = sm.bt_cache[k & 1];
-      const bool has_next = it + G < n_items;
+      const bool has_next = sidx + 1 < W.cnt;
       Item item_after{};
       if (has_next) {
         bt_prefetch(a.block_table + (int64_t)item_next.seq * a.max_blocks, a.max_blocks,
                     bt_window(item_next.kv_begin, item_next.kv_end, a.block_size), lane, nb);
-        if (it + 2 * G < n_items) item_after = items[it + 2 * G];
+        if (sidx + 2 < W.cnt) item_after = items[W.at(sidx + 2)];
       }
       // both tiles' Q rows. The buffer is free once both chains issued the item's last
       // S: q_free then completed phase k - 1. It cannot be further ahead, since phase k
@@ -176,6 +190,10 @@ __global__ void __launch_bounds__(kThreads2, 1)
         if (!ok || *(volatile int*)&sm.abort_flag) { ok = false; break; }
       }
       if (lane == 0) {
+        // the item's description for the other warps, published by the q_full phase
+        sm.info[k % 3] = item;
+        sm.info_L[k % 3] = __ldg(a.context_lens + item.seq);
+        sm.info_ql[k % 3] = __ldg(a.query_lens + item.seq);
         mbar_arrive_expect_tx(&sm.q_full, 4u * kHalf);
 #pragma unroll
         for (int t = 0; t < 2; ++t) {
@@ -247,10 +265,12 @@ __global__ void __launch_bounds__(kThreads2, 1)
       int n = 0, k = 0;   // tile, item of the CTA (each chain sees every tile)
       bool ok = true;
       // tile counts are read one item ahead, off the critical path
-      int nt_next = (int)blockIdx.x < n_items ? tiles_of(items[blockIdx.x]) : 0;
-      for (int it = blockIdx.x; it < n_items && ok; it += G, ++k) {
-        const int nt = nt_next;
-        if (it + G < n_items) nt_next = tiles_of(items[it + G]);
+      Item nx{};
+      if (W.cnt > 0) nx = items[W.at(0)];
+      for (int sidx = 0; sidx < W.cnt && ok; ++sidx, ++k) {
+        const int kv_begin = nx.kv_begin, kv_end = nx.kv_end;
+        const int nt = tiles_of(nx);
+        if (sidx + 1 < W.cnt) nx = items[W.at(sidx + 1)];
         if (!mbar_wait(&sm.q_full, (uint32_t)k & 1u, a.err)) { ok = false; break; }
         if (t == 0) sm.q_consumed += 1;
         tc::fence_after_sync();
@@ -280,6 +300,26 @@ __global__ void __launch_bounds__(kThreads2, 1)
           }
           if (!mbar_wait(&sm.v_full[st], ph(n, kStages), a.err)) { ok = false; break; }
           if (t == 0) sm.v_consumed[st] += 1;
+          // Keys of the tile in the item's range, rounded up to the 16-key step of P V:
+          // only those V rows are read. At the item's last tile the rows between the
+          // range's end and that step hold whatever the block tail holds: zero them
+          // (at most 15 rows) so that 0 * (non-finite) never reaches O. Both chains
+          // write the same zeros, each before its own P V.
+          const int key0 = kv_begin + j * kKeys;
+          const int valid = min(kKeys, kv_end - key0);
+          const int kk_end = (valid + 15) >> 4;
+          if (valid < kk_end * 16) {
+            for (int r = valid; r < kk_end * 16; ++r) {
+              uint4* v0 = reinterpret_cast<uint4*>(&sm.v[st][0][r * 128]);
+              uint4* v1 = reinterpret_cast<uint4*>(&sm.v[st][1][r * 128]);
+#pragma unroll
+              for (int q = 0; q < 8; ++q) {
+                v0[q] = make_uint4(0, 0, 0, 0);
+                v1[q] = make_uint4(0, 0, 0, 0);
+              }
+            }
+            tc::fence_async_shared();
+          }
           // V as the MN-major B operand: step kk covers keys 16 kk .. 16 kk + 15 (rows
           // of 128 bytes), the two D halves are kHalf apart
           const uint64_t vd = tc::smem_desc_sw128(smem_addr(&sm.v[st][0][0]), kHalf, 1024);
@@ -293,12 +333,14 @@ __global__ void __launch_bounds__(kThreads2, 1)
             for (int kk = 4 * hk; kk < 4 * hk + 4; ++kk) {
               const uint32_t pa = tmem + s_col(t) + (uint32_t)kk * 8u;
               const uint64_t vk = vd + (uint64_t)((kk * 16 * 128) >> 4);
-              if (kk > 0)
+              if (kk == 0) {
+                if (j > 0)
+                  tc::mma_bf16_ts_c<true>(tmem + o_col(t), pa, vk, kIdescO);
+                else
+                  tc::mma_bf16_ts_c<false>(tmem + o_col(t), pa, vk, kIdescO);
+              } else if (kk < kk_end) {
                 tc::mma_bf16_ts_c<true>(tmem + o_col(t), pa, vk, kIdescO);
-              else if (j > 0)
-                tc::mma_bf16_ts_c<true>(tmem + o_col(t), pa, vk, kIdescO);
-              else
-                tc::mma_bf16_ts_c<false>(tmem + o_col(t), pa, vk, kIdescO);
+              }
             }
           }
           if (!ok) break;
@@ -314,246 +356,200 @@ __global__ void __launch_bounds__(kThreads2, 1)
     }
     __syncwarp();
   } else {
-    // ------------------------------------------------------------ softmax (both chains)
-    // All 8 warps take every tile of chain A, then the same tile of chain B. Warp w
-    // reads TMEM lane quadrant w % 4 (32 rows) and key columns 64 hf .. 64 hf + 63 of
-    // S, hf = (w - 3) / 4; the two warps of a quadrant exchange their row maxima (and,
-    // at the end of an item, their row sums) through shared memory and meet on an
-    // mbarrier of 64 arrivals (a bounded wait, unlike a named barrier). The meeting
-    // also orders both warps' reads of S before either writes P over it. Both warps
-    // meet the same number of times in the same order (x counts the meetings), so the
-    // barrier is never two phases ahead of a wait.
+    // ------------------------------------------------------------ softmax of chain t
+    // One thread per row (its TMEM lane): the whole 128-key score row is read from
+    // TMEM with one load, so S is never re-read and no other thread needs the row's
+    // maximum or sum. P goes back over S 16 columns at a time and is handed to the
+    // issuer in two key halves.
     // Phase bounds: s_full[t](n + 1) needs p_full[t](n), which these threads arrive
-    // on; o_done[t](n + 1) needs p_full[t](n + 1); v_full of tile n + 2 needs both
-    // chains' P V of tile n. So no barrier is ever two phases ahead of a wait here.
+    // on; o_done[t](n + 1) needs p_full[t](n + 1); v_full of tile n + 2 needs this
+    // chain's P V of tile n. So no barrier is ever two phases ahead of a wait here.
+    const int t = (warp - 3) >> 2;                // 0 = tile A (warps 3-6), 1 = tile B
     const int quad = warp & 3;
-    const int hf = (warp - 3) >> 2;               // key half of S (and D half of O)
-    const int row = quad * 32 + lane;             // row within a tile = TMEM lane
+    const int row = quad * 32 + lane;             // row within the tile = TMEM lane
     const uint32_t t_lane = tmem + ((uint32_t)(quad * 32) << 16);
-    uint64_t* xbar = &sm.xbar[quad];
-    uint32_t x = 0;                               // meetings so far
     float* stg = sm.stage[warp - 3];
     int n = 0;                                    // tile of the CTA
     bool ok = true;
-    // the next item and its lengths are read one item ahead, off the critical path
-    Item item_next{};
-    int L_next = 0, ql_next = 0;
-    if ((int)blockIdx.x < n_items) {
-      item_next = items[blockIdx.x];
-      L_next = __ldg(a.context_lens + item_next.seq);
-      ql_next = __ldg(a.query_lens + item_next.seq);
-    }
-    for (int it = blockIdx.x; it < n_items && ok; it += G) {
-      const Item item = item_next;
-      const int L = L_next, ql = ql_next;
-      if (it + G < n_items) {
-        item_next = items[it + G];
-        L_next = __ldg(a.context_lens + item_next.seq);
-        ql_next = __ldg(a.query_lens + item_next.seq);
+    for (int sidx = 0, k = 0; sidx < W.cnt && ok; ++sidx, ++k) {
+      // The producer wrote the item's description before its Q load; q_full(k) is at
+      // most one phase ahead (the Q of item k + 1 needs every S of item k). Slot k % 3
+      // is rewritten (for item k + 3) only after every S of item k + 2, and those need
+      // this chain's P of item k + 1: it stays valid through this item's epilogue.
+      if (!mbar_wait_warp(&sm.q_full, (uint32_t)k & 1u, a.err)) { ok = false; break; }
+      const Item& info = sm.info[k % 3];
+      const int kv_begin = info.kv_begin, kv_end = info.kv_end, row_count = info.row_count;
+      int lim = -1;                               // causal limit of this row (-1: not a row)
+      {
+        const int L = sm.info_L[k % 3], ql = sm.info_ql[k % 3];
+        if (kv_end > L || info.row_begin + row_count > ql * a.g)
+          record_error(a.err, PA_DEVERR_LENS);
+        if (t * 128 + row < row_count)
+          lim = min(kv_end - 1, L - ql + (info.row_begin + t * 128 + row) / a.g);
       }
-      if (item.kv_end > L || item.row_begin + item.row_count > ql * a.g)
-        record_error(a.err, PA_DEVERR_LENS);
-      const int nt = tiles_of(item);
-      // this thread's row in each chain: causal limit (-1: not a row of the item)
-      int lim[2];
-      float m_used[2], l[2];
-#pragma unroll
-      for (int t = 0; t < 2; ++t) {
-        const int trow = t * 128 + row;
-        lim[t] = -1;
-        if (trow < item.row_count) {
-          const int qt = (item.row_begin + trow) / a.g;
-          lim[t] = min(item.kv_end - 1, L - ql + qt);
-        }
-        m_used[t] = -INFINITY;
-        l[t] = 0.f;
-      }
+      const int nt = (kv_end - kv_begin + kKeys - 1) / kKeys;
+      const int trow = t * 128 + row;             // row within the item
+      const bool warp_live = t * 128 + quad * 32 < row_count;
+      float m_used = -INFINITY, l = 0.f;
       for (int j = 0; j < nt; ++j, ++n) {
-        const int key0 = item.kv_begin + j * kKeys;
-        const int st = n % kStages;
+        if (!mbar_wait_warp(&sm.s_full[t], (uint32_t)n & 1u, a.err)) { ok = false; break; }
+        tc::fence_after_sync();
+        const int key0 = kv_begin + j * kKeys;
+        if (warp_live) {
+          const bool masked = key0 + kKeys - 1 > lim;
+          float s[128];
+          tc::tmem_ld128(t_lane + s_col(t), s);
+          if (masked) {
 #pragma unroll
-        for (int t = 0; t < 2; ++t) {
-          const bool warp_live = t * 128 + quad * 32 < item.row_count;
-          if (!mbar_wait_warp(&sm.s_full[t], (uint32_t)n & 1u, a.err)) { ok = false; break; }
-          tc::fence_after_sync();
-          // The item's last tile may hold keys past its range, and those V rows hold
-          // whatever the block tail holds: zero them (after V_n landed, before either
-          // chain's P V of the tile) so that 0 * (non-finite) never reaches O.
-          if (t == 0 && key0 + kKeys > item.kv_end) {
-            if (!mbar_wait_warp(&sm.v_full[st], ph(n, kStages), a.err)) { ok = false; break; }
-            if (key0 + row >= item.kv_end) {
-              uint4* v = reinterpret_cast<uint4*>(&sm.v[st][hf][row * 128]);
-#pragma unroll
-              for (int i = 0; i < 8; ++i) v[i] = make_uint4(0, 0, 0, 0);
-              tc::fence_async_shared();
-            }
+            for (int i = 0; i < 128; ++i)
+              if (key0 + i > lim) s[i] = -INFINITY;
           }
-          const int k0 = key0 + hf * 64;           // first key of this warp's columns
-          const bool masked = k0 + 63 > lim[t];
-          float s[64];
-          if (warp_live) {
-            tc::tmem_ld64(t_lane + s_col(t) + (uint32_t)hf * 64u, s);
-            if (masked) {
+          // running maximum of the raw scores (the scale is positive)
+          float m4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
 #pragma unroll
-              for (int i = 0; i < 64; ++i)
-                if (k0 + i > lim[t]) s[i] = -INFINITY;
-            }
-            float m4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
-#pragma unroll
-            for (int i = 0; i < 32; ++i) m4[i & 3] = fmax3(m4[i & 3], s[2 * i], s[2 * i + 1]);
-            sm.xmax[t][hf][row] = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3]));
+          for (int i = 0; i < 64; ++i) m4[i & 3] = fmax3(m4[i & 3], s[2 * i], s[2 * i + 1]);
+          const float m_new =
+              fmaxf(m_used, fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3])) * a.scale_log2);
+          if (m_used == -INFINITY) m_used = m_new;
+          // O_t is rescaled by 2^(m_used - m_new) only when the maximum grew by more
+          // than 2^8; otherwise P keeps the older (smaller) maximum as its reference.
+          const bool need = m_new > m_used + kRescaleLog2;
+          const bool warp_rescale = __any_sync(0xffffffffu, need);
+          const float alpha = need ? fast_exp2(m_used - m_new) : 1.f;
+          if (need) {
+            l *= alpha;
+            m_used = m_new;
           }
-          tc::fence_before_sync();
-          mbar_arrive(xbar);
-          if (!mbar_wait_warp(xbar, x++ & 1u, a.err)) { ok = false; break; }
-          tc::fence_after_sync();
-          if (warp_live) {
-            // running maximum of the raw scores (the scale is positive)
-            const float mx = fmaxf(sm.xmax[t][0][row], sm.xmax[t][1][row]);
-            const float m_new = fmaxf(m_used[t], mx * a.scale_log2);
-            if (m_used[t] == -INFINITY) m_used[t] = m_new;
-            // O_t is idle: its issuer waited for the previous P V before this S. Both
-            // warps of the quadrant take the same decision per row; each rescales its
-            // own D half (tcgen05.ld / st are warp-collective: the warp goes together)
-            const bool need = m_new > m_used[t] + kRescaleLog2;
-            if (__any_sync(0xffffffffu, need)) {
-              const float alpha = need ? fast_exp2(m_used[t] - m_new) : 1.f;
+          // P = 2^(scale * s - m) as bf16 pairs: keys 16 c .. 16 c + 15 go to
+          // columns 8 c .. 8 c + 7; a masked score is -inf and gives exactly 0
+          const float neg_m = (m_used == -INFINITY) ? 0.f : -m_used;
+          const uint64_t sc2 = f2_pack(a.scale_log2, a.scale_log2);
+          const uint64_t nm2 = f2_pack(neg_m, neg_m);
+          uint64_t sum2[2] = {0ull, 0ull};
+#pragma unroll
+          for (int c = 0; c < 8; ++c) {
+            float pk[8];
+#pragma unroll
+            for (int i2 = 0; i2 < 8; ++i2) {
+              const int i = c * 8 + i2;
+              float x0, x1;
+              f2_unpack(f2_fma(f2_pack(s[2 * i], s[2 * i + 1]), sc2, nm2), x0, x1);
+              const float p0 = fast_exp2(x0), p1 = fast_exp2(x1);
+              sum2[i & 1] = f2_add(sum2[i & 1], f2_pack(p0, p1));
+              pk[i2] = __uint_as_float(pack_bf16(p0, p1));
+            }
+            tc::tmem_st8(t_lane + s_col(t) + (uint32_t)c * 8u, pk);
+            if (c == 3 && warp_rescale) {
+              // O_t is idle until the first half's P V: its issuer waited for the
+              // previous P V before this S. Done here, once half the score row is dead,
+              // 16 columns at a time; tcgen05.ld / st are warp-collective, so the warp
+              // rescales together (factor 1 for rows that need none).
 #pragma unroll 1
-              for (int c4 = 0; c4 < 2; ++c4) {
-                float o[32];
-                const uint32_t addr = t_lane + o_col(t) + (uint32_t)(hf * 64 + c4 * 32);
-                tc::tmem_ld32(addr, o);
+              for (int c8 = 0; c8 < kD / 16; ++c8) {
+                float o[16];
+                const uint32_t addr = t_lane + o_col(t) + (uint32_t)c8 * 16u;
+                tc::tmem_ld16(addr, o);
 #pragma unroll
-                for (int i = 0; i < 32; ++i) o[i] *= alpha;
-                tc::tmem_st32(addr, o);
-              }
-              if (need) {
-                l[t] *= alpha;
-                m_used[t] = m_new;
+                for (int i = 0; i < 16; ++i) o[i] *= alpha;
+                tc::tmem_st16(addr, o);
               }
             }
-            // P = 2^(scale * s - m) as bf16 pairs; keys 64 hf .. 64 hf + 63 go to
-            // columns 32 hf .. 32 hf + 31 (the pair barrier ordered the reads of S),
-            // written 16 columns at a time
-            const float neg_m = (m_used[t] == -INFINITY) ? 0.f : -m_used[t];
-            const uint64_t sc2 = f2_pack(a.scale_log2, a.scale_log2);
-            const uint64_t nm2 = f2_pack(neg_m, neg_m);
-            uint64_t sum2[4] = {0ull, 0ull, 0ull, 0ull};
-#pragma unroll
-            for (int c = 0; c < 2; ++c) {
-              float pk[16];
-#pragma unroll
-              for (int i2 = 0; i2 < 16; ++i2) {
-                const int i = c * 16 + i2;
-                float x0, x1;
-                f2_unpack(f2_fma(f2_pack(s[2 * i], s[2 * i + 1]), sc2, nm2), x0, x1);
-                if (masked) {
-                  if (k0 + 2 * i > lim[t]) x0 = -INFINITY;
-                  if (k0 + 2 * i + 1 > lim[t]) x1 = -INFINITY;
-                }
-                const float p0 = fast_exp2(x0), p1 = fast_exp2(x1);
-                sum2[i & 3] = f2_add(sum2[i & 3], f2_pack(p0, p1));
-                pk[i2] = __uint_as_float(pack_bf16(p0, p1));
-              }
-              tc::tmem_st16(t_lane + s_col(t) + (uint32_t)(hf * 32 + c * 16), pk);
+            if ((c & 3) == 3) {
+              // keys 64 (c / 4) .. + 63 are in TMEM: that half's P V may start
+              tc::tmem_wait_st();
+              tc::fence_before_sync();
+              mbar_arrive(&sm.p_full[t][c >> 2]);
             }
-            float sa, sb;
-            f2_unpack(f2_add(f2_add(sum2[0], sum2[1]), f2_add(sum2[2], sum2[3])), sa, sb);
-            l[t] += sa + sb;
-          } else {
-            // rows past the item: zero P, so that no stale bits reach the tensor core
-            float z[16];
-#pragma unroll
-            for (int i = 0; i < 16; ++i) z[i] = 0.f;
-            tc::tmem_st16(t_lane + s_col(t) + (uint32_t)hf * 32u, z);
-            tc::tmem_st16(t_lane + s_col(t) + (uint32_t)hf * 32u + 16u, z);
           }
-          tc::tmem_wait_st();
-          tc::fence_before_sync();
-          mbar_arrive(&sm.p_full[t][hf]);
+          float sa, sb;
+          f2_unpack(f2_add(sum2[0], sum2[1]), sa, sb);
+          l += sa + sb;
+        } else {
+          // rows past the item: zero P, so that no stale bits reach the tensor core
+          float z[16];
+#pragma unroll
+          for (int i = 0; i < 16; ++i) z[i] = 0.f;
+#pragma unroll
+          for (int c = 0; c < 4; ++c) {
+            tc::tmem_st16(t_lane + s_col(t) + (uint32_t)c * 16u, z);
+            if (c & 1) {
+              tc::tmem_wait_st();
+              tc::fence_before_sync();
+              mbar_arrive(&sm.p_full[t][c >> 1]);
+            }
+          }
         }
-        if (!ok) break;
       }
       if (!ok) break;
-      // ---- epilogue of each chain: its last P V (the issuer waited for the one
-      // before, so o_done is at most one phase ahead); O / l for this warp's D half
-#pragma unroll
-      for (int t = 0; t < 2; ++t) {
-        const bool warp_live = t * 128 + quad * 32 < item.row_count;
-        if (!mbar_wait_warp(&sm.o_done[t], (uint32_t)(n - 1) & 1u, a.err)) { ok = false; break; }
-        tc::fence_after_sync();
-        sm.xsum[t][hf][row] = l[t];
-        mbar_arrive(xbar);
-        if (!mbar_wait_warp(xbar, x++ & 1u, a.err)) { ok = false; break; }
-        const float l_tot = sm.xsum[t][0][row] + sm.xsum[t][1][row];
-        const int trow = t * 128 + row;
-        if (warp_live) {
-          // destination of this lane's row piece (nullptr: not a row of the item)
-          char* dst_row = nullptr;
-          float inv = 1.f;
-          if (trow < item.row_count) {
-            if (item.part < 0) {
-              inv = (l_tot > 0.f) ? 1.f / l_tot : 0.f;
-              const int rho = item.row_begin + trow;
-              const int qt = rho / a.g;
-              const int h = item.kv_head * a.g + (rho - qt * a.g);
-              const int64_t off = ((int64_t)(item.q_row0 + qt) * a.Hq + h) * kD + hf * 64;
-              dst_row = reinterpret_cast<char*>(a.out) + off * (a.out_bf16 ? 2 : 4);
-            } else {
-              const int64_t prow = (int64_t)item.part + trow;
-              dst_row = reinterpret_cast<char*>(a.part_acc + prow * kD + hf * 64);
-              if (hf == 0) {
-                a.part_ml[prow * 2 + 0] = m_used[t];
-                a.part_ml[prow * 2 + 1] = l_tot;
-              }
-            }
-          }
-          const bool bf = a.out_bf16 && item.part < 0;
-#pragma unroll 1
-          for (int c4 = 0; c4 < 2; ++c4) {
-            float o[32];
-            tc::tmem_ld32(t_lane + o_col(t) + (uint32_t)(hf * 64 + c4 * 32), o);
-#pragma unroll
-            for (int hh = 0; hh < 2; ++hh) {
-              // this lane's 16 values -> staging row `lane`; 16-byte chunk cj sits at
-              // position cj ^ ((row / 2) % 4), which keeps both the row-wise writes
-              // and the column-wise reads below free of bank conflicts
-#pragma unroll
-              for (int cj = 0; cj < 4; ++cj) {
-                const int pos = cj ^ ((lane >> 1) & 3);
-                reinterpret_cast<float4*>(stg + lane * kStageCols)[pos] =
-                    make_float4(o[hh * 16 + 4 * cj] * inv, o[hh * 16 + 4 * cj + 1] * inv,
-                                o[hh * 16 + 4 * cj + 2] * inv, o[hh * 16 + 4 * cj + 3] * inv);
-              }
-              __syncwarp();
-              // 8 rows x 64 bytes per store instruction: lane -> row 8 qq + lane / 4,
-              // 16-byte chunk lane % 4
-              const int col0 = c4 * 32 + hh * 16 + (lane & 3) * 4;
-#pragma unroll
-              for (int qq = 0; qq < 4; ++qq) {
-                const int r = qq * 8 + (lane >> 2);
-                char* d = reinterpret_cast<char*>(__shfl_sync(
-                    0xffffffffu, reinterpret_cast<unsigned long long>(dst_row), r));
-                const float4 v = reinterpret_cast<const float4*>(
-                    stg + r * kStageCols)[(lane & 3) ^ ((r >> 1) & 3)];
-                if (d) {
-                  if (bf) {
-                    uint2 w;
-                    w.x = pack_bf16(v.x, v.y);
-                    w.y = pack_bf16(v.z, v.w);
-                    *reinterpret_cast<uint2*>(d + col0 * 2) = w;
-                  } else {
-                    *reinterpret_cast<float4*>(d + col0 * 4) = v;
-                  }
-                }
-              }
-              __syncwarp();
-            }
+      // ---- epilogue: the chain's last P V (its issuer waited for the one before, so
+      // o_done is at most one phase ahead)
+      if (!mbar_wait_warp(&sm.o_done[t], (uint32_t)(n - 1) & 1u, a.err)) { ok = false; break; }
+      tc::fence_after_sync();
+      if (warp_live) {
+        // destination of this lane's row (nullptr: not a row of the item)
+        char* dst_row = nullptr;
+        float inv = 1.f;
+        const int part = info.part;
+        if (trow < row_count) {
+          if (part < 0) {
+            inv = (l > 0.f) ? 1.f / l : 0.f;
+            const int rho = info.row_begin + trow;
+            const int qt = rho / a.g;
+            const int h = info.kv_head * a.g + (rho - qt * a.g);
+            const int64_t off = ((int64_t)(info.q_row0 + qt) * a.Hq + h) * kD;
+            dst_row = reinterpret_cast<char*>(a.out) + off * (a.out_bf16 ? 2 : 4);
+          } else {
+            const int64_t prow = (int64_t)part + trow;
+            dst_row = reinterpret_cast<char*>(a.part_acc + prow * kD);
+            a.part_ml[prow * 2 + 0] = m_used;
+            a.part_ml[prow * 2 + 1] = l;
           }
         }
-        tc::fence_before_sync();
-        mbar_arrive(&sm.o_free[t]);
+        const bool bf = a.out_bf16 && part < 0;
+#pragma unroll 1
+        for (int c4 = 0; c4 < kD / 32; ++c4) {
+          float o[32];
+          tc::tmem_ld32(t_lane + o_col(t) + (uint32_t)c4 * 32u, o);
+#pragma unroll
+          for (int hh = 0; hh < 2; ++hh) {
+            // this lane's 16 values -> staging row `lane`; 16-byte chunk cj sits at
+            // position cj ^ ((row / 2) % 4), which keeps both the row-wise writes and
+            // the column-wise reads below free of bank conflicts
+#pragma unroll
+            for (int cj = 0; cj < 4; ++cj) {
+              const int pos = cj ^ ((lane >> 1) & 3);
+              reinterpret_cast<float4*>(stg + lane * kStageCols)[pos] =
+                  make_float4(o[hh * 16 + 4 * cj] * inv, o[hh * 16 + 4 * cj + 1] * inv,
+                              o[hh * 16 + 4 * cj + 2] * inv, o[hh * 16 + 4 * cj + 3] * inv);
+            }
+            __syncwarp();
+            // 8 rows x 64 bytes per store instruction: lane -> row 8 qq + lane / 4,
+            // 16-byte chunk lane % 4
+            const int col0 = c4 * 32 + hh * 16 + (lane & 3) * 4;
+#pragma unroll
+            for (int qq = 0; qq < 4; ++qq) {
+              const int r = qq * 8 + (lane >> 2);
+              char* d = reinterpret_cast<char*>(__shfl_sync(
+                  0xffffffffu, reinterpret_cast<unsigned long long>(dst_row), r));
+              const float4 v = reinterpret_cast<const float4*>(
+                  stg + r * kStageCols)[(lane & 3) ^ ((r >> 1) & 3)];
+              if (d) {
+                if (bf) {
+                  uint2 w;
+                  w.x = pack_bf16(v.x, v.y);
+                  w.y = pack_bf16(v.z, v.w);
+                  *reinterpret_cast<uint2*>(d + col0 * 2) = w;
+                } else {
+                  *reinterpret_cast<float4*>(d + col0 * 4) = v;
+                }
+              }
+            }
+            __syncwarp();
+          }
+        }
       }
+      tc::fence_before_sync();
+      mbar_arrive(&sm.o_free[t]);
     }
     if (!ok) sm.abort_flag = 1;
   }
