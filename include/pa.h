@@ -139,7 +139,10 @@ typedef struct {
   int32_t tc_pair;           /* 0: default (on): tensor-core rows go in 256-row items (two
                                 128-row tiles per CTA sharing every K/V tile) while more than
                                 128 rows remain; <0: 128-row items only */
-  int32_t reserved[4];       /* must be zero */
+  int32_t tc_decode;         /* 0: default (on): a (sequence, KV head) pair with at most 16
+                                tensor-core rows runs with keys on the 128-row side (needs
+                                Hq / Hkv dividing 16); <0: never */
+  int32_t reserved[3];       /* must be zero */
 } pa_plan_options;
 
 typedef struct {
@@ -153,7 +156,7 @@ typedef struct {
   int64_t kv_tokens;         /* sum of context_lens (keys read once per KV head) */
   int64_t workspace_bytes;
   int32_t n_tc_pair_items;   /* of which 256-row (two-tile) items */
-  int32_t pad;
+  int32_t n_tc_decode_items; /* of which items of at most 16 rows (keys on the 128-row side) */
 } pa_plan_stats;
 
 /* Build a plan from HOST copies of the lengths. Validates 0 <= query_len <=
@@ -175,7 +178,8 @@ pa_status pa_plan_get_stats(pa_plan_t plan, pa_plan_stats* out);
 /* Copies the plan's work items to host memory, 9 int32 per item:
  * (path, seq, kv_head, row_begin, row_count, kv_begin, kv_end, part, q_row0),
  * path 0 = CUDA-core kernel, 1 = tensor-core kernel (128-row tile), 2 = tensor-core
- * kernel with two 128-row tiles per item; packed row rho of a
+ * kernel with two 128-row tiles per item, 3 = tensor-core kernel for items of at most
+ * 16 rows (keys on the 128-row side); packed row rho of a
  * (seq, kv_head) pair is query token rho / g and query head kv_head * g + rho % g;
  * part = first partial-result row (-1 = written straight to out); q_row0 = row
  * of the sequence's first query in q. Writes at most max_items items and the

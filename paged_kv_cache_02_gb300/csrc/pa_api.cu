@@ -73,12 +73,13 @@ pa_status make_pool_map(CUtensorMap* map, const void* pool, int64_t num_blocks, 
   return r == CUDA_SUCCESS ? PA_OK : PA_ERR_CUDA;
 }
 
-pa_status make_q_map(CUtensorMap* map, const void* q, int64_t total_q, int Hq, int D, int g) {
+pa_status make_q_map(CUtensorMap* map, const void* q, int64_t total_q, int Hq, int D, int g,
+                     int rows) {
   auto fn = encode_fn();
   if (!fn) return PA_ERR_CUDA;
   cuuint64_t dims[3] = {(cuuint64_t)D, (cuuint64_t)Hq, (cuuint64_t)total_q};
   cuuint64_t strides[2] = {(cuuint64_t)D * 2, (cuuint64_t)Hq * D * 2};
-  cuuint32_t box[3] = {64u, (cuuint32_t)g, (cuuint32_t)(kTcRows / g)};
+  cuuint32_t box[3] = {64u, (cuuint32_t)g, (cuuint32_t)(rows / g)};
   cuuint32_t estr[3] = {1u, 1u, 1u};
   CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(q), dims, strides,
                   box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
@@ -93,13 +94,13 @@ pa_status make_q_map(CUtensorMap* map, const void* q, int64_t total_q, int Hq, i
 struct pa_plan_s {
   int32_t num_seqs, Hq, Hkv, D, block_size, max_blocks, g;
   int64_t total_q;
-  int32_t n_dec, n_tc, n_tc2, n_groups;
+  int32_t n_dec, n_tc, n_tc2, n_tcd, n_groups;
   int32_t dec_rows_max;
   int64_t n_part_rows;
   int32_t chunk;
   int64_t kv_tokens;
   // workspace layout (byte offsets)
-  size_t off_dec, off_tc, off_tc2, off_groups, off_acc, off_ml, ws_bytes;
+  size_t off_dec, off_tc, off_tc2, off_tcd, off_groups, off_acc, off_ml, ws_bytes;
   size_t table_bytes;       // bytes of the item / group tables (copied each call)
   void* host_tables;        // table image: [dec][tc][tc pair items][groups] at their offsets
   bool host_pinned;
@@ -124,7 +125,7 @@ int device_sms() {
 }
 
 // Kernel a work item runs on (the path number pa_plan_export reports).
-enum Path : int { kPathDec = 0, kPathTc = 1, kPathTcPair = 2 };
+enum Path : int { kPathDec = 0, kPathTc = 1, kPathTcPair = 2, kPathTcDecode = 3 };
 
 struct Unit {
   int32_t seq, kvh, row_begin, row_count, keys, q_row0;
@@ -233,7 +234,7 @@ pa_status pa_plan_create(const int32_t* h_context_lens, const int32_t* h_query_l
   memset(&o, 0, sizeof o);
   if (opts) {
     o = *opts;
-    for (int i = 0; i < 4; ++i)
+    for (int i = 0; i < 3; ++i)
       if (o.reserved[i]) return PA_ERR_INVALID_ARG;
   }
   const int g = Hq / Hkv;
@@ -255,6 +256,8 @@ pa_status pa_plan_create(const int32_t* h_context_lens, const int32_t* h_query_l
                           o.tc_min_rows >= 0;
   const int tc_min_rows = o.tc_min_rows > 0 ? o.tc_min_rows : pa::kTcMinRowsDefault;
   const bool pair_enabled = tc_enabled && o.tc_pair >= 0;
+  // (sequence, KV head) pairs with at most 16 rows: keys on the 128-row side
+  const bool tcd_enabled = tc_enabled && (pa::kTcdRows % g == 0) && o.tc_decode >= 0;
 
   // ---- units: (sequence, KV head, row tile). Tensor-core rows go in tiles of 256
   // (two 128-row halves sharing every K/V tile) while more than 128 rows remain,
@@ -273,6 +276,8 @@ pa_status pa_plan_create(const int32_t* h_context_lens, const int32_t* h_query_l
           int path, rt;
           if (!tc) {
             path = kPathDec; rt = pa::kDecRows;
+          } else if (tcd_enabled && rows <= pa::kTcdRows) {
+            path = kPathTcDecode; rt = pa::kTcdRows;
           } else if (pair_enabled && left > pa::kTcRows) {
             path = kPathTcPair; rt = 2 * pa::kTcRows;
           } else {
@@ -298,14 +303,17 @@ pa_status pa_plan_create(const int32_t* h_context_lens, const int32_t* h_query_l
     chunk = std::max<int64_t>(256, align_up((size_t)(total_keys / (3 * (int64_t)sms) + 1),
                                             pa::kChunkAlign));
   }
-  std::vector<Item> dec, tc, tc2;
+  std::vector<Item> dec, tc, tc2, tcd;
   std::vector<SplitGroup> groups;
   int64_t part_rows = 0;
   int32_t dec_rows_max = 1;
   bool any_split = false;
   for (const Unit& u : units) {
     const int64_t n_chunks = (u.keys + chunk - 1) / chunk;
-    std::vector<Item>& dst = u.path == kPathDec ? dec : (u.path == kPathTc ? tc : tc2);
+    std::vector<Item>& dst = u.path == kPathDec ? dec
+                             : u.path == kPathTc ? tc
+                             : u.path == kPathTcPair ? tc2
+                                                     : tcd;
     if (u.path == kPathDec) dec_rows_max = std::max(dec_rows_max, u.row_count);
     if (n_chunks <= 1) {
       dst.push_back({u.seq, u.kvh, u.row_begin, u.row_count, 0, u.keys, -1, u.q_row0});
@@ -331,12 +339,14 @@ pa_status pa_plan_create(const int32_t* h_context_lens, const int32_t* h_query_l
   std::stable_sort(dec.begin(), dec.end(), longer);
   std::stable_sort(tc.begin(), tc.end(), longer);
   std::stable_sort(tc2.begin(), tc2.end(), longer);
+  std::stable_sort(tcd.begin(), tcd.end(), longer);
 
   pa_plan_s* p = new (std::nothrow) pa_plan_s();
   if (!p) return PA_ERR_INVALID_ARG;
   p->num_seqs = num_seqs; p->Hq = Hq; p->Hkv = Hkv; p->D = D; p->block_size = block_size;
   p->max_blocks = max_blocks_per_seq; p->g = g; p->total_q = total_q;
   p->n_dec = (int32_t)dec.size(); p->n_tc = (int32_t)tc.size(); p->n_tc2 = (int32_t)tc2.size();
+  p->n_tcd = (int32_t)tcd.size();
   p->n_groups = (int32_t)groups.size();
   p->dec_rows_max = dec_rows_max; p->n_part_rows = part_rows;
   p->chunk = any_split ? (int32_t)chunk : 0; p->kv_tokens = kv_tokens;
@@ -344,6 +354,7 @@ pa_status pa_plan_create(const int32_t* h_context_lens, const int32_t* h_query_l
   p->off_dec = off; off = align_up(off + dec.size() * sizeof(Item), 256);
   p->off_tc = off; off = align_up(off + tc.size() * sizeof(Item), 256);
   p->off_tc2 = off; off = align_up(off + tc2.size() * sizeof(Item), 256);
+  p->off_tcd = off; off = align_up(off + tcd.size() * sizeof(Item), 256);
   p->off_groups = off; off = align_up(off + groups.size() * sizeof(SplitGroup), 256);
   p->table_bytes = off;
   p->off_acc = off; off = align_up(off + (size_t)part_rows * D * sizeof(float), 256);
@@ -364,6 +375,7 @@ pa_status pa_plan_create(const int32_t* h_context_lens, const int32_t* h_query_l
     if (!dec.empty()) memcpy(h + p->off_dec, dec.data(), dec.size() * sizeof(Item));
     if (!tc.empty()) memcpy(h + p->off_tc, tc.data(), tc.size() * sizeof(Item));
     if (!tc2.empty()) memcpy(h + p->off_tc2, tc2.data(), tc2.size() * sizeof(Item));
+    if (!tcd.empty()) memcpy(h + p->off_tcd, tcd.data(), tcd.size() * sizeof(Item));
     if (!groups.empty())
       memcpy(h + p->off_groups, groups.data(), groups.size() * sizeof(SplitGroup));
   }
@@ -389,9 +401,9 @@ pa_status pa_plan_get_stats(pa_plan_t p, pa_plan_stats* out) {
   out->total_q = p->total_q;
   out->num_seqs = p->num_seqs;
   out->n_dec_items = p->n_dec;
-  out->n_tc_items = p->n_tc + p->n_tc2;
+  out->n_tc_items = p->n_tc + p->n_tc2 + p->n_tcd;
   out->n_tc_pair_items = p->n_tc2;
-  out->pad = 0;
+  out->n_tc_decode_items = p->n_tcd;
   out->n_split_groups = p->n_groups;
   out->n_partials = (int32_t)p->n_part_rows;
   out->chunk_tokens = p->chunk;
@@ -402,12 +414,18 @@ pa_status pa_plan_get_stats(pa_plan_t p, pa_plan_stats* out) {
 
 pa_status pa_plan_export(pa_plan_t p, int32_t* h_items, int32_t max_items, int32_t* n_items) {
   if (!p || !n_items || max_items < 0 || (max_items > 0 && !h_items)) return PA_ERR_INVALID_ARG;
-  *n_items = p->n_dec + p->n_tc + p->n_tc2;
+  *n_items = p->n_dec + p->n_tc + p->n_tc2 + p->n_tcd;
   const uint8_t* h = static_cast<const uint8_t*>(p->host_tables);
   int32_t k = 0;
-  for (int path = 0; path < 3; ++path) {
-    const int32_t n = path == kPathDec ? p->n_dec : (path == kPathTc ? p->n_tc : p->n_tc2);
-    const size_t off = path == kPathDec ? p->off_dec : (path == kPathTc ? p->off_tc : p->off_tc2);
+  for (int path = 0; path < 4; ++path) {
+    const int32_t n = path == kPathDec ? p->n_dec
+                      : path == kPathTc ? p->n_tc
+                      : path == kPathTcPair ? p->n_tc2
+                                            : p->n_tcd;
+    const size_t off = path == kPathDec ? p->off_dec
+                       : path == kPathTc ? p->off_tc
+                       : path == kPathTcPair ? p->off_tc2
+                                             : p->off_tcd;
     const Item* it = reinterpret_cast<const Item*>(h + off);
     for (int32_t i = 0; i < n && k < max_items; ++i, ++k) {
       int32_t* r = h_items + (int64_t)k * 9;
@@ -478,7 +496,7 @@ pa_status pa_attention(pa_plan_t p, void* d_out, pa_dtype out_dtype, const void*
                                       p->n_dec, p->D, p->dec_rows_max, box_t, grid, s);
     if (e != cudaSuccess) return PA_ERR_CUDA;
   }
-  if (p->n_tc + p->n_tc2 > 0) {
+  if (p->n_tc + p->n_tc2 + p->n_tcd > 0) {
     const int box_t = std::min(p->block_size, 64);
     CUtensorMap kmap, vmap;
     pa_status st = pa::make_pool_map(&kmap, d_k_pool, num_blocks, p->block_size, p->Hkv, p->D,
@@ -487,11 +505,21 @@ pa_status pa_attention(pa_plan_t p, void* d_out, pa_dtype out_dtype, const void*
     st = pa::make_pool_map(&vmap, d_v_pool, num_blocks, p->block_size, p->Hkv, p->D, 64, box_t,
                            true);
     if (st != PA_OK) return st;
-    CUtensorMap qmap;
-    st = pa::make_q_map(&qmap, d_q, p->total_q, p->Hq, p->D, p->g);
-    if (st != PA_OK) return st;
     int sms = device_sms();
     if (sms <= 0) return PA_ERR_CUDA;
+    if (p->n_tcd > 0) {
+      CUtensorMap qmap16;
+      st = pa::make_q_map(&qmap16, d_q, p->total_q, p->Hq, p->D, p->g, pa::kTcdRows);
+      if (st != PA_OK) return st;
+      const int grid = std::min(p->n_tcd, sms);
+      cudaError_t e = pa::launch_tcd(a, kmap, vmap, qmap16,
+                                     reinterpret_cast<const Item*>(ws + p->off_tcd), p->n_tcd,
+                                     box_t, grid, s);
+      if (e != cudaSuccess) return PA_ERR_CUDA;
+    }
+    CUtensorMap qmap;
+    st = pa::make_q_map(&qmap, d_q, p->total_q, p->Hq, p->D, p->g, pa::kTcRows);
+    if (st != PA_OK) return st;
     if (p->n_tc2 > 0) {
       const int grid = std::min(p->n_tc2, sms);
       cudaError_t e = pa::launch_tc2(a, kmap, vmap, qmap,

@@ -38,6 +38,7 @@ static_assert(sizeof(SplitGroup) == 32, "SplitGroup is 32 bytes");
 
 constexpr int kDecRows = 8;     // rows a CUDA-core item holds at most
 constexpr int kTcRows = 128;    // rows of a tensor-core item (one M tile)
+constexpr int kTcdRows = 16;    // rows of a key-major tensor-core decode item (N)
 constexpr int kKeyTile = 64;    // keys per pipeline stage of the decode kernel
 constexpr int kChunkAlign = 64;   // split-KV chunk boundaries are multiples of this
 
@@ -87,15 +88,21 @@ int decode_smem_bytes(int D, int rows_max);
 cudaError_t launch_tc(const AttnArgs& a, const CUtensorMap& kmap, const CUtensorMap& vmap,
                       const CUtensorMap& qmap, const Item* items, int32_t n_items, int box_t,
                       int grid, cudaStream_t s);
-// 3-D tiled map over q viewed as [total_q][Hq][D] bf16 with box (64, g, 128 / g), 128-byte
-// swizzle: one box is the 128 packed rows (tokens x the g heads of a KV head) of one D half.
-pa_status make_q_map(CUtensorMap* map, const void* q, int64_t total_q, int Hq, int D, int g);
+// 3-D tiled map over q viewed as [total_q][Hq][D] bf16 with box (64, g, rows / g), 128-byte
+// swizzle: one box is `rows` packed rows (tokens x the g heads of a KV head) of one D half.
+pa_status make_q_map(CUtensorMap* map, const void* q, int64_t total_q, int Hq, int D, int g,
+                     int rows);
 int tc_smem_bytes();
 // Items of 129..256 rows: two 128-row tiles per CTA that share every K/V tile.
 cudaError_t launch_tc2(const AttnArgs& a, const CUtensorMap& kmap, const CUtensorMap& vmap,
                        const CUtensorMap& qmap, const Item* items, int32_t n_items, int box_t,
                        int grid, cudaStream_t s);
 int tc2_smem_bytes();
+// Items of at most 16 rows: keys on the 128-row side (S^T = K Q^T, O^T = V^T P^T).
+cudaError_t launch_tcd(const AttnArgs& a, const CUtensorMap& kmap, const CUtensorMap& vmap,
+                       const CUtensorMap& qmap, const Item* items, int32_t n_items, int box_t,
+                       int grid, cudaStream_t s);
+int tcd_smem_bytes();
 constexpr int kTcMinRowsDefault = 4;   // items with at least this many rows use tensor cores
 
 }  // namespace pa

@@ -154,6 +154,30 @@ def test_plan_pair_tiles(pa):
     assert p1.stats()["n_tc_pair_items"] == 0
 
 
+def test_plan_decode_items(pa):
+    """A (sequence, KV head) pair with at most 16 tensor-core rows becomes one item of
+    path 3 (keys on the 128-row side) when Hq / Hkv divides 16; tc_decode=-1 disables it."""
+    L = [300, 1000, 700, 40, 2000]
+    q = [1, 2, 3, 40, 1]
+    for g in (1, 2, 4, 8, 16):
+        Hkv = 2
+        p = plan(pa, L, q, Hq=g * Hkv, Hkv=Hkv, D=128, max_chunk_tokens=256, tc_min_rows=1)
+        items = p.items()
+        _coverage(items, L, q, g, Hkv)
+        for path, s, kvh, rb, rc, *_ in items:
+            if q[s] * g <= 16:
+                assert path == 3 and rb == 0 and rc == q[s] * g
+            else:
+                assert path in (1, 2)
+        st = p.stats()
+        assert st["n_tc_decode_items"] == sum(1 for it in items if it[0] == 3)
+        p1 = plan(pa, L, q, Hq=g * Hkv, Hkv=Hkv, D=128, tc_min_rows=1, tc_decode=-1)
+        assert 3 not in set(p1.items()[:, 0].tolist())
+    # g = 3 does not divide 16: no such items
+    p3 = plan(pa, L, q, Hq=6, Hkv=2, D=128, tc_min_rows=1)
+    assert p3.stats()["n_tc_decode_items"] == 0
+
+
 def test_plan_orders_longest_first(pa):
     L = list(range(100, 2100, 50))
     p = plan(pa, L, [1] * len(L))

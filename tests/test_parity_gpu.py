@@ -132,6 +132,57 @@ def test_tensor_core_pair_tiny_first(pa):
     assert got["plan"].stats()["n_tc_pair_items"] == 1
 
 
+DECODE_CASES = [
+    # (g, block_size, chunk): items of at most 16 rows, keys on the 128-row side
+    (1, 16, 0), (2, 32, 0), (4, 16, 128), (8, 8, 0), (8, 256, 64), (16, 64, 0),
+]
+
+
+@pytest.mark.parametrize("g,B,chunk", DECODE_CASES)
+def test_tensor_core_decode_items(pa, g, B, chunk):
+    """Decode-like items (q x g <= 16 rows) on the key-major tensor-core kernel: ragged
+    contexts around the 16- and 128-key edges, oracle and the other paths agree."""
+    q = [1, 1, 1, 1, max(1, 16 // g), 1, max(1, 8 // g)]
+    L = [1, 15, 128, 129, 300, 1000, 2049]
+    w = workloads.make_custom(L, q, Hq=2 * g, Hkv=2, D=128, block_size=B, seed=500 + g + B)
+    kw = dict(tc_min_rows=1)
+    if chunk:
+        kw["max_chunk_tokens"] = chunk
+    (_, _), run, want = full_check(pa, w, **kw)
+    assert run["plan"].stats()["n_tc_decode_items"] > 0
+    (_, _), other, _ = full_check(pa, w, tc_decode=-1, **kw)
+    assert other["plan"].stats()["n_tc_decode_items"] == 0
+    assert torch.allclose(run["out"], other["out"], atol=gu.ATOL_MAX, rtol=0)
+
+
+def test_tensor_core_decode_tiny_first(pa):
+    """Smallest key-major case: one row, one key."""
+    w = workloads.make_custom([1], [1], Hq=1, Hkv=1, D=128, block_size=16, seed=13)
+    (_, _), got, _ = full_check(pa, w, tc_min_rows=1)
+    assert got["plan"].stats()["n_tc_decode_items"] == 1
+
+
+def test_tensor_core_decode_nan_tail_and_bf16(pa):
+    """Slots past each context hold NaN; the block tail inside the last 16-key step must
+    not reach the output. bf16 output too."""
+    w = workloads.make_custom([9, 20, 3, 130, 1001], [1, 1, 1, 1, 1], Hq=8, Hkv=2, D=128,
+                              block_size=32, seed=15)
+    used = np.zeros((w.num_blocks, w.block_size), bool)
+    for s_, l_ in enumerate(w.context_lens):
+        for t_ in range(int(l_)):
+            used[w.block_table[s_, t_ // w.block_size], t_ % w.block_size] = True
+    nan = torch.tensor(float("nan"), dtype=torch.bfloat16)
+    w.k_pool[torch.from_numpy(~used)] = nan
+    w.v_pool[torch.from_numpy(~used)] = nan
+    got = gu.gpu_step(pa, w, tc_min_rows=1)
+    assert got["plan"].stats()["n_tc_decode_items"] > 0
+    want = gu.oracle_rows(w, gu.oracle_step(w))
+    gu.assert_attention_close(got["out"].cpu().numpy(), want, "nan tail")
+    got16 = gu.gpu_step(pa, w, out_dtype=torch.bfloat16, tc_min_rows=1)
+    d = np.abs(got16["out"].float().cpu().numpy() - want)
+    assert np.all(np.isfinite(d)) and d.max() <= 2e-2
+
+
 def test_unused_slots_hold_nan(pa):
     """Slots past each context (tail of the last block, unused blocks) hold NaN: no effect."""
     w = workloads.make_custom([9, 20, 3, 130], [2, 3, 3, 1], Hq=4, Hkv=2, D=128, block_size=16,
