@@ -31,7 +31,12 @@ METRIC = "paged attn tokens/s and achieved HBM GB/s / TC util vs roofline (1×GB
 UNIT = "tokens/s"
 PROFILE_TRAFFIC = os.path.join(ROOT, "profiles", "traffic.json")
 KERNEL_SOURCES = {"decode": ["pa_dec.cu", "pa_ptx.cuh", "pa_internal.h"],
-                  "tc": ["pa_tc.cu", "pa_tc.cuh", "pa_ptx.cuh", "pa_internal.h"]}
+                  "tc": ["pa_tc.cu", "pa_tc.cuh", "pa_ptx.cuh", "pa_internal.h"],
+                  "tc2": ["pa_tc2.cu", "pa_tc.cuh", "pa_ptx.cuh", "pa_internal.h"],
+                  "tcd": ["pa_tcd.cu", "pa_tc.cuh", "pa_ptx.cuh", "pa_internal.h"]}
+# kernel symbol of each (for the launch-list summaries)
+KERNEL_NAMES = {"decode": "decode_kernel", "tc": "tc_kernel", "tc2": "tc2_kernel",
+                "tcd": "tcd_kernel"}
 
 
 def log(*a):
@@ -317,10 +322,10 @@ def run_gpu(args, w, cfg_name, rank, local, world):
 
     T = w.total_q
     value = T * args.steps * world / (elapsed_ms / 1000.0)
-    n_tc1 = st["n_tc_items"] - st["n_tc_pair_items"]
+    n_tc1 = st["n_tc_items"] - st["n_tc_pair_items"] - st["n_tc_decode_items"]
     launches_per_step = 1 + (1 if n_pairs else 0) + 1 + (1 if st["n_dec_items"] else 0) + \
         (1 if n_tc1 else 0) + (1 if st["n_tc_pair_items"] else 0) + \
-        (1 if st["n_split_groups"] else 0)
+        (1 if st["n_tc_decode_items"] else 0) + (1 if st["n_split_groups"] else 0)
 
     # ---- roofline of the dominant kernel (paged attention)
     peaks = measured_peaks()
@@ -334,11 +339,11 @@ def run_gpu(args, w, cfg_name, rank, local, world):
     bound = "hbm" if t_hbm >= t_tc else "tensor"
     # the attention call runs one kernel when the plan holds one kind of item; its
     # committed DRAM counters apply while that kernel's sources are unchanged
-    kernel = None
-    if st["n_dec_items"] and not st["n_tc_items"]:
-        kernel = "decode"
-    elif st["n_tc_items"] and not st["n_dec_items"]:
-        kernel = "tc"
+    n_tcd, n_tc2 = st["n_tc_decode_items"], st["n_tc_pair_items"]
+    n_tc1 = st["n_tc_items"] - n_tcd - n_tc2
+    kinds = {k: n for k, n in (("decode", st["n_dec_items"]), ("tc", n_tc1), ("tc2", n_tc2),
+                               ("tcd", n_tcd)) if n}
+    kernel = next(iter(kinds)) if len(kinds) == 1 and not st["n_split_groups"] else None
     traffic = None
     if kernel and os.path.exists(PROFILE_TRAFFIC):
         with open(PROFILE_TRAFFIC) as f:
@@ -350,12 +355,14 @@ def run_gpu(args, w, cfg_name, rank, local, world):
         achieved = (kv_b + q_b) / attn_s / 1e9
         roof = {"bound": "hbm", "achieved": achieved, "peak": hbm_peak, "unit": "GB/s",
                 "frac": achieved / hbm_peak, "traffic": traffic,
-                "peak_source": f"{peaks['_source']} hbm_gbs"}
+                "peak_source": f"{peaks['_source']} hbm_gbs",
+                "kernels": [KERNEL_NAMES[k] for k in kinds]}
     else:
         achieved = flops / attn_s / 1e12
         roof = {"bound": "tensor", "achieved": achieved, "peak": tc_peak, "unit": "TFLOP/s",
                 "frac": achieved / tc_peak, "traffic": traffic,
-                "peak_source": f"{peaks['_source']} bf16_tflops"}
+                "peak_source": f"{peaks['_source']} bf16_tflops",
+                "kernels": [KERNEL_NAMES[k] for k in kinds]}
 
     # ---- end to end through the public API, host buffers in pinned memory
     pin = lambda t: t.cpu().pin_memory()

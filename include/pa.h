@@ -131,9 +131,11 @@ typedef struct pa_plan_s* pa_plan_t;
 typedef struct {
   int32_t max_chunk_tokens;  /* 0: automatic split-KV; >0: split key ranges into chunks of at
                                 most this many tokens (rounded up to 64) */
-  int32_t tc_min_rows;       /* 0: default (4); >0: items with at least this many rows (query
-                                tokens x packed heads) use the tensor-core kernel; <0: never.
-                                Tensor-core items need D = 128, block_size >= 8 and
+  int32_t tc_min_rows;       /* 0: default: 1 where the key-major kernel takes pairs of at
+                                most 16 rows (tc_decode on, Hq / Hkv dividing 16), else 4;
+                                >0: (sequence, KV head) pairs with at least this many rows
+                                (query tokens x packed heads) use the tensor cores; <0:
+                                never. Tensor-core items need D = 128, block_size >= 8 and
                                 Hq / Hkv dividing 128. */
   int32_t num_sms;           /* 0: query the current device */
   int32_t tc_pair;           /* 0: default (on): tensor-core rows go in 256-row items (two

@@ -254,10 +254,14 @@ pa_status pa_plan_create(const int32_t* h_context_lens, const int32_t* h_query_l
   // g dividing the 128-row tile (a tile is whole tokens x the g heads of one KV head).
   const bool tc_enabled = (D == 128) && (block_size >= 8) && (pa::kTcRows % g == 0) &&
                           o.tc_min_rows >= 0;
-  const int tc_min_rows = o.tc_min_rows > 0 ? o.tc_min_rows : pa::kTcMinRowsDefault;
   const bool pair_enabled = tc_enabled && o.tc_pair >= 0;
   // (sequence, KV head) pairs with at most 16 rows: keys on the 128-row side
   const bool tcd_enabled = tc_enabled && (pa::kTcdRows % g == 0) && o.tc_decode >= 0;
+  // by default every row count goes to the tensor cores when the key-major kernel takes
+  // the small ones; otherwise pairs with fewer than kTcMinRowsDefault rows stay on the
+  // CUDA cores
+  const int tc_min_rows =
+      o.tc_min_rows > 0 ? o.tc_min_rows : (tcd_enabled ? 1 : pa::kTcMinRowsDefault);
 
   // ---- units: (sequence, KV head, row tile). Tensor-core rows go in tiles of 256
   // (two 128-row halves sharing every K/V tile) while more than 128 rows remain,

@@ -103,6 +103,7 @@ cudaError_t launch_tcd(const AttnArgs& a, const CUtensorMap& kmap, const CUtenso
                        const CUtensorMap& qmap, const Item* items, int32_t n_items, int box_t,
                        int grid, cudaStream_t s);
 int tcd_smem_bytes();
-constexpr int kTcMinRowsDefault = 4;   // items with at least this many rows use tensor cores
+constexpr int kTcMinRowsDefault = 4;   // without the key-major kernel: rows from which the
+                                       // tensor cores take a (sequence, KV head) pair
 
 }  // namespace pa

@@ -15,8 +15,10 @@
 //
 // Warps (6, one persistent CTA per SM):
 //   0     TMA producer: the item's 16 query rows (double-buffered across items),
-//         K and V tiles of 128 keys per block piece into a 3-stage ring.
-//   1     MMA issuer: S^T of tile n + 1 is issued before P V of tile n.
+//         K and V tiles of 128 keys per block piece into two 3-stage rings with
+//         their own barriers (a K stage is free once its S^T is done).
+//   1     MMA issuer: issues whichever of the next S^T (up to two tiles ahead)
+//         and the next P V is ready, so neither waits behind the other's data.
 //   2-5   softmax: thread = key of the tile (TMEM lane), then = head dimension for
 //         the O rescale and the epilogue. P^T goes to shared memory (bf16, the
 //         K-major B operand of the second product).
@@ -58,7 +60,8 @@ struct TcdSmem {
   uint8_t p[2][2][kQHalf];              // P^T [tile parity][key half], 16 rows x 64 keys
   float red[2][4][kN];                  // cross-warp partial maxima / sums [parity][warp][row]
   int bt_cache[2][kBtCache];
-  uint64_t kv_full[kStages], kv_empty[kStages];
+  uint64_t k_full[kStages], k_empty[kStages];
+  uint64_t v_full[kStages], v_empty[kStages];
   uint64_t q_full[2], q_free[2];
   uint64_t s_full[2], s_free[2];
   uint64_t p_full[2], p_free[2];
@@ -67,7 +70,8 @@ struct TcdSmem {
   uint64_t xbar;                        // the 4 softmax warps met (128 arrivals)
   uint64_t drain;
   uint32_t tmem_base;
-  int issued[kStages], consumed[kStages];
+  int k_issued[kStages], k_consumed[kStages];
+  int v_issued[kStages], v_consumed[kStages];
   int q_issued[2], q_consumed[2];
   int abort_flag;
 };
@@ -120,10 +124,12 @@ __global__ void __launch_bounds__(kThreadsD, 1)
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < kStages; ++s) {
-      mbar_init(&sm.kv_full[s], 1);
-      mbar_init(&sm.kv_empty[s], 1);
-      sm.issued[s] = 0;
-      sm.consumed[s] = 0;
+      mbar_init(&sm.k_full[s], 1);
+      mbar_init(&sm.k_empty[s], 1);
+      mbar_init(&sm.v_full[s], 1);
+      mbar_init(&sm.v_empty[s], 1);
+      sm.k_issued[s] = sm.k_consumed[s] = 0;
+      sm.v_issued[s] = sm.v_consumed[s] = 0;
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(&sm.q_full[b], 1);
@@ -201,8 +207,6 @@ __global__ void __launch_bounds__(kThreadsD, 1)
       const int32_t* bt = a.block_table + (int64_t)item.seq * a.max_blocks;
       for (int t0 = item.kv_begin; t0 < item.kv_end; t0 += kKeys, ++n) {
         const int st = n % kStages;
-        ok = mbar_wait_warp(&sm.kv_empty[st], ph(n, kStages) ^ 1u, a.err);
-        if (!ok || *(volatile int*)&sm.abort_flag) { ok = false; break; }
         bool valid = false;
         int tok = 0;
         if (lane < pieces) {
@@ -220,17 +224,28 @@ __global__ void __launch_bounds__(kThreadsD, 1)
             }
           }
         }
-        const uint32_t cnt = __popc(__ballot_sync(0xffffffffu, valid));
-        if (lane == 0) mbar_arrive_expect_tx(&sm.kv_full[st], cnt * piece_bytes * 4u);
+        const uint32_t tile_bytes = __popc(__ballot_sync(0xffffffffu, valid)) * piece_bytes * 2u;
+        const uint32_t row_off = (uint32_t)lane * box_t * 128u;
+        // K_n: its stage is free once S^T of tile n - 3 is done
+        ok = mbar_wait_warp(&sm.k_empty[st], ph(n, kStages) ^ 1u, a.err);
+        if (!ok || *(volatile int*)&sm.abort_flag) { ok = false; break; }
+        if (lane == 0) mbar_arrive_expect_tx(&sm.k_full[st], tile_bytes);
         __syncwarp();
         if (valid) {
-          const uint32_t row_off = (uint32_t)lane * box_t * 128u;
-          tma_load_3d(&sm.k[st][0][row_off], &kmap, &sm.kv_full[st], 0, item.kv_head, tok);
-          tma_load_3d(&sm.k[st][1][row_off], &kmap, &sm.kv_full[st], 64, item.kv_head, tok);
-          tma_load_3d(&sm.v[st][0][row_off], &vmap, &sm.kv_full[st], 0, item.kv_head, tok);
-          tma_load_3d(&sm.v[st][1][row_off], &vmap, &sm.kv_full[st], 64, item.kv_head, tok);
+          tma_load_3d(&sm.k[st][0][row_off], &kmap, &sm.k_full[st], 0, item.kv_head, tok);
+          tma_load_3d(&sm.k[st][1][row_off], &kmap, &sm.k_full[st], 64, item.kv_head, tok);
         }
-        if (lane == 0) sm.issued[st] += 1;
+        if (lane == 0) sm.k_issued[st] += 1;
+        // V_n: free once P V of tile n - 3 is done
+        ok = mbar_wait_warp(&sm.v_empty[st], ph(n, kStages) ^ 1u, a.err);
+        if (!ok || *(volatile int*)&sm.abort_flag) { ok = false; break; }
+        if (lane == 0) mbar_arrive_expect_tx(&sm.v_full[st], tile_bytes);
+        __syncwarp();
+        if (valid) {
+          tma_load_3d(&sm.v[st][0][row_off], &vmap, &sm.v_full[st], 0, item.kv_head, tok);
+          tma_load_3d(&sm.v[st][1][row_off], &vmap, &sm.v_full[st], 64, item.kv_head, tok);
+        }
+        if (lane == 0) sm.v_issued[st] += 1;
       }
       if (has_next) {
         bt_store(sm.bt_cache[(k + 1) & 1], nb, lane);
@@ -241,117 +256,130 @@ __global__ void __launch_bounds__(kThreadsD, 1)
     if (!ok) sm.abort_flag = 1;
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
-    // S^T of tile n + 1 goes out before P V of tile n, so the softmax of the next tile
-    // can start while this one's P V runs. Phase bounds: kv_full of tile n + 3 needs
-    // kv_empty(n), committed after P V(n); s_free / p_full of tile n + 2 need the
-    // softmax of tile n + 2, which needs s_full(n + 2) from here; q_full of item k + 2
-    // needs q_free(k) from here; o_free of item k + 1 needs the P V of item k + 1.
+    // An event loop over two cursors: the next S^T (at most two tiles ahead of P V, one
+    // per S^T buffer) and the next P V, each issued as soon as its barriers show it is
+    // ready. Phase bounds: k_full / v_full of tile n + 3 need S^T / P V of tile n;
+    // s_free / p_full of tile n + 2 need the softmax of tile n + 2, which needs
+    // s_full(n + 2) from here; q_full of item k + 2 needs q_free(k) from here; o_free
+    // of item k + 1 needs the P V of item k + 1. So every check below looks at the
+    // phase it means.
     if (lane == 0) {
       bool ok = true;
-      // S^T cursor (item index it_s, k_s-th item of the CTA, tile j_s of it, global n_s)
+      // S^T cursor: item index it_s, the CTA's k_s-th item, its tile j_s, CTA tile n_s
       int it_s = blockIdx.x, k_s = 0, j_s = 0, n_s = 0;
       int nt_s = it_s < n_items ? tiles_of(items[it_s]) : 0;
+      uint64_t qd = 0;
       // P V cursor
       int it_p = blockIdx.x, k_p = 0, j_p = 0, n_p = 0;
       Item item_p = it_p < n_items ? items[it_p] : Item{};
       int nt_p = it_p < n_items ? tiles_of(item_p) : 0;
-      uint64_t qd = 0;
-      auto issue_s = [&]() -> bool {
-        const int st = n_s % kStages;
-        const int b = n_s & 1;
-        if (j_s == 0) {
-          if (!mbar_wait(&sm.q_full[k_s & 1], ph(k_s, 2), a.err)) return false;
-          sm.q_consumed[k_s & 1] += 1;
-          tc::fence_after_sync();
-          qd = tc::smem_desc_sw128(smem_addr(&sm.q[k_s & 1][0][0]), 16, 1024);
-        }
-        if (!mbar_wait(&sm.kv_full[st], ph(n_s, kStages), a.err)) return false;
-        sm.consumed[st] += 1;
-        if (!mbar_wait(&sm.s_free[b], ph(n_s, 2) ^ 1u, a.err)) return false;
-        tc::fence_after_sync();
-        // S^T = K Q^T: 8 steps of 16 dims; step kk starts (kk / 4) D halves and (kk % 4)
-        // 32-byte chunks into both operands
-        const uint64_t kd = tc::smem_desc_sw128(smem_addr(&sm.k[st][0][0]), 16, 1024);
-        tc::mma_bf16_c<false>(tmem + (uint32_t)b * kN, kd, qd, kIdescS);
+      uint64_t t_idle = global_timer_ns();
+      while (it_p < n_items) {
+        bool progress = false;
+        if (it_s < n_items && n_s < n_p + 2) {
+          const int st = n_s % kStages;
+          const int b = n_s & 1;
+          if ((j_s > 0 || mbar_try_wait(smem_addr(&sm.q_full[k_s & 1]), ph(k_s, 2))) &&
+              mbar_try_wait(smem_addr(&sm.k_full[st]), ph(n_s, kStages)) &&
+              mbar_try_wait(smem_addr(&sm.s_free[b]), ph(n_s, 2) ^ 1u)) {
+            if (j_s == 0) {
+              sm.q_consumed[k_s & 1] += 1;
+              qd = tc::smem_desc_sw128(smem_addr(&sm.q[k_s & 1][0][0]), 16, 1024);
+            }
+            sm.k_consumed[st] += 1;
+            tc::fence_after_sync();
+            // S^T = K Q^T: 8 steps of 16 dims; step kk starts (kk / 4) D halves and
+            // (kk % 4) 32-byte chunks into both operands
+            const uint64_t kd = tc::smem_desc_sw128(smem_addr(&sm.k[st][0][0]), 16, 1024);
+            tc::mma_bf16_c<false>(tmem + (uint32_t)b * kN, kd, qd, kIdescS);
 #pragma unroll
-        for (int kk = 1; kk < kD / 16; ++kk) {
-          const uint64_t ko = (uint64_t)(((kk >> 2) * kHalf + (kk & 3) * 32) >> 4);
-          const uint64_t qo = (uint64_t)(((kk >> 2) * kQHalf + (kk & 3) * 32) >> 4);
-          tc::mma_bf16_c<true>(tmem + (uint32_t)b * kN, kd + ko, qd + qo, kIdescS);
+            for (int kk = 1; kk < kD / 16; ++kk) {
+              const uint64_t ko = (uint64_t)(((kk >> 2) * kHalf + (kk & 3) * 32) >> 4);
+              const uint64_t qo = (uint64_t)(((kk >> 2) * kQHalf + (kk & 3) * 32) >> 4);
+              tc::mma_bf16_c<true>(tmem + (uint32_t)b * kN, kd + ko, qd + qo, kIdescS);
+            }
+            tc::commit(&sm.s_full[b]);
+            tc::commit(&sm.k_empty[st]);
+            if (j_s + 1 == nt_s) tc::commit(&sm.q_free[k_s & 1]);  // the item's last S^T
+            ++n_s;
+            if (++j_s == nt_s) {
+              j_s = 0;
+              ++k_s;
+              it_s += G;
+              nt_s = it_s < n_items ? tiles_of(items[it_s]) : 0;
+            }
+            progress = true;
+          }
         }
-        tc::commit(&sm.s_full[b]);
-        if (j_s + 1 == nt_s) tc::commit(&sm.q_free[k_s & 1]);  // the item's last S^T
-        ++n_s;
-        if (++j_s == nt_s) {
-          j_s = 0;
-          ++k_s;
-          it_s += G;
-          nt_s = it_s < n_items ? tiles_of(items[it_s]) : 0;
+        if (n_p < n_s) {
+          const int st = n_p % kStages;
+          const int b = n_p & 1;
+          // at an item's first tile, O^T must have been read out by the previous epilogue
+          if (mbar_try_wait(smem_addr(&sm.p_full[b]), ph(n_p, 2)) &&
+              (j_p > 0 || mbar_try_wait(smem_addr(&sm.o_free), ((uint32_t)k_p & 1u) ^ 1u)) &&
+              mbar_try_wait(smem_addr(&sm.v_full[st]), ph(n_p, kStages))) {
+            sm.v_consumed[st] += 1;
+            // Keys of the tile in the item's range, rounded up to the 16-key step: only
+            // those V rows are read. At the item's last tile, the rows between the
+            // range's end and that step hold whatever the block tail holds: zero them (at
+            // most 15) so that 0 * (non-finite) never reaches O.
+            const int key0 = item_p.kv_begin + j_p * kKeys;
+            const int valid = min(kKeys, item_p.kv_end - key0);
+            const int kk_end = (valid + 15) >> 4;
+            if (valid < kk_end * 16) {
+              for (int r = valid; r < kk_end * 16; ++r) {
+                uint4* v0 = reinterpret_cast<uint4*>(&sm.v[st][0][r * 128]);
+                uint4* v1 = reinterpret_cast<uint4*>(&sm.v[st][1][r * 128]);
+#pragma unroll
+                for (int q = 0; q < 8; ++q) {
+                  v0[q] = make_uint4(0, 0, 0, 0);
+                  v1[q] = make_uint4(0, 0, 0, 0);
+                }
+              }
+              tc::fence_async_shared();
+            }
+            tc::fence_after_sync();
+            // O^T += V^T P^T: step kk covers keys 16 kk .. 16 kk + 15: V rows (the
+            // MN-major A operand, D halves kHalf apart) and P^T columns (K-major B, key
+            // halves kQHalf apart)
+            const uint64_t vd = tc::smem_desc_sw128(smem_addr(&sm.v[st][0][0]), kHalf, 1024);
+            const uint64_t pd = tc::smem_desc_sw128(smem_addr(&sm.p[b][0][0]), 16, 1024);
+            if (j_p > 0)
+              tc::mma_bf16_c<true>(tmem + kColO, vd, pd, kIdescO);
+            else
+              tc::mma_bf16_c<false>(tmem + kColO, vd, pd, kIdescO);
+#pragma unroll
+            for (int kk = 1; kk < kKeys / 16; ++kk) {
+              if (kk < kk_end) {
+                const uint64_t vo = (uint64_t)((kk * 16 * 128) >> 4);
+                const uint64_t po = (uint64_t)(((kk >> 2) * kQHalf + (kk & 3) * 32) >> 4);
+                tc::mma_bf16_c<true>(tmem + kColO, vd + vo, pd + po, kIdescO);
+              }
+            }
+            tc::commit(&sm.v_empty[st]);
+            tc::commit(&sm.p_free[b]);
+            tc::commit(&sm.o_tile[b]);
+            ++n_p;
+            if (++j_p == nt_p) {
+              j_p = 0;
+              ++k_p;
+              it_p += G;
+              if (it_p < n_items) {
+                item_p = items[it_p];
+                nt_p = tiles_of(item_p);
+              }
+            }
+            progress = true;
+          }
         }
-        return true;
-      };
-      if (it_s < n_items) ok = issue_s();
-      while (ok && it_p < n_items) {
-        if (it_s < n_items && n_s <= n_p + 1) ok = issue_s();
-        if (!ok) break;
-        const int st = n_p % kStages;
-        const int b = n_p & 1;
-        if (!mbar_wait(&sm.p_full[b], ph(n_p, 2), a.err)) { ok = false; break; }
-        // at an item's first tile, O^T must have been read out by the previous epilogue
-        if (j_p == 0 && !mbar_wait(&sm.o_free, ((uint32_t)k_p & 1u) ^ 1u, a.err)) {
+        if (progress) {
+          t_idle = global_timer_ns();
+        } else if (global_timer_ns() - t_idle > kWaitLimitNs) {
+          record_error(a.err, PA_DEVERR_TIMEOUT);
           ok = false;
           break;
         }
-        // Keys of the tile in the item's range, rounded up to the 16-key step: only
-        // those V rows are read. At the item's last tile, the rows between the range's
-        // end and that step hold whatever the block tail holds: zero them (at most 15)
-        // so that 0 * (non-finite) never reaches O.
-        const int key0 = item_p.kv_begin + j_p * kKeys;
-        const int valid = min(kKeys, item_p.kv_end - key0);
-        const int kk_end = (valid + 15) >> 4;
-        if (valid < kk_end * 16) {
-          for (int r = valid; r < kk_end * 16; ++r) {
-            uint4* v0 = reinterpret_cast<uint4*>(&sm.v[st][0][r * 128]);
-            uint4* v1 = reinterpret_cast<uint4*>(&sm.v[st][1][r * 128]);
-#pragma unroll
-            for (int q = 0; q < 8; ++q) {
-              v0[q] = make_uint4(0, 0, 0, 0);
-              v1[q] = make_uint4(0, 0, 0, 0);
-            }
-          }
-          tc::fence_async_shared();
-        }
-        tc::fence_after_sync();
-        // O^T += V^T P^T: step kk covers keys 16 kk .. 16 kk + 15: V rows (the MN-major
-        // A operand, D halves kHalf apart) and P^T columns (K-major B, key halves kQHalf
-        // apart)
-        const uint64_t vd = tc::smem_desc_sw128(smem_addr(&sm.v[st][0][0]), kHalf, 1024);
-        const uint64_t pd = tc::smem_desc_sw128(smem_addr(&sm.p[b][0][0]), 16, 1024);
-        if (j_p > 0)
-          tc::mma_bf16_c<true>(tmem + kColO, vd, pd, kIdescO);
-        else
-          tc::mma_bf16_c<false>(tmem + kColO, vd, pd, kIdescO);
-#pragma unroll
-        for (int kk = 1; kk < kKeys / 16; ++kk) {
-          if (kk < kk_end) {
-            const uint64_t vo = (uint64_t)((kk * 16 * 128) >> 4);
-            const uint64_t po = (uint64_t)(((kk >> 2) * kQHalf + (kk & 3) * 32) >> 4);
-            tc::mma_bf16_c<true>(tmem + kColO, vd + vo, pd + po, kIdescO);
-          }
-        }
-        tc::commit(&sm.kv_empty[st]);
-        tc::commit(&sm.p_free[b]);
-        tc::commit(&sm.o_tile[b]);
-        ++n_p;
-        if (++j_p == nt_p) {
-          j_p = 0;
-          ++k_p;
-          it_p += G;
-          if (it_p < n_items) {
-            item_p = items[it_p];
-            nt_p = tiles_of(item_p);
-          }
-        }
+        if (*(volatile int*)&sm.abort_flag) { ok = false; break; }
       }
       if (!ok) sm.abort_flag = 1;
       tc::commit(&sm.drain);
@@ -555,9 +583,14 @@ __global__ void __launch_bounds__(kThreadsD, 1)
   if (sm.abort_flag && threadIdx.x == 0) {
     const uint64_t t0 = global_timer_ns();
     for (int s = 0; s < kStages; ++s) {
-      if (sm.issued[s] > sm.consumed[s]) {
-        const uint32_t parity = (uint32_t)(sm.issued[s] - 1) & 1u;
-        while (!mbar_try_wait(smem_addr(&sm.kv_full[s]), parity))
+      if (sm.k_issued[s] > sm.k_consumed[s]) {
+        const uint32_t parity = (uint32_t)(sm.k_issued[s] - 1) & 1u;
+        while (!mbar_try_wait(smem_addr(&sm.k_full[s]), parity))
+          if (global_timer_ns() - t0 > kWaitLimitNs) break;
+      }
+      if (sm.v_issued[s] > sm.v_consumed[s]) {
+        const uint32_t parity = (uint32_t)(sm.v_issued[s] - 1) & 1u;
+        while (!mbar_try_wait(smem_addr(&sm.v_full[s]), parity))
           if (global_timer_ns() - t0 > kWaitLimitNs) break;
       }
     }

@@ -190,7 +190,7 @@ def test_plan_auto_split_fills_the_gpu(pa):
     p = pa.Plan([100_000], [1], 8, 8, 128, 16, 100_000 // 16 + 1, num_sms=152)
     st = p.stats()
     assert st["n_split_groups"] == 8
-    assert st["n_dec_items"] >= 152
+    assert st["n_dec_items"] + st["n_tc_items"] >= 152
     # a large decode batch needs no split
     L = [1000 + 3 * i for i in range(256)]
     p2 = pa.Plan(L, [1] * 256, 40, 40, 128, 16, 200, num_sms=152)
