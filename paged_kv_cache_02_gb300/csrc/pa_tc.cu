@@ -131,6 +131,9 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
 
   if (warp == 0) {
     // ------------------------------------------------------------ TMA producer
+    // Phase bounds: q_free[b] of item k + 2 needs q_full(k + 2) from here, and
+    // kv_empty of tile n + 2 needs kv_full(n + 2) from here, so neither barrier is
+    // ever two phases ahead of the wait below.
     if (lane == 0) {
       prefetch_tensormap(&kmap);
       prefetch_tensormap(&vmap);
@@ -219,6 +222,9 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
     if (!ok) sm.abort_flag = 1;
   } else if (warp == 1) {
     // ------------------------------------------------------------ S issuer
+    // Phase bounds: q_full of item k + 2 needs q_free(k), committed here; kv_full of
+    // tile n + 2 needs kv_empty(n), i.e. P V(n), which needs s_full(n) from here;
+    // s_free of tile n + 2 needs S(n + 2) from here.
     if (lane == 0) {
       int n = 0, k = 0;
       bool ok = true;
@@ -256,6 +262,8 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
     __syncwarp();
   } else if (warp == 2) {
     // ------------------------------------------------------------ P V issuer
+    // Phase bounds: p_full of tile n + 2 needs s_full(n + 2), which needs s_free(n)
+    // committed here; o_free of item k + 1 needs the P V of item k + 1 from here.
     if (lane == 0) {
       int n = 0, k = 0;
       bool ok = true;
@@ -295,6 +303,10 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
     __syncwarp();
   } else {
     // ------------------------------------------------------------ softmax / epilogue
+    // Phase bounds: s_full of tile n + 2 needs s_free(n), i.e. P V(n), which needs
+    // p_full(n) from here; o_done[b] completes one phase per P V of tiles of parity
+    // b, and P V(n + 1) needs p_full(n + 1) from here, so the waits for P V(n - 1)
+    // (rescale) and for the item's last P V (epilogue) are never two phases behind.
     const int quad = warp & 3;                    // TMEM lane quadrant of this warp
     const int row = quad * 32 + lane;             // tile row = TMEM lane
     const uint32_t t_lane = tmem + ((uint32_t)(quad * 32) << 16);
