@@ -58,7 +58,7 @@ struct TcdSmem {
   uint8_t v[kStages][2][kHalf];
   uint8_t q[2][2][kQHalf];              // [item parity][D half], 16 rows
   uint8_t p[2][2][kQHalf];              // P^T [tile parity][key half], 16 rows x 64 keys
-  float red[2][4][kN];                  // cross-warp partial maxima / sums [parity][warp][row]
+  float4 red[2][4][kN / 4];             // cross-warp partial maxima / sums [parity][warp][row]
   int bt_cache[2][kBtCache];
   uint64_t k_full[kStages], k_empty[kStages];
   uint64_t v_full[kStages], v_empty[kStages];
@@ -91,16 +91,18 @@ __device__ __forceinline__ int tiles_of(const Item& x) {
   return (x.kv_end - x.kv_begin + kKeys - 1) / kKeys;
 }
 
-// Reduces v[0..15] over the 32 lanes of the warp with op (max or sum): afterwards
-// lane L holds in v[0] the result for row (L >> 1) & 15. Each step halves the rows a
-// lane carries and exchanges the other half with the lane `o` away.
-template <bool MAX>
-__device__ __forceinline__ void warp_reduce16(float (&v)[kN], int lane) {
+// Reduces v[0..NR) over the 32 lanes of the warp with op (max or sum). The first
+// log2(NR) steps halve the rows a lane carries (exchanging the other half with the
+// lane `o` away), the rest combine whole values; afterwards lane L holds in v[0] the
+// result for row (L >> (5 - log2 NR)) & (NR - 1), and the lanes whose low 5 - log2 NR
+// bits are zero are the writers (one per row).
+template <int NR, bool MAX>
+__device__ __forceinline__ void warp_reduce_rows(float (&v)[NR], int lane) {
 #pragma unroll
-  for (int o = 16, w = 8; o >= 2; o >>= 1, w >>= 1) {
+  for (int o = 16, w = NR / 2; w >= 1; o >>= 1, w >>= 1) {
     const bool hi = (lane & o) != 0;
 #pragma unroll
-    for (int i = 0; i < 8; ++i) {
+    for (int i = 0; i < NR / 2; ++i) {
       if (i < w) {
         const float keep = hi ? v[i + w] : v[i];
         const float give = hi ? v[i] : v[i + w];
@@ -109,8 +111,231 @@ __device__ __forceinline__ void warp_reduce16(float (&v)[kN], int lane) {
       }
     }
   }
-  const float got = __shfl_xor_sync(0xffffffffu, v[0], 1);
-  v[0] = MAX ? fmaxf(v[0], got) : v[0] + got;
+#pragma unroll
+  for (int o = 32 / NR / 2; o >= 1; o >>= 1) {
+    const float got = __shfl_xor_sync(0xffffffffu, v[0], o);
+    v[0] = MAX ? fmaxf(v[0], got) : v[0] + got;
+  }
+}
+
+template <int NR>
+__device__ __forceinline__ constexpr int log2i() {
+  return NR >= 16 ? 4 : NR >= 8 ? 3 : NR >= 4 ? 2 : NR >= 2 ? 1 : 0;
+}
+
+// The four warps' partials of rows 0..NR-1 (vector loads, all issued before use),
+// combined with op.
+template <int NR, bool MAX>
+__device__ __forceinline__ void combine4(const float4 (&red)[4][kN / 4], float (&out)[NR]) {
+  constexpr int V = (NR + 3) / 4;
+  float4 w[4][V];
+#pragma unroll
+  for (int q = 0; q < 4; ++q)
+#pragma unroll
+    for (int c = 0; c < V; ++c) w[q][c] = red[q][c];
+#pragma unroll
+  for (int r = 0; r < NR; ++r) {
+    float e[4];
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      const float4 f = w[q][r >> 2];
+      e[q] = (r & 3) == 0 ? f.x : (r & 3) == 1 ? f.y : (r & 3) == 2 ? f.z : f.w;
+    }
+    out[r] = MAX ? fmaxf(fmaxf(e[0], e[1]), fmaxf(e[2], e[3])) : (e[0] + e[1]) + (e[2] + e[3]);
+  }
+}
+
+template <int NR>
+__device__ __forceinline__ void tmem_ld_rows(uint32_t taddr, float (&v)[NR]) {
+  if constexpr (NR == 16)
+    tc::tmem_ld16(taddr, v);
+  else
+    tc::tmem_ld_n<NR>(taddr, v);
+}
+
+template <int NR>
+__device__ __forceinline__ void tmem_st_rows(uint32_t taddr, const float (&v)[NR]) {
+  if constexpr (NR == 16)
+    tc::tmem_st16(taddr, v);
+  else
+    tc::tmem_st_n<NR>(taddr, v);
+}
+
+// State of one softmax thread across items.
+struct SoftmaxThread {
+  uint32_t t_lane;  // TMEM address of this warp's lane quadrant
+  int quad, lane;
+  int kl;           // key in the tile (S^T, P^T) / head dimension (O^T)
+  uint32_t x;       // meetings of the four softmax warps so far
+  int n;            // tiles of the CTA so far
+};
+
+// Meets the other softmax warps: red[x % 2][quad][*] written before, read after.
+__device__ __forceinline__ bool meet(TcdSmem& sm, SoftmaxThread& th, int* err) {
+  tc::fence_before_sync();
+  mbar_arrive(&sm.xbar);
+  const bool r = mbar_wait_warp(&sm.xbar, th.x & 1u, err);
+  ++th.x;
+  tc::fence_after_sync();
+  return r;
+}
+
+// One item on the softmax warps, for items of at most NR rows: only the first NR
+// columns of S^T, P^T and O^T are touched (the others feed output rows that are
+// never stored). Returns false if a bounded wait ran out.
+template <int NR>
+__device__ bool softmax_item(TcdSmem& sm, const AttnArgs& a, const Item& item, int L, int ql,
+                             SoftmaxThread& th) {
+  constexpr int H = (NR + 1) / 2;            // P^T rows written by the even lane of a pair
+  const int nt = tiles_of(item);
+  // causal limit of each row (-1: not a row of the item)
+  int lim[NR];
+  float m_used[NR], l_part[NR];
+#pragma unroll
+  for (int r = 0; r < NR; ++r) {
+    lim[r] = r < item.row_count ? min(item.kv_end - 1, L - ql + (item.row_begin + r) / a.g) : -1;
+    m_used[r] = -INFINITY;
+    l_part[r] = 0.f;
+  }
+  for (int j = 0; j < nt; ++j, ++th.n) {
+    const int n = th.n;
+    const int b = n & 1;
+    const int key = item.kv_begin + j * kKeys + th.kl;
+    // ---- scores of this thread's key for the rows; the buffer is free again after
+    float s[NR];
+    if (!mbar_wait_warp(&sm.s_full[b], ph(n, 2), a.err)) return false;
+    tc::fence_after_sync();
+    tmem_ld_rows<NR>(th.t_lane + (uint32_t)b * kN, s);
+    tc::fence_before_sync();
+    mbar_arrive(&sm.s_free[b]);
+    // causal mask (keys past the range fail it too); a masked score is -inf
+#pragma unroll
+    for (int r = 0; r < NR; ++r)
+      if (key > lim[r]) s[r] = -INFINITY;
+    // ---- row maxima over the tile's 128 keys
+    {
+      float v[NR];
+#pragma unroll
+      for (int r = 0; r < NR; ++r) v[r] = s[r];
+      warp_reduce_rows<NR, true>(v, th.lane);
+      constexpr int sh = 5 - log2i<NR>();
+      if ((th.lane & ((1 << sh) - 1)) == 0)
+        reinterpret_cast<float*>(sm.red[th.x & 1][th.quad])[(th.lane >> sh) & (NR - 1)] = v[0];
+    }
+    const uint32_t xb = th.x & 1;
+    if (!meet(sm, th, a.err)) return false;
+    float mt[NR];
+    combine4<NR, true>(sm.red[xb], mt);
+    float alpha[NR];
+    bool any_rescale = false;
+#pragma unroll
+    for (int r = 0; r < NR; ++r) {
+      const float m_new = fmaxf(m_used[r], mt[r] * a.scale_log2);
+      alpha[r] = 1.f;
+      if (m_used[r] == -INFINITY) {
+        m_used[r] = m_new;                      // nothing accumulated yet
+      } else if (m_new > m_used[r] + kRescaleLog2) {
+        alpha[r] = fast_exp2(m_used[r] - m_new);
+        m_used[r] = m_new;
+        any_rescale = true;
+      }
+    }
+    // every thread saw the same maxima: the decision is uniform across the warps
+    if (any_rescale) {
+      // O^T must be idle: wait for the previous tile's P V
+      if (!mbar_wait_warp(&sm.o_tile[(n - 1) & 1], ph(n - 1, 2), a.err)) return false;
+      tc::fence_after_sync();
+      float o[NR];
+      tmem_ld_rows<NR>(th.t_lane + kColO, o);
+#pragma unroll
+      for (int r = 0; r < NR; ++r) o[r] *= alpha[r];
+      tmem_st_rows<NR>(th.t_lane + kColO, o);
+      tc::tmem_wait_st();
+#pragma unroll
+      for (int r = 0; r < NR; ++r) l_part[r] *= alpha[r];
+    }
+    // ---- P^T = 2^(scale s - m): bf16 pairs of neighbouring keys, one row each
+    float p[NR];
+#pragma unroll
+    for (int r = 0; r < NR; ++r) {
+      const float neg_m = (m_used[r] == -INFINITY) ? 0.f : -m_used[r];
+      p[r] = fast_exp2(fmaf(s[r], a.scale_log2, neg_m));
+      l_part[r] += p[r];
+    }
+    // P^T buffer b is free once the P V of tile n - 2 is done
+    if (!mbar_wait_warp(&sm.p_free[b], ph(n, 2) ^ 1u, a.err)) return false;
+    {
+      // the even lane of a pair writes rows 0..H-1 for keys (kl, kl + 1), the odd lane
+      // rows H..NR-1; K-major, 128-byte swizzle: row r, key k at key half k / 64,
+      // 16-byte chunk (k % 64) / 8 ^ (r % 8)
+      const bool odd = th.lane & 1;
+      const int k0 = th.kl & ~1;
+      uint8_t* pb = &sm.p[b][k0 >> 6][0];
+      const int kh = k0 & 63;
+#pragma unroll
+      for (int i = 0; i < H; ++i) {
+        const float give = odd ? p[i] : (H + i < NR ? p[H + i] : 0.f);
+        const float got = __shfl_xor_sync(0xffffffffu, give, 1);
+        const int r = odd ? H + i : i;
+        if (r < NR) {
+          const uint32_t w = odd ? pack_bf16(got, p[(H + i) < NR ? H + i : 0])
+                                 : pack_bf16(p[i], got);
+          const int off = r * 128 + ((((kh >> 3) ^ (r & 7))) << 4) + (kh & 7) * 2;
+          *reinterpret_cast<uint32_t*>(pb + off) = w;
+        }
+      }
+    }
+    tc::fence_async_shared();
+    tc::fence_before_sync();
+    mbar_arrive(&sm.p_full[b]);
+  }
+  // ---- epilogue: row sums across the 128 key positions, then O^T / l with one thread
+  // per head dimension (row r of the output is 128 consecutive threads)
+  {
+    float v[NR];
+#pragma unroll
+    for (int r = 0; r < NR; ++r) v[r] = l_part[r];
+    warp_reduce_rows<NR, false>(v, th.lane);
+    constexpr int sh = 5 - log2i<NR>();
+    if ((th.lane & ((1 << sh) - 1)) == 0)
+      reinterpret_cast<float*>(sm.red[th.x & 1][th.quad])[(th.lane >> sh) & (NR - 1)] = v[0];
+  }
+  const uint32_t xb = th.x & 1;
+  if (!meet(sm, th, a.err)) return false;
+  float l_row[NR];
+  combine4<NR, false>(sm.red[xb], l_row);
+  // the item's last P V (its phase is at most one ahead: see the phase bounds)
+  const int n_last = th.n - 1;
+  if (!mbar_wait_warp(&sm.o_tile[n_last & 1], ph(n_last, 2), a.err)) return false;
+  tc::fence_after_sync();
+  float o[NR];
+  tmem_ld_rows<NR>(th.t_lane + kColO, o);
+#pragma unroll
+  for (int r = 0; r < NR; ++r) {
+    if (r < item.row_count) {
+      const int rho = item.row_begin + r;
+      const int qt = rho / a.g;
+      if (item.part < 0) {
+        const int h = item.kv_head * a.g + (rho - qt * a.g);
+        const int64_t off = ((int64_t)(item.q_row0 + qt) * a.Hq + h) * kD + th.kl;
+        const float val = (l_row[r] > 0.f) ? o[r] / l_row[r] : 0.f;
+        if (a.out_bf16)
+          reinterpret_cast<__nv_bfloat16*>(a.out)[off] = __float2bfloat16_rn(val);
+        else
+          reinterpret_cast<float*>(a.out)[off] = val;
+      } else {
+        const int64_t prow = (int64_t)item.part + r;
+        a.part_acc[prow * kD + th.kl] = o[r];
+        if (th.kl == 0) {
+          a.part_ml[prow * 2 + 0] = m_used[r];
+          a.part_ml[prow * 2 + 1] = l_row[r];
+        }
+      }
+    }
+  }
+  tc::fence_before_sync();
+  mbar_arrive(&sm.o_free);
+  return true;
 }
 
 __global__ void __launch_bounds__(kThreadsD, 1)
@@ -392,15 +617,18 @@ __global__ void __launch_bounds__(kThreadsD, 1)
     // head dimension for O^T. The four warps meet on an mbarrier of 128 arrivals
     // (bounded wait) to combine their partial row maxima / sums in shared memory;
     // meeting x uses buffer x % 2, and a warp cannot write it again before the other
-    // warps passed meeting x + 1, i.e. read meeting x.
+    // warps passed meeting x + 1, i.e. read meeting x. Each item runs the variant for
+    // the smallest of 1, 2, 4, 8, 16 rows that holds it.
     // Phase bounds: s_full(n + 2) needs s_free(n) from here; p_free(n + 2) needs
     // p_full(n + 2); o_tile(n + 1) needs p_full(n + 1); so no barrier is ever two
     // phases ahead of a wait here.
-    const int quad = warp & 3;
-    const int kl = quad * 32 + lane;              // key in the tile / head dimension
-    const uint32_t t_lane = tmem + ((uint32_t)(quad * 32) << 16);
-    uint32_t x = 0;                               // meetings so far
-    int n = 0;
+    SoftmaxThread th;
+    th.quad = warp & 3;
+    th.lane = lane;
+    th.kl = th.quad * 32 + lane;
+    th.t_lane = tmem + ((uint32_t)(th.quad * 32) << 16);
+    th.x = 0;
+    th.n = 0;
     bool ok = true;
     // the next item and its lengths are read one item ahead, off the critical path
     Item item_next{};
@@ -410,15 +638,6 @@ __global__ void __launch_bounds__(kThreadsD, 1)
       L_next = __ldg(a.context_lens + item_next.seq);
       ql_next = __ldg(a.query_lens + item_next.seq);
     }
-    // meet the other softmax warps: red[x % 2][quad][*] written before, read after
-    auto meet = [&]() -> bool {
-      tc::fence_before_sync();
-      mbar_arrive(&sm.xbar);
-      const bool r = mbar_wait_warp(&sm.xbar, x & 1u, a.err);
-      ++x;
-      tc::fence_after_sync();
-      return r;
-    };
     for (int it = blockIdx.x; it < n_items && ok; it += G) {
       const Item item = item_next;
       const int L = L_next, ql = ql_next;
@@ -429,154 +648,20 @@ __global__ void __launch_bounds__(kThreadsD, 1)
       }
       if (item.kv_end > L || item.row_begin + item.row_count > ql * a.g)
         record_error(a.err, PA_DEVERR_LENS);
-      const int nt = tiles_of(item);
-      // causal limit of each row (-1: not a row of the item)
-      int lim[kN];
-      float m_used[kN], l_part[kN];
-#pragma unroll
-      for (int r = 0; r < kN; ++r) {
-        lim[r] = r < item.row_count
-                     ? min(item.kv_end - 1, L - ql + (item.row_begin + r) / a.g)
-                     : -1;
-        m_used[r] = -INFINITY;
-        l_part[r] = 0.f;
-      }
-      for (int j = 0; j < nt; ++j, ++n) {
-        const int b = n & 1;
-        const int key = item.kv_begin + j * kKeys + kl;
-        // ---- scores of this thread's key for the 16 rows; the buffer is free again
-        float s[kN];
-        if (!mbar_wait_warp(&sm.s_full[b], ph(n, 2), a.err)) { ok = false; break; }
-        tc::fence_after_sync();
-        tc::tmem_ld16(t_lane + (uint32_t)b * kN, s);
-        tc::fence_before_sync();
-        mbar_arrive(&sm.s_free[b]);
-        // causal mask (keys past the range fail it too); a masked score is -inf
-#pragma unroll
-        for (int r = 0; r < kN; ++r)
-          if (key > lim[r]) s[r] = -INFINITY;
-        // ---- row maxima over the tile's 128 keys
-        {
-          float v[kN];
-#pragma unroll
-          for (int r = 0; r < kN; ++r) v[r] = s[r];
-          warp_reduce16<true>(v, lane);
-          if ((lane & 1) == 0) sm.red[x & 1][quad][(lane >> 1) & 15] = v[0];
-        }
-        const uint32_t xb = x & 1;
-        if (!meet()) { ok = false; break; }
-        float alpha[kN];
-        bool any_rescale = false;
-#pragma unroll
-        for (int r = 0; r < kN; ++r) {
-          const float mt = fmaxf(fmaxf(sm.red[xb][0][r], sm.red[xb][1][r]),
-                                 fmaxf(sm.red[xb][2][r], sm.red[xb][3][r]));
-          const float m_new = fmaxf(m_used[r], mt * a.scale_log2);
-          alpha[r] = 1.f;
-          if (m_used[r] == -INFINITY) {
-            m_used[r] = m_new;                    // nothing accumulated yet
-          } else if (m_new > m_used[r] + kRescaleLog2) {
-            alpha[r] = fast_exp2(m_used[r] - m_new);
-            m_used[r] = m_new;
-            any_rescale = true;
-          }
-        }
-        // every thread saw the same maxima: the decision is uniform across the warps
-        if (any_rescale) {
-          // O^T must be idle: wait for the previous tile's P V
-          if (!mbar_wait_warp(&sm.o_tile[(n - 1) & 1], ph(n - 1, 2), a.err)) { ok = false; break; }
-          tc::fence_after_sync();
-          float o[kN];
-          tc::tmem_ld16(t_lane + kColO, o);
-#pragma unroll
-          for (int r = 0; r < kN; ++r) o[r] *= alpha[r];
-          tc::tmem_st16(t_lane + kColO, o);
-          tc::tmem_wait_st();
-#pragma unroll
-          for (int r = 0; r < kN; ++r) l_part[r] *= alpha[r];
-        }
-        // ---- P^T = 2^(scale s - m): bf16 pairs of neighbouring keys, one row each
-        float p[kN];
-#pragma unroll
-        for (int r = 0; r < kN; ++r) {
-          const float neg_m = (m_used[r] == -INFINITY) ? 0.f : -m_used[r];
-          p[r] = fast_exp2(fmaf(s[r], a.scale_log2, neg_m));
-          l_part[r] += p[r];
-        }
-        // P^T buffer b is free once the P V of tile n - 2 is done
-        if (!mbar_wait_warp(&sm.p_free[b], ph(n, 2) ^ 1u, a.err)) { ok = false; break; }
-        {
-          // the even lane of a pair writes rows 0..7 for keys (kl, kl + 1), the odd lane
-          // rows 8..15; K-major, 128-byte swizzle: row r, key k at key half k / 64,
-          // 16-byte chunk (k % 64) / 8 ^ (r % 8)
-          const bool odd = lane & 1;
-          const int k0 = kl & ~1;
-          uint8_t* pb = &sm.p[b][k0 >> 6][0];
-          const int kh = k0 & 63;
-#pragma unroll
-          for (int i = 0; i < 8; ++i) {
-            const float give = odd ? p[i] : p[i + 8];
-            const float got = __shfl_xor_sync(0xffffffffu, give, 1);
-            const int r = odd ? i + 8 : i;
-            const uint32_t w = odd ? pack_bf16(got, p[i + 8]) : pack_bf16(p[i], got);
-            const int off = r * 128 + ((((kh >> 3) ^ (r & 7))) << 4) + (kh & 7) * 2;
-            *reinterpret_cast<uint32_t*>(pb + off) = w;
-          }
-        }
-        tc::fence_async_shared();
-        tc::fence_before_sync();
-        mbar_arrive(&sm.p_full[b]);
-      }
-      if (!ok) break;
-      // ---- epilogue: row sums across the 128 key positions, then O^T / l with one
-      // thread per head dimension (row r of the output is 128 consecutive threads)
-      {
-        float v[kN];
-#pragma unroll
-        for (int r = 0; r < kN; ++r) v[r] = l_part[r];
-        warp_reduce16<false>(v, lane);
-        if ((lane & 1) == 0) sm.red[x & 1][quad][(lane >> 1) & 15] = v[0];
-      }
-      const uint32_t xb = x & 1;
-      if (!meet()) { ok = false; break; }
-      float l_row[kN];
-#pragma unroll
-      for (int r = 0; r < kN; ++r)
-        l_row[r] = (sm.red[xb][0][r] + sm.red[xb][1][r]) + (sm.red[xb][2][r] + sm.red[xb][3][r]);
-      // the item's last P V (its phase is at most one ahead: see above)
-      if (!mbar_wait_warp(&sm.o_tile[(n - 1) & 1], ph(n - 1, 2), a.err)) { ok = false; break; }
-      tc::fence_after_sync();
-      float o[kN];
-      tc::tmem_ld16(t_lane + kColO, o);
-#pragma unroll
-      for (int r = 0; r < kN; ++r) {
-        if (r < item.row_count) {
-          const int rho = item.row_begin + r;
-          const int qt = rho / a.g;
-          if (item.part < 0) {
-            const int h = item.kv_head * a.g + (rho - qt * a.g);
-            const int64_t off = ((int64_t)(item.q_row0 + qt) * a.Hq + h) * kD + kl;
-            const float val = (l_row[r] > 0.f) ? o[r] / l_row[r] : 0.f;
-            if (a.out_bf16)
-              reinterpret_cast<__nv_bfloat16*>(a.out)[off] = __float2bfloat16_rn(val);
-            else
-              reinterpret_cast<float*>(a.out)[off] = val;
-          } else {
-            const int64_t prow = (int64_t)item.part + r;
-            a.part_acc[prow * kD + kl] = o[r];
-            if (kl == 0) {
-              a.part_ml[prow * 2 + 0] = m_used[r];
-              a.part_ml[prow * 2 + 1] = l_row[r];
-            }
-          }
-        }
-      }
-      tc::fence_before_sync();
-      mbar_arrive(&sm.o_free);
+      const int rc = item.row_count;
+      if (rc <= 1)
+        ok = softmax_item<1>(sm, a, item, L, ql, th);
+      else if (rc <= 2)
+        ok = softmax_item<2>(sm, a, item, L, ql, th);
+      else if (rc <= 4)
+        ok = softmax_item<4>(sm, a, item, L, ql, th);
+      else if (rc <= 8)
+        ok = softmax_item<8>(sm, a, item, L, ql, th);
+      else
+        ok = softmax_item<16>(sm, a, item, L, ql, th);
     }
     if (!ok) sm.abort_flag = 1;
   }
-
   tc::fence_before_sync();
   __syncthreads();
   // After an abort, give copies still in flight a bounded time to land.

@@ -155,6 +155,16 @@ def test_tensor_core_decode_items(pa, g, B, chunk):
     assert torch.allclose(run["out"], other["out"], atol=gu.ATOL_MAX, rtol=0)
 
 
+def test_tensor_core_decode_row_counts(pa):
+    """Every row count 1..16 (the kernel runs the 1-, 2-, 4-, 8- or 16-row variant)."""
+    q = list(range(1, 17))
+    L = [q_ + 37 * i + 5 for i, q_ in enumerate(q)]
+    w = workloads.make_custom(L, q, Hq=2, Hkv=2, D=128, block_size=16, seed=707)
+    (_, _), got, _ = full_check(pa, w)
+    items = got["plan"].items()
+    assert sorted(set(items[items[:, 0] == 3][:, 4].tolist())) == q
+
+
 def test_tensor_core_decode_tiny_first(pa):
     """Smallest key-major case: one row, one key."""
     w = workloads.make_custom([1], [1], Hq=1, Hkv=1, D=128, block_size=16, seed=13)
