@@ -335,15 +335,25 @@ pa_status pa_plan_create(const int32_t* h_context_lens, const int32_t* h_query_l
       part_rows += n_chunks * u.row_count;
     }
   }
-  // longest key range first: with the round-robin walk of the persistent
-  // kernel this balances the SMs (longest-processing-time order)
+  // Longest key range first, then every other round of G items (G = the kernel's grid,
+  // one CTA per SM) reversed: a persistent CTA c walks items c, c + G, c + 2G, ..., so
+  // it takes the c-th longest of round 0, the c-th shortest of round 1, and so on (a
+  // snake), which evens out the CTAs' totals better than plain round-robin. Items of
+  // one round stay together, so CTAs still work on similar items at the same time.
   auto longer = [](const Item& x, const Item& y) {
     return (x.kv_end - x.kv_begin) > (y.kv_end - y.kv_begin);
   };
-  std::stable_sort(dec.begin(), dec.end(), longer);
-  std::stable_sort(tc.begin(), tc.end(), longer);
-  std::stable_sort(tc2.begin(), tc2.end(), longer);
-  std::stable_sort(tcd.begin(), tcd.end(), longer);
+  auto snake = [&](std::vector<Item>& v) {
+    std::stable_sort(v.begin(), v.end(), longer);
+    const size_t G = std::min<size_t>(v.size(), (size_t)sms);
+    if (G == 0) return;
+    for (size_t r0 = G; r0 < v.size(); r0 += 2 * G)
+      std::reverse(v.begin() + r0, v.begin() + std::min(v.size(), r0 + G));
+  };
+  snake(dec);
+  snake(tc);
+  snake(tc2);
+  snake(tcd);
 
   pa_plan_s* p = new (std::nothrow) pa_plan_s();
   if (!p) return PA_ERR_INVALID_ARG;

@@ -180,9 +180,22 @@ def test_plan_decode_items(pa):
 
 def test_plan_orders_longest_first(pa):
     L = list(range(100, 2100, 50))
-    p = plan(pa, L, [1] * len(L))
+    p = plan(pa, L, [1] * len(L), num_sms=1000)    # one round of the walk
     lens = [ke - kb for *_, kb, ke, _, _ in p.items()]
     assert lens == sorted(lens, reverse=True)
+
+
+def test_plan_snake_rounds(pa):
+    """Longest first, every other round of G = num_sms items reversed: CTA c (which walks
+    items c, c + G, ...) gets the c-th longest of round 0, the c-th shortest of round 1."""
+    L = [100 + 37 * i for i in range(10)]
+    p = plan(pa, L, [1] * len(L), num_sms=4)
+    lens = [int(ke - kb) for *_, kb, ke, _, _ in p.items()]
+    desc = sorted(lens, reverse=True)
+    assert lens == desc[0:4] + desc[4:8][::-1] + desc[8:10]
+    loads = [sum(lens[c::4]) for c in range(4)]
+    plain = [sum(desc[c::4]) for c in range(4)]
+    assert max(loads) - min(loads) <= max(plain) - min(plain)
 
 
 def test_plan_auto_split_fills_the_gpu(pa):
