@@ -189,7 +189,7 @@ def test_plan_snake_rounds(pa):
     """Longest first, every other round of G = num_sms items reversed: CTA c (which walks
     items c, c + G, ...) gets the c-th longest of round 0, the c-th shortest of round 1."""
     L = [100 + 37 * i for i in range(10)]
-    p = plan(pa, L, [1] * len(L), Hq=1, Hkv=1, num_sms=4)
+    p = plan(pa, L, [1] * len(L), Hq=1, Hkv=1, num_sms=4, max_chunk_tokens=4096)
     lens = [int(ke - kb) for *_, kb, ke, _, _ in p.items()]
     desc = sorted(lens, reverse=True)
     assert lens == desc[0:4] + desc[4:8][::-1] + desc[8:10]
