@@ -87,6 +87,23 @@ pa_status make_q_map(CUtensorMap* map, const void* q, int64_t total_q, int Hq, i
   return r == CUDA_SUCCESS ? PA_OK : PA_ERR_CUDA;
 }
 
+pa_status make_out_map(CUtensorMap* map, void* out, int64_t total_q, int Hq, int D, int g,
+                       bool bf16) {
+  auto fn = encode_fn();
+  if (!fn) return PA_ERR_CUDA;
+  const int es = bf16 ? 2 : 4;
+  const int gb = g < 32 ? g : 32;
+  cuuint64_t dims[3] = {(cuuint64_t)D, (cuuint64_t)Hq, (cuuint64_t)total_q};
+  cuuint64_t strides[2] = {(cuuint64_t)D * es, (cuuint64_t)Hq * D * es};
+  cuuint32_t box[3] = {16u, (cuuint32_t)gb, (cuuint32_t)(32 / gb)};
+  cuuint32_t estr[3] = {1u, 1u, 1u};
+  CUresult r = fn(map, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32,
+                  3, out, dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                  CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_NONE,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? PA_OK : PA_ERR_CUDA;
+}
+
 }  // namespace pa
 
 // ====================================================================== plan
@@ -535,8 +552,11 @@ pa_status pa_attention(pa_plan_t p, void* d_out, pa_dtype out_dtype, const void*
     st = pa::make_q_map(&qmap, d_q, p->total_q, p->Hq, p->D, p->g, pa::kTcRows);
     if (st != PA_OK) return st;
     if (p->n_tc2 > 0) {
+      CUtensorMap omap;
+      st = pa::make_out_map(&omap, d_out, p->total_q, p->Hq, p->D, p->g, a.out_bf16 != 0);
+      if (st != PA_OK) return st;
       const int grid = std::min(p->n_tc2, sms);
-      cudaError_t e = pa::launch_tc2(a, kmap, vmap, qmap,
+      cudaError_t e = pa::launch_tc2(a, kmap, vmap, qmap, omap,
                                      reinterpret_cast<const Item*>(ws + p->off_tc2), p->n_tc2,
                                      box_t, grid, s);
       if (e != cudaSuccess) return PA_ERR_CUDA;

@@ -95,8 +95,13 @@ pa_status make_q_map(CUtensorMap* map, const void* q, int64_t total_q, int Hq, i
 int tc_smem_bytes();
 // Items of 129..256 rows: two 128-row tiles per CTA that share every K/V tile.
 cudaError_t launch_tc2(const AttnArgs& a, const CUtensorMap& kmap, const CUtensorMap& vmap,
-                       const CUtensorMap& qmap, const Item* items, int32_t n_items, int box_t,
-                       int grid, cudaStream_t s);
+                       const CUtensorMap& qmap, const CUtensorMap& omap, const Item* items,
+                       int32_t n_items, int box_t, int grid, cudaStream_t s);
+// 3-D tiled map over the output viewed as [total_q][Hq][D] (fp32 or bf16), no swizzle,
+// box (16, min(g, 32), 32 / min(g, 32)): one box is 16 columns of the 32 packed rows
+// (tokens x heads of one KV head) of a warp.
+pa_status make_out_map(CUtensorMap* map, void* out, int64_t total_q, int Hq, int D, int g,
+                       bool bf16);
 int tc2_smem_bytes();
 // Items of at most 16 rows: keys on the 128-row side (S^T = K Q^T, O^T = V^T P^T).
 cudaError_t launch_tcd(const AttnArgs& a, const CUtensorMap& kmap, const CUtensorMap& vmap,

@@ -111,7 +111,8 @@ __device__ __forceinline__ ItemWalk item_walk(int n_items) {
 __global__ void __launch_bounds__(kThreads2, 1)
     tc2_kernel(const __grid_constant__ AttnArgs a, const __grid_constant__ CUtensorMap kmap,
                const __grid_constant__ CUtensorMap vmap, const __grid_constant__ CUtensorMap qmap,
-               const Item* __restrict__ items, int n_items, int box_t) {
+               const __grid_constant__ CUtensorMap omap, const Item* __restrict__ items,
+               int n_items, int box_t) {
   extern __shared__ uint8_t smem_raw[];
   Tc2Smem& sm = *reinterpret_cast<Tc2Smem*>(align1024(smem_raw));
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -485,7 +486,53 @@ __global__ void __launch_bounds__(kThreads2, 1)
       // o_done is at most one phase ahead)
       if (!mbar_wait_warp(&sm.o_done[t], (uint32_t)(n - 1) & 1u, a.err)) { ok = false; break; }
       tc::fence_after_sync();
-      if (warp_live) {
+      // A warp whose 32 rows all belong to the item (and go to the output, not to
+      // split partials) hands O / l to the TMA: it writes 16-column pieces of its rows
+      // into its staging buffer in the output box's layout (packed row-major, which is
+      // tokens x heads x columns) and one lane issues an asynchronous tensor store, so
+      // the warp moves on while the bytes drain. Other warps store rows themselves.
+      const int rho0 = info.row_begin + t * 128 + quad * 32;
+      const bool whole = info.part < 0 && t * 128 + quad * 32 + 32 <= row_count;
+      if (whole) {
+        const float inv = (l > 0.f) ? 1.f / l : 0.f;
+        const int c1 = info.kv_head * a.g + rho0 % a.g;
+        const int c2 = info.q_row0 + rho0 / a.g;
+#pragma unroll 1
+        for (int c4 = 0; c4 < kD / 32; ++c4) {
+          float o[32];
+          tc::tmem_ld32(t_lane + o_col(t) + (uint32_t)c4 * 32u, o);
+#pragma unroll
+          for (int hh = 0; hh < 2; ++hh) {
+            // the previous store has read the staging buffer
+            if (lane == 0) bulk_wait_read();
+            __syncwarp();
+            if (a.out_bf16) {
+              uint4* d = reinterpret_cast<uint4*>(reinterpret_cast<uint8_t*>(stg) + lane * 32);
+#pragma unroll
+              for (int i = 0; i < 2; ++i) {
+                uint4 w;
+                w.x = pack_bf16(o[hh * 16 + 8 * i + 0] * inv, o[hh * 16 + 8 * i + 1] * inv);
+                w.y = pack_bf16(o[hh * 16 + 8 * i + 2] * inv, o[hh * 16 + 8 * i + 3] * inv);
+                w.z = pack_bf16(o[hh * 16 + 8 * i + 4] * inv, o[hh * 16 + 8 * i + 5] * inv);
+                w.w = pack_bf16(o[hh * 16 + 8 * i + 6] * inv, o[hh * 16 + 8 * i + 7] * inv);
+                d[i] = w;
+              }
+            } else {
+              float4* d = reinterpret_cast<float4*>(stg + lane * kStageCols);
+#pragma unroll
+              for (int i = 0; i < 4; ++i)
+                d[i] = make_float4(o[hh * 16 + 4 * i] * inv, o[hh * 16 + 4 * i + 1] * inv,
+                                   o[hh * 16 + 4 * i + 2] * inv, o[hh * 16 + 4 * i + 3] * inv);
+            }
+            tc::fence_async_shared();
+            __syncwarp();
+            if (lane == 0) {
+              tma_store_3d(&omap, stg, c4 * 32 + hh * 16, c1, c2);
+              bulk_commit();
+            }
+          }
+        }
+      } else if (warp_live) {
         // destination of this lane's row (nullptr: not a row of the item)
         char* dst_row = nullptr;
         float inv = 1.f;
@@ -506,6 +553,9 @@ __global__ void __launch_bounds__(kThreads2, 1)
           }
         }
         const bool bf = a.out_bf16 && part < 0;
+        // the staging buffer may still feed an earlier tensor store of this warp
+        if (lane == 0) bulk_wait_read();
+        __syncwarp();
 #pragma unroll 1
         for (int c4 = 0; c4 < kD / 32; ++c4) {
           float o[32];
@@ -551,6 +601,9 @@ __global__ void __launch_bounds__(kThreads2, 1)
       tc::fence_before_sync();
       mbar_arrive(&sm.o_free[t]);
     }
+    // every tensor store of this warp has landed before the CTA exits
+    if (lane == 0) bulk_wait_all();
+    __syncwarp();
     if (!ok) sm.abort_flag = 1;
   }
   tc::fence_before_sync();
@@ -587,14 +640,14 @@ __global__ void __launch_bounds__(kThreads2, 1)
 int tc2_smem_bytes() { return (int)sizeof(Tc2Smem) + 1024; }
 
 cudaError_t launch_tc2(const AttnArgs& a, const CUtensorMap& kmap, const CUtensorMap& vmap,
-                       const CUtensorMap& qmap, const Item* items, int32_t n_items, int box_t,
-                       int grid, cudaStream_t s) {
+                       const CUtensorMap& qmap, const CUtensorMap& omap, const Item* items,
+                       int32_t n_items, int box_t, int grid, cudaStream_t s) {
   if (n_items <= 0) return cudaSuccess;
   const int smem = tc2_smem_bytes();
   cudaError_t e =
       cudaFuncSetAttribute(tc2_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
-  tc2_kernel<<<grid, kThreads2, smem, s>>>(a, kmap, vmap, qmap, items, n_items, box_t);
+  tc2_kernel<<<grid, kThreads2, smem, s>>>(a, kmap, vmap, qmap, omap, items, n_items, box_t);
   return cudaGetLastError();
 }
 
