@@ -125,6 +125,24 @@ def test_tensor_core_pair_tiles(pa, g, B, chunk):
     assert torch.allclose(pair_run["out"], one_run["out"], atol=gu.ATOL_MAX, rtol=0)
 
 
+@pytest.mark.parametrize("g", [8, 64, 128])
+def test_tensor_core_pair_bf16_and_wide_groups(pa, g):
+    """Two-tile items with bf16 output (the epilogue's tensor stores in bf16) and with
+    64 or 128 query heads per KV head (a warp's 32 rows are heads of one token)."""
+    q = [max(1, 300 // g) + 1, max(1, 129 // g) + 1, 1]
+    L = [qq + extra for qq, extra in zip(q, [400, 33, 17])]
+    w = workloads.make_custom(L, q, Hq=g, Hkv=1, D=128, block_size=32, seed=900 + g)
+    want = gu.oracle_rows(w, gu.oracle_step(w))
+    got = gu.gpu_step(pa, w)
+    assert got["plan"].stats()["n_tc_pair_items"] > 0
+    gu.assert_attention_close(got["out"].cpu().numpy(), want, f"g={g} fp32")
+    got16 = gu.gpu_step(pa, w, out_dtype=torch.bfloat16)
+    d = np.abs(got16["out"].float().cpu().numpy() - want)
+    # bf16 rounding of outputs of magnitude up to a few units: half an ulp is <= 2^-8 * |o|
+    bound = np.abs(want) * 2.0 ** -8 + gu.ATOL_MAX
+    assert np.all(d <= bound), float((d - bound).max())
+
+
 def test_tensor_core_pair_tiny_first(pa):
     """Smallest two-tile case: 129 rows, one key tile."""
     w = workloads.make_custom([129], [129], Hq=1, Hkv=1, D=128, block_size=16, seed=11)
