@@ -62,7 +62,8 @@ struct Tc2Smem {
   float stage[kSoftmaxWarps][32 * kStageCols];
   int bt_cache[2][kBtCache];
   Item info[3];                         // item k and its lengths, by k % 3 (written by the
-  int info_L[3], info_ql[3];            // producer before item k's Q load)
+  int info_L[3], info_ql[3];            // producer before item k's Q load, published by
+  uint64_t info_full[3];                // info_full[k % 3])
   uint64_t k_full[kStages], k_empty[kStages];
   uint64_t v_full[kStages], v_empty[kStages];
   uint64_t q_full, q_free;
@@ -129,6 +130,7 @@ __global__ void __launch_bounds__(kThreads2, 1)
     }
     mbar_init(&sm.q_full, 1);
     mbar_init(&sm.q_free, 2);          // both chains' last S of the item
+    for (int i = 0; i < 3; ++i) mbar_init(&sm.info_full[i], 1);
     for (int t = 0; t < 2; ++t) {
       mbar_init(&sm.s_full[t], 1);
       mbar_init(&sm.p_full[t][0], 128);
@@ -191,10 +193,11 @@ __global__ void __launch_bounds__(kThreads2, 1)
         if (!ok || *(volatile int*)&sm.abort_flag) { ok = false; break; }
       }
       if (lane == 0) {
-        // the item's description for the other warps, published by the q_full phase
+        // the item's description for the softmax warps (the arrive releases the writes)
         sm.info[k % 3] = item;
         sm.info_L[k % 3] = __ldg(a.context_lens + item.seq);
         sm.info_ql[k % 3] = __ldg(a.query_lens + item.seq);
+        mbar_arrive(&sm.info_full[k % 3]);
         mbar_arrive_expect_tx(&sm.q_full, 4u * kHalf);
 #pragma unroll
         for (int t = 0; t < 2; ++t) {
@@ -373,11 +376,12 @@ __global__ void __launch_bounds__(kThreads2, 1)
     int n = 0;                                    // tile of the CTA
     bool ok = true;
     for (int sidx = 0, k = 0; sidx < W.cnt && ok; ++sidx, ++k) {
-      // The producer wrote the item's description before its Q load; q_full(k) is at
-      // most one phase ahead (the Q of item k + 1 needs every S of item k). Slot k % 3
-      // is rewritten (for item k + 3) only after every S of item k + 2, and those need
-      // this chain's P of item k + 1: it stays valid through this item's epilogue.
-      if (!mbar_wait_warp(&sm.q_full, (uint32_t)k & 1u, a.err)) { ok = false; break; }
+      // The producer published the item's description in slot k % 3 before its Q load.
+      // The slot (and its barrier's next phase) is rewritten for item k + 3 only after
+      // every S of item k + 2, and the first of those needs this chain's P of item
+      // k + 1's last tile: the slot stays valid through this item's epilogue, and the
+      // barrier is never two phases ahead of this wait.
+      if (!mbar_wait_warp(&sm.info_full[k % 3], ph(k, 3), a.err)) { ok = false; break; }
       const Item& info = sm.info[k % 3];
       const int kv_begin = info.kv_begin, kv_end = info.kv_end, row_count = info.row_count;
       int lim = -1;                               // causal limit of this row (-1: not a row)

@@ -143,6 +143,24 @@ def test_tensor_core_pair_bf16_and_wide_groups(pa, g):
     assert np.all(d <= bound), float((d - bound).max())
 
 
+def test_tensor_core_pair_single_tile_items(pa):
+    """Many consecutive two-tile items of one key tile each: every item's last S follows
+    its first, so the next item's Q can land while the softmax warps still finish the
+    previous item; they must take each item's description from its own barrier."""
+    n = 600
+    rng = np.random.default_rng(31)
+    q = [32] * n
+    L = [int(x) for x in rng.integers(32, 129, size=n)]
+    w = workloads.make_custom(L, q, Hq=8, Hkv=1, D=128, block_size=16, seed=32,
+                              write_new=False)
+    got = gu.gpu_step(pa, w)
+    assert got["err"] == 0, pa.DEVERR.get(got["err"])
+    assert got["plan"].stats()["n_tc_pair_items"] == n
+    rows = gu.sample_rows(w, 400, seed=33)
+    want = gu.oracle_rows(w, gu.oracle_step(w), rows=rows)
+    gu.assert_attention_close(got["out"].cpu().numpy()[rows], want, "single-tile items")
+
+
 def test_tensor_core_pair_tiny_first(pa):
     """Smallest two-tile case: 129 rows, one key tile."""
     w = workloads.make_custom([129], [129], Hq=1, Hkv=1, D=128, block_size=16, seed=11)
