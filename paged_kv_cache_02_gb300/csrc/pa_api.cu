@@ -551,10 +551,12 @@ pa_status pa_attention(pa_plan_t p, void* d_out, pa_dtype out_dtype, const void*
     CUtensorMap qmap;
     st = pa::make_q_map(&qmap, d_q, p->total_q, p->Hq, p->D, p->g, pa::kTcRows);
     if (st != PA_OK) return st;
-    if (p->n_tc2 > 0) {
-      CUtensorMap omap;
+    CUtensorMap omap;
+    if (p->n_tc2 + p->n_tc > 0) {
       st = pa::make_out_map(&omap, d_out, p->total_q, p->Hq, p->D, p->g, a.out_bf16 != 0);
       if (st != PA_OK) return st;
+    }
+    if (p->n_tc2 > 0) {
       const int grid = std::min(p->n_tc2, sms);
       cudaError_t e = pa::launch_tc2(a, kmap, vmap, qmap, omap,
                                      reinterpret_cast<const Item*>(ws + p->off_tc2), p->n_tc2,
@@ -563,7 +565,7 @@ pa_status pa_attention(pa_plan_t p, void* d_out, pa_dtype out_dtype, const void*
     }
     if (p->n_tc > 0) {
       const int grid = std::min(p->n_tc, sms);
-      cudaError_t e = pa::launch_tc(a, kmap, vmap, qmap,
+      cudaError_t e = pa::launch_tc(a, kmap, vmap, qmap, omap,
                                     reinterpret_cast<const Item*>(ws + p->off_tc), p->n_tc, box_t,
                                     grid, s);
       if (e != cudaSuccess) return PA_ERR_CUDA;

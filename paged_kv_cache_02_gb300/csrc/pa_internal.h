@@ -86,8 +86,8 @@ cudaError_t launch_combine(const AttnArgs& a, const SplitGroup* groups, int32_t 
                            cudaStream_t s);
 int decode_smem_bytes(int D, int rows_max);
 cudaError_t launch_tc(const AttnArgs& a, const CUtensorMap& kmap, const CUtensorMap& vmap,
-                      const CUtensorMap& qmap, const Item* items, int32_t n_items, int box_t,
-                      int grid, cudaStream_t s);
+                      const CUtensorMap& qmap, const CUtensorMap& omap, const Item* items,
+                      int32_t n_items, int box_t, int grid, cudaStream_t s);
 // 3-D tiled map over q viewed as [total_q][Hq][D] bf16 with box (64, g, rows / g), 128-byte
 // swizzle: one box is `rows` packed rows (tokens x the g heads of a KV head) of one D half.
 pa_status make_q_map(CUtensorMap* map, const void* q, int64_t total_q, int Hq, int D, int g,

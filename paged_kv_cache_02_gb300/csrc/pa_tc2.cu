@@ -431,6 +431,7 @@ __global__ void __launch_bounds__(kThreads2, 1)
           const uint64_t sc2 = f2_pack(a.scale_log2, a.scale_log2);
           const uint64_t nm2 = f2_pack(neg_m, neg_m);
           uint64_t sum2[2] = {0ull, 0ull};
+          __syncwarp();  // tcgen05.st is .sync.aligned: reconverge after the per-row update
 #pragma unroll
           for (int c = 0; c < 8; ++c) {
             float pk[8];
@@ -504,6 +505,7 @@ __global__ void __launch_bounds__(kThreads2, 1)
 #pragma unroll 1
         for (int c4 = 0; c4 < kD / 32; ++c4) {
           float o[32];
+          __syncwarp();  // tcgen05.ld is .sync.aligned: reconverge after the single-lane store
           tc::tmem_ld32(t_lane + o_col(t) + (uint32_t)c4 * 32u, o);
 #pragma unroll
           for (int hh = 0; hh < 2; ++hh) {
