@@ -453,7 +453,8 @@ def main():
     ap.add_argument("--out", choices=["f32", "bf16"], default="f32",
                     help="attention output dtype")
     ap.add_argument("--tc-pair", type=int, default=0,
-                    help="plan option: 0 = 256-row tensor-core items (default), -1 = 128-row only")
+                    help="plan option: 0 = automatic (default), 1 = 256-row tensor-core items, "
+                         "-1 = 128-row only")
     ap.add_argument("--max-chunk", type=int, default=0,
                     help="plan option: split-KV chunk length (0 = automatic)")
     ap.add_argument("--subset", choices=["prefill", "decode"], default=None,

@@ -279,10 +279,29 @@ pa_status pa_plan_create(const int32_t* h_context_lens, const int32_t* h_query_l
   // CUDA cores
   const int tc_min_rows =
       o.tc_min_rows > 0 ? o.tc_min_rows : (tcd_enabled ? 1 : pa::kTcMinRowsDefault);
+  // 256-row items (two query tiles sharing every K/V tile) read half the K/V bytes per
+  // query row of 128-row items; 128-row items pipeline better (a CTA keeps two score
+  // buffers and eight softmax warps for one tile). By default pairs are used when the
+  // multi-token tensor-core work of the batch is memory-bound: fewer FLOPs per byte of
+  // K/V (read once per sequence and KV head), Q and output than the machine balance.
+  bool use_pair = pair_enabled && o.tc_pair > 0;
+  if (pair_enabled && o.tc_pair == 0) {
+    double flops = 0.0, bytes = 0.0;
+    for (int32_t s = 0; s < num_seqs; ++s) {
+      const double L = h_context_lens[s], q = h_query_lens[s];
+      const int64_t rows = (int64_t)h_query_lens[s] * g;
+      if (rows < tc_min_rows || (tcd_enabled && rows <= pa::kTcdRows)) continue;
+      // causal: query token t (0-based among the q) sees L - q + t + 1 keys
+      const double keys = q * (L - q) + q * (q + 1) / 2;
+      flops += 4.0 * D * g * Hkv * keys;                // Q K^T and P V
+      bytes += 4.0 * D * Hkv * L + 6.0 * D * Hq * q;    // K + V bf16, Q bf16, O fp32
+    }
+    use_pair = flops < pa::kTcMachineBalance * bytes;
+  }
 
-  // ---- units: (sequence, KV head, row tile). Tensor-core rows go in tiles of 256
-  // (two 128-row halves sharing every K/V tile) while more than 128 rows remain,
-  // the rest in one 128-row tile.
+  // ---- units: (sequence, KV head, row tile). With pairs, tensor-core rows go in tiles
+  // of 256 (two 128-row halves sharing every K/V tile) while more than 128 rows remain,
+  // the rest in one 128-row tile; without, all in 128-row tiles.
   std::vector<Unit> units;
   int64_t total_keys = 0;
   int64_t q_row0 = 0;
@@ -299,7 +318,7 @@ pa_status pa_plan_create(const int32_t* h_context_lens, const int32_t* h_query_l
             path = kPathDec; rt = pa::kDecRows;
           } else if (tcd_enabled && rows <= pa::kTcdRows) {
             path = kPathTcDecode; rt = pa::kTcdRows;
-          } else if (pair_enabled && left > pa::kTcRows) {
+          } else if (use_pair && left > pa::kTcRows) {
             path = kPathTcPair; rt = 2 * pa::kTcRows;
           } else {
             path = kPathTc; rt = pa::kTcRows;

@@ -38,6 +38,9 @@ static_assert(sizeof(SplitGroup) == 32, "SplitGroup is 32 bytes");
 
 constexpr int kDecRows = 8;     // rows a CUDA-core item holds at most
 constexpr int kTcRows = 128;    // rows of a tensor-core item (one M tile)
+// GB300 machine balance for bf16 attention: dense tensor rate (~1.9 PFLOP/s) over HBM
+// bandwidth (~6.8 TB/s), in FLOPs per byte
+constexpr double kTcMachineBalance = 280.0;
 constexpr int kTcdRows = 16;    // rows of a key-major tensor-core decode item (N)
 constexpr int kKeyTile = 64;    // keys per pipeline stage of the decode kernel
 constexpr int kChunkAlign = 64;   // split-KV chunk boundaries are multiples of this

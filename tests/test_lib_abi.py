@@ -131,12 +131,13 @@ def test_plan_covers_every_row_and_key(pa, chunk):
 
 
 def test_plan_pair_tiles(pa):
-    """Tensor-core rows go in 256-row items (two 128-row tiles) while more than 128 rows
-    remain, the rest in one 128-row item; tc_pair=-1 keeps 128-row items only."""
+    """With tc_pair=1 tensor-core rows go in 256-row items (two 128-row tiles) while more
+    than 128 rows remain, the rest in one 128-row item; tc_pair=-1 keeps 128-row items
+    only."""
     L = [300, 1000, 700, 129, 2000]
     q = [300, 40, 33, 129, 1]
     g, Hkv = 8, 2
-    p = plan(pa, L, q, Hq=g * Hkv, Hkv=Hkv, D=128, max_chunk_tokens=256)
+    p = plan(pa, L, q, Hq=g * Hkv, Hkv=Hkv, D=128, max_chunk_tokens=256, tc_pair=1)
     items = p.items()
     _coverage(items, L, q, g, Hkv)
     rows_by_path = {}
@@ -152,6 +153,41 @@ def test_plan_pair_tiles(pa):
     _coverage(items1, L, q, g, Hkv)
     assert 2 not in set(items1[:, 0].tolist())
     assert p1.stats()["n_tc_pair_items"] == 0
+
+
+def _tc_intensity(L, q, g, Hkv, D=128):
+    """FLOPs per byte of the multi-token tensor-core work (rows > 16): Q K^T and P V over
+    the causally visible keys, against K and V read once per (sequence, KV head), Q in
+    bf16 and the output in fp32."""
+    flops = byts = 0.0
+    for l, n in zip(L, q):
+        if n * g <= 16:
+            continue
+        visible = sum(l - n + t + 1 for t in range(n))
+        flops += 4.0 * D * g * Hkv * visible
+        byts += 4.0 * D * Hkv * l + 6.0 * D * g * Hkv * n
+    return flops / byts
+
+
+def test_plan_pair_automatic(pa):
+    """By default 256-row items are used only when the multi-token work is memory-bound:
+    FLOPs per byte of K/V, Q and output below the machine balance of 280."""
+    g, Hkv = 1, 8
+    # short prompts over long histories: little work per K/V byte
+    L_lo, q_lo = [3000, 2500, 2800], [200, 180, 250]
+    # long prompts packed 8 heads per KV head: much work per K/V byte
+    L_hi, q_hi = [1500, 1200, 1800], [256, 200, 240]
+    assert _tc_intensity(L_lo, q_lo, g, Hkv) < 280
+    assert _tc_intensity(L_hi, q_hi, 8, Hkv) > 280
+    lo = plan(pa, L_lo, q_lo, Hq=g * Hkv, Hkv=Hkv, D=128)
+    hi = plan(pa, L_hi, q_hi, Hq=8 * Hkv, Hkv=Hkv, D=128)
+    assert lo.stats()["n_tc_pair_items"] > 0
+    assert hi.stats()["n_tc_pair_items"] == 0 and hi.stats()["n_tc_items"] > 0
+    # the explicit settings override the choice either way
+    assert plan(pa, L_hi, q_hi, Hq=8 * Hkv, Hkv=Hkv, D=128,
+                tc_pair=1).stats()["n_tc_pair_items"] > 0
+    assert plan(pa, L_lo, q_lo, Hq=g * Hkv, Hkv=Hkv, D=128,
+                tc_pair=-1).stats()["n_tc_pair_items"] == 0
 
 
 def test_plan_decode_items(pa):

@@ -118,7 +118,7 @@ def test_tensor_core_pair_tiles(pa, g, B, chunk):
     L = [qq + extra for qq, extra in zip(q, [0, 37, 300, 5, 900, 128, 700])]
     w = workloads.make_custom(L, q, Hq=2 * g, Hkv=2, D=128, block_size=B, seed=300 + g + B)
     kw = dict(max_chunk_tokens=chunk) if chunk else {}
-    (_, _), pair_run, want = full_check(pa, w, **kw)
+    (_, _), pair_run, want = full_check(pa, w, tc_pair=1, **kw)
     assert pair_run["plan"].stats()["n_tc_pair_items"] > 0
     (_, _), one_run, _ = full_check(pa, w, tc_pair=-1, **kw)
     assert one_run["plan"].stats()["n_tc_pair_items"] == 0
@@ -133,10 +133,10 @@ def test_tensor_core_pair_bf16_and_wide_groups(pa, g):
     L = [qq + extra for qq, extra in zip(q, [400, 33, 17])]
     w = workloads.make_custom(L, q, Hq=g, Hkv=1, D=128, block_size=32, seed=900 + g)
     want = gu.oracle_rows(w, gu.oracle_step(w))
-    got = gu.gpu_step(pa, w)
+    got = gu.gpu_step(pa, w, tc_pair=1)
     assert got["plan"].stats()["n_tc_pair_items"] > 0
     gu.assert_attention_close(got["out"].cpu().numpy(), want, f"g={g} fp32")
-    got16 = gu.gpu_step(pa, w, out_dtype=torch.bfloat16)
+    got16 = gu.gpu_step(pa, w, out_dtype=torch.bfloat16, tc_pair=1)
     d = np.abs(got16["out"].float().cpu().numpy() - want)
     # bf16 rounding of outputs of magnitude up to a few units: half an ulp is <= 2^-8 * |o|
     bound = np.abs(want) * 2.0 ** -8 + gu.ATOL_MAX
@@ -153,7 +153,7 @@ def test_tensor_core_pair_single_tile_items(pa):
     L = [int(x) for x in rng.integers(32, 129, size=n)]
     w = workloads.make_custom(L, q, Hq=8, Hkv=1, D=128, block_size=16, seed=32,
                               write_new=False)
-    got = gu.gpu_step(pa, w)
+    got = gu.gpu_step(pa, w, tc_pair=1)
     assert got["err"] == 0, pa.DEVERR.get(got["err"])
     assert got["plan"].stats()["n_tc_pair_items"] == n
     rows = gu.sample_rows(w, 400, seed=33)
@@ -164,7 +164,7 @@ def test_tensor_core_pair_single_tile_items(pa):
 def test_tensor_core_pair_tiny_first(pa):
     """Smallest two-tile case: 129 rows, one key tile."""
     w = workloads.make_custom([129], [129], Hq=1, Hkv=1, D=128, block_size=16, seed=11)
-    (_, _), got, _ = full_check(pa, w)
+    (_, _), got, _ = full_check(pa, w, tc_pair=1)
     assert got["plan"].stats()["n_tc_pair_items"] == 1
 
 
@@ -269,7 +269,7 @@ def test_subrequests_match_single_request(pa):
     two_w.k_pool, two_w.v_pool, two_w.num_blocks = full.k_pool, full.v_pool, full.num_blocks
     two_w.q = torch.cat([full.q[:r], full.q[L - qn:]])
     want = gu.oracle_rows(full, gu.oracle_step(full))
-    for kw in ({}, {"tc_pair": -1}):
+    for kw in ({}, {"tc_pair": 1}, {"tc_pair": -1}):
         one = gu.gpu_step(pa, full, **kw)["out"]
         two = gu.gpu_step(pa, two_w, **kw)["out"]
         gu.assert_attention_close(one.cpu().numpy(), want, "one request")
@@ -278,8 +278,8 @@ def test_subrequests_match_single_request(pa):
     # With 128-row tiles only, every row takes the same arithmetic in both batches (the
     # same key tiles, the same exponentials); the rows only land in different work
     # items, so the two agree far inside the oracle tolerance. (With 256-row items the
-    # full request's rows take the polynomial exponentials for part of the keys, and
-    # then only the oracle comparison above applies.)
+    # full request's rows run in the two-tile kernel, whose per-row arithmetic differs
+    # from the one-tile kernel's, and then only the oracle comparison above applies.)
     d_a = float((two[:r] - one[:r]).abs().max())
     d_b = float((two[r:] - one[L - qn:]).abs().max())
     assert d_a <= 2e-4 and d_b <= 2e-4, (d_a, d_b)
