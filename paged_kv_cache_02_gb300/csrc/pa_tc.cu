@@ -11,12 +11,14 @@
 //
 // How (GB300): one persistent CTA per SM, warp-specialised, 12 warps.
 //   warps 0, 3 TMA producers: warp 0 loads the item's 128 Q rows (one 3-D box per
-//              D half, double-buffered across items) and, per 128-key tile, K; warp 3
-//              loads V. Each gathers the tile per block piece straight from the
-//              physical blocks named by the block table, 128-byte swizzled, into its
-//              own 2-stage ring, so that a K tile never waits behind a V slot that
-//              the P V products still hold. Block ids come from a shared-memory cache
-//              per producer, filled one item ahead.
+//              D half; the next item's Q loads while the current item's last tiles
+//              and epilogue run) and, per 128-key tile, K into a 2-stage ring; warp 3
+//              loads V into a 3-stage ring (a V tile is consumed one softmax later
+//              than its K tile). Each gathers a tile per block piece straight from the
+//              physical blocks named by the block table, 128-byte swizzled, with its
+//              own barriers, so that a K tile never waits behind a V slot that the
+//              P V products still hold. Block ids come from a shared-memory cache per
+//              producer, filled one item ahead.
 //   warp 1     issues S_j = Q K_j^T (M = N = 128) into TMEM buffer j % 2, so S_{j+1}
 //              is computed while the softmax works on S_j.
 //   warp 2     issues O_h += P_{j,h} V_{j,h} for the two key halves h of the tile
@@ -51,7 +53,10 @@ namespace {
 constexpr int kRows = kTcRows;          // 128 rows per tile (M)
 constexpr int kKeys = 128;              // keys per tile (N of S, K of P V)
 constexpr int kD = 128;                 // head dim of this kernel
-constexpr int kStagesTc = 2;
+constexpr int kKStages = 2;             // K ring
+constexpr int kVStages = 3;             // V ring: a V tile is needed a softmax later than K
+constexpr int kQBuf = 1;                // Q buffers (the next item's Q loads under the
+                                        // current item's last softmax and epilogue)
 constexpr int kSoftmaxWarps = 8;
 constexpr int kThreadsTc = (4 + kSoftmaxWarps) * 32;
 constexpr int kHalf = 128 * 128;        // 128 rows x 64 elements, swizzled (16 KB)
@@ -66,15 +71,15 @@ __host__ __device__ constexpr uint32_t s_col(int b) { return (uint32_t)b * 128u;
 __host__ __device__ constexpr uint32_t o_col(int h) { return 256u + (uint32_t)h * 128u; }
 
 struct TcSmem {
-  uint8_t q[2][2][kHalf];               // [buffer][D half]
-  uint8_t k[kStagesTc][2][kHalf];       // [stage][D half], rows = keys
-  uint8_t v[kStagesTc][2][kHalf];       // [stage][D half], rows = keys
+  uint8_t q[kQBuf][2][kHalf];           // [buffer][D half]
+  uint8_t k[kKStages][2][kHalf];        // [stage][D half], rows = keys
+  uint8_t v[kVStages][2][kHalf];        // [stage][D half], rows = keys
   float stage[kSoftmaxWarps][32 * kStageCols];
   float xm[2][2][kRows], xl[2][2][kRows];  // [item parity][key half][row]: (m, l) at the end
   int bt_cache[2][2][kBtCache];         // [K / V producer][item parity]: block ids
-  uint64_t k_full[kStagesTc], k_empty[kStagesTc];
-  uint64_t v_full[kStagesTc], v_empty[kStagesTc];
-  uint64_t q_full[2], q_free[2];
+  uint64_t k_full[kKStages], k_empty[kKStages];
+  uint64_t v_full[kVStages], v_empty[kVStages];
+  uint64_t q_full[kQBuf], q_free[kQBuf];
   uint64_t s_full[2], s_free[2];
   uint64_t p_full[2][2];                // [S buffer][key half]: P of that half written
   uint64_t o_done[2][2];                // [key half][tile parity]: P V of that half done
@@ -82,9 +87,9 @@ struct TcSmem {
   uint64_t xbar[4];                     // per lane quadrant: its two softmax warps met
   uint64_t drain[2];
   uint32_t tmem_base;
-  int k_issued[kStagesTc], k_consumed[kStagesTc];
-  int v_issued[kStagesTc], v_consumed[kStagesTc];
-  int q_issued[2], q_consumed[2];
+  int k_issued[kKStages], k_consumed[kKStages];
+  int v_issued[kVStages], v_consumed[kVStages];
+  int q_issued[kQBuf], q_consumed[kQBuf];
   int abort_flag;
 };
 static_assert(sizeof(TcSmem) + 1024 <= 227 * 1024, "shared memory of the one-tile kernel");
@@ -105,14 +110,15 @@ __device__ __forceinline__ int tiles_of(const Item& x) {
 }
 
 // TMA producer of K (kIsK, also the item's Q) or of V. Phase bounds: q_free[b] of
-// item k + 2 needs q_full(k + 2) from here; the ring's empty barrier of tile n + 2
-// needs its full barrier of tile n + 2 from here. So no barrier is ever two phases
-// ahead of the waits below.
+// item k + kQBuf needs q_full(k + kQBuf) from here; the ring's empty barrier of tile
+// n + R (R stages) needs its full barrier of tile n + R from here. So no barrier is
+// ever two phases ahead of the waits below.
 template <bool kIsK>
 __device__ __forceinline__ void produce(TcSmem& sm, const AttnArgs& a, const CUtensorMap& map,
                                         const CUtensorMap& qmap, const Item* __restrict__ items,
                                         int n_items, int box_t, int lane) {
   const int G = gridDim.x;
+  constexpr int kStages = kIsK ? kKStages : kVStages;
   uint64_t* full = kIsK ? sm.k_full : sm.v_full;
   uint64_t* empty = kIsK ? sm.k_empty : sm.v_empty;
   uint8_t(*ring)[2][kHalf] = kIsK ? sm.k : sm.v;
@@ -150,8 +156,8 @@ __device__ __forceinline__ void produce(TcSmem& sm, const AttnArgs& a, const CUt
     }
     if (kIsK) {
       // the item's 128 Q rows: tokens x the g heads of its KV head, one box per D half
-      const int qb = k & 1;
-      ok = mbar_wait_warp(&sm.q_free[qb], ph(k, 2) ^ 1u, a.err);
+      const int qb = k % kQBuf;
+      ok = mbar_wait_warp(&sm.q_free[qb], ph(k, kQBuf) ^ 1u, a.err);
       if (!ok || *(volatile int*)&sm.abort_flag) { ok = false; break; }
       if (lane == 0) {
         mbar_arrive_expect_tx(&sm.q_full[qb], 2u * kHalf);
@@ -164,7 +170,7 @@ __device__ __forceinline__ void produce(TcSmem& sm, const AttnArgs& a, const CUt
     }
     const int32_t* bt = a.block_table + (int64_t)item.seq * a.max_blocks;
     for (int t0 = item.kv_begin; t0 < item.kv_end; t0 += kKeys, ++n) {
-      const int st = n % kStagesTc;
+      const int st = n % kStages;
       bool valid = false;
       int tok = 0;
       if (lane < pieces) {
@@ -184,7 +190,7 @@ __device__ __forceinline__ void produce(TcSmem& sm, const AttnArgs& a, const CUt
       }
       const uint32_t tile_bytes = __popc(__ballot_sync(0xffffffffu, valid)) * piece_bytes * 2u;
       // K_n is free once S of tile n - 2 completed, V_n once both halves' P V of it did
-      ok = mbar_wait_warp(&empty[st], ph(n, kStagesTc) ^ 1u, a.err);
+      ok = mbar_wait_warp(&empty[st], ph(n, kStages) ^ 1u, a.err);
       if (!ok || *(volatile int*)&sm.abort_flag) { ok = false; break; }
       if (lane == 0) mbar_arrive_expect_tx(&full[st], tile_bytes);
       __syncwarp();
@@ -215,17 +221,22 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
   const int G = gridDim.x;
 
   if (threadIdx.x == 0) {
-    for (int s = 0; s < kStagesTc; ++s) {
+    for (int s = 0; s < kKStages; ++s) {
       mbar_init(&sm.k_full[s], 1);
       mbar_init(&sm.k_empty[s], 1);
+      sm.k_issued[s] = sm.k_consumed[s] = 0;
+    }
+    for (int s = 0; s < kVStages; ++s) {
       mbar_init(&sm.v_full[s], 1);
       mbar_init(&sm.v_empty[s], 1);
-      sm.k_issued[s] = sm.k_consumed[s] = 0;
       sm.v_issued[s] = sm.v_consumed[s] = 0;
     }
-    for (int b = 0; b < 2; ++b) {
+    for (int b = 0; b < kQBuf; ++b) {
       mbar_init(&sm.q_full[b], 1);
       mbar_init(&sm.q_free[b], 1);
+      sm.q_issued[b] = sm.q_consumed[b] = 0;
+    }
+    for (int b = 0; b < 2; ++b) {
       mbar_init(&sm.s_full[b], 1);
       mbar_init(&sm.s_free[b], 1);
       mbar_init(&sm.p_full[b][0], kRows);
@@ -233,8 +244,6 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
       mbar_init(&sm.o_done[0][b], 1);
       mbar_init(&sm.o_done[1][b], 1);
       mbar_init(&sm.drain[b], 1);
-      sm.q_issued[b] = 0;
-      sm.q_consumed[b] = 0;
     }
     mbar_init(&sm.o_free, kSoftmaxWarps * 32);
     for (int qd = 0; qd < 4; ++qd) mbar_init(&sm.xbar[qd], 64);
@@ -256,7 +265,7 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
     produce<false>(sm, a, vmap, qmap, items, n_items, box_t, lane);
   } else if (warp == 1) {
     // ------------------------------------------------------------ S issuer
-    // Phase bounds: q_full of item k + 2 needs q_free(k), committed here; k_full of
+    // Phase bounds: q_full of item k + kQBuf needs q_free(k), committed here; k_full of
     // tile n + 2 needs k_empty(n), committed here; s_free of tile n + 2 needs the P V
     // of tile n + 2, which needs s_full(n + 2) from here.
     if (lane == 0) {
@@ -266,15 +275,15 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
       for (int it = blockIdx.x; it < n_items && ok; it += G, ++k) {
         const int nt = nt_next;
         if (it + G < n_items) nt_next = tiles_of(items[it + G]);
-        const int qb = k & 1;
-        if (!mbar_wait(&sm.q_full[qb], ph(k, 2), a.err)) { ok = false; break; }
+        const int qb = k % kQBuf;
+        if (!mbar_wait(&sm.q_full[qb], ph(k, kQBuf), a.err)) { ok = false; break; }
         sm.q_consumed[qb] += 1;
         tc::fence_after_sync();
         const uint64_t qd = tc::smem_desc_sw128(smem_addr(&sm.q[qb][0][0]), 16, 1024);
         for (int j = 0; j < nt; ++j, ++n) {
-          const int st = n % kStagesTc;
+          const int st = n % kKStages;
           const int b = n & 1;
-          if (!mbar_wait(&sm.k_full[st], ph(n, kStagesTc), a.err)) { ok = false; break; }
+          if (!mbar_wait(&sm.k_full[st], ph(n, kKStages), a.err)) { ok = false; break; }
           sm.k_consumed[st] += 1;
           // the buffer's last readers, both halves' P V of tile n - 2, are done
           if (!mbar_wait(&sm.s_free[b], ph(n, 2) ^ 1u, a.err)) { ok = false; break; }
@@ -301,8 +310,8 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
   } else if (warp == 2) {
     // ------------------------------------------------------------ P V issuer
     // Phase bounds: p_full[b][h] of tile n + 2 needs s_full(n + 2), which needs
-    // s_free(n), committed here after the P V of tile n; v_full of tile n + 2 needs
-    // v_empty(n), committed here; o_free of item k + 1 needs the P V of item k + 1.
+    // s_free(n), committed here after the P V of tile n; v_full of tile n + kVStages
+    // needs v_empty(n), committed here; o_free of item k + 1 needs the P V of item k + 1.
     if (lane == 0) {
       int n = 0, k = 0;
       bool ok = true;
@@ -311,9 +320,9 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
         const int nt = tiles_of(item);
         bool o_init0 = false, o_init1 = false;  // O_h written in this item
         for (int j = 0; j < nt; ++j, ++n) {
-          const int st = n % kStagesTc;
+          const int st = n % kVStages;
           const int b = n & 1;
-          if (!mbar_wait(&sm.v_full[st], ph(n, kStagesTc), a.err)) { ok = false; break; }
+          if (!mbar_wait(&sm.v_full[st], ph(n, kVStages), a.err)) { ok = false; break; }
           sm.v_consumed[st] += 1;
           // at an item's first tile, O_0 and O_1 must have been read out by the previous
           // item's epilogue
@@ -652,19 +661,21 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
   // After an abort, give copies still in flight a bounded time to land.
   if (sm.abort_flag && threadIdx.x == 0) {
     const uint64_t t0 = global_timer_ns();
-    for (int s = 0; s < kStagesTc; ++s) {
+    for (int s = 0; s < kKStages; ++s) {
       if (sm.k_issued[s] > sm.k_consumed[s]) {
         const uint32_t parity = (uint32_t)(sm.k_issued[s] - 1) & 1u;
         while (!mbar_try_wait(smem_addr(&sm.k_full[s]), parity))
           if (global_timer_ns() - t0 > kWaitLimitNs) break;
       }
+    }
+    for (int s = 0; s < kVStages; ++s) {
       if (sm.v_issued[s] > sm.v_consumed[s]) {
         const uint32_t parity = (uint32_t)(sm.v_issued[s] - 1) & 1u;
         while (!mbar_try_wait(smem_addr(&sm.v_full[s]), parity))
           if (global_timer_ns() - t0 > kWaitLimitNs) break;
       }
     }
-    for (int b = 0; b < 2; ++b) {
+    for (int b = 0; b < kQBuf; ++b) {
       if (sm.q_issued[b] > sm.q_consumed[b]) {
         const uint32_t parity = (uint32_t)(sm.q_issued[b] - 1) & 1u;
         while (!mbar_try_wait(smem_addr(&sm.q_full[b]), parity))
