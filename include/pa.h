@@ -210,6 +210,30 @@ pa_status pa_attention(pa_plan_t plan, void* d_out, pa_dtype out_dtype, const vo
                        int32_t num_blocks, float scale, void* d_workspace,
                        size_t workspace_bytes, void* stream);
 
+/* ---------------------------------------------------------------- one plan, many calls
+ * pa_attention = pa_plan_upload + pa_attention_planned. A step's plan is the same for
+ * every layer (the lengths and block tables do not change between layers), so a model
+ * uploads the plan once per step and launches the kernels once per layer.
+ *
+ * pa_plan_upload enqueues on `stream` the copy of the plan's work-item tables (pinned
+ * host memory, written at plan creation) into the first bytes of d_workspace
+ * (workspace_bytes >= the plan's workspace_bytes, 256-byte aligned; else
+ * PA_ERR_SHAPE / PA_ERR_UNSUPPORTED). Nothing else in the workspace is touched.
+ *
+ * pa_attention_planned takes pa_attention's arguments and launches its kernels
+ * without the upload: the workspace must hold this plan's tables from a
+ * pa_plan_upload (or pa_attention) of this plan ordered before it on the GPU, with no
+ * other plan's upload in between. Kernels read the tables and write the split-KV
+ * partials behind them, so calls with one plan and workspace must not overlap on the
+ * GPU. Argument checks and errors as for pa_attention. */
+pa_status pa_plan_upload(pa_plan_t plan, void* d_workspace, size_t workspace_bytes,
+                         void* stream);
+pa_status pa_attention_planned(pa_plan_t plan, void* d_out, pa_dtype out_dtype,
+                               const void* d_q, const void* d_k_pool, const void* d_v_pool,
+                               const int32_t* d_block_table, const int32_t* d_context_lens,
+                               const int32_t* d_query_lens, int32_t num_blocks, float scale,
+                               void* d_workspace, size_t workspace_bytes, void* stream);
+
 /* ---------------------------------------------------------------- no-alloc variant
  * The pages have no counterpart to this entry point; it exists for callers
  * that cannot allocate device memory for a workspace. A serving engine

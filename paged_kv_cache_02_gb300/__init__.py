@@ -5,10 +5,11 @@ ABI of ``include/pa.h``); this package is its thin Python binding. See
 ``_binding`` for the functions, which carry the C entry points' names.
 """
 from ._binding import (DEVERR, LIB_PATH, STATIC_WORKSPACE_BYTES, PagedAttentionError, Plan,
-                       library, pa_attention, pa_attention_static, pa_copy_blocks,
-                       pa_get_device_error, pa_plan_create, pa_slot_mapping, pa_write_kv, version)
+                       library, pa_attention, pa_attention_planned, pa_attention_static,
+                       pa_copy_blocks, pa_get_device_error, pa_plan_create, pa_plan_upload,
+                       pa_slot_mapping, pa_write_kv, version)
 
 __all__ = ["DEVERR", "LIB_PATH", "STATIC_WORKSPACE_BYTES", "PagedAttentionError", "Plan",
-           "library", "pa_attention", "pa_attention_static",
-           "pa_copy_blocks", "pa_get_device_error", "pa_plan_create", "pa_slot_mapping",
-           "pa_write_kv", "version"]
+           "library", "pa_attention", "pa_attention_planned", "pa_attention_static",
+           "pa_copy_blocks", "pa_get_device_error", "pa_plan_create", "pa_plan_upload",
+           "pa_slot_mapping", "pa_write_kv", "version"]

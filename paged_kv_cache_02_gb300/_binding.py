@@ -68,9 +68,13 @@ def _lib() -> C.CDLL:
                                      C.c_size_t, _P]
         lib.pa_attention_static.argtypes = [_P, _P, C.c_int, _P, _P, _P, _P, _P, _P, _I32,
                                             C.c_float, _P]
+        lib.pa_plan_upload.argtypes = [_P, _P, C.c_size_t, _P]
+        lib.pa_attention_planned.argtypes = [_P, _P, C.c_int, _P, _P, _P, _P, _P, _P, _I32,
+                                             C.c_float, _P, C.c_size_t, _P]
         for f in ("pa_get_device_error", "pa_slot_mapping", "pa_write_kv", "pa_copy_blocks",
                   "pa_plan_create", "pa_plan_destroy", "pa_plan_get_stats", "pa_plan_export",
-                  "pa_attention", "pa_attention_static"):
+                  "pa_attention", "pa_attention_static", "pa_plan_upload",
+                  "pa_attention_planned"):
             getattr(lib, f).restype = C.c_int
         _LIB = lib
     return _LIB
@@ -218,10 +222,33 @@ def pa_plan_create(context_lens, query_lens, Hq, Hkv, D, block_size, max_blocks_
     return Plan(context_lens, query_lens, Hq, Hkv, D, block_size, max_blocks_per_seq, **options)
 
 
+def pa_plan_upload(plan: Plan, workspace: torch.Tensor) -> None:
+    """Enqueues the copy of the plan's work-item tables into the workspace (on the
+    current stream): one upload per step serves every layer's pa_attention_planned."""
+    if not workspace.is_cuda:
+        raise ValueError("workspace must be a CUDA tensor")
+    if workspace.data_ptr() % 256:
+        raise ValueError("workspace must be 256-byte aligned")
+    _check(_lib().pa_plan_upload(plan._h, workspace.data_ptr(), workspace.numel(),
+                                 _stream(workspace)), "pa_plan_upload")
+
+
+def pa_attention_planned(plan: Plan, q: torch.Tensor, k_pool: torch.Tensor,
+                         v_pool: torch.Tensor, block_table: torch.Tensor,
+                         context_lens: torch.Tensor, query_lens: torch.Tensor,
+                         workspace: torch.Tensor, out: torch.Tensor | None = None,
+                         out_dtype=torch.float32, scale: float = 0.0) -> torch.Tensor:
+    """pa_attention without the table upload: ``workspace`` must hold this plan's tables
+    from pa_plan_upload (or pa_attention) with no other plan's upload since."""
+    return pa_attention(plan, q, k_pool, v_pool, block_table, context_lens, query_lens,
+                        out=out, out_dtype=out_dtype, scale=scale, workspace=workspace,
+                        _upload=False)
+
+
 def pa_attention(plan: Plan, q: torch.Tensor, k_pool: torch.Tensor, v_pool: torch.Tensor,
                  block_table: torch.Tensor, context_lens: torch.Tensor, query_lens: torch.Tensor,
                  out: torch.Tensor | None = None, out_dtype=torch.float32, scale: float = 0.0,
-                 workspace: torch.Tensor | None = None) -> torch.Tensor:
+                 workspace: torch.Tensor | None = None, _upload: bool = True) -> torch.Tensor:
     nb, B, Hkv, D = k_pool.shape
     if (Hkv, D, B) != (plan.Hkv, plan.D, plan.block_size):
         raise ValueError("pool shape does not match the plan")
@@ -240,15 +267,15 @@ def pa_attention(plan: Plan, q: torch.Tensor, k_pool: torch.Tensor, v_pool: torc
         workspace = plan.workspace(q.device)
     if workspace.data_ptr() % 256:
         raise ValueError("workspace must be 256-byte aligned")
-    _check(_lib().pa_attention(plan._h, _dev(out, out.dtype, "out", 3), dt,
+    fn = "pa_attention" if _upload else "pa_attention_planned"
+    _check(getattr(_lib(), fn)(plan._h, _dev(out, out.dtype, "out", 3), dt,
                                _dev(q, torch.bfloat16, "q", 3),
                                _dev(k_pool, torch.bfloat16, "k_pool", 4),
                                _dev(v_pool, torch.bfloat16, "v_pool", 4),
                                _dev(block_table, torch.int32, "block_table", 2),
                                _dev(context_lens, torch.int32, "context_lens", 1),
                                _dev(query_lens, torch.int32, "query_lens", 1), nb, float(scale),
-                               workspace.data_ptr(), workspace.numel(), _stream(q)),
-           "pa_attention")
+                               workspace.data_ptr(), workspace.numel(), _stream(q)), fn)
     return out
 
 

@@ -151,6 +151,13 @@ struct Unit {
 
 }  // namespace
 
+static pa_status attention_impl(pa_plan_t p, void* d_out, pa_dtype out_dtype, const void* d_q,
+                                const void* d_k_pool, const void* d_v_pool,
+                                const int32_t* d_block_table, const int32_t* d_context_lens,
+                                const int32_t* d_query_lens, int32_t num_blocks, float scale,
+                                void* d_workspace, size_t workspace_bytes, void* stream,
+                                bool upload);
+
 extern "C" {
 
 const char* pa_status_string(pa_status s) {
@@ -487,11 +494,50 @@ pa_status pa_plan_export(pa_plan_t p, int32_t* h_items, int32_t max_items, int32
   return PA_OK;
 }
 
+pa_status pa_plan_upload(pa_plan_t p, void* d_workspace, size_t workspace_bytes,
+                         void* stream) {
+  if (!p) return PA_ERR_INVALID_ARG;
+  if (p->total_q == 0) return PA_OK;
+  if (!d_workspace) return PA_ERR_INVALID_ARG;
+  if (workspace_bytes < p->ws_bytes) return PA_ERR_SHAPE;
+  if (reinterpret_cast<uintptr_t>(d_workspace) % 256) return PA_ERR_UNSUPPORTED;
+  if (p->table_bytes &&
+      cudaMemcpyAsync(d_workspace, p->host_tables, p->table_bytes, cudaMemcpyHostToDevice,
+                      static_cast<cudaStream_t>(stream)) != cudaSuccess)
+    return PA_ERR_CUDA;
+  return PA_OK;
+}
+
 pa_status pa_attention(pa_plan_t p, void* d_out, pa_dtype out_dtype, const void* d_q,
                        const void* d_k_pool, const void* d_v_pool, const int32_t* d_block_table,
                        const int32_t* d_context_lens, const int32_t* d_query_lens,
                        int32_t num_blocks, float scale, void* d_workspace,
                        size_t workspace_bytes, void* stream) {
+  return attention_impl(p, d_out, out_dtype, d_q, d_k_pool, d_v_pool, d_block_table,
+                        d_context_lens, d_query_lens, num_blocks, scale, d_workspace,
+                        workspace_bytes, stream, true);
+}
+
+pa_status pa_attention_planned(pa_plan_t p, void* d_out, pa_dtype out_dtype, const void* d_q,
+                               const void* d_k_pool, const void* d_v_pool,
+                               const int32_t* d_block_table, const int32_t* d_context_lens,
+                               const int32_t* d_query_lens, int32_t num_blocks, float scale,
+                               void* d_workspace, size_t workspace_bytes, void* stream) {
+  return attention_impl(p, d_out, out_dtype, d_q, d_k_pool, d_v_pool, d_block_table,
+                        d_context_lens, d_query_lens, num_blocks, scale, d_workspace,
+                        workspace_bytes, stream, false);
+}
+
+}  // extern "C"
+
+// Arguments are checked before anything is enqueued; then the plan's tables are
+// uploaded (unless the caller did it with pa_plan_upload) and the kernels launched.
+static pa_status attention_impl(pa_plan_t p, void* d_out, pa_dtype out_dtype, const void* d_q,
+                                const void* d_k_pool, const void* d_v_pool,
+                                const int32_t* d_block_table, const int32_t* d_context_lens,
+                                const int32_t* d_query_lens, int32_t num_blocks, float scale,
+                                void* d_workspace, size_t workspace_bytes, void* stream,
+                                bool upload) {
   if (!p) return PA_ERR_INVALID_ARG;
   if (out_dtype != PA_F32 && out_dtype != PA_BF16) return PA_ERR_INVALID_ARG;
   if (num_blocks <= 0) return PA_ERR_INVALID_ARG;
@@ -508,7 +554,7 @@ pa_status pa_attention(pa_plan_t p, void* d_out, pa_dtype out_dtype, const void*
   int* err = pa::device_error_word();
   if (!err) return PA_ERR_CUDA;
   uint8_t* ws = static_cast<uint8_t*>(d_workspace);
-  if (p->table_bytes &&
+  if (upload && p->table_bytes &&
       cudaMemcpyAsync(ws, p->host_tables, p->table_bytes, cudaMemcpyHostToDevice, s) !=
           cudaSuccess)
     return PA_ERR_CUDA;
@@ -598,7 +644,6 @@ pa_status pa_attention(pa_plan_t p, void* d_out, pa_dtype out_dtype, const void*
   return PA_OK;
 }
 
-}  // extern "C"
 
 // ====================================================================== no-alloc variant
 // Scratch for pa_attention_static: a fixed device array instead of a caller

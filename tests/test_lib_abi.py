@@ -34,7 +34,8 @@ def declared_entry_points():
 def test_header_declares_the_boundary():
     names = declared_entry_points()
     for must in ("pa_write_kv", "pa_copy_blocks", "pa_attention", "pa_plan_create",
-                 "pa_plan_destroy", "pa_status_string", "pa_slot_mapping"):
+                 "pa_plan_destroy", "pa_status_string", "pa_slot_mapping", "pa_plan_upload",
+                 "pa_attention_planned"):
         assert must in names, names
 
 
@@ -249,3 +250,18 @@ def test_plan_auto_split_fills_the_gpu(pa):
 def test_empty_batch(pa):
     p = pa.Plan([0, 0], [0, 0], 4, 4, 64, 16, 1)
     assert p.stats()["total_q"] == 0 and len(p.items()) == 0
+
+
+def test_plan_upload_checks_arguments_before_enqueuing(pa):
+    """pa_plan_upload rejects a missing, short or misaligned workspace synchronously,
+    before any copy is enqueued (so these checks run without a GPU)."""
+    import ctypes as C
+    lib = pa.library()
+    p = pa.Plan([300, 40], [20, 1], 8, 2, 128, 16, 32, num_sms=152)
+    need = p.workspace_bytes
+    assert lib.pa_plan_upload(None, C.c_void_p(4096), need, None) == 1     # no plan
+    assert lib.pa_plan_upload(p._h, None, need, None) == 1                  # no workspace
+    assert lib.pa_plan_upload(p._h, C.c_void_p(4096), need - 1, None) == 2  # too small
+    assert lib.pa_plan_upload(p._h, C.c_void_p(4096 + 16), need, None) == 4  # misaligned
+    empty = pa.Plan([0], [0], 8, 2, 128, 16, 1)
+    assert lib.pa_plan_upload(empty._h, None, 0, None) == 0                 # nothing to do

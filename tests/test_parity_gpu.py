@@ -285,6 +285,35 @@ def test_subrequests_match_single_request(pa):
     assert d_a <= 2e-4 and d_b <= 2e-4, (d_a, d_b)
 
 
+def test_plan_upload_serves_several_calls(pa):
+    """One pa_plan_upload serves several pa_attention_planned calls, as a model's layers
+    share a step's plan: each call equals pa_attention on the same inputs bit for bit,
+    with a mix of key-major, one-tile, two-tile and split items."""
+    w = workloads.make_custom([300, 130, 40, 1000, 700], [40, 20, 1, 3, 200], Hq=8, Hkv=2,
+                              D=128, block_size=16, seed=77, write_new=False)
+    dev = "cuda"
+    bt = torch.from_numpy(w.block_table).to(dev)
+    cl = torch.from_numpy(w.context_lens).to(dev)
+    ql = torch.from_numpy(w.query_lens).to(dev)
+    kp, vp = w.k_pool.to(dev), w.v_pool.to(dev)
+    plan = pa.Plan(w.context_lens, w.query_lens, w.Hq, w.Hkv, w.D, w.block_size, w.max_blocks,
+                   tc_pair=1, max_chunk_tokens=256)
+    st = plan.stats()
+    assert st["n_tc_pair_items"] and st["n_tc_decode_items"] and st["n_split_groups"]
+    g = torch.Generator().manual_seed(78)
+    qs = [w.q.to(dev)] + [torch.randn(w.q.shape, generator=g).to(torch.bfloat16).to(dev)
+                          for _ in range(2)]
+    want = [pa.pa_attention(plan, q, kp, vp, bt, cl, ql) for q in qs]
+    ws = plan.workspace(dev)
+    pa.pa_plan_upload(plan, ws)
+    got = [pa.pa_attention_planned(plan, q, kp, vp, bt, cl, ql, ws) for q in qs]
+    assert pa.pa_get_device_error(reset=True) == 0
+    for a, b in zip(got, want):
+        assert torch.equal(a, b)
+    ref = gu.oracle_rows(w, gu.oracle_step(w))
+    gu.assert_attention_close(got[0].cpu().numpy(), ref, "planned call")
+
+
 def test_bf16_output(pa):
     w = workloads.make(1)
     got = gu.gpu_step(pa, w, out_dtype=torch.bfloat16)
