@@ -143,6 +143,25 @@ def test_tensor_core_pair_bf16_and_wide_groups(pa, g):
     assert np.all(d <= bound), float((d - bound).max())
 
 
+@pytest.mark.parametrize("g", [1, 8, 64, 128])
+def test_tensor_core_one_tile_bf16_and_wide_groups(pa, g):
+    """One-tile items only (tc_pair=-1): fp32 and bf16 outputs (the epilogue's tensor
+    stores in both layouts), 1 to 128 query heads per KV head, full and partial 128-row
+    tiles over several key tiles."""
+    q = [max(1, 384 // g), max(1, 200 // g) + 1, max(1, 129 // g), 1]
+    L = [qq + extra for qq, extra in zip(q, [500, 77, 260, 40])]
+    w = workloads.make_custom(L, q, Hq=g, Hkv=1, D=128, block_size=32, seed=700 + g)
+    want = gu.oracle_rows(w, gu.oracle_step(w))
+    got = gu.gpu_step(pa, w, tc_pair=-1)
+    st = got["plan"].stats()
+    assert st["n_tc_pair_items"] == 0 and st["n_tc_items"] > st["n_tc_decode_items"]
+    gu.assert_attention_close(got["out"].cpu().numpy(), want, f"g={g} fp32")
+    got16 = gu.gpu_step(pa, w, out_dtype=torch.bfloat16, tc_pair=-1)
+    d = np.abs(got16["out"].float().cpu().numpy() - want)
+    bound = np.abs(want) * 2.0 ** -8 + gu.ATOL_MAX
+    assert np.all(d <= bound), float((d - bound).max())
+
+
 def test_tensor_core_pair_single_tile_items(pa):
     """Many consecutive two-tile items of one key tile each: every item's last S follows
     its first, so the next item's Q can land while the softmax warps still finish the
@@ -227,6 +246,54 @@ def test_tensor_core_decode_nan_tail_and_bf16(pa):
     got16 = gu.gpu_step(pa, w, out_dtype=torch.bfloat16, tc_min_rows=1)
     d = np.abs(got16["out"].float().cpu().numpy() - want)
     assert np.all(np.isfinite(d)) and d.max() <= 2e-2
+
+
+def _growing_scores(w, slope=1.0 / 96, seed=5):
+    """Rewrites a batch so that every query row's scores grow along the keys: K at
+    position p is c(p) = p * slope on every dimension (plus small noise) and query rows
+    are a_r on every dimension with a_r alternating between 1 and 1/20 by token. With
+    D = 128 a row with a_r = 1 gains about 16 * 128 * slope in log2 units per 128 keys,
+    so the kernels' lazy O rescale (when the running maximum grows by more than 2^8)
+    fires on nearly every key tile for those rows and never for the others, in the
+    same warps."""
+    g = torch.Generator().manual_seed(seed)
+    D = w.D
+    kp = w.k_pool.float()
+    for s, L in enumerate(w.context_lens):
+        for p in range(int(L)):
+            phys = int(w.block_table[s, p // w.block_size])
+            kp[phys, p % w.block_size] = p * slope + 0.05 * torch.randn(w.Hkv, D, generator=g)
+    w.k_pool = kp.to(torch.bfloat16)
+    q = torch.empty(w.q.shape)
+    tok = 0
+    for n in w.query_lens:
+        for t in range(int(n)):
+            q[tok + t] = 1.0 if t % 2 == 0 else 0.05
+        tok += int(n)
+    w.q = q.to(torch.bfloat16)
+    return w
+
+
+NO_SPLIT = 1 << 14   # a chunk longer than every key range: no split-KV items
+
+
+@pytest.mark.parametrize("kw", [{}, {"max_chunk_tokens": NO_SPLIT},
+                                {"tc_pair": 1, "max_chunk_tokens": NO_SPLIT},
+                                {"tc_pair": -1, "max_chunk_tokens": NO_SPLIT},
+                                {"tc_min_rows": -1, "max_chunk_tokens": NO_SPLIT},
+                                {"tc_decode": -1}, {"max_chunk_tokens": 192}])
+def test_lazy_rescale_on_growing_scores(pa, kw):
+    """Scores that keep growing along the keys force the online softmax to move its
+    reference maximum tile after tile (the O rescale in TMEM, or in registers on the
+    CUDA cores) in every kernel: key-major (q = 1, 3), one-tile (q = 40 or remainders),
+    two-tile (q = 300 x 4 heads) and split items; checked against the oracle."""
+    w = workloads.make_custom([900, 333, 700, 1100, 260], [1, 3, 40, 300, 2], Hq=8, Hkv=2,
+                              D=128, block_size=16, seed=55, write_new=False)
+    w = _growing_scores(w)
+    want = gu.oracle_rows(w, gu.oracle_step(w))
+    got = gu.gpu_step(pa, w, **kw)
+    assert got["err"] == 0, pa.DEVERR.get(got["err"])
+    gu.assert_attention_close(got["out"].cpu().numpy(), want, f"growing scores {kw}")
 
 
 def test_unused_slots_hold_nan(pa):
