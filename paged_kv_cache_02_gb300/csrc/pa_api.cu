@@ -121,12 +121,59 @@ struct pa_plan_s {
   size_t table_bytes;       // bytes of the item / group tables (copied each call)
   void* host_tables;        // table image: [dec][tc][tc pair items][groups] at their offsets
   bool host_pinned;
+  size_t host_cap;          // bytes of the pinned buffer (>= table_bytes)
+  cudaEvent_t upload_ev;    // recorded after each upload of the tables (pinned only)
+  bool upload_recorded;
+  bool host_reusable;       // every upload is covered by upload_ev
 };
 
 namespace {
 
 using pa::Item;
 using pa::SplitGroup;
+
+// Pinned host buffers of destroyed plans, kept for the next plans: a serving loop creates
+// and destroys a plan every step, and page-locking fresh memory costs more than building
+// the plan (about 0.27 ms per allocate + free pair on the GB300's Grace host). A buffer
+// is reused only once the last copy from it has completed (its upload event).
+struct PinnedBuf {
+  void* ptr;
+  size_t cap;
+  cudaEvent_t ev;
+  bool recorded;
+};
+std::mutex g_pinned_mu;
+std::vector<PinnedBuf> g_pinned_free;
+constexpr size_t kPinnedCacheMax = 8;
+
+bool pinned_take(size_t bytes, PinnedBuf* out) {
+  std::lock_guard<std::mutex> lock(g_pinned_mu);
+  int best = -1;
+  for (size_t i = 0; i < g_pinned_free.size(); ++i) {
+    const PinnedBuf& b = g_pinned_free[i];
+    if (b.cap < bytes || (best >= 0 && b.cap >= g_pinned_free[best].cap)) continue;
+    if (b.recorded && cudaEventQuery(b.ev) != cudaSuccess) continue;  // copy in flight
+    best = (int)i;
+  }
+  if (best < 0) return false;
+  *out = g_pinned_free[best];
+  out->recorded = false;
+  g_pinned_free.erase(g_pinned_free.begin() + best);
+  return true;
+}
+
+void pinned_give(const PinnedBuf& b) {
+  {
+    std::lock_guard<std::mutex> lock(g_pinned_mu);
+    if (g_pinned_free.size() < kPinnedCacheMax) {
+      g_pinned_free.push_back(b);
+      return;
+    }
+  }
+  if (b.recorded) cudaEventSynchronize(b.ev);
+  cudaFreeHost(b.ptr);
+  if (b.ev) cudaEventDestroy(b.ev);
+}
 
 bool is_pow2(int x) { return x > 0 && (x & (x - 1)) == 0; }
 size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
@@ -157,6 +204,24 @@ static pa_status attention_impl(pa_plan_t p, void* d_out, pa_dtype out_dtype, co
                                 const int32_t* d_query_lens, int32_t num_blocks, float scale,
                                 void* d_workspace, size_t workspace_bytes, void* stream,
                                 bool upload);
+
+// Marks the stream position after a copy from the plan's pinned table buffer, so that the
+// buffer is handed to a later plan only once the copy has completed.
+static pa_status note_upload(pa_plan_t p, cudaStream_t s) {
+  if (!p->host_pinned) return PA_OK;
+  if (!p->upload_ev &&
+      cudaEventCreateWithFlags(&p->upload_ev, cudaEventDisableTiming) != cudaSuccess) {
+    p->upload_ev = nullptr;
+    p->host_reusable = false;
+    return PA_ERR_CUDA;
+  }
+  if (cudaEventRecord(p->upload_ev, s) != cudaSuccess) {
+    p->host_reusable = false;
+    return PA_ERR_CUDA;
+  }
+  p->upload_recorded = true;
+  return PA_OK;
+}
 
 extern "C" {
 
@@ -419,9 +484,20 @@ pa_status pa_plan_create(const int32_t* h_context_lens, const int32_t* h_query_l
   p->ws_bytes = std::max<size_t>(off, 256);
   p->host_tables = nullptr;
   p->host_pinned = false;
+  p->host_cap = 0;
+  p->upload_ev = nullptr;
+  p->upload_recorded = false;
+  p->host_reusable = true;
   if (p->table_bytes > 0) {
-    if (cudaMallocHost(&p->host_tables, p->table_bytes) == cudaSuccess) {
+    PinnedBuf b;
+    if (pinned_take(p->table_bytes, &b)) {
+      p->host_tables = b.ptr;
+      p->host_cap = b.cap;
+      p->upload_ev = b.ev;
       p->host_pinned = true;
+    } else if (cudaMallocHost(&p->host_tables, p->table_bytes) == cudaSuccess) {
+      p->host_pinned = true;
+      p->host_cap = p->table_bytes;
     } else {
       cudaGetLastError();
       p->host_tables = malloc(p->table_bytes);
@@ -444,10 +520,15 @@ pa_status pa_plan_create(const int32_t* h_context_lens, const int32_t* h_query_l
 pa_status pa_plan_destroy(pa_plan_t p) {
   if (!p) return PA_OK;
   if (p->host_tables) {
-    if (p->host_pinned)
+    if (p->host_pinned && p->host_reusable) {
+      pinned_give({p->host_tables, p->host_cap, p->upload_ev, p->upload_recorded});
+    } else if (p->host_pinned) {
+      cudaDeviceSynchronize();  // an upload not covered by the event may be in flight
       cudaFreeHost(p->host_tables);
-    else
+      if (p->upload_ev) cudaEventDestroy(p->upload_ev);
+    } else {
       free(p->host_tables);
+    }
   }
   delete p;
   return PA_OK;
@@ -505,7 +586,7 @@ pa_status pa_plan_upload(pa_plan_t p, void* d_workspace, size_t workspace_bytes,
       cudaMemcpyAsync(d_workspace, p->host_tables, p->table_bytes, cudaMemcpyHostToDevice,
                       static_cast<cudaStream_t>(stream)) != cudaSuccess)
     return PA_ERR_CUDA;
-  return PA_OK;
+  return note_upload(p, static_cast<cudaStream_t>(stream));
 }
 
 pa_status pa_attention(pa_plan_t p, void* d_out, pa_dtype out_dtype, const void* d_q,
@@ -554,10 +635,13 @@ static pa_status attention_impl(pa_plan_t p, void* d_out, pa_dtype out_dtype, co
   int* err = pa::device_error_word();
   if (!err) return PA_ERR_CUDA;
   uint8_t* ws = static_cast<uint8_t*>(d_workspace);
-  if (upload && p->table_bytes &&
-      cudaMemcpyAsync(ws, p->host_tables, p->table_bytes, cudaMemcpyHostToDevice, s) !=
-          cudaSuccess)
-    return PA_ERR_CUDA;
+  if (upload && p->table_bytes) {
+    if (cudaMemcpyAsync(ws, p->host_tables, p->table_bytes, cudaMemcpyHostToDevice, s) !=
+        cudaSuccess)
+      return PA_ERR_CUDA;
+    const pa_status st = note_upload(p, s);
+    if (st != PA_OK) return st;
+  }
 
   pa::AttnArgs a;
   a.q = static_cast<const uint16_t*>(d_q);

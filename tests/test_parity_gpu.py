@@ -381,6 +381,40 @@ def test_plan_upload_serves_several_calls(pa):
     gu.assert_attention_close(got[0].cpu().numpy(), ref, "planned call")
 
 
+def test_plan_tables_outlive_early_destroy(pa):
+    """Destroyed plans hand their pinned table buffers to later plans only once the
+    uploads from them have completed: plans created, launched and destroyed while the
+    stream is still busy (so every upload is still queued) and replaced by new plans
+    with other tables all give the results of plans run one at a time."""
+    dev = "cuda"
+    ws_ = [workloads.make_custom([300 + 40 * i, 90 + i, 1000 - 30 * i], [1 + i, 20 + 3 * i, 2],
+                                 Hq=8, Hkv=2, D=128, block_size=16, seed=500 + i,
+                                 write_new=False) for i in range(6)]
+    # device inputs first: a copy from pageable memory would wait for the busy stream
+    dev_in = [(torch.from_numpy(w.block_table).to(dev), torch.from_numpy(w.context_lens).to(dev),
+               torch.from_numpy(w.query_lens).to(dev), w.q.to(dev), w.k_pool.to(dev),
+               w.v_pool.to(dev)) for w in ws_]
+    torch.cuda.synchronize()
+
+    def run(w, t):
+        bt, cl, ql, q, kp, vp = t
+        plan = pa.Plan(w.context_lens, w.query_lens, w.Hq, w.Hkv, w.D, w.block_size,
+                       w.max_blocks)
+        out = pa.pa_attention(plan, q, kp, vp, bt, cl, ql)
+        plan.close()
+        return out
+    want = []
+    for w, t in zip(ws_, dev_in):
+        want.append(run(w, t))
+        torch.cuda.synchronize()
+    torch.cuda._sleep(200_000_000)       # keep the stream busy: the uploads below queue up
+    got = [run(w, t) for w, t in zip(ws_, dev_in)]
+    torch.cuda.synchronize()
+    assert pa.pa_get_device_error(reset=True) == 0
+    for a, b in zip(got, want):
+        assert torch.equal(a, b)
+
+
 def test_bf16_output(pa):
     w = workloads.make(1)
     got = gu.gpu_step(pa, w, out_dtype=torch.bfloat16)
