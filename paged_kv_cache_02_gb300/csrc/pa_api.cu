@@ -73,6 +73,24 @@ pa_status make_pool_map(CUtensorMap* map, const void* pool, int64_t num_blocks, 
   return r == CUDA_SUCCESS ? PA_OK : PA_ERR_CUDA;
 }
 
+pa_status make_pool_map_grouped(CUtensorMap* map, const void* pool, int64_t num_blocks,
+                                int block_size, int Hkv, int box_t) {
+  auto fn = encode_fn();
+  if (!fn) return PA_ERR_CUDA;
+  constexpr int D = 128;
+  // dims: 64 elements of a D half, 8 tokens, the 2 D halves, groups of 8 tokens, heads
+  cuuint64_t dims[5] = {64u, 8u, 2u, (cuuint64_t)(num_blocks * block_size / 8),
+                        (cuuint64_t)Hkv};
+  cuuint64_t strides[4] = {(cuuint64_t)Hkv * D * 2, 128u, (cuuint64_t)8 * Hkv * D * 2,
+                           (cuuint64_t)D * 2};
+  cuuint32_t box[5] = {64u, 8u, 2u, (cuuint32_t)(box_t / 8), 1u};
+  cuuint32_t estr[5] = {1u, 1u, 1u, 1u, 1u};
+  CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 5, const_cast<void*>(pool), dims,
+                  strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? PA_OK : PA_ERR_CUDA;
+}
+
 pa_status make_q_map(CUtensorMap* map, const void* q, int64_t total_q, int Hq, int D, int g,
                      int rows) {
   auto fn = encode_fn();
@@ -688,11 +706,15 @@ static pa_status attention_impl(pa_plan_t p, void* d_out, pa_dtype out_dtype, co
     int sms = device_sms();
     if (sms <= 0) return PA_ERR_CUDA;
     if (p->n_tcd > 0) {
-      CUtensorMap qmap16;
+      CUtensorMap qmap16, kmap_g, vmap_g;
       st = pa::make_q_map(&qmap16, d_q, p->total_q, p->Hq, p->D, p->g, pa::kTcdRows);
       if (st != PA_OK) return st;
+      st = pa::make_pool_map_grouped(&kmap_g, d_k_pool, num_blocks, p->block_size, p->Hkv, box_t);
+      if (st != PA_OK) return st;
+      st = pa::make_pool_map_grouped(&vmap_g, d_v_pool, num_blocks, p->block_size, p->Hkv, box_t);
+      if (st != PA_OK) return st;
       const int grid = std::min(p->n_tcd, sms);
-      cudaError_t e = pa::launch_tcd(a, kmap, vmap, qmap16,
+      cudaError_t e = pa::launch_tcd(a, kmap_g, vmap_g, qmap16,
                                      reinterpret_cast<const Item*>(ws + p->off_tcd), p->n_tcd,
                                      box_t, grid, s);
       if (e != cudaSuccess) return PA_ERR_CUDA;

@@ -68,6 +68,12 @@ int* device_error_word();
 
 // Builds a 3-D tiled tensor map over a pool viewed as [num_blocks * B][Hkv][D] bf16.
 // box = (box_d, 1, box_t); swizzle128 selects the 128-byte swizzle.
+// 5-D tiled map over a pool [num_blocks * B][Hkv][128] bf16 whose box is a block piece of
+// box_t tokens (a multiple of 8) of one KV head, both D halves, 128-byte swizzled: the box
+// lands as box_t / 8 groups of 2 KB, each [D half][8 rows x 128 B], so that one copy per
+// piece fills both halves (see the key-major kernel's tile layout).
+pa_status make_pool_map_grouped(CUtensorMap* map, const void* pool, int64_t num_blocks,
+                                int block_size, int Hkv, int box_t);
 pa_status make_pool_map(CUtensorMap* map, const void* pool, int64_t num_blocks, int block_size,
                         int Hkv, int D, int box_d, int box_t, bool swizzle128);
 

@@ -15,8 +15,9 @@
 //
 // Warps (6, one persistent CTA per SM):
 //   0     TMA producer: the item's 16 query rows (double-buffered across items),
-//         K and V tiles of 128 keys per block piece into two 3-stage rings with
-//         their own barriers (a K stage is free once its S^T is done).
+//         K and V tiles of 128 keys into two 3-stage rings with their own barriers
+//         (a K stage is free once its S^T is done); one 5-D copy per block piece
+//         and tile brings both D halves of the piece's keys.
 //   1     MMA issuer: issues whichever of the next S^T (up to two tiles ahead)
 //         and the next P V is ready, so neither waits behind the other's data.
 //   2-5   softmax: thread = key of the tile (TMEM lane), then = head dimension for
@@ -43,6 +44,12 @@ constexpr int kN = kTcdRows;            // query rows per item (N), 16
 constexpr int kStages = 3;
 constexpr int kThreadsD = 192;
 constexpr int kHalf = 128 * 128;        // 128 rows x 64 elements, swizzled (16 KB)
+// A K or V tile is 16 groups of 8 keys, 2 KB each: [D half][8 rows x 128 B], every half
+// one 128-byte swizzle atom. A block piece is then a run of whole groups, which one TMA
+// copy of a 5-D box fills with both D halves (a box of box_t tokens x 256 bytes instead
+// of two of 128 bytes per token: twice the bytes per copy, half the copies).
+constexpr int kGroup = 2048;            // 8 keys, both D halves
+constexpr int kGroupHalf = 1024;        // one D half of a group
 constexpr int kQHalf = kN * 128;        // 16 rows x 64 elements (2 KB)
 constexpr float kRescaleLog2 = 8.f;
 constexpr uint32_t kTmemCols = 64;
@@ -54,8 +61,8 @@ constexpr uint32_t kIdescS = tc::idesc_bf16_f32(128, kN, false);
 constexpr uint32_t kIdescO = tc::idesc_bf16_f32(128, kN, false) | (1u << 15);
 
 struct TcdSmem {
-  uint8_t k[kStages][2][kHalf];         // [stage][D half], rows = keys
-  uint8_t v[kStages][2][kHalf];
+  uint8_t k[kStages][2 * kHalf];        // [stage][group of 8 keys][D half][8 rows]
+  uint8_t v[kStages][2 * kHalf];
   uint8_t q[2][2][kQHalf];              // [item parity][D half], 16 rows
   uint8_t p[2][2][kQHalf];              // P^T [tile parity][key half], 16 rows x 64 keys
   float4 red[2][4][kN / 4];             // cross-warp partial maxima / sums [parity][warp][row]
@@ -390,7 +397,7 @@ __global__ void __launch_bounds__(kThreadsD, 1)
       prefetch_tensormap(&qmap);
     }
     const int pieces = kKeys / box_t;
-    const uint32_t piece_bytes = (uint32_t)box_t * 128u;
+    const uint32_t piece_bytes = (uint32_t)box_t * 128u;  // one D half of one piece
     int n = 0, k = 0;
     bool ok = true;
     int nb[kBtPerLane];
@@ -450,26 +457,22 @@ __global__ void __launch_bounds__(kThreadsD, 1)
           }
         }
         const uint32_t tile_bytes = __popc(__ballot_sync(0xffffffffu, valid)) * piece_bytes * 2u;
-        const uint32_t row_off = (uint32_t)lane * box_t * 128u;
+        const uint32_t piece_off = (uint32_t)lane * box_t * 256u;  // whole groups
         // K_n: its stage is free once S^T of tile n - 3 is done
         ok = mbar_wait_warp(&sm.k_empty[st], ph(n, kStages) ^ 1u, a.err);
         if (!ok || *(volatile int*)&sm.abort_flag) { ok = false; break; }
         if (lane == 0) mbar_arrive_expect_tx(&sm.k_full[st], tile_bytes);
         __syncwarp();
-        if (valid) {
-          tma_load_3d(&sm.k[st][0][row_off], &kmap, &sm.k_full[st], 0, item.kv_head, tok);
-          tma_load_3d(&sm.k[st][1][row_off], &kmap, &sm.k_full[st], 64, item.kv_head, tok);
-        }
+        if (valid)
+          tma_load_5d(&sm.k[st][piece_off], &kmap, &sm.k_full[st], 0, 0, 0, tok >> 3, item.kv_head);
         if (lane == 0) sm.k_issued[st] += 1;
         // V_n: free once P V of tile n - 3 is done
         ok = mbar_wait_warp(&sm.v_empty[st], ph(n, kStages) ^ 1u, a.err);
         if (!ok || *(volatile int*)&sm.abort_flag) { ok = false; break; }
         if (lane == 0) mbar_arrive_expect_tx(&sm.v_full[st], tile_bytes);
         __syncwarp();
-        if (valid) {
-          tma_load_3d(&sm.v[st][0][row_off], &vmap, &sm.v_full[st], 0, item.kv_head, tok);
-          tma_load_3d(&sm.v[st][1][row_off], &vmap, &sm.v_full[st], 64, item.kv_head, tok);
-        }
+        if (valid)
+          tma_load_5d(&sm.v[st][piece_off], &vmap, &sm.v_full[st], 0, 0, 0, tok >> 3, item.kv_head);
         if (lane == 0) sm.v_issued[st] += 1;
       }
       if (has_next) {
@@ -513,13 +516,14 @@ __global__ void __launch_bounds__(kThreadsD, 1)
             }
             sm.k_consumed[st] += 1;
             tc::fence_after_sync();
-            // S^T = K Q^T: 8 steps of 16 dims; step kk starts (kk / 4) D halves and
-            // (kk % 4) 32-byte chunks into both operands
-            const uint64_t kd = tc::smem_desc_sw128(smem_addr(&sm.k[st][0][0]), 16, 1024);
+            // S^T = K Q^T: 8 steps of 16 dims; step kk starts (kk % 4) 32-byte chunks into
+            // D half kk / 4 of both operands (K's 8-row groups are kGroup apart, its
+            // halves kGroupHalf; Q's halves kQHalf)
+            const uint64_t kd = tc::smem_desc_sw128(smem_addr(&sm.k[st][0]), 16, kGroup);
             tc::mma_bf16_c<false>(tmem + (uint32_t)b * kN, kd, qd, kIdescS);
 #pragma unroll
             for (int kk = 1; kk < kD / 16; ++kk) {
-              const uint64_t ko = (uint64_t)(((kk >> 2) * kHalf + (kk & 3) * 32) >> 4);
+              const uint64_t ko = (uint64_t)(((kk >> 2) * kGroupHalf + (kk & 3) * 32) >> 4);
               const uint64_t qo = (uint64_t)(((kk >> 2) * kQHalf + (kk & 3) * 32) >> 4);
               tc::mma_bf16_c<true>(tmem + (uint32_t)b * kN, kd + ko, qd + qo, kIdescS);
             }
@@ -553,8 +557,8 @@ __global__ void __launch_bounds__(kThreadsD, 1)
             const int kk_end = (valid + 15) >> 4;
             if (valid < kk_end * 16) {
               for (int r = valid; r < kk_end * 16; ++r) {
-                uint4* v0 = reinterpret_cast<uint4*>(&sm.v[st][0][r * 128]);
-                uint4* v1 = reinterpret_cast<uint4*>(&sm.v[st][1][r * 128]);
+                uint4* v0 = reinterpret_cast<uint4*>(&sm.v[st][(r >> 3) * kGroup + (r & 7) * 128]);
+                uint4* v1 = v0 + kGroupHalf / 16;
 #pragma unroll
                 for (int q = 0; q < 8; ++q) {
                   v0[q] = make_uint4(0, 0, 0, 0);
@@ -564,10 +568,11 @@ __global__ void __launch_bounds__(kThreadsD, 1)
               tc::fence_async_shared();
             }
             tc::fence_after_sync();
-            // O^T += V^T P^T: step kk covers keys 16 kk .. 16 kk + 15: V rows (the
-            // MN-major A operand, D halves kHalf apart) and P^T columns (K-major B, key
-            // halves kQHalf apart)
-            const uint64_t vd = tc::smem_desc_sw128(smem_addr(&sm.v[st][0][0]), kHalf, 1024);
+            // O^T += V^T P^T: step kk covers keys 16 kk .. 16 kk + 15: two 8-key groups of
+            // V (the MN-major A operand: D halves kGroupHalf apart, groups kGroup) and P^T
+            // columns (K-major B, key halves kQHalf apart)
+            const uint64_t vd =
+                tc::smem_desc_sw128(smem_addr(&sm.v[st][0]), kGroupHalf, kGroup);
             const uint64_t pd = tc::smem_desc_sw128(smem_addr(&sm.p[b][0][0]), 16, 1024);
             if (j_p > 0)
               tc::mma_bf16_c<true>(tmem + kColO, vd, pd, kIdescO);
@@ -576,7 +581,7 @@ __global__ void __launch_bounds__(kThreadsD, 1)
 #pragma unroll
             for (int kk = 1; kk < kKeys / 16; ++kk) {
               if (kk < kk_end) {
-                const uint64_t vo = (uint64_t)((kk * 16 * 128) >> 4);
+                const uint64_t vo = (uint64_t)((kk * 2 * kGroup) >> 4);
                 const uint64_t po = (uint64_t)(((kk >> 2) * kQHalf + (kk & 3) * 32) >> 4);
                 tc::mma_bf16_c<true>(tmem + kColO, vd + vo, pd + po, kIdescO);
               }
