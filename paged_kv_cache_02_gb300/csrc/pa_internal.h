@@ -106,9 +106,11 @@ int tc_smem_bytes();
 cudaError_t launch_tc2(const AttnArgs& a, const CUtensorMap& kmap, const CUtensorMap& vmap,
                        const CUtensorMap& qmap, const CUtensorMap& omap, const Item* items,
                        int32_t n_items, int box_t, int grid, cudaStream_t s);
-// 3-D tiled map over the output viewed as [total_q][Hq][D] (fp32 or bf16), no swizzle,
-// box (16, min(g, 32), 32 / min(g, 32)): one box is 16 columns of the 32 packed rows
-// (tokens x heads of one KV head) of a warp.
+// 3-D tiled map over the output viewed as [total_q][Hq][D] (fp32 or bf16), box (16,
+// min(g, 32), 32 / min(g, 32)): one box is 16 columns of the 32 packed rows (tokens x
+// heads of one KV head) of a warp. The staging side is swizzled (64-byte rows of fp32
+// with the 64-byte pattern, 32-byte rows of bf16 with the 32-byte one) so that a warp
+// writes its rows there without bank conflicts.
 pa_status make_out_map(CUtensorMap* map, void* out, int64_t total_q, int Hq, int D, int g,
                        bool bf16);
 int tc2_smem_bytes();

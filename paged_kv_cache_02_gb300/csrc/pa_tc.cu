@@ -588,7 +588,10 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
           if (lane == 0) bulk_wait_read();
           __syncwarp();
           if (whole) {
-            // the output box's layout: packed row-major (tokens x heads x columns)
+            // the output box's layout: row-major rows (tokens x heads) of 16 columns,
+            // swizzled as the tensor map says (fp32: 16-byte chunk c of row r at
+            // c ^ ((r / 2) % 4); bf16: at c ^ ((r / 4) % 2)), so that the eight lanes of
+            // each quarter-warp write to distinct banks
             if (a.out_bf16) {
               uint4* d = reinterpret_cast<uint4*>(reinterpret_cast<uint8_t*>(stg) + lane * 32);
 #pragma unroll
@@ -598,13 +601,14 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
                 w.y = pack_bf16(o[8 * i + 2], o[8 * i + 3]);
                 w.z = pack_bf16(o[8 * i + 4], o[8 * i + 5]);
                 w.w = pack_bf16(o[8 * i + 6], o[8 * i + 7]);
-                d[i] = w;
+                d[i ^ ((lane >> 2) & 1)] = w;
               }
             } else {
               float4* d = reinterpret_cast<float4*>(stg + lane * kStageCols);
 #pragma unroll
               for (int i = 0; i < 4; ++i)
-                d[i] = make_float4(o[4 * i], o[4 * i + 1], o[4 * i + 2], o[4 * i + 3]);
+                d[i ^ ((lane >> 1) & 3)] =
+                    make_float4(o[4 * i], o[4 * i + 1], o[4 * i + 2], o[4 * i + 3]);
             }
             tc::fence_async_shared();
             __syncwarp();

@@ -512,6 +512,9 @@ __global__ void __launch_bounds__(kThreads2, 1)
             // the previous store has read the staging buffer
             if (lane == 0) bulk_wait_read();
             __syncwarp();
+            // rows of 16 columns swizzled as the tensor map says (fp32: 16-byte chunk c
+            // of row r at c ^ ((r / 2) % 4); bf16: at c ^ ((r / 4) % 2)): the eight
+            // lanes of each quarter-warp write to distinct banks
             if (a.out_bf16) {
               uint4* d = reinterpret_cast<uint4*>(reinterpret_cast<uint8_t*>(stg) + lane * 32);
 #pragma unroll
@@ -521,14 +524,15 @@ __global__ void __launch_bounds__(kThreads2, 1)
                 w.y = pack_bf16(o[hh * 16 + 8 * i + 2] * inv, o[hh * 16 + 8 * i + 3] * inv);
                 w.z = pack_bf16(o[hh * 16 + 8 * i + 4] * inv, o[hh * 16 + 8 * i + 5] * inv);
                 w.w = pack_bf16(o[hh * 16 + 8 * i + 6] * inv, o[hh * 16 + 8 * i + 7] * inv);
-                d[i] = w;
+                d[i ^ ((lane >> 2) & 1)] = w;
               }
             } else {
               float4* d = reinterpret_cast<float4*>(stg + lane * kStageCols);
 #pragma unroll
               for (int i = 0; i < 4; ++i)
-                d[i] = make_float4(o[hh * 16 + 4 * i] * inv, o[hh * 16 + 4 * i + 1] * inv,
-                                   o[hh * 16 + 4 * i + 2] * inv, o[hh * 16 + 4 * i + 3] * inv);
+                d[i ^ ((lane >> 1) & 3)] =
+                    make_float4(o[hh * 16 + 4 * i] * inv, o[hh * 16 + 4 * i + 1] * inv,
+                                o[hh * 16 + 4 * i + 2] * inv, o[hh * 16 + 4 * i + 3] * inv);
             }
             tc::fence_async_shared();
             __syncwarp();
