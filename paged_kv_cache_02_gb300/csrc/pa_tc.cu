@@ -413,21 +413,25 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
     float* stg = sm.stage[warp - 4];
     int n = 0, k = 0;
     bool ok = true;
-    // the next item and its lengths are read one item ahead, off the critical path
-    Item item_next{};
+    // Items are read two ahead and their lengths one ahead: the length loads need the
+    // item's sequence index, so with one stage they would wait for the item load
+    // itself right at the item switch.
+    Item item_next{}, item_next2{};
     int L_next = 0, ql_next = 0;
     if ((int)blockIdx.x < n_items) {
       item_next = items[blockIdx.x];
       L_next = __ldg(a.context_lens + item_next.seq);
       ql_next = __ldg(a.query_lens + item_next.seq);
+      if ((int)blockIdx.x + G < n_items) item_next2 = items[blockIdx.x + G];
     }
     for (int it = blockIdx.x; it < n_items && ok; it += G, ++k) {
       const Item item = item_next;
       const int L = L_next, ql = ql_next;
       if (it + G < n_items) {
-        item_next = items[it + G];
+        item_next = item_next2;
         L_next = __ldg(a.context_lens + item_next.seq);
         ql_next = __ldg(a.query_lens + item_next.seq);
+        if (it + 2 * G < n_items) item_next2 = items[it + 2 * G];
       }
       if (item.kv_end > L || item.row_begin + item.row_count > ql * a.g)
         record_error(a.err, PA_DEVERR_LENS);

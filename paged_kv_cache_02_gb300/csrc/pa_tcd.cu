@@ -494,12 +494,16 @@ __global__ void __launch_bounds__(kThreadsD, 1)
     if (lane == 0) {
       bool ok = true;
       // S^T cursor: item index it_s, the CTA's k_s-th item, its tile j_s, CTA tile n_s
+      // (each cursor holds its next item already loaded, so that an item switch does
+      // not wait for a global load)
       int it_s = blockIdx.x, k_s = 0, j_s = 0, n_s = 0;
       int nt_s = it_s < n_items ? tiles_of(items[it_s]) : 0;
+      int nt_s_next = it_s + G < n_items ? tiles_of(items[it_s + G]) : 0;
       uint64_t qd = 0;
       // P V cursor
       int it_p = blockIdx.x, k_p = 0, j_p = 0, n_p = 0;
       Item item_p = it_p < n_items ? items[it_p] : Item{};
+      Item item_p_next = it_p + G < n_items ? items[it_p + G] : Item{};
       int nt_p = it_p < n_items ? tiles_of(item_p) : 0;
       uint64_t t_idle = global_timer_ns();
       while (it_p < n_items) {
@@ -535,7 +539,8 @@ __global__ void __launch_bounds__(kThreadsD, 1)
               j_s = 0;
               ++k_s;
               it_s += G;
-              nt_s = it_s < n_items ? tiles_of(items[it_s]) : 0;
+              nt_s = nt_s_next;
+              nt_s_next = it_s + G < n_items ? tiles_of(items[it_s + G]) : 0;
             }
             progress = true;
           }
@@ -595,8 +600,9 @@ __global__ void __launch_bounds__(kThreadsD, 1)
               ++k_p;
               it_p += G;
               if (it_p < n_items) {
-                item_p = items[it_p];
+                item_p = item_p_next;
                 nt_p = tiles_of(item_p);
+                if (it_p + G < n_items) item_p_next = items[it_p + G];
               }
             }
             progress = true;
@@ -635,21 +641,25 @@ __global__ void __launch_bounds__(kThreadsD, 1)
     th.x = 0;
     th.n = 0;
     bool ok = true;
-    // the next item and its lengths are read one item ahead, off the critical path
-    Item item_next{};
+    // Items are read two ahead and their lengths one ahead: the length loads need the
+    // item's sequence index, so with one stage they would wait for the item load
+    // itself right at the item switch.
+    Item item_next{}, item_next2{};
     int L_next = 0, ql_next = 0;
     if ((int)blockIdx.x < n_items) {
       item_next = items[blockIdx.x];
       L_next = __ldg(a.context_lens + item_next.seq);
       ql_next = __ldg(a.query_lens + item_next.seq);
+      if ((int)blockIdx.x + G < n_items) item_next2 = items[blockIdx.x + G];
     }
     for (int it = blockIdx.x; it < n_items && ok; it += G) {
       const Item item = item_next;
       const int L = L_next, ql = ql_next;
       if (it + G < n_items) {
-        item_next = items[it + G];
+        item_next = item_next2;
         L_next = __ldg(a.context_lens + item_next.seq);
         ql_next = __ldg(a.query_lens + item_next.seq);
+        if (it + 2 * G < n_items) item_next2 = items[it + 2 * G];
       }
       if (item.kv_end > L || item.row_begin + item.row_count > ql * a.g)
         record_error(a.err, PA_DEVERR_LENS);
