@@ -1,0 +1,178 @@
+"""Pins for a KV block manager (the oracle's, and the same checks for the library's).
+
+Each ``check_*`` takes a factory ``make(num_blocks, block_size, free_order)`` that
+returns an object with the oracle's interface (add, fork, free_seq, append,
+append_batch, table, filled, num_free, refcount) and raises AssertionError when
+the manager disagrees with something that does not come from the manager itself:
+
+* the vLLM post's worked example ("1. overall architecture": slots, #filled, the
+  third block) and its copy-on-write example ("2.1 parallel sampling"), stored in
+  ``tests/golden``;
+* the property a KV manager exists for, checked by brute force: after any seeded
+  sequence of add / fork / append / free, replaying the returned writes and block
+  copies on a model pool (one token id per slot) lets every live sequence read back
+  exactly its own tokens at every position;
+* bookkeeping invariants: a block's count equals the number of block-table entries
+  naming it, free and referenced blocks partition the pool, a table has
+  ceil(L / B) entries;
+* all-or-nothing on an exhausted pool.
+"""
+import json
+import os
+import random
+
+GOLDEN = os.path.join(os.path.dirname(os.path.abspath(__file__)), "golden")
+
+
+def _golden(name):
+    with open(os.path.join(GOLDEN, name)) as f:
+        return json.load(f)
+
+
+def _order_first(first, num_blocks):
+    return list(first) + [b for b in range(num_blocks) if b not in first]
+
+
+def check_worked_example(make):
+    g = _golden("worked_example_slots.json")
+    B, bt = g["block_size"], g["block_table"]
+    bm = make(16, B, _order_first(bt, 16))
+    bm.add("req")
+    for step in g["steps"]:
+        slots, copies = bm.append("req", len(step["positions"]))
+        assert copies == [], step["what"]
+        assert slots == step["slots"], (step["what"], slots, step["slots"])
+        table = bm.table("req")
+        # #filled of the request's last block, as the block table records it
+        last = str(table[-1])
+        assert bm.filled("req") == step["filled_after"][last], step["what"]
+    assert bm.table("req") == bt
+
+
+def check_cow_example(make):
+    g = _golden("cow_example.json")
+    B = g["block_size"]
+    first = g["tables_before"]["A1"] + [c[1] for c in g["copies"]]
+    bm = make(16, B, _order_first(first, 16))
+    bm.add("A1")
+    bm.append("A1", g["prompt_len"])
+    bm.fork("A1", "A2")
+    assert bm.table("A1") == g["tables_before"]["A1"] and bm.table("A2") == g["tables_before"]["A2"]
+    for b, c in g["refcount_before"].items():
+        assert bm.refcount(int(b)) == c, ("before", b)
+    all_copies = []
+    for wr in g["writes"]:
+        slots, copies = bm.append(wr["sample"], 1)
+        assert slots == [wr["slot"]], (wr, slots)
+        all_copies += [list(c) for c in copies]
+    assert all_copies == g["copies"], all_copies
+    for name, t in g["tables_after"].items():
+        assert bm.table(name) == t, name
+    for b, c in g["refcount_after"].items():
+        assert bm.refcount(int(b)) == c, ("after", b)
+
+
+def _invariants(bm, model, num_blocks, B):
+    refs = [0] * num_blocks
+    for s in model:
+        t = bm.table(s)
+        assert len(t) == -(-len(model[s]) // B), ("table length", s)
+        for b in t:
+            refs[b] += 1
+    for b in range(num_blocks):
+        assert bm.refcount(b) == refs[b], ("refcount", b, bm.refcount(b), refs[b])
+    used = sum(1 for r in refs if r > 0)
+    assert bm.num_free() + used == num_blocks, ("free + used", bm.num_free(), used)
+
+
+def random_ops(seed, n_ops=300):
+    """Seeded operation list: ("add", s), ("fork", parent, child), ("append", [(s, n)]),
+    ("free", s), over at most 12 live sequences."""
+    rng = random.Random(seed)
+    ops, live, nxt = [], [], 0
+    for _ in range(n_ops):
+        r = rng.random()
+        if not live or (r < 0.15 and len(live) < 12):
+            ops.append(("add", nxt)); live.append(nxt); nxt += 1
+        elif r < 0.30 and len(live) < 12:
+            p = rng.choice(live)
+            ops.append(("fork", p, nxt)); live.append(nxt); nxt += 1
+        elif r < 0.40 and len(live) > 1:
+            s = rng.choice(live)
+            ops.append(("free", s)); live.remove(s)
+        else:
+            k = rng.randint(1, len(live))
+            batch = rng.sample(live, k)
+            ops.append(("append", [(s, rng.choice([1, 1, 1, 2, 3, 5, 9, 17])) for s in batch]))
+    return ops
+
+
+def run_ops(bm, ops, num_blocks, B, log=None):
+    """Replays ops on bm and on a model pool; checks every read-back and invariant.
+    Appends that the pool cannot hold must raise and change nothing."""
+    pool = [None] * (num_blocks * B)       # token id held by each slot
+    model = {}                              # sequence -> its token ids by position
+    tok = 0
+    for op in ops:
+        if op[0] == "add":
+            bm.add(op[1]); model[op[1]] = []
+        elif op[0] == "fork":
+            bm.fork(op[1], op[2]); model[op[2]] = list(model[op[1]])
+        elif op[0] == "free":
+            bm.free_seq(op[1]); del model[op[1]]
+        else:
+            seqs = [s for s, _ in op[1]]
+            ns = [n for _, n in op[1]]
+            before = {s: bm.table(s) for s in model}, bm.num_free()
+            try:
+                slots, copies = bm.append_batch(seqs, ns)
+            except Exception as e:   # pool exhausted: nothing may have changed
+                if "block" not in str(e).lower() and "space" not in str(e).lower():
+                    raise
+                assert ({s: bm.table(s) for s in model}, bm.num_free()) == before, "not atomic"
+                if log is not None:
+                    log.append(("full",))
+                continue
+            for src, dst in copies:             # copies happen before the writes
+                pool[dst * B:(dst + 1) * B] = pool[src * B:(src + 1) * B]
+            k = 0
+            for s, n in zip(seqs, ns):
+                for _ in range(n):
+                    pool[slots[k]] = tok
+                    model[s].append(tok)
+                    tok += 1; k += 1
+            assert k == len(slots)
+            if log is not None:
+                log.append((tuple(slots), tuple(map(tuple, copies))))
+        for s, toks in model.items():
+            t = bm.table(s)
+            for p, want in enumerate(toks):
+                got = pool[t[p // B] * B + p % B]
+                assert got == want, ("read-back", s, p, got, want)
+        _invariants(bm, model, num_blocks, B)
+    return model
+
+
+def check_random_histories(make):
+    for seed, (nb, B) in enumerate([(64, 4), (40, 16), (200, 1), (24, 8)]):
+        run_ops(make(nb, B, None), random_ops(seed), nb, B)
+
+
+def check_exhaustion_is_atomic(make):
+    bm = make(4, 4, None)
+    bm.add(0); bm.add(1)
+    bm.append(0, 6)                          # blocks 0, 1
+    bm.fork(0, 2)
+    failed = False
+    try:
+        bm.append_batch([1, 2], [9, 1])      # 3 new blocks + 1 copy > 2 free
+    except Exception:
+        failed = True
+    assert failed, "an append beyond the pool must fail"
+    assert bm.table(1) == [] and bm.table(2) == [0, 1] and bm.num_free() == 2
+    slots, copies = bm.append(2, 1)          # one copy of the shared partial block
+    assert copies == [(1, 2)] and slots == [2 * 4 + 2]
+
+
+ALL_CHECKS = [check_worked_example, check_cow_example, check_random_histories,
+              check_exhaustion_is_atomic]
