@@ -429,8 +429,51 @@ def run_gpu(args, w, cfg_name, rank, local, world):
         "bytes": {"kv": kv_b, "q": q_b, "o_write": o_b}, "flops": flops,
     }
     if rank == 0:
+        line["block_manager"] = block_manager_host(w)
         line["cpu_baseline"] = cpu_baseline(args, w)
         print(json.dumps(line), flush=True)
+
+
+def block_manager_host(w, steps=32):
+    """Host cost of the KV block manager (pa_bm_*) at this workload's scale: the
+    sequences' histories are appended once, then each timed step appends one token to
+    every sequence (slots and the copy-on-write decision) and exports all block-table
+    rows and context lengths, as a decode step of a serving loop would."""
+    import ctypes as C
+    import numpy as np
+    import paged_kv_cache_02_gb300 as pa
+    nb, B = int(w.k_pool.shape[0]), int(w.block_size)
+    N = len(w.context_lens)
+    L = np.asarray(w.context_lens, np.int64)
+    hist = np.maximum(L - np.asarray(w.query_lens, np.int64), 0).astype(np.int32)
+    spare = nb - int(sum(-(-int(x) // B) for x in hist))
+    steps = max(1, min(steps, (spare // max(1, N)) * B // 2))
+    mb = int(max(-(-(int(x) + steps) // B) for x in hist)) + 1
+    bm = pa.BlockManager(nb, B)
+    ids = np.arange(N, dtype=np.int64)
+    for s in range(N):
+        bm.add(s)
+    bm.append_batch(ids.tolist(), hist.tolist())
+    lib = pa.library()
+    ones = np.ones(N, np.int32)
+    slots = np.zeros(N, np.int64)
+    src = np.zeros(N, np.int32)
+    dst = np.zeros(N, np.int32)
+    bt = np.zeros((N, mb), np.int32)
+    cl = np.zeros(N, np.int32)
+    n_cow = C.c_int32(0)
+    t0 = time.perf_counter()
+    for _ in range(steps):
+        st = lib.pa_bm_append(bm._h, ids.ctypes.data, ones.ctypes.data, N, slots.ctypes.data,
+                              src.ctypes.data, dst.ctypes.data, C.byref(n_cow))
+        st |= lib.pa_bm_tables(bm._h, ids.ctypes.data, N, mb, bt.ctypes.data, cl.ctypes.data)
+        if st:
+            return {"error": int(st)}
+    dt = time.perf_counter() - t0
+    bm.close()
+    return {"us_per_step": dt / steps * 1e6, "seqs": N, "steps": steps,
+            "includes": "one token appended to every sequence (slots, copy-on-write decision) "
+                        "and every block-table row and context length exported, host only"}
 
 
 def cpu_baseline(args, w):

@@ -60,7 +60,8 @@ typedef enum {
   PA_ERR_RANGE = 3,        /* a block id, slot or length outside its range */
   PA_ERR_UNSUPPORTED = 4,  /* valid but not built: head dim, alignment, dtype, device */
   PA_ERR_CUDA = 5,         /* a CUDA runtime call failed */
-  PA_ERR_TIMEOUT = 6       /* a bounded device wait ran out */
+  PA_ERR_TIMEOUT = 6,      /* a bounded device wait ran out */
+  PA_ERR_NO_SPACE = 7      /* the block manager's pool has too few free blocks */
 } pa_status;
 
 typedef enum { PA_F32 = 0, PA_BF16 = 1 } pa_dtype;
@@ -266,6 +267,81 @@ pa_status pa_attention_static(pa_plan_t plan, void* d_out, pa_dtype out_dtype, c
                               const int32_t* d_block_table, const int32_t* d_context_lens,
                               const int32_t* d_query_lens, int32_t num_blocks, float scale,
                               void* stream);
+
+/* ---------------------------------------------------------------------------
+ * Host KV block manager: the physical block allocator, reference counts,
+ * fork / append / free and the copy-on-write decision, in host memory only.
+ *
+ * Follows the vLLM post (devpress), "1. overall architecture" (a request is a
+ * list of logical blocks filled left to right; the block table maps them to
+ * physical blocks of a pre-cut pool and records how full the last one is; a
+ * new physical block is taken only when the last logical block is full; a
+ * finished request's blocks are freed) and "2.1 parallel sampling" (a physical
+ * block carries a reference count; a request about to write into a block
+ * whose count is above one gets a newly taken block into which the shared
+ * block is copied, and the shared count drops by one, so the last holder
+ * writes in place); the vLLM-SOSP23 note, "core method" (fork / append / free).
+ * Pensieve's sub-requests over one context are forks whose block-table rows
+ * list the same physical blocks.
+ *
+ * The manager decides; the caller moves data: the slots an append returns are
+ * the slot_mapping of pa_write_kv, its copy pairs are the input of
+ * pa_copy_blocks (run before the write), and pa_bm_tables gives the
+ * block_table and context_lens rows of pa_plan_create / pa_attention.
+ *
+ * Free pool: blocks are handed out first in, first out, initially in
+ * h_free_order (host, num_blocks distinct ids; NULL = 0, 1, 2, ...); a freed
+ * block joins the back of the pool. Sequence ids are caller-chosen int64.
+ * Errors: PA_ERR_INVALID_ARG for a null handle or pointer, an unknown or
+ * duplicate sequence id, a negative count; PA_ERR_NO_SPACE when an append
+ * needs more free blocks than the pool holds -- the manager is then unchanged.
+ * A manager is not thread-safe: use one per thread or lock around calls.
+ * --------------------------------------------------------------------------- */
+typedef struct pa_bm_s* pa_bm_t;
+
+/* A pool of num_blocks blocks of block_size tokens, all free. */
+pa_status pa_bm_create(int32_t num_blocks, int32_t block_size, const int32_t* h_free_order,
+                       pa_bm_t* out);
+pa_status pa_bm_destroy(pa_bm_t bm);
+
+/* A new request holding no tokens. */
+pa_status pa_bm_add(pa_bm_t bm, int64_t seq);
+
+/* A new request `child` sharing every block of `parent` (each count + 1). */
+pa_status pa_bm_fork(pa_bm_t bm, int64_t parent, int64_t child);
+
+/* A finished request: each of its blocks loses one reference; blocks left with
+ * none return to the free pool, in table order. */
+pa_status pa_bm_free(pa_bm_t bm, int64_t seq);
+
+/* One step's new tokens: h_counts[i] tokens for request h_seqs[i] (each listed
+ * at most once), at positions L_i .. L_i + h_counts[i] - 1, in the listed order.
+ * Writes the slot of every new token to h_slots (int64, sum of counts, request
+ * by request, block * block_size + offset) and the copies the write needs
+ * first to h_cow_src / h_cow_dst (int32, room for n_seqs pairs; *n_cow pairs
+ * written; at most one per request: only a partially filled last block can be
+ * shared). All host pointers. All-or-nothing: PA_ERR_NO_SPACE leaves every
+ * table and count as it was. */
+pa_status pa_bm_append(pa_bm_t bm, const int64_t* h_seqs, const int32_t* h_counts,
+                       int32_t n_seqs, int64_t* h_slots, int32_t* h_cow_src,
+                       int32_t* h_cow_dst, int32_t* n_cow);
+
+/* Block-table rows and context lengths of the listed requests, for the
+ * attention calls: h_block_table [n_seqs, max_blocks] int32 padded with -1
+ * (NULL to skip; PA_ERR_SHAPE if a request holds more than max_blocks
+ * blocks), h_context_lens [n_seqs] int32 (NULL to skip). Host pointers. */
+pa_status pa_bm_tables(pa_bm_t bm, const int64_t* h_seqs, int32_t n_seqs, int32_t max_blocks,
+                       int32_t* h_block_table, int32_t* h_context_lens);
+
+/* Tokens held and blocks listed by one request (either pointer may be NULL);
+ * #filled of its last block is len - block_size * (n_blocks - 1). */
+pa_status pa_bm_seq_info(pa_bm_t bm, int64_t seq, int64_t* len, int32_t* n_blocks);
+
+/* Reference count of one physical block (PA_ERR_RANGE outside the pool). */
+pa_status pa_bm_refcount(pa_bm_t bm, int32_t block, int32_t* count);
+
+/* Blocks in the free pool. */
+pa_status pa_bm_num_free(pa_bm_t bm, int32_t* n_free);
 
 #ifdef __cplusplus
 }

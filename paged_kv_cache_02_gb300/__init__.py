@@ -4,12 +4,13 @@ The computation lives in ``libpa.so`` (hand-written CUDA kernels behind the C
 ABI of ``include/pa.h``); this package is its thin Python binding. See
 ``_binding`` for the functions, which carry the C entry points' names.
 """
-from ._binding import (DEVERR, LIB_PATH, STATIC_WORKSPACE_BYTES, PagedAttentionError, Plan,
-                       library, pa_attention, pa_attention_planned, pa_attention_static,
+from ._binding import (DEVERR, LIB_PATH, STATIC_WORKSPACE_BYTES, BlockManager, OutOfBlocks,
+                       PagedAttentionError, Plan, library, pa_attention, pa_attention_planned, pa_attention_static,
                        pa_copy_blocks, pa_get_device_error, pa_plan_create, pa_plan_upload,
                        pa_slot_mapping, pa_write_kv, version)
 
-__all__ = ["DEVERR", "LIB_PATH", "STATIC_WORKSPACE_BYTES", "PagedAttentionError", "Plan",
+__all__ = ["DEVERR", "LIB_PATH", "STATIC_WORKSPACE_BYTES", "BlockManager", "OutOfBlocks",
+           "PagedAttentionError", "Plan",
            "library", "pa_attention", "pa_attention_planned", "pa_attention_static",
            "pa_copy_blocks", "pa_get_device_error", "pa_plan_create", "pa_plan_upload",
            "pa_slot_mapping", "pa_write_kv", "version"]

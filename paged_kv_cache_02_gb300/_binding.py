@@ -71,10 +71,22 @@ def _lib() -> C.CDLL:
         lib.pa_plan_upload.argtypes = [_P, _P, C.c_size_t, _P]
         lib.pa_attention_planned.argtypes = [_P, _P, C.c_int, _P, _P, _P, _P, _P, _P, _I32,
                                              C.c_float, _P, C.c_size_t, _P]
+        lib.pa_bm_create.argtypes = [_I32, _I32, _P, C.POINTER(_P)]
+        lib.pa_bm_destroy.argtypes = [_P]
+        lib.pa_bm_add.argtypes = [_P, _I64]
+        lib.pa_bm_fork.argtypes = [_P, _I64, _I64]
+        lib.pa_bm_free.argtypes = [_P, _I64]
+        lib.pa_bm_append.argtypes = [_P, _P, _P, _I32, _P, _P, _P, C.POINTER(_I32)]
+        lib.pa_bm_tables.argtypes = [_P, _P, _I32, _I32, _P, _P]
+        lib.pa_bm_seq_info.argtypes = [_P, _I64, C.POINTER(_I64), C.POINTER(_I32)]
+        lib.pa_bm_refcount.argtypes = [_P, _I32, C.POINTER(_I32)]
+        lib.pa_bm_num_free.argtypes = [_P, C.POINTER(_I32)]
         for f in ("pa_get_device_error", "pa_slot_mapping", "pa_write_kv", "pa_copy_blocks",
                   "pa_plan_create", "pa_plan_destroy", "pa_plan_get_stats", "pa_plan_export",
                   "pa_attention", "pa_attention_static", "pa_plan_upload",
-                  "pa_attention_planned"):
+                  "pa_attention_planned", "pa_bm_create", "pa_bm_destroy", "pa_bm_add",
+                  "pa_bm_fork", "pa_bm_free", "pa_bm_append", "pa_bm_tables",
+                  "pa_bm_seq_info", "pa_bm_refcount", "pa_bm_num_free"):
             getattr(lib, f).restype = C.c_int
         _LIB = lib
     return _LIB
@@ -314,3 +326,128 @@ def pa_attention_static(plan: Plan, q: torch.Tensor, k_pool: torch.Tensor, v_poo
                                       float(scale), _stream(q)),
            "pa_attention_static")
     return out
+
+
+PA_ERR_NO_SPACE = 7
+
+
+class OutOfBlocks(PagedAttentionError):
+    """pa_bm_append found too few free blocks; the manager is unchanged."""
+
+
+class BlockManager:
+    """Host KV block manager (pa_bm_*): allocator, reference counts, fork / append / free
+    and the copy-on-write decision. Sequence ids may be any hashable; non-integer ids are
+    mapped to int64 here. Host-only: no GPU is touched."""
+
+    def __init__(self, num_blocks: int, block_size: int, free_order=None):
+        import numpy as np
+        self._h = None
+        order = None
+        if free_order is not None:
+            order = np.ascontiguousarray(np.asarray(free_order, dtype=np.int32))
+            if order.shape != (num_blocks,):
+                raise ValueError("free_order must list num_blocks block ids")
+        h = C.c_void_p()
+        _check(_lib().pa_bm_create(num_blocks, block_size,
+                                   None if order is None else order.ctypes.data, C.byref(h)),
+               "pa_bm_create")
+        self._h = h
+        self.num_blocks, self.block_size = num_blocks, block_size
+        self._ids = {}
+
+    def _id(self, seq, new=False) -> int:
+        if isinstance(seq, (int,)) and not isinstance(seq, bool):
+            return int(seq)
+        if seq not in self._ids:
+            if not new:
+                raise KeyError(f"unknown sequence {seq!r}")
+            self._ids[seq] = -(len(self._ids) + 1) - (1 << 62)
+        return self._ids[seq]
+
+    def _call(self, what, *args):
+        st = getattr(_lib(), what)(self._h, *args)
+        if st == PA_ERR_NO_SPACE:
+            raise OutOfBlocks(st, what)
+        if st == 1 and what != "pa_bm_create":
+            raise KeyError(f"{what}: unknown or duplicate sequence, or a bad count")
+        _check(st, what)
+
+    def add(self, seq) -> None:
+        self._call("pa_bm_add", self._id(seq, new=True))
+
+    def fork(self, parent, child) -> None:
+        self._call("pa_bm_fork", self._id(parent), self._id(child, new=True))
+
+    def free_seq(self, seq) -> None:
+        self._call("pa_bm_free", self._id(seq))
+
+    def append_batch(self, seqs, counts):
+        """Slots of the new tokens (list, request by request) and the (src, dst) block
+        copies to run first (list of tuples)."""
+        import numpy as np
+        ids = np.ascontiguousarray(np.array([self._id(s) for s in seqs], dtype=np.int64))
+        ns = np.ascontiguousarray(np.asarray(counts, dtype=np.int32))
+        if ids.shape != ns.shape:
+            raise ValueError("one count per sequence")
+        if (ns < 0).any():
+            raise ValueError("negative token count")
+        slots = np.zeros(max(1, int(ns.astype(np.int64).sum())), dtype=np.int64)
+        src = np.zeros(max(1, len(ids)), dtype=np.int32)
+        dst = np.zeros(max(1, len(ids)), dtype=np.int32)
+        n_cow = C.c_int32(0)
+        if len(set(ids.tolist())) != len(ids):
+            raise ValueError("a sequence appears twice in one step")
+        self._call("pa_bm_append", ids.ctypes.data, ns.ctypes.data, len(ids), slots.ctypes.data,
+                   src.ctypes.data, dst.ctypes.data, C.byref(n_cow))
+        k = n_cow.value
+        return (slots[:int(ns.astype(np.int64).sum())].tolist(),
+                list(zip(src[:k].tolist(), dst[:k].tolist())))
+
+    def append(self, seq, n: int):
+        return self.append_batch([seq], [n])
+
+    def tables(self, seqs, max_blocks: int):
+        """(block_table [n, max_blocks] int32 padded with -1, context_lens [n] int32)."""
+        import numpy as np
+        ids = np.ascontiguousarray(np.array([self._id(s) for s in seqs], dtype=np.int64))
+        bt = np.zeros((len(ids), max_blocks), dtype=np.int32)
+        cl = np.zeros(len(ids), dtype=np.int32)
+        self._call("pa_bm_tables", ids.ctypes.data, len(ids), max_blocks, bt.ctypes.data,
+                   cl.ctypes.data)
+        return bt, cl
+
+    def seq_info(self, seq):
+        ln, nb = C.c_int64(0), C.c_int32(0)
+        self._call("pa_bm_seq_info", self._id(seq), C.byref(ln), C.byref(nb))
+        return ln.value, nb.value
+
+    def table(self, seq):
+        _, nb = self.seq_info(seq)
+        bt, _ = self.tables([seq], nb)
+        return bt[0].tolist()
+
+    def filled(self, seq) -> int:
+        ln, nb = self.seq_info(seq)
+        return 0 if ln == 0 else ln - self.block_size * (nb - 1)
+
+    def refcount(self, block: int) -> int:
+        c = C.c_int32(0)
+        self._call("pa_bm_refcount", int(block), C.byref(c))
+        return c.value
+
+    def num_free(self) -> int:
+        c = C.c_int32(0)
+        self._call("pa_bm_num_free", C.byref(c))
+        return c.value
+
+    def close(self):
+        if self._h is not None and _LIB is not None:
+            _LIB.pa_bm_destroy(self._h)
+        self._h = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass

@@ -12,7 +12,8 @@ HERE = os.path.dirname(os.path.abspath(__file__))
 CSRC = os.path.join(HERE, "csrc")
 BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "libpa.so")
-SOURCES = ["pa_api.cu", "pa_kv.cu", "pa_dec.cu", "pa_tc.cu", "pa_tc2.cu", "pa_tcd.cu"]
+SOURCES = ["pa_api.cu", "pa_kv.cu", "pa_dec.cu", "pa_tc.cu", "pa_tc2.cu", "pa_tcd.cu",
+           "pa_bm.cpp"]
 HEADERS = ["pa_internal.h", "pa_ptx.cuh", "pa_tc.cuh", os.path.join("..", "..", "include", "pa.h")]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "-Xcompiler", "-Wall",
@@ -41,7 +42,7 @@ def build(force: bool = False, verbose: bool = False) -> str:
     cc = nvcc()
 
     def compile_one(src):
-        obj = os.path.join(BUILD, src.replace(".cu", ".o"))
+        obj = os.path.join(BUILD, os.path.splitext(src)[0] + ".o")
         cmd = [cc, *ARCH, *FLAGS, "-c", os.path.join(CSRC, src), "-o", obj]
         if verbose:
             cmd.insert(1, "-Xptxas=-v")

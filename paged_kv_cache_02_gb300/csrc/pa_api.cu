@@ -253,6 +253,7 @@ const char* pa_status_string(pa_status s) {
     case PA_ERR_UNSUPPORTED: return "unsupported configuration";
     case PA_ERR_CUDA: return "CUDA runtime error";
     case PA_ERR_TIMEOUT: return "bounded device wait ran out";
+    case PA_ERR_NO_SPACE: return "too few free blocks in the pool";
   }
   return "unknown status";
 }

@@ -35,7 +35,8 @@ def test_header_declares_the_boundary():
     names = declared_entry_points()
     for must in ("pa_write_kv", "pa_copy_blocks", "pa_attention", "pa_plan_create",
                  "pa_plan_destroy", "pa_status_string", "pa_slot_mapping", "pa_plan_upload",
-                 "pa_attention_planned"):
+                 "pa_attention_planned", "pa_bm_create", "pa_bm_append", "pa_bm_fork",
+                 "pa_bm_free", "pa_bm_tables"):
         assert must in names, names
 
 
@@ -47,8 +48,8 @@ def test_library_exports_every_declared_symbol(pa):
 
 def test_status_strings_and_version(pa):
     lib = pa.library()
-    for s in range(7):
-        assert lib.pa_status_string(s)
+    for s in range(8):
+        assert lib.pa_status_string(s) != b"unknown status"
     assert lib.pa_status_string(99) == b"unknown status"
     assert "sm_103a" in pa.version()
 
