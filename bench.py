@@ -429,9 +429,51 @@ def run_gpu(args, w, cfg_name, rank, local, world):
         "bytes": {"kv": kv_b, "q": q_b, "o_write": o_b}, "flops": flops,
     }
     if rank == 0:
+        line["swap"] = swap_measure(w, dev)
         line["block_manager"] = block_manager_host(w)
         line["cpu_baseline"] = cpu_baseline(args, w)
         print(json.dumps(line), flush=True)
+
+
+def swap_measure(w, dev, reps=20):
+    """pa_swap_blocks bandwidth at this workload's block shape: n scattered blocks of
+    both pools out to page-locked host pools and back in, CUDA-event timed, beside one
+    contiguous copy-engine transfer of the same bytes (pinned host -> device)."""
+    import torch
+    import paged_kv_cache_02_gb300 as pa
+    nb = int(w.k_pool.shape[0])
+    n = max(1, min(512, nb // 2))
+    shape = tuple(w.k_pool.shape[1:])
+    kh = torch.empty((n,) + shape, dtype=torch.bfloat16).pin_memory()
+    vh = torch.empty((n,) + shape, dtype=torch.bfloat16).pin_memory()
+    g = torch.Generator().manual_seed(7)
+    src = torch.randperm(nb, generator=g)[:n].to(torch.int32).to(dev)
+    dst = torch.randperm(n, generator=g).to(torch.int32).to(dev)
+    nbytes = 2 * n * kh[0].numel() * 2
+    flat = torch.empty(nbytes // 2, dtype=torch.bfloat16).pin_memory()
+    flat_d = torch.empty(nbytes // 2, dtype=torch.bfloat16, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def timed(fn):
+        for _ in range(3):
+            fn()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        torch.cuda.synchronize(dev)
+        a.record(stream)
+        for _ in range(reps):
+            fn()
+        b.record(stream)
+        b.synchronize()
+        return a.elapsed_time(b) / reps / 1e3
+
+    t_out = timed(lambda: pa.pa_swap_blocks(w.k_pool, w.v_pool, kh, vh, src, dst, "out"))
+    t_in = timed(lambda: pa.pa_swap_blocks(w.k_pool, w.v_pool, kh, vh, dst, src, "in"))
+    t_ce = timed(lambda: flat_d.copy_(flat, non_blocking=True))
+    err = pa.pa_get_device_error()
+    return {"blocks": n, "bytes_per_call": nbytes, "out_gbs": nbytes / t_out / 1e9,
+            "in_gbs": nbytes / t_in / 1e9, "copy_engine_h2d_gbs": nbytes / t_ce / 1e9,
+            "device_error": err,
+            "note": "scattered block ids both sides; copy engine = one contiguous pinned copy"}
 
 
 def block_manager_host(w, steps=32):

@@ -268,6 +268,30 @@ pa_status pa_attention_static(pa_plan_t plan, void* d_out, pa_dtype out_dtype, c
                               const int32_t* d_query_lens, int32_t num_blocks, float scale,
                               void* stream);
 
+/* Block swaps between the device pools and host pools of the same layout
+ * (vLLM post, "3. scheduling and preemption": evicted blocks are copied to CPU
+ * memory and copied back when their request resumes; Pensieve summary,
+ * ahead-of-time swapping of KV tokens to the CPU cache and their restore).
+ * Pair i moves one whole block of both pools:
+ *   PA_SWAP_OUT: device block d_src[i] -> host block d_dst[i]
+ *   PA_SWAP_IN:  host block d_src[i]   -> device block d_dst[i]
+ * d_k_pool, d_v_pool [num_blocks, block_size, Hkv, D] bf16, device;
+ * h_k_pool, h_v_pool [num_host_blocks, block_size, Hkv, D] bf16, host memory
+ * that CUDA has page-locked and mapped (cudaHostAlloc, or cudaHostRegister with
+ * mapping) -- the kernel reads or writes it directly over the CPU-GPU link, so
+ * one launch moves any number of scattered blocks; anything else is
+ * PA_ERR_INVALID_ARG. d_src, d_dst int32 [n_pairs], device; destinations must
+ * be distinct. Asynchronous on `stream`: the host pool must stay allocated
+ * until the stream has passed the call. Block ids out of range are skipped
+ * and recorded as PA_DEVERR_BLOCK_RANGE. All pools 16-byte aligned, D % 8 == 0
+ * (else PA_ERR_UNSUPPORTED). */
+#define PA_SWAP_OUT 0
+#define PA_SWAP_IN 1
+pa_status pa_swap_blocks(void* d_k_pool, void* d_v_pool, int32_t num_blocks, void* h_k_pool,
+                         void* h_v_pool, int32_t num_host_blocks, const int32_t* d_src,
+                         const int32_t* d_dst, int32_t n_pairs, int32_t block_size, int32_t Hkv,
+                         int32_t D, int32_t direction, void* stream);
+
 /* ---------------------------------------------------------------------------
  * Host KV block manager: the physical block allocator, reference counts,
  * fork / append / free and the copy-on-write decision, in host memory only.

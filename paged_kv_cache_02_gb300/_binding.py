@@ -71,6 +71,8 @@ def _lib() -> C.CDLL:
         lib.pa_plan_upload.argtypes = [_P, _P, C.c_size_t, _P]
         lib.pa_attention_planned.argtypes = [_P, _P, C.c_int, _P, _P, _P, _P, _P, _P, _I32,
                                              C.c_float, _P, C.c_size_t, _P]
+        lib.pa_swap_blocks.argtypes = [_P, _P, _I32, _P, _P, _I32, _P, _P, _I32, _I32, _I32,
+                                       _I32, _I32, _P]
         lib.pa_bm_create.argtypes = [_I32, _I32, _P, C.POINTER(_P)]
         lib.pa_bm_destroy.argtypes = [_P]
         lib.pa_bm_add.argtypes = [_P, _I64]
@@ -84,7 +86,7 @@ def _lib() -> C.CDLL:
         for f in ("pa_get_device_error", "pa_slot_mapping", "pa_write_kv", "pa_copy_blocks",
                   "pa_plan_create", "pa_plan_destroy", "pa_plan_get_stats", "pa_plan_export",
                   "pa_attention", "pa_attention_static", "pa_plan_upload",
-                  "pa_attention_planned", "pa_bm_create", "pa_bm_destroy", "pa_bm_add",
+                  "pa_attention_planned", "pa_swap_blocks", "pa_bm_create", "pa_bm_destroy", "pa_bm_add",
                   "pa_bm_fork", "pa_bm_free", "pa_bm_append", "pa_bm_tables",
                   "pa_bm_seq_info", "pa_bm_refcount", "pa_bm_num_free"):
             getattr(lib, f).restype = C.c_int
@@ -171,6 +173,42 @@ def pa_copy_blocks(k_pool: torch.Tensor, v_pool: torch.Tensor, src: torch.Tensor
                                  _dev(v_pool, torch.bfloat16, "v_pool", 4),
                                  _dev(src, torch.int32, "src", 1), _dev(dst, torch.int32, "dst", 1),
                                  src.numel(), nb, B, Hkv, D, _stream(k_pool)), "pa_copy_blocks")
+
+
+PA_SWAP_OUT, PA_SWAP_IN = 0, 1
+
+
+def _host(t: torch.Tensor, name: str) -> int:
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch.Tensor")
+    if t.is_cuda:
+        raise ValueError(f"{name} must live in host memory")
+    if t.dtype != torch.bfloat16 or t.dim() != 4 or not t.is_contiguous():
+        raise ValueError(f"{name} must be a contiguous 4-D bfloat16 tensor")
+    return t.data_ptr()
+
+
+def pa_swap_blocks(k_pool: torch.Tensor, v_pool: torch.Tensor, k_host: torch.Tensor,
+                   v_host: torch.Tensor, src: torch.Tensor, dst: torch.Tensor,
+                   direction: str) -> None:
+    """Whole blocks between the device pools and page-locked host pools of the same
+    layout: direction "out" copies device block src[i] to host block dst[i], "in" host
+    block src[i] to device block dst[i]. The host pools must be pinned
+    (``pin_memory=True``); src / dst are device int32."""
+    nb, B, Hkv, D = k_pool.shape
+    nhb = k_host.shape[0]
+    if tuple(k_host.shape[1:]) != (B, Hkv, D) or v_host.shape != k_host.shape:
+        raise ValueError("host pools must be [num_host_blocks, B, Hkv, D] like the device pools")
+    if v_pool.shape != k_pool.shape:
+        raise ValueError("k_pool and v_pool differ in shape")
+    if src.numel() != dst.numel():
+        raise ValueError("src and dst need the same length")
+    d = {"out": PA_SWAP_OUT, "in": PA_SWAP_IN}[direction]
+    _check(_lib().pa_swap_blocks(_dev(k_pool, torch.bfloat16, "k_pool", 4),
+                                 _dev(v_pool, torch.bfloat16, "v_pool", 4), nb,
+                                 _host(k_host, "k_host"), _host(v_host, "v_host"), nhb,
+                                 _dev(src, torch.int32, "src", 1), _dev(dst, torch.int32, "dst", 1),
+                                 src.numel(), B, Hkv, D, d, _stream(k_pool)), "pa_swap_blocks")
 
 
 class Plan:

@@ -328,6 +328,56 @@ pa_status pa_copy_blocks(void* d_k_pool, void* d_v_pool, const int32_t* d_src,
   return e == cudaSuccess ? PA_OK : PA_ERR_CUDA;
 }
 
+// Device view of `bytes` of page-locked host memory at h: both ends must lie in memory
+// that CUDA has mapped (cudaHostAlloc, or cudaHostRegister with mapping), contiguously.
+static bool host_device_view(void* h, int64_t bytes, void** d) {
+  cudaPointerAttributes a0, a1;
+  if (cudaPointerGetAttributes(&a0, h) != cudaSuccess ||
+      cudaPointerGetAttributes(&a1, static_cast<char*>(h) + (bytes - 1)) != cudaSuccess) {
+    cudaGetLastError();
+    return false;
+  }
+  if (a0.type != cudaMemoryTypeHost || a1.type != cudaMemoryTypeHost || !a0.devicePointer ||
+      !a1.devicePointer)
+    return false;
+  if (static_cast<char*>(a1.devicePointer) - static_cast<char*>(a0.devicePointer) != bytes - 1)
+    return false;
+  *d = a0.devicePointer;
+  return true;
+}
+
+pa_status pa_swap_blocks(void* d_k_pool, void* d_v_pool, int32_t num_blocks, void* h_k_pool,
+                         void* h_v_pool, int32_t num_host_blocks, const int32_t* d_src,
+                         const int32_t* d_dst, int32_t n_pairs, int32_t block_size, int32_t Hkv,
+                         int32_t D, int32_t direction, void* stream) {
+  if (n_pairs < 0 || num_blocks <= 0 || num_host_blocks <= 0 || block_size <= 0 || Hkv <= 0 ||
+      D <= 0 || (direction != PA_SWAP_OUT && direction != PA_SWAP_IN))
+    return PA_ERR_INVALID_ARG;
+  if (n_pairs == 0) return PA_OK;
+  if (!d_k_pool || !d_v_pool || !h_k_pool || !h_v_pool || !d_src || !d_dst)
+    return PA_ERR_INVALID_ARG;
+  if (D % 8) return PA_ERR_UNSUPPORTED;
+  for (const void* ptr : {(const void*)d_k_pool, (const void*)d_v_pool, (const void*)h_k_pool,
+                          (const void*)h_v_pool})
+    if (reinterpret_cast<uintptr_t>(ptr) % 16) return PA_ERR_UNSUPPORTED;
+  const int64_t block_bytes = (int64_t)block_size * Hkv * D * 2;
+  void* hk = nullptr;
+  void* hv = nullptr;
+  if (!host_device_view(h_k_pool, (int64_t)num_host_blocks * block_bytes, &hk) ||
+      !host_device_view(h_v_pool, (int64_t)num_host_blocks * block_bytes, &hv))
+    return PA_ERR_INVALID_ARG;
+  int* err = pa::device_error_word();
+  if (!err) return PA_ERR_CUDA;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  cudaError_t e =
+      direction == PA_SWAP_OUT
+          ? pa::launch_swap_blocks(d_k_pool, d_v_pool, hk, hv, d_src, d_dst, n_pairs,
+                                   num_blocks, num_host_blocks, block_bytes, err, s)
+          : pa::launch_swap_blocks(hk, hv, d_k_pool, d_v_pool, d_src, d_dst, n_pairs,
+                                   num_host_blocks, num_blocks, block_bytes, err, s);
+  return e == cudaSuccess ? PA_OK : PA_ERR_CUDA;
+}
+
 pa_status pa_plan_create(const int32_t* h_context_lens, const int32_t* h_query_lens,
                          int32_t num_seqs, int32_t Hq, int32_t Hkv, int32_t D,
                          int32_t block_size, int32_t max_blocks_per_seq,

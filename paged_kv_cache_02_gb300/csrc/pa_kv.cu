@@ -1,13 +1,17 @@
-// pa_kv.cu -- cache maintenance kernels: slot mapping, KV write, copy-on-write block copy.
+// pa_kv.cu -- cache maintenance kernels: slot mapping, KV write, copy-on-write block copy,
+// block swaps between the device pools and page-locked host pools.
 //
 // vLLM post (devpress), "1. overall architecture": token position p of a
 // sequence lives in slot block_table[p / B] * B + p % B of the pool, a pool row
 // being the Hkv * D values of one token. vLLM wiki note, "kernel layer": the
 // new tokens' K/V are scattered into their slots (fused reshape + block write)
 // and whole blocks are copied for copy-on-write (batched block copy; vLLM post,
-// "2.1 parallel sampling").
+// "2.1 parallel sampling"). Swapping (vLLM post, "3. scheduling and preemption":
+// evicted blocks are copied to CPU memory and back; Pensieve summary, ahead-of-time
+// swapping of KV tokens to the CPU cache and their restore) moves whole blocks between
+// the device pools and host pools of the same layout.
 //
-// All three are HBM-bound byte movers: 16-byte vector accesses, a grid sized to
+// All are bandwidth-bound byte movers: 16-byte vector accesses, a grid sized to
 // a multiple of the SM count, every index range-checked (a bad index is
 // skipped and recorded in the device error word, never dereferenced).
 #include <cuda_runtime.h>
@@ -123,6 +127,46 @@ __global__ void __launch_bounds__(kCopyThreads) copy_blocks_kernel(
   }
 }
 
+// Moves whole blocks from one pool to another (device <-> page-locked host memory,
+// the host side through its device mapping): vector i is 16-byte chunk
+// i % vec_per_block of pair i / vec_per_block; K and V move in the same thread.
+__global__ void __launch_bounds__(kCopyThreads) swap_blocks_kernel(
+    const uint4* __restrict__ k_from, const uint4* __restrict__ v_from, uint4* __restrict__ k_to,
+    uint4* __restrict__ v_to, const int32_t* __restrict__ src, const int32_t* __restrict__ dst,
+    int64_t n_vec, int64_t vec_per_block, int32_t n_from, int32_t n_to, int* err) {
+  const int64_t stride = (int64_t)gridDim.x * kCopyThreads;
+  for (int64_t base = blockIdx.x * (int64_t)kCopyThreads + threadIdx.x; base < n_vec;
+       base += stride * kCopyUnroll) {
+    uint4 kv[kCopyUnroll], vv[kCopyUnroll];
+    int64_t to[kCopyUnroll];
+#pragma unroll
+    for (int u = 0; u < kCopyUnroll; ++u) {
+      const int64_t i = base + u * stride;
+      to[u] = -1;
+      if (i < n_vec) {
+        const int64_t pair = i / vec_per_block;
+        const int64_t off = i - pair * vec_per_block;
+        const int32_t s = __ldg(src + pair), d = __ldg(dst + pair);
+        if (s < 0 || s >= n_from || d < 0 || d >= n_to) {
+          record_error(err, PA_DEVERR_BLOCK_RANGE);
+        } else {
+          to[u] = (int64_t)d * vec_per_block + off;
+          const int64_t from = (int64_t)s * vec_per_block + off;
+          kv[u] = __ldcs(k_from + from);
+          vv[u] = __ldcs(v_from + from);
+        }
+      }
+    }
+#pragma unroll
+    for (int u = 0; u < kCopyUnroll; ++u) {
+      if (to[u] >= 0) {
+        __stcs(k_to + to[u], kv[u]);
+        __stcs(v_to + to[u], vv[u]);
+      }
+    }
+  }
+}
+
 int copy_grid(int64_t n_vec) {
   static int sms = 0;
   if (sms == 0) {
@@ -172,6 +216,20 @@ cudaError_t launch_copy_blocks(void* k_pool, void* v_pool, const int32_t* src, c
   copy_blocks_kernel<<<copy_grid(n_vec), kCopyThreads, 0, s>>>(
       static_cast<uint4*>(k_pool), static_cast<uint4*>(v_pool), src, dst, n_vec, vec_per_block,
       num_blocks, err);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_swap_blocks(const void* k_from, const void* v_from, void* k_to, void* v_to,
+                               const int32_t* src, const int32_t* dst, int32_t n_pairs,
+                               int32_t n_from, int32_t n_to, int64_t block_bytes, int* err,
+                               cudaStream_t s) {
+  const int64_t vec_per_block = block_bytes / 16;
+  const int64_t n_vec = (int64_t)n_pairs * vec_per_block;
+  if (n_vec == 0) return cudaSuccess;
+  swap_blocks_kernel<<<copy_grid(n_vec), kCopyThreads, 0, s>>>(
+      static_cast<const uint4*>(k_from), static_cast<const uint4*>(v_from),
+      static_cast<uint4*>(k_to), static_cast<uint4*>(v_to), src, dst, n_vec, vec_per_block,
+      n_from, n_to, err);
   return cudaGetLastError();
 }
 

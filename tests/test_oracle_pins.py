@@ -104,3 +104,26 @@ def test_planted_mistake_is_caught(mutation):
             except (AssertionError, oracle.OracleError):
                 caught.append(check.__name__)
         assert caught, f"mutation {MUTANTS[mutation]} passed every pin"
+
+
+def test_swap_oracle_agrees_with_copy_blocks(orc):
+    """A swap from pool A to pool B is the oracle's copy_blocks (the C implementation)
+    on the stacked pool [B; A] with A's ids shifted; and a swap out then in restores."""
+    from oracle.swap import swap_blocks
+    rng = np.random.default_rng(5)
+    shape = (6, 4, 2, 8)
+    A_k, A_v = (rng.integers(0, 2**16, (9,) + shape[1:], dtype=np.uint16) for _ in range(2))
+    B_k, B_v = (rng.integers(0, 2**16, shape, dtype=np.uint16) for _ in range(2))
+    src, dst = np.array([8, 0, 3, 3], np.int32), np.array([5, 1, 0, 2], np.int32)
+    stk_k, stk_v = np.concatenate([B_k, A_k]), np.concatenate([B_v, A_v])
+    orc.copy_blocks(stk_k, stk_v, src + len(B_k), dst)
+    swap_blocks(A_k, A_v, B_k, B_v, src, dst)
+    assert np.array_equal(B_k, stk_k[:len(B_k)]) and np.array_equal(B_v, stk_v[:len(B_v)])
+    back_k, back_v = np.zeros_like(A_k), np.zeros_like(A_v)
+    swap_blocks(B_k, B_v, back_k, back_v, dst[:3], src[:3])
+    for s in src[:3]:
+        assert np.array_equal(back_k[s], A_k[s]) and np.array_equal(back_v[s], A_v[s])
+    with pytest.raises(ValueError):
+        swap_blocks(A_k, A_v, B_k, B_v, [0, 1], [2, 2])
+    with pytest.raises(ValueError):
+        swap_blocks(A_k, A_v, B_k, B_v, [9], [0])
