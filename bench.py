@@ -553,6 +553,10 @@ def main():
                     help="run only the prefill or decode sequences of a mixed batch (3, 4)")
     ap.add_argument("--max-seqs", type=int, default=None,
                     help="keep only the first N sequences (profiler captures of config 2)")
+    ap.add_argument("--block-size", type=int, default=None,
+                    help="block-size sweep: config 2 with another block size")
+    ap.add_argument("--contiguous", action="store_true",
+                    help="block-size sweep: config 2 with each sequence's blocks consecutive")
     args = ap.parse_args()
     args.warmup = max(3, args.warmup)
     args.config_key = f"cfg{args.config}"
@@ -570,7 +574,12 @@ def main():
 
     import torch
     torch.cuda.set_device(local)
-    w = workloads.make(cfg, device=f"cuda:{local}", max_seqs=args.max_seqs)
+    w = workloads.make(cfg, device=f"cuda:{local}", max_seqs=args.max_seqs,
+                       block_size=args.block_size, contiguous=args.contiguous)
+    if args.block_size is not None:
+        args.config_key += f"_B{args.block_size}"
+    if args.contiguous:
+        args.config_key += "_contiguous"
     if args.subset:
         w = w.subset(w.groups[f"{args.subset}_seqs"])
         args.config_key += f"_{args.subset}"

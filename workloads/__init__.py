@@ -217,10 +217,15 @@ def _cfg1(device):
     return _finish(CONFIG_NAMES[1], seed, 4, 4, 64, B, nb, L, ql, bt, seqs, pos, device)
 
 
-def _cfg2(device, max_seqs=None):
+def _cfg2(device, max_seqs=None, block_size=None, contiguous=False):
+    """Decode-only batch. ``block_size`` and ``contiguous`` give the block-size sweep's
+    variants of the same draw (same lengths and values): another block size, or each
+    sequence's blocks at consecutive physical ids instead of a seeded permutation."""
     seed = 1002
     g = torch.Generator().manual_seed(seed)
     N, B, H, D = 256, 16, 40, 128
+    if block_size is not None:
+        B = int(block_size)
     L = _randint(g, 128, 2048, N)
     if max_seqs is not None:
         N, L = min(N, max_seqs), L[:max_seqs]
@@ -228,8 +233,17 @@ def _cfg2(device, max_seqs=None):
     need = [_cdiv(int(l), B) for l in L]
     nb = int(math.ceil(1.2 * sum(need)))
     bt = _place(g, need, nb, max(need))
+    name = CONFIG_NAMES[2]
+    if block_size is not None and B != 16:
+        name = name.replace("B=16", f"B={B}")
+    if contiguous:
+        off = 0
+        for s, n in enumerate(need):
+            bt[s, :n] = np.arange(off, off + n, dtype=np.int32)
+            off += n
+        name += ", contiguous blocks"
     seqs, pos = _last_tokens(L, ql)
-    return _finish(CONFIG_NAMES[2], seed, H, H, D, B, nb, L, ql, bt, seqs, pos, device,
+    return _finish(name, seed, H, H, D, B, nb, L, ql, bt, seqs, pos, device,
                    q_scale=1.0 / math.sqrt(D))
 
 
@@ -376,16 +390,19 @@ def _cfg5(device, cow: bool):
                    cow=(np.array(src, np.int32), np.array(dst, np.int32)))
 
 
-def make(config, device="cpu", max_seqs=None) -> Workload:
+def make(config, device="cpu", max_seqs=None, block_size=None, contiguous=False) -> Workload:
     """Workload for config 1..5 or "5cow", values drawn on ``device``.
 
     ``max_seqs`` keeps only the first sequences of the decode-only batch (config 2): the
-    same draw, smaller, for profiler captures that must stay small.
+    same draw, smaller, for profiler captures that must stay small. ``block_size`` and
+    ``contiguous`` (config 2 only) give the block-size sweep's variants.
     """
+    if (block_size is not None or contiguous) and config not in (2, "2"):
+        raise ValueError("block_size / contiguous variants exist for config 2 only")
     if config in (1, "1"):
         return _cfg1(device)
     if config in (2, "2"):
-        return _cfg2(device, max_seqs)
+        return _cfg2(device, max_seqs, block_size, contiguous)
     if config in (3, "3"):
         return _cfg3(device)
     if config in (4, "4"):
