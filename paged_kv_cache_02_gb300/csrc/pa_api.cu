@@ -242,6 +242,15 @@ static pa_status note_upload(pa_plan_t p, cudaStream_t s) {
   return PA_OK;
 }
 
+namespace pa {
+// Whole blocks from pool (k_from, v_from) to pool (k_to, v_to), defined in pa_kv.cu:
+// either side may be the device mapping of page-locked host memory.
+cudaError_t launch_swap_blocks(const void* k_from, const void* v_from, void* k_to, void* v_to,
+                               const int32_t* src, const int32_t* dst, int32_t n_pairs,
+                               int32_t n_from, int32_t n_to, int64_t block_bytes, int* err,
+                               cudaStream_t s);
+}  // namespace pa
+
 extern "C" {
 
 const char* pa_status_string(pa_status s) {

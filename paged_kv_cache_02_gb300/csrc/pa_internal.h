@@ -88,12 +88,6 @@ cudaError_t launch_write_kv(const void* k_new, const void* v_new, const int64_t*
 cudaError_t launch_copy_blocks(void* k_pool, void* v_pool, const int32_t* src, const int32_t* dst,
                                int32_t n_pairs, int32_t num_blocks, int64_t block_bytes, int* err,
                                cudaStream_t s);
-// Whole blocks from pool (k_from, v_from) to pool (k_to, v_to): either side may be the
-// device mapping of page-locked host memory.
-cudaError_t launch_swap_blocks(const void* k_from, const void* v_from, void* k_to, void* v_to,
-                               const int32_t* src, const int32_t* dst, int32_t n_pairs,
-                               int32_t n_from, int32_t n_to, int64_t block_bytes, int* err,
-                               cudaStream_t s);
 cudaError_t launch_decode(const AttnArgs& a, const CUtensorMap& kmap, const CUtensorMap& vmap,
                           const Item* items, int32_t n_items, int D, int rows_max, int box_t,
                           int grid, cudaStream_t s);
