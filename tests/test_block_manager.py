@@ -168,3 +168,28 @@ def test_config5cow_copies_are_the_managers(pa, impl):
     pos = np.asarray(w.context_lens, np.int64) - 1
     want = [int(bt[i, pos[i] // B]) * B + int(pos[i] % B) for i in range(P * S)]
     assert slots == want
+
+
+@pytest.mark.parametrize("impl", ["oracle", "library"])
+def test_edge_cases(pa, impl):
+    make = oracle_factory() if impl == "oracle" else library_factory(pa)
+    bm = make(8, 4, None)
+    bm.add(0)
+    assert bm.append(0, 0) == ([], []) and bm.table(0) == [] and bm.filled(0) == 0
+    bm.fork(0, 1)                                  # fork of an empty request
+    s0, c0 = bm.append(0, 2)
+    s1, c1 = bm.append(1, 2)
+    assert c0 == c1 == [] and bm.table(0) != bm.table(1) and bm.num_free() == 6
+    bm.free_seq(1)
+    bm.add(1)                                      # an id can be reused after free
+    assert bm.table(1) == [] and bm.num_free() == 7
+    bm.append(0, 2)                                # fills block of 0 exactly (4 tokens)
+    bm.fork(0, 2)
+    s, c = bm.append(2, 1)                         # full shared block: new block, no copy
+    assert c == [] and len(bm.table(2)) == 2 and bm.table(2)[0] == bm.table(0)[0]
+    assert bm.refcount(bm.table(0)[0]) == 2
+    # block size 1: every token takes a block; forks never need a copy
+    one = make(6, 1, None)
+    one.add("x"); one.append("x", 3); one.fork("x", "y")
+    assert one.append_batch(["x", "y"], [1, 1])[1] == []
+    assert one.num_free() == 1
