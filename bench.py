@@ -550,7 +550,9 @@ def cpu_baseline(args, w):
             "k_new": u16(w.k_new), "v_new": u16(w.v_new)}
     n = os.cpu_count() or 1
     v, sample, _ = oracle_step_sample(w, orc, host, n, budget_s=args.cpu_budget)
-    return {"value": v, "unit": UNIT, "cores": n, "kind": "oracle", "sample": sample}
+    v1, sample1, _ = oracle_step_sample(w, orc, host, 1, budget_s=max(1.0, args.cpu_budget / 4))
+    return {"value": v, "unit": UNIT, "cores": n, "kind": "oracle", "sample": sample,
+            "one_core": {"value": v1, "unit": UNIT, "sample": sample1}}
 
 
 def main():
