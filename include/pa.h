@@ -319,6 +319,7 @@ pa_status pa_swap_blocks(void* d_k_pool, void* d_v_pool, int32_t num_blocks, voi
  * Errors: PA_ERR_INVALID_ARG for a null handle or pointer, an unknown or
  * duplicate sequence id, a negative count; PA_ERR_NO_SPACE when an append
  * needs more free blocks than the pool holds -- the manager is then unchanged.
+ * A request that is swapped out (below) may only be swapped in or freed.
  * A manager is not thread-safe: use one per thread or lock around calls.
  * --------------------------------------------------------------------------- */
 typedef struct pa_bm_s* pa_bm_t;
@@ -357,9 +358,34 @@ pa_status pa_bm_append(pa_bm_t bm, const int64_t* h_seqs, const int32_t* h_count
 pa_status pa_bm_tables(pa_bm_t bm, const int64_t* h_seqs, int32_t n_seqs, int32_t max_blocks,
                        int32_t* h_block_table, int32_t* h_context_lens);
 
-/* Tokens held and blocks listed by one request (either pointer may be NULL);
- * #filled of its last block is len - block_size * (n_blocks - 1). */
-pa_status pa_bm_seq_info(pa_bm_t bm, int64_t seq, int64_t* len, int32_t* n_blocks);
+/* Tokens held, blocks listed and residency (1: swapped out to the host pool) of
+ * one request (any pointer may be NULL); #filled of its last block is
+ * len - block_size * (n_blocks - 1). */
+pa_status pa_bm_seq_info(pa_bm_t bm, int64_t seq, int64_t* len, int32_t* n_blocks,
+                         int32_t* on_host);
+
+/* Swapping (vLLM post, "3. scheduling and preemption": eviction moves all of a
+ * request's blocks to CPU memory, managed by a CPU block allocator, and copies
+ * them back when the request resumes). pa_bm_set_host_pool gives the manager a
+ * host pool of num_host_blocks blocks (once; h_free_order as for the device
+ * pool). pa_bm_swap_out moves every listed request (each once, all on the
+ * device) to the host pool: each distinct device block they name gets one host
+ * block, so blocks they share stay shared; the (device block, host block) copies
+ * to make -- with pa_swap_blocks(PA_SWAP_OUT), before the freed device blocks
+ * are written again -- go to h_dev / h_host (room for `capacity` pairs;
+ * *n_pairs written), in the order the tables name the blocks. Device blocks
+ * left without references return to the free pool. pa_bm_swap_in is the
+ * reverse for requests on the host (copies with PA_SWAP_IN before they run).
+ * A swapped-out request may only be swapped in or freed; its table names host
+ * blocks. All-or-nothing: PA_ERR_NO_SPACE when the receiving pool has too few
+ * free blocks, PA_ERR_SHAPE when capacity is too small; nothing changes then. */
+pa_status pa_bm_set_host_pool(pa_bm_t bm, int32_t num_host_blocks, const int32_t* h_free_order);
+pa_status pa_bm_swap_out(pa_bm_t bm, const int64_t* h_seqs, int32_t n_seqs, int32_t* h_dev,
+                         int32_t* h_host, int32_t capacity, int32_t* n_pairs);
+pa_status pa_bm_swap_in(pa_bm_t bm, const int64_t* h_seqs, int32_t n_seqs, int32_t* h_host,
+                        int32_t* h_dev, int32_t capacity, int32_t* n_pairs);
+pa_status pa_bm_host_refcount(pa_bm_t bm, int32_t block, int32_t* count);
+pa_status pa_bm_host_num_free(pa_bm_t bm, int32_t* n_free);
 
 /* Reference count of one physical block (PA_ERR_RANGE outside the pool). */
 pa_status pa_bm_refcount(pa_bm_t bm, int32_t block, int32_t* count);

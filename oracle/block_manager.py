@@ -21,12 +21,20 @@ What it follows (sources are the web pages on the subject):
   then writes in place.
 * vLLM-SOSP23 note, "core method": fork / append / free are the primitives that
   parallel sampling, beam search and shared prefixes are built from.
+* vLLM post, "3. scheduling and preemption", swapping: eviction is all-or-nothing per
+  request (all of its blocks move together) to CPU memory, whose blocks a CPU block
+  allocator manages; when the request resumes its blocks are copied back. Here a
+  swap of several requests maps each distinct device block they name to one host
+  block (so blocks they share stay shared), returns the (from, to) copies, moves the
+  references from one pool to the other and frees blocks left without any.
 
 Readings where the pages are silent: the free pool hands out blocks first in, first
 out, in an order the caller may give (default 0, 1, 2, ...), and freed blocks join
 its back in table order; a request's append either completes or, when the pool has
 too few free blocks, changes nothing; positions are written in increasing order, so
-only a sequence's last (partially filled) block can need a copy.
+only a sequence's last (partially filled) block can need a copy. The host pool
+follows the same rules; a request swapped out can be swapped in or freed, nothing
+else; a swap takes blocks in the order the listed requests' tables name them.
 """
 from collections import deque
 
@@ -41,22 +49,38 @@ class BlockManager:
     ``mutation`` != 0 plants a deliberate mistake (used only by the test that
     checks that the pins catch it): 1 copy-on-write keeps the shared block's count,
     2 shared blocks are written in place, 3 the offset in the block is off by one,
-    4 freed blocks are not returned, 5 fork does not count the child's references.
+    4 freed blocks are not returned, 5 fork does not count the child's references,
+    6 a swap copies a shared block once per reference, 7 a swap keeps the references
+    in the pool it leaves.
     """
 
-    def __init__(self, num_blocks: int, block_size: int, free_order=None, mutation: int = 0):
-        if num_blocks <= 0 or block_size <= 0:
+    def __init__(self, num_blocks: int, block_size: int, free_order=None, mutation: int = 0,
+                 num_host_blocks: int = 0, host_free_order=None):
+        if num_blocks <= 0 or block_size <= 0 or num_host_blocks < 0:
             raise ValueError("num_blocks and block_size must be positive")
         order = list(range(num_blocks)) if free_order is None else [int(b) for b in free_order]
         if sorted(order) != list(range(num_blocks)):
             raise ValueError("free_order must list every block once")
+        horder = (list(range(num_host_blocks)) if host_free_order is None
+                  else [int(b) for b in host_free_order])
+        if sorted(horder) != list(range(num_host_blocks)):
+            raise ValueError("host_free_order must list every host block once")
         self.B = block_size
         self.num_blocks = num_blocks
         self.free = deque(order)
         self.ref = [0] * num_blocks
+        self.hfree = deque(horder)
+        self.href = [0] * num_host_blocks
         self.tables = {}     # sequence id -> physical block ids of its logical blocks
         self.lens = {}       # sequence id -> tokens held
+        self.on_host = set() # sequences whose blocks are in the host pool
         self.mutation = mutation
+
+    def _on_device(self, seq):
+        if seq not in self.tables:
+            raise KeyError(f"unknown sequence {seq}")
+        if seq in self.on_host:
+            raise KeyError(f"sequence {seq} is swapped out")
 
     # ---- primitives
     def add(self, seq) -> None:
@@ -70,6 +94,7 @@ class BlockManager:
         """The child shares every block of the parent (each count + 1)."""
         if parent not in self.tables or child in self.tables:
             raise KeyError("fork needs an existing parent and a new child")
+        self._on_device(parent)
         self.tables[child] = list(self.tables[parent])
         self.lens[child] = self.lens[parent]
         if self.mutation != 5:
@@ -79,10 +104,15 @@ class BlockManager:
     def free_seq(self, seq) -> None:
         """A finished request: each of its blocks loses one reference; blocks left with
         none return to the pool."""
+        if seq in self.on_host:
+            self.on_host.discard(seq)
+            ref, free = self.href, self.hfree
+        else:
+            ref, free = self.ref, self.free
         for b in self.tables.pop(seq):
-            self.ref[b] -= 1
-            if self.ref[b] == 0 and self.mutation != 4:
-                self.free.append(b)
+            ref[b] -= 1
+            if ref[b] == 0 and self.mutation != 4:
+                free.append(b)
         del self.lens[seq]
 
     def _blocks_needed(self, seq, n, shared_left) -> int:
@@ -116,8 +146,7 @@ class BlockManager:
         if len(set(seqs)) != len(seqs):
             raise ValueError("a sequence appears twice in one step")
         for s, n in zip(seqs, ns):
-            if s not in self.tables:
-                raise KeyError(f"unknown sequence {s}")
+            self._on_device(s)
             if n < 0:
                 raise ValueError("negative token count")
         shared_left = {}
@@ -147,6 +176,54 @@ class BlockManager:
             self.lens[s] += n
         return slots, copies
 
+    def _swap(self, seqs, out: bool):
+        if len(set(seqs)) != len(seqs):
+            raise ValueError("a sequence appears twice in one swap")
+        for q in seqs:
+            if q not in self.tables:
+                raise KeyError(f"unknown sequence {q}")
+            if (q in self.on_host) == out:
+                raise KeyError(f"sequence {q} is already {'out' if out else 'in'}")
+        src_ref, src_free = (self.ref, self.free) if out else (self.href, self.hfree)
+        dst_ref, dst_free = (self.href, self.hfree) if out else (self.ref, self.free)
+        distinct = []
+        for q in seqs:
+            for b in self.tables[q]:
+                if b not in distinct or self.mutation == 6:
+                    distinct.append(b)
+        if len(distinct) > len(dst_free):
+            raise OutOfBlocks(f"{len(distinct)} blocks needed, {len(dst_free)} free")
+        to = {}
+        pairs = []
+        for b in distinct:
+            c = dst_free.popleft()
+            to[b] = c
+            pairs.append((b, c))
+        for q in seqs:
+            t = self.tables[q]
+            for j, b in enumerate(t):
+                dst_ref[to[b]] += 1
+                if self.mutation != 7:
+                    src_ref[b] -= 1
+                    if src_ref[b] == 0:
+                        src_free.append(b)
+                t[j] = to[b]
+            if out:
+                self.on_host.add(q)
+            else:
+                self.on_host.discard(q)
+        return pairs
+
+    def swap_out(self, seqs):
+        """All blocks of the listed requests go to the host pool; returns the
+        (device block, host block) copies to make before the device blocks are reused."""
+        return self._swap(list(seqs), True)
+
+    def swap_in(self, seqs):
+        """The listed swapped-out requests come back; returns the (host block, device
+        block) copies to make before they run."""
+        return self._swap(list(seqs), False)
+
     # ---- views
     def table(self, seq):
         return list(self.tables[seq])
@@ -161,3 +238,14 @@ class BlockManager:
 
     def refcount(self, block: int) -> int:
         return self.ref[block]
+
+    def host_refcount(self, block: int) -> int:
+        return self.href[block]
+
+    def num_free_host(self) -> int:
+        return len(self.hfree)
+
+    def is_on_host(self, seq) -> bool:
+        if seq not in self.tables:
+            raise KeyError(f"unknown sequence {seq}")
+        return seq in self.on_host

@@ -80,7 +80,13 @@ def _lib() -> C.CDLL:
         lib.pa_bm_free.argtypes = [_P, _I64]
         lib.pa_bm_append.argtypes = [_P, _P, _P, _I32, _P, _P, _P, C.POINTER(_I32)]
         lib.pa_bm_tables.argtypes = [_P, _P, _I32, _I32, _P, _P]
-        lib.pa_bm_seq_info.argtypes = [_P, _I64, C.POINTER(_I64), C.POINTER(_I32)]
+        lib.pa_bm_seq_info.argtypes = [_P, _I64, C.POINTER(_I64), C.POINTER(_I32),
+                                       C.POINTER(_I32)]
+        lib.pa_bm_set_host_pool.argtypes = [_P, _I32, _P]
+        lib.pa_bm_swap_out.argtypes = [_P, _P, _I32, _P, _P, _I32, C.POINTER(_I32)]
+        lib.pa_bm_swap_in.argtypes = [_P, _P, _I32, _P, _P, _I32, C.POINTER(_I32)]
+        lib.pa_bm_host_refcount.argtypes = [_P, _I32, C.POINTER(_I32)]
+        lib.pa_bm_host_num_free.argtypes = [_P, C.POINTER(_I32)]
         lib.pa_bm_refcount.argtypes = [_P, _I32, C.POINTER(_I32)]
         lib.pa_bm_num_free.argtypes = [_P, C.POINTER(_I32)]
         for f in ("pa_get_device_error", "pa_slot_mapping", "pa_write_kv", "pa_copy_blocks",
@@ -88,7 +94,9 @@ def _lib() -> C.CDLL:
                   "pa_attention", "pa_attention_static", "pa_plan_upload",
                   "pa_attention_planned", "pa_swap_blocks", "pa_bm_create", "pa_bm_destroy", "pa_bm_add",
                   "pa_bm_fork", "pa_bm_free", "pa_bm_append", "pa_bm_tables",
-                  "pa_bm_seq_info", "pa_bm_refcount", "pa_bm_num_free"):
+                  "pa_bm_seq_info", "pa_bm_refcount", "pa_bm_num_free",
+                  "pa_bm_set_host_pool", "pa_bm_swap_out", "pa_bm_swap_in",
+                  "pa_bm_host_refcount", "pa_bm_host_num_free"):
             getattr(lib, f).restype = C.c_int
         _LIB = lib
     return _LIB
@@ -378,20 +386,32 @@ class BlockManager:
     and the copy-on-write decision. Sequence ids may be any hashable; non-integer ids are
     mapped to int64 here. Host-only: no GPU is touched."""
 
-    def __init__(self, num_blocks: int, block_size: int, free_order=None):
+    def __init__(self, num_blocks: int, block_size: int, free_order=None,
+                 num_host_blocks: int = 0, host_free_order=None):
         import numpy as np
         self._h = None
-        order = None
-        if free_order is not None:
-            order = np.ascontiguousarray(np.asarray(free_order, dtype=np.int32))
-            if order.shape != (num_blocks,):
-                raise ValueError("free_order must list num_blocks block ids")
+
+        def order_of(o, n, what):
+            if o is None:
+                return None
+            o = np.ascontiguousarray(np.asarray(o, dtype=np.int32))
+            if o.shape != (n,):
+                raise ValueError(f"{what} must list {n} block ids")
+            return o
+
+        order = order_of(free_order, num_blocks, "free_order")
+        horder = order_of(host_free_order, num_host_blocks, "host_free_order")
         h = C.c_void_p()
         _check(_lib().pa_bm_create(num_blocks, block_size,
                                    None if order is None else order.ctypes.data, C.byref(h)),
                "pa_bm_create")
         self._h = h
+        if num_host_blocks:
+            _check(_lib().pa_bm_set_host_pool(h, num_host_blocks,
+                                              None if horder is None else horder.ctypes.data),
+                   "pa_bm_set_host_pool")
         self.num_blocks, self.block_size = num_blocks, block_size
+        self.num_host_blocks = num_host_blocks
         self._ids = {}
 
     def _id(self, seq, new=False) -> int:
@@ -456,9 +476,45 @@ class BlockManager:
         return bt, cl
 
     def seq_info(self, seq):
-        ln, nb = C.c_int64(0), C.c_int32(0)
-        self._call("pa_bm_seq_info", self._id(seq), C.byref(ln), C.byref(nb))
+        ln, nb, oh = C.c_int64(0), C.c_int32(0), C.c_int32(0)
+        self._call("pa_bm_seq_info", self._id(seq), C.byref(ln), C.byref(nb), C.byref(oh))
         return ln.value, nb.value
+
+    def is_on_host(self, seq) -> bool:
+        ln, nb, oh = C.c_int64(0), C.c_int32(0), C.c_int32(0)
+        self._call("pa_bm_seq_info", self._id(seq), C.byref(ln), C.byref(nb), C.byref(oh))
+        return bool(oh.value)
+
+    def _swap(self, what, seqs):
+        import numpy as np
+        ids = np.ascontiguousarray(np.array([self._id(s) for s in seqs], dtype=np.int64))
+        if len(set(ids.tolist())) != len(ids):
+            raise ValueError("a sequence appears twice in one swap")
+        cap = sum(self.seq_info(s)[1] for s in seqs)
+        a = np.zeros(max(1, cap), dtype=np.int32)
+        b = np.zeros(max(1, cap), dtype=np.int32)
+        n = C.c_int32(0)
+        self._call(what, ids.ctypes.data, len(ids), a.ctypes.data, b.ctypes.data, cap,
+                   C.byref(n))
+        return list(zip(a[:n.value].tolist(), b[:n.value].tolist()))
+
+    def swap_out(self, seqs):
+        """(device block, host block) copies; the requests now live in the host pool."""
+        return self._swap("pa_bm_swap_out", list(seqs))
+
+    def swap_in(self, seqs):
+        """(host block, device block) copies; the requests are back on the device."""
+        return self._swap("pa_bm_swap_in", list(seqs))
+
+    def host_refcount(self, block: int) -> int:
+        c = C.c_int32(0)
+        self._call("pa_bm_host_refcount", int(block), C.byref(c))
+        return c.value
+
+    def num_free_host(self) -> int:
+        c = C.c_int32(0)
+        self._call("pa_bm_host_num_free", C.byref(c))
+        return c.value
 
     def table(self, seq):
         _, nb = self.seq_info(seq)

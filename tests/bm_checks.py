@@ -1,8 +1,9 @@
 """Pins for a KV block manager (the oracle's, and the same checks for the library's).
 
-Each ``check_*`` takes a factory ``make(num_blocks, block_size, free_order)`` that
-returns an object with the oracle's interface (add, fork, free_seq, append,
-append_batch, table, filled, num_free, refcount) and raises AssertionError when
+Each ``check_*`` takes a factory ``make(num_blocks, block_size, free_order,
+num_host_blocks=0)`` that returns an object with the oracle's interface (add, fork,
+free_seq, append, append_batch, swap_out, swap_in, table, filled, num_free,
+refcount, host_refcount, num_free_host, is_on_host) and raises AssertionError when
 the manager disagrees with something that does not come from the manager itself:
 
 * the vLLM post's worked example ("1. overall architecture": slots, #filled, the
@@ -15,7 +16,10 @@ the manager disagrees with something that does not come from the manager itself:
 * bookkeeping invariants: a block's count equals the number of block-table entries
   naming it, free and referenced blocks partition the pool, a table has
   ceil(L / B) entries;
-* all-or-nothing on an exhausted pool.
+* all-or-nothing on an exhausted pool;
+* swapping (vLLM post, "3. scheduling and preemption"): after any seeded history
+  with swaps out and in, every request reads back its tokens from the pool it lives
+  in, and blocks shared by requests swapped together stay shared.
 """
 import json
 import os
@@ -72,26 +76,42 @@ def check_cow_example(make):
         assert bm.refcount(int(b)) == c, ("after", b)
 
 
-def _invariants(bm, model, num_blocks, B):
+def _invariants(bm, model, num_blocks, B, host=None, num_host_blocks=0):
     refs = [0] * num_blocks
+    hrefs = [0] * num_host_blocks
     for s in model:
         t = bm.table(s)
         assert len(t) == -(-len(model[s]) // B), ("table length", s)
+        on_host = host is not None and s in host
         for b in t:
-            refs[b] += 1
+            if on_host:
+                hrefs[b] += 1
+            else:
+                refs[b] += 1
     for b in range(num_blocks):
         assert bm.refcount(b) == refs[b], ("refcount", b, bm.refcount(b), refs[b])
     used = sum(1 for r in refs if r > 0)
     assert bm.num_free() + used == num_blocks, ("free + used", bm.num_free(), used)
+    if num_host_blocks:
+        for b in range(num_host_blocks):
+            assert bm.host_refcount(b) == hrefs[b], ("host refcount", b)
+        hused = sum(1 for r in hrefs if r > 0)
+        assert bm.num_free_host() + hused == num_host_blocks, "host free + used"
 
 
-def random_ops(seed, n_ops=300):
+def random_ops(seed, n_ops=300, swaps=False):
     """Seeded operation list: ("add", s), ("fork", parent, child), ("append", [(s, n)]),
-    ("free", s), over at most 12 live sequences."""
+    ("free", s), and with ``swaps`` ("swap_out", [s...]) / ("swap_in", [s...]), over at
+    most 12 live sequences. Operations that do not apply when replayed (an append to a
+    swapped-out request, ...) are dropped by ``run_ops``."""
     rng = random.Random(seed)
     ops, live, nxt = [], [], 0
     for _ in range(n_ops):
         r = rng.random()
+        if swaps and live and rng.random() < 0.2:
+            k = rng.randint(1, min(3, len(live)))
+            ops.append((rng.choice(["swap_out", "swap_in"]), rng.sample(live, k)))
+            continue
         if not live or (r < 0.15 and len(live) < 12):
             ops.append(("add", nxt)); live.append(nxt); nxt += 1
         elif r < 0.30 and len(live) < 12:
@@ -107,29 +127,69 @@ def random_ops(seed, n_ops=300):
     return ops
 
 
-def run_ops(bm, ops, num_blocks, B, log=None):
-    """Replays ops on bm and on a model pool; checks every read-back and invariant.
-    Appends that the pool cannot hold must raise and change nothing."""
-    pool = [None] * (num_blocks * B)       # token id held by each slot
+def _is_full(e):
+    return "block" in str(e).lower() or "space" in str(e).lower()
+
+
+def run_ops(bm, ops, num_blocks, B, log=None, num_host_blocks=0):
+    """Replays ops on bm and on model pools (device and host); checks every read-back and
+    invariant. Appends and swaps that a pool cannot hold must raise and change nothing."""
+    pool = [None] * (num_blocks * B)       # token id held by each device slot
+    hpool = [None] * (num_host_blocks * B)  # and by each host slot
     model = {}                              # sequence -> its token ids by position
+    host = set()                            # sequences swapped out
     tok = 0
+
+    def snapshot():
+        return ({s: bm.table(s) for s in model}, bm.num_free(),
+                bm.num_free_host() if num_host_blocks else 0)
+
     for op in ops:
         if op[0] == "add":
             bm.add(op[1]); model[op[1]] = []
         elif op[0] == "fork":
+            if op[1] not in model or op[1] in host:    # a swapped-out parent: dropped
+                continue
             bm.fork(op[1], op[2]); model[op[2]] = list(model[op[1]])
         elif op[0] == "free":
-            bm.free_seq(op[1]); del model[op[1]]
+            if op[1] not in model:
+                continue
+            bm.free_seq(op[1]); del model[op[1]]; host.discard(op[1])
+        elif op[0] in ("swap_out", "swap_in"):
+            out = op[0] == "swap_out"
+            seqs = [s for s in op[1] if s in model and (s in host) != out]
+            if not seqs:
+                continue
+            before = snapshot()
+            try:
+                pairs = bm.swap_out(seqs) if out else bm.swap_in(seqs)
+            except Exception as e:
+                if not _is_full(e):
+                    raise
+                assert snapshot() == before, "swap not atomic"
+                if log is not None:
+                    log.append(("full",))
+                continue
+            src_pool, dst_pool = (pool, hpool) if out else (hpool, pool)
+            for a, b in pairs:                  # copies read before any block is reused
+                dst_pool[b * B:(b + 1) * B] = src_pool[a * B:(a + 1) * B]
+            for s in seqs:
+                (host.add if out else host.discard)(s)
+            if log is not None:
+                log.append((op[0], tuple(map(tuple, pairs))))
         else:
-            seqs = [s for s, _ in op[1]]
-            ns = [n for _, n in op[1]]
-            before = {s: bm.table(s) for s in model}, bm.num_free()
+            batch = [(s, n) for s, n in op[1] if s in model and s not in host]
+            if not batch:
+                continue
+            seqs = [s for s, _ in batch]
+            ns = [n for _, n in batch]
+            before = snapshot()
             try:
                 slots, copies = bm.append_batch(seqs, ns)
             except Exception as e:   # pool exhausted: nothing may have changed
-                if "block" not in str(e).lower() and "space" not in str(e).lower():
+                if not _is_full(e):
                     raise
-                assert ({s: bm.table(s) for s in model}, bm.num_free()) == before, "not atomic"
+                assert snapshot() == before, "not atomic"
                 if log is not None:
                     log.append(("full",))
                 continue
@@ -146,16 +206,44 @@ def run_ops(bm, ops, num_blocks, B, log=None):
                 log.append((tuple(slots), tuple(map(tuple, copies))))
         for s, toks in model.items():
             t = bm.table(s)
+            src = hpool if s in host else pool
             for p, want in enumerate(toks):
-                got = pool[t[p // B] * B + p % B]
+                got = src[t[p // B] * B + p % B]
                 assert got == want, ("read-back", s, p, got, want)
-        _invariants(bm, model, num_blocks, B)
+            if num_host_blocks:
+                assert bm.is_on_host(s) == (s in host), ("residency", s)
+        _invariants(bm, model, num_blocks, B, host, num_host_blocks)
     return model
 
 
 def check_random_histories(make):
     for seed, (nb, B) in enumerate([(64, 4), (40, 16), (200, 1), (24, 8)]):
         run_ops(make(nb, B, None), random_ops(seed), nb, B)
+
+
+def check_swap_histories(make):
+    """Seeded histories with swaps out and in: after every operation each request
+    reads back its own tokens from the pool it lives in (vLLM post, 3, swapping)."""
+    for seed, (nb, nhb, B) in enumerate([(40, 24, 4), (30, 60, 8), (64, 8, 2)]):
+        run_ops(make(nb, B, None, nhb), random_ops(100 + seed, swaps=True), nb, B,
+                num_host_blocks=nhb)
+
+
+def check_swap_keeps_sharing(make):
+    """Two samples sharing a prompt swap out together: each shared block is copied
+    once and stays shared in the host pool; back in, they share again."""
+    bm = make(12, 4, None, 12)
+    bm.add("A1")
+    bm.append("A1", 7)                         # blocks 0, 1
+    bm.fork("A1", "A2")
+    bm.append("A1", 1)                         # copy 1 -> 2, A1 [0, 2], A2 [0, 1]
+    pairs = bm.swap_out(["A1", "A2"])
+    assert pairs == [(0, 0), (2, 1), (1, 2)], pairs
+    assert bm.table("A1") == [0, 1] and bm.table("A2") == [0, 2]
+    assert bm.host_refcount(0) == 2 and bm.num_free() == 12 and bm.num_free_host() == 9
+    back = bm.swap_in(["A2"])                  # only A2 returns: host block 0 stays for A1
+    assert back == [(0, 3), (2, 4)], back
+    assert bm.host_refcount(0) == 1 and bm.refcount(3) == 1 and bm.num_free_host() == 10
 
 
 def check_exhaustion_is_atomic(make):
@@ -175,4 +263,4 @@ def check_exhaustion_is_atomic(make):
 
 
 ALL_CHECKS = [check_worked_example, check_cow_example, check_random_histories,
-              check_exhaustion_is_atomic]
+              check_exhaustion_is_atomic, check_swap_histories, check_swap_keeps_sharing]

@@ -10,7 +10,8 @@ from tests import bm_checks as bc
 
 
 def oracle_factory(mutation=0):
-    return lambda nb, B, order: BlockManager(nb, B, free_order=order, mutation=mutation)
+    return lambda nb, B, order, nhb=0: BlockManager(nb, B, free_order=order, mutation=mutation,
+                                                     num_host_blocks=nhb)
 
 
 @pytest.mark.parametrize("check", bc.ALL_CHECKS, ids=lambda c: c.__name__)
@@ -19,7 +20,8 @@ def test_oracle_pin(check):
 
 
 MUTANTS = {1: "copy keeps the shared count", 2: "shared block written in place",
-           3: "offset off by one", 4: "freed blocks lost", 5: "fork not counted"}
+           3: "offset off by one", 4: "freed blocks lost", 5: "fork not counted",
+           6: "swap copies shared blocks twice", 7: "swap keeps source references"}
 
 
 @pytest.mark.parametrize("mutation", sorted(MUTANTS), ids=lambda m: MUTANTS[m])
@@ -61,7 +63,8 @@ def pa():
 
 
 def library_factory(pa):
-    return lambda nb, B, order: pa.BlockManager(nb, B, free_order=order)
+    return lambda nb, B, order, nhb=0: pa.BlockManager(nb, B, free_order=order,
+                                                        num_host_blocks=nhb)
 
 
 @pytest.mark.parametrize("check", bc.ALL_CHECKS, ids=lambda c: c.__name__)
@@ -86,6 +89,24 @@ def test_library_matches_oracle(pa, seed, nb, B):
         assert lib.table(s) == orc.table(s) and lib.filled(s) == orc.filled(s)
     assert [lib.refcount(b) for b in range(nb)] == [orc.refcount(b) for b in range(nb)]
     assert lib.num_free() == orc.num_free()
+
+
+@pytest.mark.parametrize("seed,nb,nhb,B", [(21, 40, 24, 4), (22, 30, 60, 8), (25, 64, 8, 2)])
+def test_library_matches_oracle_with_swaps(pa, seed, nb, nhb, B):
+    """Histories with swaps out and in: the same pairs, tables, counts, residency."""
+    ops = bc.random_ops(seed, n_ops=400, swaps=True)
+    lib = pa.BlockManager(nb, B, num_host_blocks=nhb)
+    orc = BlockManager(nb, B, num_host_blocks=nhb)
+    log_lib, log_orc = [], []
+    live = bc.run_ops(lib, ops, nb, B, log_lib, num_host_blocks=nhb)
+    bc.run_ops(orc, ops, nb, B, log_orc, num_host_blocks=nhb)
+    assert log_lib == log_orc
+    assert any(e[0] == "swap_in" and e[1] for e in log_orc), "no swap-in exercised"
+    for s in live:
+        assert lib.table(s) == orc.table(s) and lib.is_on_host(s) == orc.is_on_host(s)
+    assert [lib.host_refcount(b) for b in range(nhb)] == [orc.host_refcount(b)
+                                                          for b in range(nhb)]
+    assert lib.num_free_host() == orc.num_free_host() and lib.num_free() == orc.num_free()
 
 
 def test_library_tables_for_attention(pa):
