@@ -264,3 +264,35 @@ def check_exhaustion_is_atomic(make):
 
 ALL_CHECKS = [check_worked_example, check_cow_example, check_random_histories,
               check_exhaustion_is_atomic, check_swap_histories, check_swap_keeps_sharing]
+
+
+def swap_roundtrip(bm, gather, scribble, move):
+    """A request and its fork swapped out, their device blocks overwritten, both swapped
+    back in to other blocks: they read back what they held, through their new tables.
+
+    gather(table) -> copy of those device blocks; scribble(blocks) overwrites device
+    blocks; move(pairs, direction) copies blocks ("out": device -> host, "in": back)."""
+    bm.add("A")
+    bm.append("A", 30)
+    bm.add("B")
+    bm.append("B", 20)
+    bm.fork("A", "C")
+    bm.append("C", 1)                            # copy-on-write of A's partial block
+    want = {s: gather(bm.table(s)) for s in ("A", "C")}
+    keep_b = gather(bm.table("B"))
+    # (the copy of C's partial block is the caller's: it moved with pa_copy_blocks or
+    # here simply with the pool contents of the shared block, which equal both tables')
+    distinct = set(bm.table("A")) | set(bm.table("C"))
+    out = bm.swap_out(["A", "C"])
+    assert sorted(d for d, _ in out) == sorted(distinct), out   # shared blocks once
+    move(out, "out")
+    freed = [d for d, _ in out]
+    scribble(freed)
+    back = bm.swap_in(["C", "A"])
+    assert len(back) == len(distinct) and all(bm.refcount(d) > 0 for _, d in back)
+    move(back, "in")
+    for s in ("A", "C"):
+        got = gather(bm.table(s))
+        assert got == want[s] if isinstance(got, list) else (got == want[s]).all(), s
+    got_b = gather(bm.table("B"))
+    assert got_b == keep_b if isinstance(got_b, list) else (got_b == keep_b).all()

@@ -214,3 +214,32 @@ def test_edge_cases(pa, impl):
     one.add("x"); one.append("x", 3); one.fork("x", "y")
     assert one.append_batch(["x", "y"], [1, 1])[1] == []
     assert one.num_free() == 1
+
+
+def test_swap_roundtrip_moves_the_right_blocks(pa):
+    """The library's swap pairs drive a model copy (the oracle's block swap) on numpy
+    pools; the same scenario runs on the GPU with pa_swap_blocks in test_swap_gpu."""
+    from oracle.swap import swap_blocks
+    rng = np.random.default_rng(3)
+    kd = rng.integers(0, 2**16, (16, 4, 2, 8), dtype=np.uint16)
+    vd = rng.integers(0, 2**16, (16, 4, 2, 8), dtype=np.uint16)
+    kh = np.zeros((12, 4, 2, 8), np.uint16)
+    vh = np.zeros_like(kh)
+    bm = pa.BlockManager(16, 4, num_host_blocks=12)
+
+    def gather(table):
+        return np.concatenate([kd[table], vd[table]])
+
+    def scribble(blocks):
+        kd[blocks] = 7
+        vd[blocks] = 9
+
+    def move(pairs, direction):
+        src = [a for a, _ in pairs]
+        dst = [b for _, b in pairs]
+        if direction == "out":
+            swap_blocks(kd, vd, kh, vh, src, dst)
+        else:
+            swap_blocks(kh, vh, kd, vd, src, dst)
+
+    bc.swap_roundtrip(bm, gather, scribble, move)

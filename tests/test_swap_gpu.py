@@ -73,3 +73,32 @@ def test_swap_rejects_pageable_host_memory_and_skips_bad_ids(pa):
     want_k, want_v = before_k.copy(), before_v.copy()
     want_k[5], want_v[5] = u16(kd)[0], u16(vd)[0]          # the valid pair still moved
     assert np.array_equal(u16(kh), want_k) and np.array_equal(u16(vh), want_v)
+
+
+def test_block_manager_drives_swaps(pa):
+    """The block manager's swap pairs moved by pa_swap_blocks: requests swapped out, their
+    device blocks overwritten, swapped back in to other blocks, read back intact."""
+    from tests import bm_checks as bc
+    dev = "cuda"
+    pa.pa_get_device_error()
+    kd, vd = _pools(16, (4, 2, 64), 5, device=dev)
+    kh, vh = _pools(12, (4, 2, 64), 6, pin=True)
+    bm = pa.BlockManager(16, 4, num_host_blocks=12)
+
+    def gather(table):
+        t = torch.tensor(table, dtype=torch.long, device=dev)
+        return torch.cat([kd[t], vd[t]]).cpu()
+
+    def scribble(blocks):
+        t = torch.tensor(blocks, dtype=torch.long, device=dev)
+        kd[t] = 7.0
+        vd[t] = 9.0
+
+    def move(pairs, direction):
+        src = torch.tensor([a for a, _ in pairs], dtype=torch.int32, device=dev)
+        dst = torch.tensor([b for _, b in pairs], dtype=torch.int32, device=dev)
+        pa.pa_swap_blocks(kd, vd, kh, vh, src, dst, direction)
+        torch.cuda.synchronize()
+
+    bc.swap_roundtrip(bm, gather, scribble, move)
+    assert pa.pa_get_device_error() == 0
