@@ -5,9 +5,13 @@ copy-on-write block copies (when the batch has any), the KV write of the step's
 new tokens, and paged attention over the block tables (CUDA-core decode items,
 tensor-core items, the split-KV combine). Inputs are resident in HBM when the
 timed region starts; the KV pools (several GB) are larger than L2, so no flush
-is needed between steps. The default workload is the decode-only batch with
-the OPT-13B attention shape (256 sequences, one query token each, Hq=Hkv=40,
-D=128, block size 16, contexts uniform in [128, 2048]).
+is needed between steps. The default workload is the largest one, the
+Pensieve-style unified batch with the Llama-2-13B attention shape (Hq=Hkv=40,
+D=128, block size 32): 64 multi-turn conversations, each a new prompt of 32-512
+tokens over a 512-3072-token history split into two sub-requests that share
+blocks, plus 128 decode sequences (about 48.6k query rows over 436k KV tokens).
+The key ``configs`` times the attention kernels of every other workload and of
+the mixed batches' prefill and decode sub-batches, each against its roofline.
 
 Prints ONE JSON line (rank 0). ``--impl reference`` times the fp64 CPU oracle on
 the host cores instead (a deliberately plain program, the baseline arm).
@@ -165,7 +169,7 @@ def oracle_step_sample(w, orc, host, n_threads, budget_s=10.0, max_passes=30):
     """Times the oracle on bounded passes over the same workload: slot mapping, copies,
     KV write and attention for a contiguous block of query rows. Returns (rows/s, sample)."""
     import numpy as np
-    from tests.oracle_checks import u16
+    from workloads import host_bits as u16
     T = w.total_q
     rows_per_pass = T
     # estimated cost per row (visible keys * heads) to bound one pass to ~budget/3
@@ -208,7 +212,7 @@ def oracle_step_sample(w, orc, host, n_threads, budget_s=10.0, max_passes=30):
 def run_reference(args, w, cfg_name):
     import numpy as np
     import oracle
-    from tests.oracle_checks import u16
+    from workloads import host_bits as u16
     orc = oracle.default()
     host = {"q": u16(w.q), "k_pool": u16(w.k_pool), "v_pool": u16(w.v_pool),
             "k_new": u16(w.k_new), "v_new": u16(w.v_new)}
@@ -373,38 +377,55 @@ def run_gpu(args, w, cfg_name, rank, local, world):
 
     # ---- end to end through the public API, host buffers in pinned memory
     pin = lambda t: t.cpu().pin_memory()
-    h_q, h_kn, h_vn = pin(w.q), pin(w.k_new), pin(w.v_new)
-    h_bt, h_cl, h_ql = pin(bt), pin(cl), pin(ql)
-    h_sid, h_pos, h_src, h_dst = pin(sid), pin(pos), pin(src), pin(dst)
-    h_out = torch.empty(out.shape, dtype=out.dtype).pin_memory()
-    h2d = sum(t.numel() * t.element_size() for t in
-              (h_q, h_kn, h_vn, h_bt, h_cl, h_ql, h_sid, h_pos, h_src, h_dst))
-    d2h = h_out.numel() * h_out.element_size()
-    d_bufs = [torch.empty_like(t, device=dev) for t in
-              (h_q, h_kn, h_vn, h_bt, h_cl, h_ql, h_sid, h_pos, h_src, h_dst)]
+    h_in = [pin(w.q), pin(w.k_new), pin(w.v_new), pin(bt), pin(cl), pin(ql), pin(sid), pin(pos),
+            pin(src), pin(dst)]
+    h_outs = [torch.empty(out.shape, dtype=out.dtype).pin_memory() for _ in range(2)]
+    h2d = sum(t.numel() * t.element_size() for t in h_in)
+    d2h = h_outs[0].numel() * h_outs[0].element_size()
+    # two sets of device buffers: step i uses set i % 2
+    d_sets = [[torch.empty_like(t, device=dev) for t in h_in] for _ in range(2)]
+    d_outs = [out, torch.empty_like(out)]
+    s_h2d = torch.cuda.Stream(dev)
+    s_d2h = torch.cuda.Stream(dev)
+    free_ev = [None, None]
 
     # Two steps in flight, as a serving loop runs them: the host builds step i's plan and
-    # enqueues its copies and kernels while the GPU still works on step i - 1, then
-    # waits for step i - 1 to finish (its output is in host memory by then). Every
-    # step still copies its own inputs in and its output out; the stream orders the
-    # reuse of the device buffers, and the timed region ends with a synchronize.
+    # enqueues its work while the GPU still works on step i - 1, then waits for step
+    # i - 1 to finish (its output is in host memory by then). Step i's inputs go up on a
+    # copy stream and its output comes back on another, so that they overlap the
+    # kernels of the neighbouring steps; events order the reuse of each buffer set (the
+    # copies into set i % 2 wait until step i - 2 has read it and its output is home).
+    # Every step still copies all of its own inputs in and its whole output out.
     inflight = []
 
-    def e2e_step():
-        for hb, db in zip((h_q, h_kn, h_vn, h_bt, h_cl, h_ql, h_sid, h_pos, h_src, h_dst), d_bufs):
-            db.copy_(hb, non_blocking=True)
-        dq, dkn, dvn, dbt, dcl, dql, dsid, dpos, dsrc, ddst = d_bufs
+    def e2e_step(i):
+        k = i % 2
+        dset, d_out, h_out = d_sets[k], d_outs[k], h_outs[k]
+        if free_ev[k] is not None:
+            s_h2d.wait_event(free_ev[k])
+        with torch.cuda.stream(s_h2d):
+            for hb, db in zip(h_in, dset):
+                db.copy_(hb, non_blocking=True)
+        in_ev = torch.cuda.Event()
+        in_ev.record(s_h2d)
+        dq, dkn, dvn, dbt, dcl, dql, dsid, dpos, dsrc, ddst = dset
         p2 = pa.Plan(w.context_lens, w.query_lens, w.Hq, w.Hkv, w.D, w.block_size, w.max_blocks,
                      **plan_kw)
+        stream.wait_event(in_ev)
         pa.pa_slot_mapping(dbt, w.num_blocks, w.block_size, dsid, dpos, out=slots)
         if n_pairs:
             pa.pa_copy_blocks(kp, vp, dsrc, ddst)
         pa.pa_write_kv(dkn, dvn, slots, kp, vp)
-        pa.pa_attention(p2, dq, kp, vp, dbt, dcl, dql, out=out, workspace=ws)
-        h_out.copy_(out, non_blocking=True)
-        ev = torch.cuda.Event()
-        ev.record(torch.cuda.current_stream(dev))
-        inflight.append((ev, p2))
+        pa.pa_attention(p2, dq, kp, vp, dbt, dcl, dql, out=d_out, workspace=ws)
+        comp_ev = torch.cuda.Event()
+        comp_ev.record(stream)
+        s_d2h.wait_event(comp_ev)
+        with torch.cuda.stream(s_d2h):
+            h_out.copy_(d_out, non_blocking=True)
+        done = torch.cuda.Event()
+        done.record(s_d2h)
+        free_ev[k] = done
+        inflight.append((done, p2))
         if len(inflight) > 1:
             ev0, p0 = inflight.pop(0)
             ev0.synchronize()
@@ -416,25 +437,29 @@ def run_gpu(args, w, cfg_name, rank, local, world):
             ev0.synchronize()
             p0.close()
 
-    for _ in range(min(3, args.warmup)):
-        e2e_step()
+    for i in range(min(3, args.warmup)):
+        e2e_step(i)
     e2e_drain()
     e2e_steps = max(3, min(args.steps, 200))
     barrier(world)
     torch.cuda.synchronize(dev)
     t0 = time.perf_counter()
-    for _ in range(e2e_steps):
-        e2e_step()
+    for i in range(e2e_steps):
+        e2e_step(i)
     e2e_drain()
     torch.cuda.synchronize(dev)
     e2e_s = max_over_ranks(time.perf_counter() - t0, world)
     e2e_value = T * e2e_steps * world / e2e_s
+    err = pa.pa_get_device_error(reset=True)
+    if err:
+        raise RuntimeError(f"device error {pa.DEVERR.get(err, err)} in the end-to-end run")
 
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": elapsed_ms / args.steps, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
         "config": cfg_name,
+        "out_dtype": args.out,
         "roofline": roof,
         "hbm_gbs_attention": (kv_b + q_b) / attn_s / 1e9,
         "tc_tflops_attention": flops / attn_s / 1e12,
@@ -444,17 +469,126 @@ def run_gpu(args, w, cfg_name, rank, local, world):
                 "includes": "H2D of the step's inputs from pinned memory, host plan build, "
                             "slot mapping, copies, KV write, attention, D2H of the output; "
                             "two steps in flight (the host prepares step i while the GPU "
-                            "runs step i - 1)"},
+                            "runs step i - 1), H2D and D2H on their own streams"},
         "gpu_launches": launches_per_step * args.steps,
         "clocks": clocks.summary(h0, h1),
         "plan": {k: st[k] for k in ("n_dec_items", "n_tc_items", "n_split_groups", "chunk_tokens")},
         "bytes": {"kv": kv_b, "q": q_b, "o_write": o_b}, "flops": flops,
     }
     if rank == 0:
+        if not args.no_configs:
+            line["configs"] = configs_sweep(args, w, dev)
         line["swap"] = swap_measure(w, dev)
         line["block_manager"] = block_manager_host(w)
         line["cpu_baseline"] = cpu_baseline(args, w)
         print(json.dumps(line), flush=True)
+
+
+def roofline_entry(w, ms, peaks, out_bytes_per_elem=4):
+    """Roofline of one attention call: the slower of K/V + Q bytes at the measured HBM
+    bandwidth and the causal FLOPs at the measured bf16 tensor rate."""
+    kv_b, q_b, flops = w.kv_bytes(), w.q_bytes(), w.flops()
+    hbm, tc = float(peaks["hbm_gbs"]), float(peaks.get("bf16_tflops", 1900.0))
+    s = ms / 1000.0
+    t_hbm, t_tc = (kv_b + q_b) / (hbm * 1e9), flops / (tc * 1e12)
+    gbs, tfs = (kv_b + q_b) / s / 1e9, flops / s / 1e12
+    bound = "hbm" if t_hbm >= t_tc else "tensor"
+    return {"bound": bound,
+            "achieved": gbs if bound == "hbm" else tfs,
+            "peak": hbm if bound == "hbm" else tc,
+            "unit": "GB/s" if bound == "hbm" else "TFLOP/s",
+            "frac": max(t_hbm, t_tc) / s,
+            "frac_hbm": t_hbm / s, "frac_tc": t_tc / s,
+            "gbs": gbs, "tflops": tfs, "ms": ms,
+            "t_hbm_ms": t_hbm * 1e3, "t_tc_ms": t_tc * 1e3,
+            "tokens_per_s": w.total_q / s,
+            "total_q": w.total_q, "kv_tokens": int(w.context_lens.sum())}
+
+
+def time_attention(w, dev, reps=30, warmup=5, **plan_kw):
+    """CUDA-event time of the attention kernels of one planned call (tables uploaded once
+    before the timed calls), averaged over ``reps`` back-to-back calls; also the plan's
+    kernels. Inputs resident in HBM; their pools exceed L2 except config 1's."""
+    import torch
+    import paged_kv_cache_02_gb300 as pa
+    bt = torch.from_numpy(w.block_table).to(dev)
+    cl = torch.from_numpy(w.context_lens).to(dev)
+    ql = torch.from_numpy(w.query_lens).to(dev)
+    q = w.q.to(dev)
+    kp, vp = w.k_pool.to(dev), w.v_pool.to(dev)
+    out = torch.empty(q.shape, dtype=torch.float32, device=dev)
+    plan = pa.Plan(w.context_lens, w.query_lens, w.Hq, w.Hkv, w.D, w.block_size, w.max_blocks,
+                   **plan_kw)
+    ws = plan.workspace(dev)
+    pa.pa_plan_upload(plan, ws)
+    for _ in range(warmup):
+        pa.pa_attention_planned(plan, q, kp, vp, bt, cl, ql, ws, out=out)
+    stream = torch.cuda.current_stream(dev)
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize(dev)
+    a.record(stream)
+    for _ in range(reps):
+        pa.pa_attention_planned(plan, q, kp, vp, bt, cl, ql, ws, out=out)
+    b.record(stream)
+    b.synchronize()
+    err = pa.pa_get_device_error(reset=True)
+    if err:
+        raise RuntimeError(f"device error {pa.DEVERR.get(err, err)} timing {w.name}")
+    st = plan.stats()
+    n_tc1 = st["n_tc_items"] - st["n_tc_pair_items"] - st["n_tc_decode_items"]
+    kernels = [n for n, c in (("decode_kernel", st["n_dec_items"]),
+                              ("tcd_kernel", st["n_tc_decode_items"]),
+                              ("tc2_kernel", st["n_tc_pair_items"]), ("tc_kernel", n_tc1),
+                              ("combine_kernel", st["n_split_groups"])) if c]
+    plan.close()
+    return a.elapsed_time(b) / reps, kernels
+
+
+def configs_sweep(args, w_head, dev):
+    """Attention kernels of every config and of the mixed batches' prefill and decode
+    sub-batches, each with its roofline (the spec bars: decode-dominated batches
+    against HBM, prefill-dominated ones against the tensor cores)."""
+    import gc
+    import torch
+    import workloads
+    peaks = measured_peaks()
+    res = {}
+
+    def add(key, w, bar=None):
+        ms, kernels = time_attention(w, dev)
+        e = roofline_entry(w, ms, peaks)
+        e["kernels"] = kernels
+        if bar:
+            # any one of the listed (roofline, fraction) alternatives meets the bar
+            e["bar"] = [f"{kind} >= {thr}" for kind, thr in bar]
+            e["bar_met"] = any(e["frac_hbm" if kind == "hbm" else "frac_tc"] >= thr
+                               for kind, thr in bar)
+        res[key] = e
+        log(f"configs: {key}: {ms:.4f} ms, frac {e['frac']:.3f} ({e['bound']})")
+
+    head = args.config
+    for cfg in [1, 2, 3, 4, 5, "5cow"]:
+        key = f"cfg{cfg}"
+        w = w_head if str(cfg) == str(head) and not args.subset else \
+            workloads.make(cfg, device=dev)
+        bar = {2: [("hbm", 0.70)], 5: [("hbm", 0.70)], "5cow": [("hbm", 0.70)]}.get(cfg)
+        add(key, w, bar)
+        if cfg in (3, 4):
+            # config 3's prefill sub-batch is HBM-bound (its K/V bytes outweigh its FLOPs
+            # at machine balance), so its binding roofline at 0.70 is accepted too
+            add(f"{key}_prefill", w.subset(w.groups["prefill_seqs"]),
+                [("tensor", 0.50), ("hbm", 0.70)] if cfg == 3 else [("tensor", 0.50)])
+            add(f"{key}_decode", w.subset(w.groups["decode_seqs"]), [("hbm", 0.70)])
+        if w is not w_head:
+            del w
+            gc.collect()
+            torch.cuda.empty_cache()
+    res["_note"] = ("attention kernels of one planned call (tables uploaded once), CUDA "
+                    "events over 30 calls after 5 warm-up calls; frac = roofline time / "
+                    "measured; bar: decode-dominated >= 0.70 of HBM, prefill-dominated >= "
+                    "0.50 of the tensor roofline (config 3's prefill is HBM-bound: its "
+                    "binding roofline is accepted too)")
+    return res
 
 
 def swap_measure(w, dev, reps=20):
@@ -544,7 +678,7 @@ def cpu_baseline(args, w):
     if args.no_cpu_baseline:
         return None
     import oracle
-    from tests.oracle_checks import u16
+    from workloads import host_bits as u16
     orc = oracle.default()
     host = {"q": u16(w.q), "k_pool": u16(w.k_pool), "v_pool": u16(w.v_pool),
             "k_new": u16(w.k_new), "v_new": u16(w.v_new)}
@@ -561,7 +695,10 @@ def main():
     ap.add_argument("--steps", type=int, default=1000)
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", choices=["gb300", "reference"], default="gb300")
-    ap.add_argument("--config", default="2", help="workload: 1..5 or 5cow (default 2)")
+    ap.add_argument("--config", default="3",
+                    help="workload: 1..5 or 5cow (default 3, the Pensieve-style mixed batch)")
+    ap.add_argument("--no-configs", action="store_true",
+                    help="skip the per-config attention sweep (key 'configs')")
     ap.add_argument("--cpu-budget", type=float, default=12.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--tc-min-rows", type=int, default=0,
@@ -607,9 +744,7 @@ def main():
     if args.subset:
         w = w.subset(w.groups[f"{args.subset}_seqs"])
         args.config_key += f"_{args.subset}"
-    cd = cfg_dict(w, cfg, args.subset)
-    cd["out_dtype"] = args.out
-    run_gpu(args, w, cd, rank, local, world)
+    run_gpu(args, w, cfg_dict(w, cfg, args.subset), rank, local, world)
     if world > 1:
         import torch.distributed as dist
         dist.destroy_process_group()

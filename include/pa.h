@@ -148,7 +148,14 @@ typedef struct {
   int32_t tc_decode;         /* 0: default (on): a (sequence, KV head) pair with at most 16
                                 tensor-core rows runs with keys on the 128-row side (needs
                                 Hq / Hkv dividing 16); <0: never */
-  int32_t reserved[3];       /* must be zero */
+  int32_t wait_limit_ns;     /* 0: default: each wait of a kernel's pipeline gives up after
+                                about one second; >0: after this many nanoseconds. A wait
+                                that runs out records PA_DEVERR_TIMEOUT and the kernel
+                                aborts: it waits (with the default bound) for its own copies
+                                and MMAs in flight, frees its tensor memory and returns,
+                                leaving the outputs undefined. Short limits exist to test
+                                that path. */
+  int32_t reserved[2];       /* must be zero */
 } pa_plan_options;
 
 typedef struct {
@@ -253,8 +260,11 @@ pa_status pa_attention_planned(pa_plan_t plan, void* d_out, pa_dtype out_dtype,
  *     rejected with PA_ERR_SHAPE before anything is enqueued; use
  *     pa_attention with a caller-provided workspace for such batches.
  *   - The first call on each device looks up the array's device address
- *     (cudaGetSymbolAddress) with that device current and caches it; make
- *     that first call before any stream capture.
+ *     (cudaGetSymbolAddress) with that device current and caches it for the
+ *     life of the process; make that first call before any stream capture.
+ *     The cached address belongs to the device's primary context: after
+ *     cudaDeviceReset, or when the calling thread runs under another context
+ *     of the device, it is stale and this entry point must not be called.
  *   - All calls on a device share the one array and it keeps the last call's
  *     contents (nothing in it needs to start at zero: every call writes the
  *     tables and partials it reads). Calls that overlap on the GPU -- on

@@ -30,7 +30,7 @@ class PagedAttentionError(RuntimeError):
 class _Options(C.Structure):
     _fields_ = [("max_chunk_tokens", C.c_int32), ("tc_min_rows", C.c_int32),
                 ("num_sms", C.c_int32), ("tc_pair", C.c_int32), ("tc_decode", C.c_int32),
-                ("reserved", C.c_int32 * 3)]
+                ("wait_limit_ns", C.c_int32), ("reserved", C.c_int32 * 2)]
 
 
 class _Stats(C.Structure):
@@ -224,13 +224,15 @@ class Plan:
 
     def __init__(self, context_lens, query_lens, Hq: int, Hkv: int, D: int, block_size: int,
                  max_blocks_per_seq: int, max_chunk_tokens: int = 0, tc_min_rows: int = 0,
-                 num_sms: int = 0, tc_pair: int = 0, tc_decode: int = 0):
+                 num_sms: int = 0, tc_pair: int = 0, tc_decode: int = 0,
+                 wait_limit_ns: int = 0):
         import numpy as np
         self._cl = np.ascontiguousarray(np.asarray(context_lens, dtype=np.int32))
         self._ql = np.ascontiguousarray(np.asarray(query_lens, dtype=np.int32))
         if self._cl.shape != self._ql.shape or self._cl.ndim != 1:
             raise ValueError("context_lens and query_lens must be 1-D of equal length")
-        opts = _Options(max_chunk_tokens, tc_min_rows, num_sms, tc_pair, tc_decode)
+        opts = _Options(max_chunk_tokens, tc_min_rows, num_sms, tc_pair, tc_decode,
+                        wait_limit_ns)
         handle = C.c_void_p()
         ws = C.c_size_t(0)
         self._h = None

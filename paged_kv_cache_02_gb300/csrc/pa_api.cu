@@ -14,6 +14,7 @@
 #include <string.h>
 
 #include <algorithm>
+#include <atomic>
 #include <cmath>
 #include <mutex>
 #include <new>
@@ -39,6 +40,21 @@ int* device_error_word() {
     cache[dev] = static_cast<int*>(p);
   }
   return cache[dev];
+}
+
+int sm_count() {
+  static std::atomic<int> cache[64];
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) { cudaGetLastError(); return 0; }
+  if (dev < 0 || dev >= 64) return 0;
+  int sms = cache[dev].load(std::memory_order_relaxed);
+  if (sms > 0) return sms;
+  if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) {
+    cudaGetLastError();
+    return 0;
+  }
+  cache[dev].store(sms, std::memory_order_relaxed);
+  return sms;
 }
 
 // ------------------------------------------------------------------ tensor maps
@@ -132,6 +148,7 @@ struct pa_plan_s {
   int64_t total_q;
   int32_t n_dec, n_tc, n_tc2, n_tcd, n_groups;
   int32_t dec_rows_max;
+  uint64_t wait_ns;         // bound on each pipeline wait of the kernels
   int64_t n_part_rows;
   int32_t chunk;
   int64_t kv_tokens;
@@ -197,15 +214,7 @@ void pinned_give(const PinnedBuf& b) {
 bool is_pow2(int x) { return x > 0 && (x & (x - 1)) == 0; }
 size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
-int device_sms() {
-  int dev = 0, sms = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess) { cudaGetLastError(); return 0; }
-  if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) {
-    cudaGetLastError();
-    return 0;
-  }
-  return sms;
-}
+int device_sms() { return pa::sm_count(); }
 
 // Kernel a work item runs on (the path number pa_plan_export reports).
 enum Path : int { kPathDec = 0, kPathTc = 1, kPathTcPair = 2, kPathTcDecode = 3 };
@@ -402,15 +411,16 @@ pa_status pa_plan_create(const int32_t* h_context_lens, const int32_t* h_query_l
   memset(&o, 0, sizeof o);
   if (opts) {
     o = *opts;
-    for (int i = 0; i < 3; ++i)
+    for (int i = 0; i < 2; ++i)
       if (o.reserved[i]) return PA_ERR_INVALID_ARG;
+    if (o.wait_limit_ns < 0) return PA_ERR_INVALID_ARG;
   }
   const int g = Hq / Hkv;
   int64_t total_q = 0, kv_tokens = 0;
   for (int32_t s = 0; s < num_seqs; ++s) {
     const int32_t L = h_context_lens[s], q = h_query_lens[s];
     if (L < 0 || q < 0 || q > L) return PA_ERR_RANGE;
-    if ((int64_t)(L + block_size - 1) / block_size > max_blocks_per_seq) return PA_ERR_RANGE;
+    if (((int64_t)L + block_size - 1) / block_size > max_blocks_per_seq) return PA_ERR_RANGE;
     total_q += q;
     kv_tokens += L;
   }
@@ -550,6 +560,7 @@ pa_status pa_plan_create(const int32_t* h_context_lens, const int32_t* h_query_l
   p->n_tcd = (int32_t)tcd.size();
   p->n_groups = (int32_t)groups.size();
   p->dec_rows_max = dec_rows_max; p->n_part_rows = part_rows;
+  p->wait_ns = o.wait_limit_ns > 0 ? (uint64_t)o.wait_limit_ns : pa::kWaitLimitNsHost;
   p->chunk = any_split ? (int32_t)chunk : 0; p->kv_tokens = kv_tokens;
   size_t off = 0;
   p->off_dec = off; off = align_up(off + dec.size() * sizeof(Item), 256);
@@ -738,6 +749,7 @@ static pa_status attention_impl(pa_plan_t p, void* d_out, pa_dtype out_dtype, co
   a.part_acc = reinterpret_cast<float*>(ws + p->off_acc);
   a.part_ml = reinterpret_cast<float*>(ws + p->off_ml);
   a.err = err;
+  a.wait_ns = p->wait_ns;
 
   if (p->n_dec > 0) {
     const int box_t = std::min(p->block_size, pa::kKeyTile);

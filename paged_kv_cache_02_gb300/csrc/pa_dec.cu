@@ -183,7 +183,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (it + 2 * G < n_items) item_after = items[it + 2 * G];
       }
       for (int t0 = cur.kv_begin; t0 < cur.kv_end; t0 += kKeyTile) {
-        ok = mbar_wait_warp(&sm.empty[stage], phase ^ 1u, a.err);
+        ok = mbar_wait_warp(&sm.empty[stage], phase ^ 1u, a.err, a.wait_ns);
         if (!ok || *(volatile int*)&sm.abort_flag) { ok = false; break; }
         // pieces lane and lane + 32 of this stage (a stage has at most 64 pieces)
         auto locate = [&](int pc, int& tok) -> bool {
@@ -290,7 +290,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int e = 0; e < 8; ++e) acc[r][e] = 0.f;
 
       for (int t0 = item.kv_begin; t0 < kv_end; t0 += kKeyTile) {
-        const bool got = mbar_wait_warp(&sm.full[stage], phase, a.err);
+        const bool got = mbar_wait_warp(&sm.full[stage], phase, a.err, a.wait_ns);
         if (!got) { alive = false; break; }
         if (warp == 0 && lane == 0) sm.consumed[stage] += 1;
         if (t0 == item.kv_begin) {

@@ -44,6 +44,7 @@ constexpr double kTcMachineBalance = 280.0;
 constexpr int kTcdRows = 16;    // rows of a key-major tensor-core decode item (N)
 constexpr int kKeyTile = 64;    // keys per pipeline stage of the decode kernel
 constexpr int kChunkAlign = 64;   // split-KV chunk boundaries are multiples of this
+constexpr uint64_t kWaitLimitNsHost = 1000000000ull;  // default bound on a pipeline wait
 
 // Common launch arguments of the attention kernels.
 struct AttnArgs {
@@ -61,10 +62,15 @@ struct AttnArgs {
   float* part_acc;            // [n_partial_rows, D]: unnormalised sum of p * v
   float* part_ml;             // [n_partial_rows, 2]: running max (log2 domain) and sum of p
   int* err;                   // device error word
+  uint64_t wait_ns;           // bound on each pipeline wait (ns)
 };
 
 // Device address of the error word of the current device (set up once per device).
 int* device_error_word();
+
+// Number of SMs of the current device (queried once per device, then cached); 0 if the
+// query fails.
+int sm_count();
 
 // Builds a 3-D tiled tensor map over a pool viewed as [num_blocks * B][Hkv][D] bf16.
 // box = (box_d, 1, box_t); swizzle128 selects the 128-byte swizzle.

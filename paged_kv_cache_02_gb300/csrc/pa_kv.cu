@@ -168,13 +168,8 @@ __global__ void __launch_bounds__(kCopyThreads) swap_blocks_kernel(
 }
 
 int copy_grid(int64_t n_vec) {
-  static int sms = 0;
-  if (sms == 0) {
-    int dev = 0;
-    cudaGetDevice(&dev);
-    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-    if (sms <= 0) sms = 1;
-  }
+  int sms = sm_count();  // of the current device
+  if (sms <= 0) sms = 1;
   const int64_t want = (n_vec + (int64_t)kCopyThreads * kCopyUnroll - 1) /
                        ((int64_t)kCopyThreads * kCopyUnroll);
   const int64_t cap = (int64_t)sms * 8;  // 8 resident 256-thread CTAs per SM

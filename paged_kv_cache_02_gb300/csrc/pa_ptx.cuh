@@ -55,16 +55,20 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
   return done != 0;
 }
 
-// Waits for the phase with the given parity to complete. Gives up after
-// about one second, records PA_DEVERR_TIMEOUT and returns false.
+// Waits for the phase with the given parity to complete. Gives up after limit_ns
+// (default about one second), records PA_DEVERR_TIMEOUT and returns false. The
+// pipeline waits of the attention kernels take the call's limit (AttnArgs::wait_ns);
+// the waits of an abort path (for the CTA's own copies and MMAs in flight) always
+// take the default, so that nothing the CTA issued is still running when it exits.
 constexpr uint64_t kWaitLimitNs = 1000000000ull;
-__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, int* err) {
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, int* err,
+                                          uint64_t limit_ns = kWaitLimitNs) {
   const uint32_t a = smem_addr(bar);
   if (mbar_try_wait(a, parity)) return true;
   const uint64_t t0 = global_timer_ns();
   while (true) {
     if (mbar_try_wait(a, parity)) return true;
-    if (global_timer_ns() - t0 > kWaitLimitNs) {
+    if (global_timer_ns() - t0 > limit_ns) {
       record_error(err, PA_DEVERR_TIMEOUT);
       return false;
     }
@@ -74,8 +78,9 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, int* e
 // mbar_wait executed by every lane of a warp, with one verdict for the whole warp:
 // warp-collective instructions that follow (shuffles, ballots, tcgen05.ld / st)
 // then never see a warp split by a wait that ran out in some lanes only.
-__device__ __forceinline__ bool mbar_wait_warp(uint64_t* bar, uint32_t parity, int* err) {
-  return __all_sync(0xffffffffu, mbar_wait(bar, parity, err));
+__device__ __forceinline__ bool mbar_wait_warp(uint64_t* bar, uint32_t parity, int* err,
+                                               uint64_t limit_ns = kWaitLimitNs) {
+  return __all_sync(0xffffffffu, mbar_wait(bar, parity, err, limit_ns));
 }
 
 // 3-D tiled TMA load into shared memory, completing on `bar` (tx bytes).

@@ -178,10 +178,10 @@ struct SoftmaxThread {
 };
 
 // Meets the other softmax warps: red[x % 2][quad][*] written before, read after.
-__device__ __forceinline__ bool meet(TcdSmem& sm, SoftmaxThread& th, int* err) {
+__device__ __forceinline__ bool meet(TcdSmem& sm, SoftmaxThread& th, const AttnArgs& a) {
   tc::fence_before_sync();
   mbar_arrive(&sm.xbar);
-  const bool r = mbar_wait_warp(&sm.xbar, th.x & 1u, err);
+  const bool r = mbar_wait_warp(&sm.xbar, th.x & 1u, a.err, a.wait_ns);
   ++th.x;
   tc::fence_after_sync();
   return r;
@@ -210,7 +210,7 @@ __device__ bool softmax_item(TcdSmem& sm, const AttnArgs& a, const Item& item, i
     const int key = item.kv_begin + j * kKeys + th.kl;
     // ---- scores of this thread's key for the rows; the buffer is free again after
     float s[NR];
-    if (!mbar_wait_warp(&sm.s_full[b], ph(n, 2), a.err)) return false;
+    if (!mbar_wait_warp(&sm.s_full[b], ph(n, 2), a.err, a.wait_ns)) return false;
     tc::fence_after_sync();
     tmem_ld_rows<NR>(th.t_lane + (uint32_t)b * kN, s);
     tc::fence_before_sync();
@@ -230,7 +230,7 @@ __device__ bool softmax_item(TcdSmem& sm, const AttnArgs& a, const Item& item, i
         reinterpret_cast<float*>(sm.red[th.x & 1][th.quad])[(th.lane >> sh) & (NR - 1)] = v[0];
     }
     const uint32_t xb = th.x & 1;
-    if (!meet(sm, th, a.err)) return false;
+    if (!meet(sm, th, a)) return false;
     float mt[NR];
     combine4<NR, true>(sm.red[xb], mt);
     float alpha[NR];
@@ -250,7 +250,7 @@ __device__ bool softmax_item(TcdSmem& sm, const AttnArgs& a, const Item& item, i
     // every thread saw the same maxima: the decision is uniform across the warps
     if (any_rescale) {
       // O^T must be idle: wait for the previous tile's P V
-      if (!mbar_wait_warp(&sm.o_tile[(n - 1) & 1], ph(n - 1, 2), a.err)) return false;
+      if (!mbar_wait_warp(&sm.o_tile[(n - 1) & 1], ph(n - 1, 2), a.err, a.wait_ns)) return false;
       tc::fence_after_sync();
       float o[NR];
       tmem_ld_rows<NR>(th.t_lane + kColO, o);
@@ -270,7 +270,7 @@ __device__ bool softmax_item(TcdSmem& sm, const AttnArgs& a, const Item& item, i
       l_part[r] += p[r];
     }
     // P^T buffer b is free once the P V of tile n - 2 is done
-    if (!mbar_wait_warp(&sm.p_free[b], ph(n, 2) ^ 1u, a.err)) return false;
+    if (!mbar_wait_warp(&sm.p_free[b], ph(n, 2) ^ 1u, a.err, a.wait_ns)) return false;
     {
       // the even lane of a pair writes rows 0..H-1 for keys (kl, kl + 1), the odd lane
       // rows H..NR-1; K-major, 128-byte swizzle: row r, key k at key half k / 64,
@@ -308,12 +308,12 @@ __device__ bool softmax_item(TcdSmem& sm, const AttnArgs& a, const Item& item, i
       reinterpret_cast<float*>(sm.red[th.x & 1][th.quad])[(th.lane >> sh) & (NR - 1)] = v[0];
   }
   const uint32_t xb = th.x & 1;
-  if (!meet(sm, th, a.err)) return false;
+  if (!meet(sm, th, a)) return false;
   float l_row[NR];
   combine4<NR, false>(sm.red[xb], l_row);
   // the item's last P V (its phase is at most one ahead: see the phase bounds)
   const int n_last = th.n - 1;
-  if (!mbar_wait_warp(&sm.o_tile[n_last & 1], ph(n_last, 2), a.err)) return false;
+  if (!mbar_wait_warp(&sm.o_tile[n_last & 1], ph(n_last, 2), a.err, a.wait_ns)) return false;
   tc::fence_after_sync();
   float o[NR];
   tmem_ld_rows<NR>(th.t_lane + kColO, o);
@@ -425,7 +425,7 @@ __global__ void __launch_bounds__(kThreadsD, 1)
       // half. Buffer k % 2 is free once the issuer issued every S^T of item k - 2.
       {
         const int qb = k & 1;
-        ok = mbar_wait_warp(&sm.q_free[qb], ph(k, 2) ^ 1u, a.err);
+        ok = mbar_wait_warp(&sm.q_free[qb], ph(k, 2) ^ 1u, a.err, a.wait_ns);
         if (!ok || *(volatile int*)&sm.abort_flag) { ok = false; break; }
         if (lane == 0) {
           mbar_arrive_expect_tx(&sm.q_full[qb], 2u * kQHalf);
@@ -459,7 +459,7 @@ __global__ void __launch_bounds__(kThreadsD, 1)
         const uint32_t tile_bytes = __popc(__ballot_sync(0xffffffffu, valid)) * piece_bytes * 2u;
         const uint32_t piece_off = (uint32_t)lane * box_t * 256u;  // whole groups
         // K_n: its stage is free once S^T of tile n - 3 is done
-        ok = mbar_wait_warp(&sm.k_empty[st], ph(n, kStages) ^ 1u, a.err);
+        ok = mbar_wait_warp(&sm.k_empty[st], ph(n, kStages) ^ 1u, a.err, a.wait_ns);
         if (!ok || *(volatile int*)&sm.abort_flag) { ok = false; break; }
         if (lane == 0) mbar_arrive_expect_tx(&sm.k_full[st], tile_bytes);
         __syncwarp();
@@ -467,7 +467,7 @@ __global__ void __launch_bounds__(kThreadsD, 1)
           tma_load_5d(&sm.k[st][piece_off], &kmap, &sm.k_full[st], 0, 0, 0, tok >> 3, item.kv_head);
         if (lane == 0) sm.k_issued[st] += 1;
         // V_n: free once P V of tile n - 3 is done
-        ok = mbar_wait_warp(&sm.v_empty[st], ph(n, kStages) ^ 1u, a.err);
+        ok = mbar_wait_warp(&sm.v_empty[st], ph(n, kStages) ^ 1u, a.err, a.wait_ns);
         if (!ok || *(volatile int*)&sm.abort_flag) { ok = false; break; }
         if (lane == 0) mbar_arrive_expect_tx(&sm.v_full[st], tile_bytes);
         __syncwarp();
@@ -610,7 +610,7 @@ __global__ void __launch_bounds__(kThreadsD, 1)
         }
         if (progress) {
           t_idle = global_timer_ns();
-        } else if (global_timer_ns() - t_idle > kWaitLimitNs) {
+        } else if (global_timer_ns() - t_idle > a.wait_ns) {
           record_error(a.err, PA_DEVERR_TIMEOUT);
           ok = false;
           break;

@@ -50,10 +50,16 @@ def oracle_step(w, orc=None):
     return dict(slots=slots, k_pool=kp, v_pool=vp)
 
 
+def oracle_threads():
+    return max(1, os.cpu_count() or 1)
+
+
 def oracle_rows(w, ref, rows=None, orc=None):
     orc = orc or oracle.default()
-    return orc.attention(u16(w.q), ref["k_pool"], ref["v_pool"], w.block_table, w.context_lens,
-                         w.query_lens, rows=rows, n_threads=max(1, min(16, os.cpu_count() or 1)))
+    if "q_bits" not in ref:
+        ref["q_bits"] = u16(w.q)
+    return orc.attention(ref["q_bits"], ref["k_pool"], ref["v_pool"], w.block_table,
+                         w.context_lens, w.query_lens, rows=rows, n_threads=oracle_threads())
 
 
 def pools_equal(gpu_pool: torch.Tensor, ref_pool: np.ndarray) -> bool:
@@ -70,6 +76,38 @@ def assert_attention_close(got, want, what=""):
     mx, mn = attn_errors(got, want)
     assert mx <= ATOL_MAX and mn <= ATOL_MEAN, f"{what}: max abs {mx:.3g}, mean abs {mn:.3g}"
     return mx, mn
+
+
+def compare_all_rows(got_out, w, ref, what, chunk=4096):
+    """Every query row of ``got_out`` (device or host tensor [T, Hq, D]) against the
+    oracle, in chunks of rows so that host memory stays bounded; returns (max abs, mean
+    abs, rows) over all rows and asserts the attention tolerance. When the environment
+    names a report file (PA_PARITY_REPORT), one JSON line per call is appended to it."""
+    import json
+    import time
+    T = w.total_q
+    got = got_out.float().cpu().numpy()
+    assert np.all(np.isfinite(got)), f"{what}: non-finite outputs"
+    mx, tot, n = 0.0, 0.0, 0
+    t0 = time.perf_counter()
+    orc = oracle.default()
+    for r0 in range(0, T, chunk):
+        rows = np.arange(r0, min(T, r0 + chunk), dtype=np.int64)
+        want = oracle_rows(w, ref, rows, orc=orc)
+        d = np.abs(got[rows].astype(np.float64) - want)
+        mx = max(mx, float(d.max()))
+        tot += float(d.sum())
+        n += d.size
+    mean = tot / max(1, n)
+    dt = time.perf_counter() - t0
+    path = os.environ.get("PA_PARITY_REPORT")
+    if path:
+        with open(path, "a") as f:
+            f.write(json.dumps({"what": what, "rows": T, "values": n, "max_abs": mx,
+                                "mean_abs": mean, "oracle_s": dt,
+                                "threads": oracle_threads()}) + "\n")
+    assert mx <= ATOL_MAX and mean <= ATOL_MEAN, f"{what}: max abs {mx:.3g}, mean abs {mean:.3g}"
+    return mx, mean, T
 
 
 def sample_rows(w, n, seed):

@@ -27,7 +27,7 @@ def _golden(name):
 
 def u16(t: torch.Tensor) -> np.ndarray:
     """bf16 tensor -> uint16 bit patterns (a copy)."""
-    return t.detach().cpu().contiguous().view(torch.int16).numpy().view(np.uint16).copy()
+    return workloads.host_bits(t)
 
 
 def bf16_bits(x) -> np.ndarray:

@@ -65,6 +65,7 @@ def plan(pa, L, q, Hq=4, Hkv=4, D=64, B=16, **kw):
     (dict(Hq=6, Hkv=4), 2),                        # heads not a multiple
     (dict(D=96), 4),                               # head dim not built
     (dict(B=12), 4),                               # block size not a power of two
+    (dict(wait_limit_ns=-5), 1),                   # a negative wait bound
 ])
 def test_plan_rejects(pa, bad, status):
     args = dict(L=[5, 9], q=[1, 2], Hq=4, Hkv=4, D=64, B=16)
@@ -75,6 +76,22 @@ def test_plan_rejects(pa, bad, status):
     with pytest.raises(pa.PagedAttentionError) as e:
         plan(pa, L, q, **args)
     assert e.value.status == status
+
+
+def test_plan_options_reserved_must_be_zero(pa):
+    import ctypes as C
+    from paged_kv_cache_02_gb300 import _binding as b
+    opts = b._Options(0, 0, 0, 0, 0, 1000)
+    opts.reserved[1] = 7
+    cl = (C.c_int32 * 1)(9)
+    ql = (C.c_int32 * 1)(1)
+    h, ws = C.c_void_p(), C.c_size_t(0)
+    assert b._lib().pa_plan_create(cl, ql, 1, 4, 4, 64, 16, 1, C.byref(opts), C.byref(h),
+                                   C.byref(ws)) == 1
+    opts.reserved[1] = 0
+    assert b._lib().pa_plan_create(cl, ql, 1, 4, 4, 64, 16, 1, C.byref(opts), C.byref(h),
+                                   C.byref(ws)) == 0
+    assert b._lib().pa_plan_destroy(h) == 0
 
 
 def test_plan_rejects_short_table(pa):

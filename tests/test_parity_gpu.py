@@ -459,6 +459,8 @@ def test_write_kv_skip_and_range(pa):
 
 
 def test_cow_config_copies_bit_exact(pa):
+    """Config 5cow (the fork step): 224 copy-on-write block copies, then the KV write,
+    bit-exact on both whole pools; attention compared with the oracle on every row."""
     w = workloads.make("5cow", device="cuda")
     got = gu.gpu_step(pa, w)
     ref = gu.oracle_step(w)
@@ -466,13 +468,15 @@ def test_cow_config_copies_bit_exact(pa):
     assert np.array_equal(got["slots"], ref["slots"])
     assert gu.pools_equal(got["k_pool"], ref["k_pool"])
     assert gu.pools_equal(got["v_pool"], ref["v_pool"])
-    rows = gu.sample_rows(w, 48, seed=5)
-    gu.assert_attention_close(got["out"].cpu().numpy()[rows], gu.oracle_rows(w, ref, rows), w.name)
+    gu.compare_all_rows(got["out"], w, ref, w.name)
 
 
 @pytest.mark.parametrize("config", [2, 3, 4, 5])
 def test_full_size_configs(pa, config):
-    """The bench's workloads at full size: bit-exact pools, sampled attention rows."""
+    """The bench's workloads at full size, in the plan the bench times: slot maps and
+    both whole pools bit-exact, and attention compared with the fp64 oracle on EVERY
+    query row and head (config 3: about 48.6k rows x 40 heads), so that every work item
+    of every kernel -- every persistent CTA round and barrier phase -- is checked."""
     w = workloads.make(config, device="cuda")
     got = gu.gpu_step(pa, w)
     assert got["err"] == 0
@@ -480,11 +484,5 @@ def test_full_size_configs(pa, config):
     assert np.array_equal(got["slots"], ref["slots"])
     assert gu.pools_equal(got["k_pool"], ref["k_pool"])
     assert gu.pools_equal(got["v_pool"], ref["v_pool"])
-    rows = gu.sample_rows(w, 64, seed=config)
-    for name, seqs in w.groups.items():
-        pref = np.concatenate([[0], np.cumsum(w.query_lens)])
-        extra = [int(pref[s]) for s in seqs[:4]] + [int(pref[s + 1] - 1) for s in seqs[-4:]]
-        rows = np.unique(np.concatenate([rows, np.array(extra, np.int64)]))
-    out = got["out"].cpu().numpy()[rows]
-    gu.assert_attention_close(out, gu.oracle_rows(w, ref, rows), w.name)
-    assert torch.isfinite(got["out"]).all()
+    del got["k_pool"], got["v_pool"]
+    gu.compare_all_rows(got["out"], w, ref, w.name)

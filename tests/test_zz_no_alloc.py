@@ -49,8 +49,10 @@ def test_static_workspace_matches_caller_workspace_on_two_calls(pa):
         got = pa.pa_attention_static(plan, **x)
         torch.cuda.synchronize()
         assert pa.pa_get_device_error(reset=True) == 0
-        d = (got - ref).abs()
-        assert float(d.max()) <= gu.ATOL_MAX and float(d.mean()) <= gu.ATOL_MEAN
+        # the same plan and kernels on the same inputs: only the scratch's address
+        # differs, so the outputs must agree bit for bit (stale tables or partials left
+        # in the shared array by the previous call would show here)
+        assert torch.equal(got, ref)
         if kw:
             assert plan.stats()["n_split_groups"] > 0
 

@@ -19,7 +19,7 @@ from dataclasses import dataclass, field
 import numpy as np
 import torch
 
-__all__ = ["Workload", "make", "make_custom", "CONFIG_NAMES", "CONFIG_IDS"]
+__all__ = ["Workload", "make", "make_custom", "host_bits", "CONFIG_NAMES", "CONFIG_IDS"]
 
 CONFIG_NAMES = {
     1: "tiny mixed batch: 4 seqs, Hq=Hkv=4, D=64, B=16",
@@ -105,6 +105,12 @@ class Workload:
 
 
 # ----------------------------------------------------------------- helpers
+
+def host_bits(t: torch.Tensor) -> np.ndarray:
+    """A bf16 tensor as a host array of its uint16 bit patterns (a copy): the form in
+    which the CPU-side consumers of these inputs take bf16 values."""
+    return t.detach().cpu().contiguous().view(torch.int16).numpy().view(np.uint16).copy()
+
 
 def _cdiv(a, b):
     return -(-a // b)
