@@ -569,8 +569,8 @@ def configs_sweep(args, w_head, dev):
     head = args.config
     for cfg in [1, 2, 3, 4, 5, "5cow"]:
         key = f"cfg{cfg}"
-        w = w_head if str(cfg) == str(head) and not args.subset else \
-            workloads.make(cfg, device=dev)
+        w = w_head if str(cfg) == str(head) and not args.subset and not args.contiguous \
+            and args.block_size is None else workloads.make(cfg, device=dev)
         bar = {2: [("hbm", 0.70)], 5: [("hbm", 0.70)], "5cow": [("hbm", 0.70)]}.get(cfg)
         add(key, w, bar)
         if cfg in (3, 4):
@@ -583,6 +583,26 @@ def configs_sweep(args, w_head, dev):
             del w
             gc.collect()
             torch.cuda.empty_cache()
+    # Pensieve's kernel microbenchmark (Fig. 12): the multi-token kernels on the
+    # prefill sub-batches with paged blocks against the same draw with every sequence's
+    # blocks consecutive, each kernel forced in turn
+    pvc = {}
+    for cfg in (3, 4):
+        wp = w_head if str(cfg) == str(head) and not args.subset and not args.contiguous \
+            and args.block_size is None else workloads.make(cfg, device=dev)
+        wc = workloads.make(cfg, device=dev, contiguous=True)
+        for kern, pair in (("tc_kernel", -1), ("tc2_kernel", 1)):
+            a_ms, _ = time_attention(wp.subset(wp.groups["prefill_seqs"]), dev, tc_pair=pair)
+            b_ms, _ = time_attention(wc.subset(wc.groups["prefill_seqs"]), dev, tc_pair=pair)
+            pvc[f"cfg{cfg}_prefill_{kern}"] = {"paged_ms": a_ms, "contiguous_ms": b_ms,
+                                               "paged_over_contiguous": a_ms / b_ms}
+            log(f"paged vs contiguous: cfg{cfg} prefill {kern}: {a_ms:.4f} / {b_ms:.4f} ms")
+        del wc
+        if wp is not w_head:
+            del wp
+        gc.collect()
+        torch.cuda.empty_cache()
+    res["paged_vs_contiguous"] = pvc
     res["_note"] = ("attention kernels of one planned call (tables uploaded once), CUDA "
                     "events over 30 calls after 5 warm-up calls; frac = roofline time / "
                     "measured; bar: decode-dominated >= 0.70 of HBM, prefill-dominated >= "
@@ -715,9 +735,9 @@ def main():
     ap.add_argument("--max-seqs", type=int, default=None,
                     help="keep only the first N sequences (profiler captures of config 2)")
     ap.add_argument("--block-size", type=int, default=None,
-                    help="block-size sweep: config 2 with another block size")
+                    help="block-size sweep: config 2 or 4 with another block size")
     ap.add_argument("--contiguous", action="store_true",
-                    help="block-size sweep: config 2 with each sequence's blocks consecutive")
+                    help="config 2, 3 or 4 with each sequence's blocks consecutive")
     args = ap.parse_args()
     args.warmup = max(3, args.warmup)
     args.config_key = f"cfg{args.config}"

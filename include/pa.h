@@ -242,6 +242,49 @@ pa_status pa_attention_planned(pa_plan_t plan, void* d_out, pa_dtype out_dtype,
                                const int32_t* d_query_lens, int32_t num_blocks, float scale,
                                void* d_workspace, size_t workspace_bytes, void* stream);
 
+/* ---------------------------------------------------------------- fused write + attention
+ * The step's KV write and its attention in one call (vLLM-SOSP23 note, "core method",
+ * kernel layer: the new tokens' reshape and block write fused with the block read and
+ * attention; Pensieve summary, unified prefill and generation: the new tokens' K/V are
+ * stored in their slots, then every query attends to its whole context). For the batch
+ * shape vLLM and Pensieve run, where a step's new tokens are exactly its query tokens,
+ *   pa_attention_write(plan, out, q, k_new, v_new, slot_mapping, ...)
+ * has the effect of
+ *   pa_write_kv(k_new, v_new, slot_mapping, total_q, ...); pa_attention(plan, out, q, ...)
+ * with:
+ *   d_k_new, d_v_new  [total_q, Hkv, D] bf16, device, 16-byte aligned: row r is the K/V
+ *                     of query row r (same order as q);
+ *   d_slot_mapping    int64 [total_q], device: the slot of row r's position, i.e.
+ *                     block_table[s][p / B] * B + p % B, or -1 to skip the row's write.
+ * Sequences whose rows go to the key-major kernel (at most 16 packed rows per KV head:
+ * decode) have their K/V written inside that kernel, just before it loads the tile
+ * holding them, so the write costs no launch and no separate pass; the other rows are
+ * written by one write kernel launched first. Writes are bit-exact copies. Requirements
+ * beyond pa_write_kv's and pa_attention's: a slot that a decode row writes is read in
+ * this call only by that row's sequence (what copy-on-write guarantees: a block being
+ * written is held by one sequence); Pensieve's sub-requests that read another
+ * sub-request's new tokens may share blocks, which is safe here as long as the writing
+ * sub-request has more than 16 packed rows per KV head (it then goes through the write
+ * kernel), and otherwise needs pa_write_kv + pa_attention. Slot range errors are
+ * recorded as PA_DEVERR_SLOT_RANGE, as in pa_write_kv.
+ * pa_attention_write_planned is the same without the table upload (see
+ * pa_attention_planned); the planned call reads the per-row write flags the upload
+ * left in the workspace. */
+pa_status pa_attention_write(pa_plan_t plan, void* d_out, pa_dtype out_dtype, const void* d_q,
+                             const void* d_k_new, const void* d_v_new,
+                             const int64_t* d_slot_mapping, void* d_k_pool, void* d_v_pool,
+                             const int32_t* d_block_table, const int32_t* d_context_lens,
+                             const int32_t* d_query_lens, int32_t num_blocks, float scale,
+                             void* d_workspace, size_t workspace_bytes, void* stream);
+pa_status pa_attention_write_planned(pa_plan_t plan, void* d_out, pa_dtype out_dtype,
+                                     const void* d_q, const void* d_k_new, const void* d_v_new,
+                                     const int64_t* d_slot_mapping, void* d_k_pool,
+                                     void* d_v_pool, const int32_t* d_block_table,
+                                     const int32_t* d_context_lens,
+                                     const int32_t* d_query_lens, int32_t num_blocks,
+                                     float scale, void* d_workspace, size_t workspace_bytes,
+                                     void* stream);
+
 /* ---------------------------------------------------------------- no-alloc variant
  * The pages have no counterpart to this entry point; it exists for callers
  * that cannot allocate device memory for a workspace. A serving engine

@@ -71,6 +71,9 @@ def _lib() -> C.CDLL:
         lib.pa_plan_upload.argtypes = [_P, _P, C.c_size_t, _P]
         lib.pa_attention_planned.argtypes = [_P, _P, C.c_int, _P, _P, _P, _P, _P, _P, _I32,
                                              C.c_float, _P, C.c_size_t, _P]
+        for f in ("pa_attention_write", "pa_attention_write_planned"):
+            getattr(lib, f).argtypes = [_P, _P, C.c_int, _P, _P, _P, _P, _P, _P, _P, _P, _P,
+                                        _I32, C.c_float, _P, C.c_size_t, _P]
         lib.pa_swap_blocks.argtypes = [_P, _P, _I32, _P, _P, _I32, _P, _P, _I32, _I32, _I32,
                                        _I32, _I32, _P]
         lib.pa_bm_create.argtypes = [_I32, _I32, _P, C.POINTER(_P)]
@@ -92,7 +95,8 @@ def _lib() -> C.CDLL:
         for f in ("pa_get_device_error", "pa_slot_mapping", "pa_write_kv", "pa_copy_blocks",
                   "pa_plan_create", "pa_plan_destroy", "pa_plan_get_stats", "pa_plan_export",
                   "pa_attention", "pa_attention_static", "pa_plan_upload",
-                  "pa_attention_planned", "pa_swap_blocks", "pa_bm_create", "pa_bm_destroy", "pa_bm_add",
+                  "pa_attention_planned", "pa_attention_write", "pa_attention_write_planned",
+                  "pa_swap_blocks", "pa_bm_create", "pa_bm_destroy", "pa_bm_add",
                   "pa_bm_fork", "pa_bm_free", "pa_bm_append", "pa_bm_tables",
                   "pa_bm_seq_info", "pa_bm_refcount", "pa_bm_num_free",
                   "pa_bm_set_host_pool", "pa_bm_swap_out", "pa_bm_swap_in",
@@ -330,6 +334,57 @@ def pa_attention(plan: Plan, q: torch.Tensor, k_pool: torch.Tensor, v_pool: torc
     fn = "pa_attention" if _upload else "pa_attention_planned"
     _check(getattr(_lib(), fn)(plan._h, _dev(out, out.dtype, "out", 3), dt,
                                _dev(q, torch.bfloat16, "q", 3),
+                               _dev(k_pool, torch.bfloat16, "k_pool", 4),
+                               _dev(v_pool, torch.bfloat16, "v_pool", 4),
+                               _dev(block_table, torch.int32, "block_table", 2),
+                               _dev(context_lens, torch.int32, "context_lens", 1),
+                               _dev(query_lens, torch.int32, "query_lens", 1), nb, float(scale),
+                               workspace.data_ptr(), workspace.numel(), _stream(q)), fn)
+    return out
+
+
+def pa_attention_write(plan: Plan, q: torch.Tensor, k_new: torch.Tensor, v_new: torch.Tensor,
+                       slot_mapping: torch.Tensor, k_pool: torch.Tensor, v_pool: torch.Tensor,
+                       block_table: torch.Tensor, context_lens: torch.Tensor,
+                       query_lens: torch.Tensor, out: torch.Tensor | None = None,
+                       out_dtype=torch.float32, scale: float = 0.0,
+                       workspace: torch.Tensor | None = None,
+                       planned: bool = False) -> torch.Tensor:
+    """Fused KV write + attention: the K/V of the step's query tokens (``k_new``,
+    ``v_new`` [total_q, Hkv, D] in q's row order) go to ``slot_mapping`` [total_q] (int64)
+    and every query row attends to its whole context, as pa_write_kv followed by
+    pa_attention. ``planned``: the workspace already holds this plan's tables
+    (pa_plan_upload)."""
+    nb, B, Hkv, D = k_pool.shape
+    if (Hkv, D, B) != (plan.Hkv, plan.D, plan.block_size):
+        raise ValueError("pool shape does not match the plan")
+    if q.dim() != 3 or q.shape[1:] != (plan.Hq, D) or q.shape[0] != plan.total_q:
+        raise ValueError("q must be [total_q, Hq, D] as planned")
+    if k_new.shape != (plan.total_q, Hkv, D) or v_new.shape != k_new.shape:
+        raise ValueError("k_new / v_new must be [total_q, Hkv, D]")
+    if slot_mapping.shape != (plan.total_q,):
+        raise ValueError("slot_mapping must be [total_q]")
+    if block_table.dim() != 2 or block_table.shape[1] != plan.max_blocks_per_seq:
+        raise ValueError("block_table must be [num_seqs, max_blocks_per_seq] as planned")
+    if out is None:
+        out = torch.empty(q.shape, dtype=out_dtype, device=q.device)
+    dt = {torch.float32: PA_F32, torch.bfloat16: PA_BF16}.get(out.dtype)
+    if dt is None:
+        raise TypeError("out must be float32 or bfloat16")
+    if out.shape != q.shape:
+        raise ValueError("out must be shaped like q")
+    if workspace is None:
+        if planned:
+            raise ValueError("a planned call needs the workspace the tables were uploaded to")
+        workspace = plan.workspace(q.device)
+    if workspace.data_ptr() % 256:
+        raise ValueError("workspace must be 256-byte aligned")
+    fn = "pa_attention_write_planned" if planned else "pa_attention_write"
+    _check(getattr(_lib(), fn)(plan._h, _dev(out, out.dtype, "out", 3), dt,
+                               _dev(q, torch.bfloat16, "q", 3),
+                               _dev(k_new, torch.bfloat16, "k_new", 3),
+                               _dev(v_new, torch.bfloat16, "v_new", 3),
+                               _dev(slot_mapping, torch.int64, "slot_mapping", 1),
                                _dev(k_pool, torch.bfloat16, "k_pool", 4),
                                _dev(v_pool, torch.bfloat16, "v_pool", 4),
                                _dev(block_table, torch.int32, "block_table", 2),

@@ -14,6 +14,7 @@
 #include <string.h>
 
 #include <algorithm>
+#include <utility>
 #include <atomic>
 #include <cmath>
 #include <mutex>
@@ -153,7 +154,9 @@ struct pa_plan_s {
   int32_t chunk;
   int64_t kv_tokens;
   // workspace layout (byte offsets)
-  size_t off_dec, off_tc, off_tc2, off_tcd, off_groups, off_acc, off_ml, ws_bytes;
+  size_t off_dec, off_tc, off_tc2, off_tcd, off_groups, off_wmask, off_acc, off_ml, ws_bytes;
+  int64_t n_fused_rows;     // rows whose K/V the key-major kernel writes in a fused call
+  bool wmask;               // the tables hold a per-row byte: 1 = written in that kernel
   size_t table_bytes;       // bytes of the item / group tables (copied each call)
   void* host_tables;        // table image: [dec][tc][tc pair items][groups] at their offsets
   bool host_pinned;
@@ -226,12 +229,19 @@ struct Unit {
 
 }  // namespace
 
+// The new tokens' K/V of a fused write + attention call (null: attention only).
+struct FusedWrite {
+  const void* k_new;       // [total_q, Hkv, D] bf16, device
+  const void* v_new;
+  const int64_t* slots;    // [total_q], device
+};
+
 static pa_status attention_impl(pa_plan_t p, void* d_out, pa_dtype out_dtype, const void* d_q,
                                 const void* d_k_pool, const void* d_v_pool,
                                 const int32_t* d_block_table, const int32_t* d_context_lens,
                                 const int32_t* d_query_lens, int32_t num_blocks, float scale,
                                 void* d_workspace, size_t workspace_bytes, void* stream,
-                                bool upload);
+                                bool upload, const FusedWrite* fw = nullptr);
 
 // Marks the stream position after a copy from the plan's pinned table buffer, so that the
 // buffer is handed to a later plan only once the copy has completed.
@@ -464,6 +474,8 @@ pa_status pa_plan_create(const int32_t* h_context_lens, const int32_t* h_query_l
   // of 256 (two 128-row halves sharing every K/V tile) while more than 128 rows remain,
   // the rest in one 128-row tile; without, all in 128-row tiles.
   std::vector<Unit> units;
+  std::vector<std::pair<int64_t, int32_t>> fused_runs;  // (first row, rows): key-major seqs
+  int64_t n_fused_rows = 0;
   int64_t total_keys = 0;
   int64_t q_row0 = 0;
   for (int32_t s = 0; s < num_seqs; ++s) {
@@ -471,6 +483,10 @@ pa_status pa_plan_create(const int32_t* h_context_lens, const int32_t* h_query_l
     if (q > 0) {
       const int64_t rows = (int64_t)q * g;
       const bool tc = tc_enabled && rows >= tc_min_rows;
+      if (tc && tcd_enabled && rows <= pa::kTcdRows) {
+        fused_runs.push_back({q_row0, q});
+        n_fused_rows += q;
+      }
       for (int32_t kvh = 0; kvh < Hkv; ++kvh) {
         for (int64_t rb = 0; rb < rows;) {
           const int64_t left = rows - rb;
@@ -568,6 +584,11 @@ pa_status pa_plan_create(const int32_t* h_context_lens, const int32_t* h_query_l
   p->off_tc2 = off; off = align_up(off + tc2.size() * sizeof(Item), 256);
   p->off_tcd = off; off = align_up(off + tcd.size() * sizeof(Item), 256);
   p->off_groups = off; off = align_up(off + groups.size() * sizeof(SplitGroup), 256);
+  // per-row byte for the fused KV write, needed only when some rows are written by the
+  // key-major kernel and some by the write kernel
+  p->n_fused_rows = n_fused_rows;
+  p->wmask = n_fused_rows > 0 && n_fused_rows < total_q;
+  p->off_wmask = off; off = align_up(off + (p->wmask ? (size_t)total_q : 0), 256);
   p->table_bytes = off;
   p->off_acc = off; off = align_up(off + (size_t)part_rows * D * sizeof(float), 256);
   p->off_ml = off; off = align_up(off + (size_t)part_rows * 2 * sizeof(float), 256);
@@ -601,6 +622,8 @@ pa_status pa_plan_create(const int32_t* h_context_lens, const int32_t* h_query_l
     if (!tcd.empty()) memcpy(h + p->off_tcd, tcd.data(), tcd.size() * sizeof(Item));
     if (!groups.empty())
       memcpy(h + p->off_groups, groups.data(), groups.size() * sizeof(SplitGroup));
+    if (p->wmask)
+      for (const auto& r : fused_runs) memset(h + p->off_wmask + r.first, 1, (size_t)r.second);
   }
   *out = p;
   *workspace_bytes = p->ws_bytes;
@@ -699,6 +722,32 @@ pa_status pa_attention_planned(pa_plan_t p, void* d_out, pa_dtype out_dtype, con
                         workspace_bytes, stream, false);
 }
 
+pa_status pa_attention_write(pa_plan_t p, void* d_out, pa_dtype out_dtype, const void* d_q,
+                             const void* d_k_new, const void* d_v_new,
+                             const int64_t* d_slot_mapping, void* d_k_pool, void* d_v_pool,
+                             const int32_t* d_block_table, const int32_t* d_context_lens,
+                             const int32_t* d_query_lens, int32_t num_blocks, float scale,
+                             void* d_workspace, size_t workspace_bytes, void* stream) {
+  const FusedWrite fw{d_k_new, d_v_new, d_slot_mapping};
+  return attention_impl(p, d_out, out_dtype, d_q, d_k_pool, d_v_pool, d_block_table,
+                        d_context_lens, d_query_lens, num_blocks, scale, d_workspace,
+                        workspace_bytes, stream, true, &fw);
+}
+
+pa_status pa_attention_write_planned(pa_plan_t p, void* d_out, pa_dtype out_dtype,
+                                     const void* d_q, const void* d_k_new, const void* d_v_new,
+                                     const int64_t* d_slot_mapping, void* d_k_pool,
+                                     void* d_v_pool, const int32_t* d_block_table,
+                                     const int32_t* d_context_lens,
+                                     const int32_t* d_query_lens, int32_t num_blocks,
+                                     float scale, void* d_workspace, size_t workspace_bytes,
+                                     void* stream) {
+  const FusedWrite fw{d_k_new, d_v_new, d_slot_mapping};
+  return attention_impl(p, d_out, out_dtype, d_q, d_k_pool, d_v_pool, d_block_table,
+                        d_context_lens, d_query_lens, num_blocks, scale, d_workspace,
+                        workspace_bytes, stream, false, &fw);
+}
+
 }  // extern "C"
 
 // Arguments are checked before anything is enqueued; then the plan's tables are
@@ -708,12 +757,17 @@ static pa_status attention_impl(pa_plan_t p, void* d_out, pa_dtype out_dtype, co
                                 const int32_t* d_block_table, const int32_t* d_context_lens,
                                 const int32_t* d_query_lens, int32_t num_blocks, float scale,
                                 void* d_workspace, size_t workspace_bytes, void* stream,
-                                bool upload) {
+                                bool upload, const FusedWrite* fw) {
   if (!p) return PA_ERR_INVALID_ARG;
   if (out_dtype != PA_F32 && out_dtype != PA_BF16) return PA_ERR_INVALID_ARG;
   if (num_blocks <= 0) return PA_ERR_INVALID_ARG;
   if ((int64_t)num_blocks * p->block_size > INT32_MAX) return PA_ERR_UNSUPPORTED;
   if (p->total_q == 0) return PA_OK;
+  if (fw) {
+    if (!fw->k_new || !fw->v_new || !fw->slots) return PA_ERR_INVALID_ARG;
+    if (reinterpret_cast<uintptr_t>(fw->k_new) % 16 || reinterpret_cast<uintptr_t>(fw->v_new) % 16)
+      return PA_ERR_UNSUPPORTED;
+  }
   if (!d_out || !d_q || !d_k_pool || !d_v_pool || !d_block_table || !d_context_lens ||
       !d_query_lens || !d_workspace)
     return PA_ERR_INVALID_ARG;
@@ -750,6 +804,28 @@ static pa_status attention_impl(pa_plan_t p, void* d_out, pa_dtype out_dtype, co
   a.part_ml = reinterpret_cast<float*>(ws + p->off_ml);
   a.err = err;
   a.wait_ns = p->wait_ns;
+  a.k_new = nullptr;
+  a.v_new = nullptr;
+  a.slots = nullptr;
+  a.n_slots = (int64_t)num_blocks * p->block_size;
+  a.k_pool = static_cast<uint4*>(const_cast<void*>(d_k_pool));
+  a.v_pool = static_cast<uint4*>(const_cast<void*>(d_v_pool));
+  if (fw) {
+    // rows the key-major kernel does not write go through the write kernel first
+    if (p->n_fused_rows < p->total_q) {
+      const uint8_t* skip = p->wmask ? ws + p->off_wmask : nullptr;
+      cudaError_t e = pa::launch_write_kv(fw->k_new, fw->v_new, fw->slots, p->total_q,
+                                          const_cast<void*>(d_k_pool),
+                                          const_cast<void*>(d_v_pool), a.n_slots,
+                                          (int64_t)p->Hkv * p->D * 2, err, s, skip);
+      if (e != cudaSuccess) return PA_ERR_CUDA;
+    }
+    if (p->n_fused_rows > 0) {
+      a.k_new = static_cast<const uint4*>(fw->k_new);
+      a.v_new = static_cast<const uint4*>(fw->v_new);
+      a.slots = fw->slots;
+    }
+  }
 
   if (p->n_dec > 0) {
     const int box_t = std::min(p->block_size, pa::kKeyTile);

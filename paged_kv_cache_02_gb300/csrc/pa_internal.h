@@ -63,6 +63,16 @@ struct AttnArgs {
   float* part_ml;             // [n_partial_rows, 2]: running max (log2 domain) and sum of p
   int* err;                   // device error word
   uint64_t wait_ns;           // bound on each pipeline wait (ns)
+  // Fused KV write (null k_new: none). The step's new tokens are its query tokens:
+  // k_new / v_new [total_q, Hkv, D] bf16 in q's row order, slots [total_q] the slot of
+  // each token's position (-1: skip). The key-major kernel writes the tokens of its
+  // items before it reads them.
+  const uint4* k_new;
+  const uint4* v_new;
+  const int64_t* slots;
+  int64_t n_slots;            // num_blocks * block_size
+  uint4* k_pool;              // the pools, for those writes
+  uint4* v_pool;
 };
 
 // Device address of the error word of the current device (set up once per device).
@@ -88,9 +98,12 @@ cudaError_t launch_slot_mapping(const int32_t* bt, int32_t num_seqs, int32_t max
                                 int32_t block_size, int32_t num_blocks, const int32_t* seq_ids,
                                 const int32_t* positions, int64_t n, int64_t* slots, int* err,
                                 cudaStream_t s);
+// skip (optional, device, one byte per row): rows with a non-zero byte are not written
+// here (the fused attention call writes them inside the key-major kernel).
 cudaError_t launch_write_kv(const void* k_new, const void* v_new, const int64_t* slots,
                             int64_t n_new, void* k_pool, void* v_pool, int64_t n_slots,
-                            int64_t row_bytes, int* err, cudaStream_t s);
+                            int64_t row_bytes, int* err, cudaStream_t s,
+                            const uint8_t* skip = nullptr);
 cudaError_t launch_copy_blocks(void* k_pool, void* v_pool, const int32_t* src, const int32_t* dst,
                                int32_t n_pairs, int32_t num_blocks, int64_t block_bytes, int* err,
                                cudaStream_t s);

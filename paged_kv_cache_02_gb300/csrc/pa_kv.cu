@@ -54,11 +54,13 @@ constexpr int kCopyUnroll = 4;
 
 // Moves `n_vec` 16-byte vectors of token rows: vector i is chunk i % vec_per_row of
 // row i / vec_per_row. Source rows are contiguous; the destination row comes
-// from the slot list. K and V are moved by the same thread.
+// from the slot list. K and V are moved by the same thread. Rows whose entry in
+// `skip` (optional, one byte per row) is non-zero are left to another kernel.
 __global__ void __launch_bounds__(kCopyThreads) write_kv_kernel(
     const uint4* __restrict__ k_new, const uint4* __restrict__ v_new,
     const int64_t* __restrict__ slots, int64_t n_vec, int64_t vec_per_row,
-    uint4* __restrict__ k_pool, uint4* __restrict__ v_pool, int64_t n_slots, int* err) {
+    uint4* __restrict__ k_pool, uint4* __restrict__ v_pool, int64_t n_slots,
+    const uint8_t* __restrict__ skip, int* err) {
   const int64_t stride = (int64_t)gridDim.x * kCopyThreads;
   for (int64_t base = blockIdx.x * (int64_t)kCopyThreads + threadIdx.x; base < n_vec;
        base += stride * kCopyUnroll) {
@@ -70,7 +72,7 @@ __global__ void __launch_bounds__(kCopyThreads) write_kv_kernel(
       dst[u] = -1;
       if (i < n_vec) {
         const int64_t row = i / vec_per_row;
-        const int64_t slot = __ldg(slots + row);
+        const int64_t slot = (skip && __ldg(skip + row)) ? -1 : __ldg(slots + row);
         if (slot >= n_slots) {
           record_error(err, PA_DEVERR_SLOT_RANGE);
         } else if (slot >= 0) {
@@ -192,13 +194,14 @@ cudaError_t launch_slot_mapping(const int32_t* bt, int32_t num_seqs, int32_t max
 
 cudaError_t launch_write_kv(const void* k_new, const void* v_new, const int64_t* slots,
                             int64_t n_new, void* k_pool, void* v_pool, int64_t n_slots,
-                            int64_t row_bytes, int* err, cudaStream_t s) {
+                            int64_t row_bytes, int* err, cudaStream_t s,
+                            const uint8_t* skip) {
   const int64_t vec_per_row = row_bytes / 16;
   const int64_t n_vec = n_new * vec_per_row;
   if (n_vec == 0) return cudaSuccess;
   write_kv_kernel<<<copy_grid(n_vec), kCopyThreads, 0, s>>>(
       static_cast<const uint4*>(k_new), static_cast<const uint4*>(v_new), slots, n_vec,
-      vec_per_row, static_cast<uint4*>(k_pool), static_cast<uint4*>(v_pool), n_slots, err);
+      vec_per_row, static_cast<uint4*>(k_pool), static_cast<uint4*>(v_pool), n_slots, skip, err);
   return cudaGetLastError();
 }
 

@@ -55,15 +55,46 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
   return done != 0;
 }
 
+// Non-suspending probe of the phase with the given parity.
+__device__ __forceinline__ bool mbar_test_wait(uint32_t bar, uint32_t parity) {
+  uint32_t done;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(done)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return done != 0;
+}
+
 // Waits for the phase with the given parity to complete. Gives up after limit_ns
 // (default about one second), records PA_DEVERR_TIMEOUT and returns false. The
 // pipeline waits of the attention kernels take the call's limit (AttnArgs::wait_ns);
 // the waits of an abort path (for the CTA's own copies and MMAs in flight) always
 // take the default, so that nothing the CTA issued is still running when it exits.
+// try_wait may suspend the thread for a hardware-chosen while before it reports a
+// phase still open, so a bound shorter than kShortWaitNs polls with the
+// non-suspending probe instead, which keeps such a bound exact (it exists to test
+// the timeout path).
 constexpr uint64_t kWaitLimitNs = 1000000000ull;
+constexpr uint64_t kShortWaitNs = 100000ull;
+// the short-bound path, kept out of line: it never runs in a normal call
+static __device__ __noinline__ bool mbar_wait_short(uint32_t a, uint32_t parity, int* err,
+                                             uint64_t limit_ns) {
+  const uint64_t t0 = global_timer_ns();
+  while (!mbar_test_wait(a, parity)) {
+    if (global_timer_ns() - t0 > limit_ns) {
+      record_error(err, PA_DEVERR_TIMEOUT);
+      return false;
+    }
+  }
+  return true;
+}
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, int* err,
                                           uint64_t limit_ns = kWaitLimitNs) {
   const uint32_t a = smem_addr(bar);
+  if (limit_ns < kShortWaitNs) return mbar_wait_short(a, parity, err, limit_ns);
   if (mbar_try_wait(a, parity)) return true;
   const uint64_t t0 = global_timer_ns();
   while (true) {

@@ -436,9 +436,50 @@ __global__ void __launch_bounds__(kThreadsD, 1)
         }
         __syncwarp();
       }
+      // Fused KV write (vLLM-SOSP23 note, kernel layer: the new tokens' reshape and block
+      // write fused with the attention that reads them): the item's new tokens -- the
+      // sequence's query tokens whose positions fall in its key range -- are copied to
+      // their slots for this KV head, 16-byte vectors spread over the lanes. They are
+      // read only by this item (no other item of the call covers these positions of
+      // this KV head), so ordering the copies before the TMA loads of the tile that
+      // holds them is enough: a proxy fence by every writing lane, then the warp
+      // barrier, before that tile is issued.
+      int first_new = item.kv_end;               // first position this item wrote
+      if (a.k_new != nullptr) {
+        const int L = __ldg(a.context_lens + item.seq);
+        const int ql = __ldg(a.query_lens + item.seq);
+        const int p0 = max(item.kv_begin, L - ql), p1 = min(item.kv_end, L);
+        if (p0 < p1) {
+          first_new = p0;
+          const int64_t vec_row = (int64_t)a.Hkv * (kD / 8);   // 16-byte vectors per token
+          const int64_t head_off = (int64_t)item.kv_head * (kD / 8);
+          const int64_t row0 = (int64_t)item.q_row0 + (p0 - (L - ql));
+          for (int v = lane; v < (p1 - p0) * (kD / 8); v += 32) {
+            const int64_t row = row0 + v / (kD / 8);
+            const int c = v % (kD / 8);
+            const int64_t slot = __ldg(a.slots + row);
+            if (slot >= a.n_slots) {
+              record_error(a.err, PA_DEVERR_SLOT_RANGE);
+            } else if (slot >= 0) {
+              const int64_t from = row * vec_row + head_off + c;
+              const int64_t to = slot * vec_row + head_off + c;
+              const uint4 kx = __ldg(a.k_new + from), vx = __ldg(a.v_new + from);
+              a.k_pool[to] = kx;
+              a.v_pool[to] = vx;
+            }
+          }
+        }
+      }
+      bool fence_due = first_new < item.kv_end;
       const int32_t* bt = a.block_table + (int64_t)item.seq * a.max_blocks;
       for (int t0 = item.kv_begin; t0 < item.kv_end; t0 += kKeys, ++n) {
         const int st = n % kStages;
+        if (fence_due && t0 + kKeys > first_new) {
+          // the generic-proxy copies above, before the async-proxy (TMA) reads below
+          asm volatile("fence.proxy.async.global;" ::: "memory");
+          __syncwarp();
+          fence_due = false;
+        }
         bool valid = false;
         int tok = 0;
         if (lane < pieces) {

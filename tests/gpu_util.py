@@ -19,8 +19,9 @@ def lib():
     return pa
 
 
-def gpu_step(pa, w, dev="cuda", out_dtype=torch.float32, **plan_kw):
-    """slot mapping -> copy-on-write copies -> KV write -> attention, all through libpa."""
+def gpu_step(pa, w, dev="cuda", out_dtype=torch.float32, fused=False, **plan_kw):
+    """slot mapping -> copy-on-write copies -> KV write -> attention, all through libpa
+    (``fused``: the KV write and the attention in one pa_attention_write call)."""
     bt = torch.from_numpy(w.block_table).to(dev)
     cl = torch.from_numpy(w.context_lens).to(dev)
     ql = torch.from_numpy(w.query_lens).to(dev)
@@ -31,10 +32,16 @@ def gpu_step(pa, w, dev="cuda", out_dtype=torch.float32, **plan_kw):
     if len(w.cow_src):
         pa.pa_copy_blocks(kp, vp, torch.from_numpy(w.cow_src).to(dev),
                           torch.from_numpy(w.cow_dst).to(dev))
-    pa.pa_write_kv(w.k_new.to(dev), w.v_new.to(dev), slots, kp, vp)
     plan = pa.Plan(w.context_lens, w.query_lens, w.Hq, w.Hkv, w.D, w.block_size, w.max_blocks,
                    **plan_kw)
-    out = pa.pa_attention(plan, w.q.to(dev), kp, vp, bt, cl, ql, out_dtype=out_dtype)
+    if fused:
+        # the step's new tokens are its query tokens, in q's row order
+        assert len(w.new_seq) == w.total_q
+        out = pa.pa_attention_write(plan, w.q.to(dev), w.k_new.to(dev), w.v_new.to(dev), slots,
+                                    kp, vp, bt, cl, ql, out_dtype=out_dtype)
+    else:
+        pa.pa_write_kv(w.k_new.to(dev), w.v_new.to(dev), slots, kp, vp)
+        out = pa.pa_attention(plan, w.q.to(dev), kp, vp, bt, cl, ql, out_dtype=out_dtype)
     err = pa.pa_get_device_error(reset=True)
     return dict(slots=slots.cpu().numpy(), k_pool=kp, v_pool=vp, out=out, err=err, plan=plan)
 

@@ -486,3 +486,50 @@ def test_full_size_configs(pa, config):
     assert gu.pools_equal(got["v_pool"], ref["v_pool"])
     del got["k_pool"], got["v_pool"]
     gu.compare_all_rows(got["out"], w, ref, w.name)
+
+
+FUSED_CASES = {
+    "config1": lambda: workloads.make(1),
+    # decode rows of g = 4 with split keys: the new tokens straddle 64-key chunk
+    # boundaries, so several chunk items of one (sequence, KV head) each write theirs
+    "split_straddle": lambda: workloads.make_custom([190, 257, 66, 1000, 4], [3, 4, 2, 1, 4],
+                                                    Hq=16, Hkv=4, D=128, block_size=16,
+                                                    seed=611),
+    # decode rows beside one-tile and two-tile rows: the write kernel skips the rows the
+    # key-major kernel writes
+    "mixed_paths": lambda: workloads.make_custom([300, 700, 40, 900, 129], [1, 200, 40, 2, 100],
+                                                 Hq=8, Hkv=2, D=128, block_size=32, seed=612),
+}
+
+
+@pytest.mark.parametrize("case", list(FUSED_CASES))
+def test_fused_write_attention(pa, case):
+    """pa_attention_write = pa_write_kv + pa_attention: both whole pools bit-exact against
+    the oracle's write, every attention row within tolerance, the output bit-identical to
+    the unfused pair of calls, and the same with split keys forced."""
+    w = FUSED_CASES[case]()
+    for kw in (dict(), dict(max_chunk_tokens=64)):
+        got = gu.gpu_step(pa, w, fused=True, **kw)
+        ref = gu.oracle_step(w)
+        assert got["err"] == 0, f"device error {pa.DEVERR.get(got['err'])}"
+        assert gu.pools_equal(got["k_pool"], ref["k_pool"]), "K pool differs after the write"
+        assert gu.pools_equal(got["v_pool"], ref["v_pool"]), "V pool differs after the write"
+        gu.compare_all_rows(got["out"], w, ref, f"fused {case} {kw}")
+        base = gu.gpu_step(pa, w, **kw)
+        assert torch.equal(got["out"], base["out"])
+    if case != "config1":
+        assert got["plan"].stats()["n_tc_decode_items"] > 0
+
+
+@pytest.mark.parametrize("config", [2, 3, "5cow"])
+def test_fused_write_attention_full_size(pa, config):
+    """The fused call on the full-size decode, mixed and copy-on-write batches: pools
+    bit-exact, every row against the oracle."""
+    w = workloads.make(config, device="cuda")
+    got = gu.gpu_step(pa, w, fused=True)
+    assert got["err"] == 0
+    ref = gu.oracle_step(w)
+    assert gu.pools_equal(got["k_pool"], ref["k_pool"])
+    assert gu.pools_equal(got["v_pool"], ref["v_pool"])
+    del got["k_pool"], got["v_pool"]
+    gu.compare_all_rows(got["out"], w, ref, f"fused {w.name}")

@@ -253,7 +253,7 @@ def _cfg2(device, max_seqs=None, block_size=None, contiguous=False):
                    q_scale=1.0 / math.sqrt(D))
 
 
-def _cfg3(device):
+def _cfg3(device, contiguous=False):
     """64 conversations (history + new turn) as two sub-requests each, plus 128 decodes.
 
     Conversation c has ``hist`` cached tokens and ``qn`` new prompt tokens. Its
@@ -263,7 +263,9 @@ def _cfg3(device):
     from region 1. Sub-request A: context r, query r (the leading tokens attend
     to themselves). Sub-request B: context hist + qn, query qn (the new prompt
     attends to the whole context). Both rows of the block table list the same
-    physical blocks for the shared part.
+    physical blocks for the shared part. ``contiguous``: the same draw with each
+    conversation's (and decode sequence's) blocks at consecutive physical ids, for the
+    paged-against-contiguous comparison of the multi-token kernels.
     """
     seed = 1003
     g = torch.Generator().manual_seed(seed)
@@ -304,6 +306,13 @@ def _cfg3(device):
         row = np.full(max_blocks, -1, np.int32)
         row[:dec_blk[s]] = perm0[o0:o0 + dec_blk[s]]; o0 += dec_blk[s]
         dec_tables.append(row)
+    if contiguous:
+        off = 0
+        for row in conv_tables + dec_tables:
+            n = int((row >= 0).sum())
+            row[:n] = np.arange(off, off + n, dtype=np.int32)
+            off += n
+        assert off <= nb
     new_seq, new_pos = [], []
     for c in range(C):
         # sub-request A: the recomputed leading tokens
@@ -322,14 +331,19 @@ def _cfg3(device):
     bt = np.stack(bt_rows).astype(np.int32)
     groups = {"prefill_seqs": list(range(n_conv_rows)),
               "decode_seqs": list(range(n_conv_rows, len(rows_L)))}
-    return _finish(CONFIG_NAMES[3], seed, Hq, Hkv, D, B, nb, rows_L, rows_q, bt, new_seq,
+    name = CONFIG_NAMES[3] + (", contiguous blocks" if contiguous else "")
+    return _finish(name, seed, Hq, Hkv, D, B, nb, rows_L, rows_q, bt, new_seq,
                    new_pos, device, groups=groups)
 
 
-def _cfg4(device):
+def _cfg4(device, block_size=None, contiguous=False):
+    """GQA batch. ``block_size`` and ``contiguous`` give the same draw with another block
+    size or with each sequence's blocks at consecutive physical ids."""
     seed = 1004
     g = torch.Generator().manual_seed(seed)
     N, Hq, Hkv, D, B = 128, 64, 8, 128, 32
+    if block_size is not None:
+        B = int(block_size)
     z = torch.randn(N, generator=g, dtype=torch.float64).numpy()
     L = np.minimum(np.rint(np.exp(math.log(1500.0) + 0.5 * z)).astype(np.int64), 4096)
     is_prefill = torch.rand(N, generator=g, dtype=torch.float64).numpy() >= 0.7
@@ -339,10 +353,19 @@ def _cfg4(device):
     need = [_cdiv(int(l), B) for l in L]
     nb = int(math.ceil(1.1 * sum(need)))
     bt = _place(g, need, nb, max(need))
+    name = CONFIG_NAMES[4]
+    if B != 32:
+        name = name.replace("B=32", f"B={B}")
+    if contiguous:
+        off = 0
+        for s, n in enumerate(need):
+            bt[s, :n] = np.arange(off, off + n, dtype=np.int32)
+            off += n
+        name += ", contiguous blocks"
     seqs, pos = _last_tokens(L, ql)
     groups = {"prefill_seqs": [int(i) for i in np.nonzero(ql > 1)[0]],
               "decode_seqs": [int(i) for i in np.nonzero(ql == 1)[0]]}
-    return _finish(CONFIG_NAMES[4], seed, Hq, Hkv, D, B, nb, L, ql, bt, seqs, pos, device,
+    return _finish(name, seed, Hq, Hkv, D, B, nb, L, ql, bt, seqs, pos, device,
                    groups=groups)
 
 
@@ -400,19 +423,22 @@ def make(config, device="cpu", max_seqs=None, block_size=None, contiguous=False)
     """Workload for config 1..5 or "5cow", values drawn on ``device``.
 
     ``max_seqs`` keeps only the first sequences of the decode-only batch (config 2): the
-    same draw, smaller, for profiler captures that must stay small. ``block_size`` and
-    ``contiguous`` (config 2 only) give the block-size sweep's variants.
+    same draw, smaller, for profiler captures that must stay small. ``block_size``
+    (configs 2 and 4) and ``contiguous`` (configs 2, 3 and 4) give the block-size sweep's
+    and the paged-against-contiguous comparison's variants of the same draw.
     """
-    if (block_size is not None or contiguous) and config not in (2, "2"):
-        raise ValueError("block_size / contiguous variants exist for config 2 only")
+    if block_size is not None and config not in (2, "2", 4, "4"):
+        raise ValueError("block_size variants exist for configs 2 and 4 only")
+    if contiguous and config not in (2, "2", 3, "3", 4, "4"):
+        raise ValueError("contiguous variants exist for configs 2, 3 and 4 only")
     if config in (1, "1"):
         return _cfg1(device)
     if config in (2, "2"):
         return _cfg2(device, max_seqs, block_size, contiguous)
     if config in (3, "3"):
-        return _cfg3(device)
+        return _cfg3(device, contiguous)
     if config in (4, "4"):
-        return _cfg4(device)
+        return _cfg4(device, block_size, contiguous)
     if config in (5, "5"):
         return _cfg5(device, cow=False)
     if config == "5cow":
