@@ -285,7 +285,8 @@ def run_gpu(args, w, cfg_name, rank, local, world):
             pa.pa_copy_blocks(kp, vp, src, dst)
         if i is not None:
             ev["c"][i].record(stream)
-        pa.pa_write_kv(kn, vn, slots, kp, vp)
+        if args.unfused:
+            pa.pa_write_kv(kn, vn, slots, kp, vp)
         if i is not None:
             ev["d"][i].record(stream)
         # the plan's tables go up once per step (a model would share them across its
@@ -293,7 +294,13 @@ def run_gpu(args, w, cfg_name, rank, local, world):
         pa.pa_plan_upload(plan, ws)
         if i is not None:
             ev["f"][i].record(stream)
-        pa.pa_attention_planned(plan, q, kp, vp, bt, cl, ql, ws, out=out)
+        if args.unfused:
+            pa.pa_attention_planned(plan, q, kp, vp, bt, cl, ql, ws, out=out)
+        else:
+            # the KV write of the decode rows inside the key-major kernel, the other rows'
+            # write kernel first (the step's new tokens are its query tokens)
+            pa.pa_attention_write(plan, q, kn, vn, slots, kp, vp, bt, cl, ql, out=out,
+                                  workspace=ws, planned=True)
         if i is not None:
             ev["e"][i].record(stream)
 
@@ -326,6 +333,9 @@ def run_gpu(args, w, cfg_name, rank, local, world):
            for k, (a, b) in {"slot_mapping": ("a", "b"), "copy_blocks": ("b", "c"),
                              "write_kv": ("c", "d"), "attention": ("d", "e"),
                              "plan_upload": ("d", "f"), "attention_kernels": ("f", "e")}.items()}
+    if not args.unfused:
+        per["write_kv"] = "inside the attention call (fused): the decode rows in the " \
+                          "key-major kernel, the other rows in one write kernel first"
     err = pa.pa_get_device_error(reset=True)
     if err:
         raise RuntimeError(f"device error {pa.DEVERR.get(err, err)} in the timed region")
@@ -333,7 +343,9 @@ def run_gpu(args, w, cfg_name, rank, local, world):
     T = w.total_q
     value = T * args.steps * world / (elapsed_ms / 1000.0)
     n_tc1 = st["n_tc_items"] - st["n_tc_pair_items"] - st["n_tc_decode_items"]
-    launches_per_step = 1 + (1 if n_pairs else 0) + 1 + (1 if st["n_dec_items"] else 0) + \
+    st_write = 1 if (args.unfused or st["n_tc_decode_items"] == 0 or
+                     plan_fused_rows(w) < T) else 0
+    launches_per_step = 1 + (1 if n_pairs else 0) + st_write + (1 if st["n_dec_items"] else 0) + \
         (1 if n_tc1 else 0) + (1 if st["n_tc_pair_items"] else 0) + \
         (1 if st["n_tc_decode_items"] else 0) + (1 if st["n_split_groups"] else 0)
 
@@ -341,8 +353,11 @@ def run_gpu(args, w, cfg_name, rank, local, world):
     peaks = measured_peaks()
     kv_b, q_b, o_b = w.kv_bytes(), w.q_bytes(), T * w.Hq * w.D * out.element_size()
     flops = w.flops()
-    # the roofline is that of the attention kernels: their time without the table upload
-    attn_s = per["attention_kernels"] / 1000.0
+    # the roofline is that of the attention kernels: timed here on their own (one planned
+    # call per timed call, tables uploaded once), since the step's call also holds the
+    # write kernel of the non-decode rows
+    attn_ms, _ = time_attention(w, dev, **plan_kw)
+    attn_s = attn_ms / 1000.0
     hbm_peak = float(peaks["hbm_gbs"])
     tc_peak = float(peaks.get("bf16_tflops", 1900.0))
     t_hbm = (kv_b + q_b) / (hbm_peak * 1e9)
@@ -460,6 +475,9 @@ def run_gpu(args, w, cfg_name, rank, local, world):
         "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
         "config": cfg_name,
         "out_dtype": args.out,
+        "step_path": ("pa_write_kv + pa_attention_planned" if args.unfused else
+                      "pa_attention_write_planned (fused KV write + attention)"),
+        "attention_kernels_ms": attn_ms,
         "roofline": roof,
         "hbm_gbs_attention": (kv_b + q_b) / attn_s / 1e9,
         "tc_tflops_attention": flops / attn_s / 1e12,
@@ -482,6 +500,17 @@ def run_gpu(args, w, cfg_name, rank, local, world):
         line["block_manager"] = block_manager_host(w)
         line["cpu_baseline"] = cpu_baseline(args, w)
         print(json.dumps(line), flush=True)
+
+
+def plan_fused_rows(w):
+    """Query rows whose sequence has at most 16 packed rows per KV head (q * Hq / Hkv <=
+    16): the rows the fused call writes inside the key-major kernel (D = 128, block size
+    >= 8, Hq / Hkv dividing 16)."""
+    g = w.Hq // w.Hkv
+    if w.D != 128 or w.block_size < 8 or 16 % g:
+        return 0
+    q = w.query_lens.astype(int)
+    return int(q[q * g <= 16].sum())
 
 
 def roofline_entry(w, ms, peaks, out_bytes_per_elem=4):
@@ -717,6 +746,8 @@ def main():
     ap.add_argument("--impl", choices=["gb300", "reference"], default="gb300")
     ap.add_argument("--config", default="3",
                     help="workload: 1..5 or 5cow (default 3, the Pensieve-style mixed batch)")
+    ap.add_argument("--unfused", action="store_true",
+                    help="the step as pa_write_kv + pa_attention instead of the fused call")
     ap.add_argument("--no-configs", action="store_true",
                     help="skip the per-config attention sweep (key 'configs')")
     ap.add_argument("--cpu-budget", type=float, default=12.0)

@@ -140,11 +140,14 @@ typedef struct {
                                 Hq / Hkv dividing 128. */
   int32_t num_sms;           /* 0: query the current device */
   int32_t tc_pair;           /* >0: tensor-core rows go in 256-row items (two 128-row tiles
-                                per CTA sharing every K/V tile) while more than 128 rows
-                                remain; <0: 128-row items only; 0: default (automatic):
-                                256-row items when the batch's multi-token tensor-core
-                                work has fewer FLOPs per byte of K/V, Q and output than
-                                the GPU's machine balance (280), else 128-row items */
+                                per CTA sharing every K/V tile); <0: 128-row items only;
+                                0: default (automatic): 256-row items when the batch's
+                                multi-token tensor-core work has fewer FLOPs per byte of
+                                K/V, Q and output than the GPU's machine balance (280),
+                                else 128-row items. Rows that do not fill whole items
+                                form a sequence's first item (the rows that see the
+                                fewest keys); with 256-row items it is a 128-row item
+                                when it has at most 128 rows */
   int32_t tc_decode;         /* 0: default (on): a (sequence, KV head) pair with at most 16
                                 tensor-core rows runs with keys on the 128-row side (needs
                                 Hq / Hkv dividing 16); <0: never */

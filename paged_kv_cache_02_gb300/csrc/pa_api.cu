@@ -471,8 +471,13 @@ pa_status pa_plan_create(const int32_t* h_context_lens, const int32_t* h_query_l
   }
 
   // ---- units: (sequence, KV head, row tile). With pairs, tensor-core rows go in tiles
-  // of 256 (two 128-row halves sharing every K/V tile) while more than 128 rows remain,
-  // the rest in one 128-row tile; without, all in 128-row tiles.
+  // of 256 (two 128-row halves sharing every K/V tile), without in tiles of 128. A
+  // sequence's rows that do not fill whole tiles form its FIRST tile, not its last: the
+  // rows are causal, so the first rows see the fewest keys, and the partial tile (which
+  // costs a whole tile's K/V reads and MMAs per key) then runs over the shortest key
+  // range. Of n full tiles and r rows left over this reads n (T - r) keys fewer than
+  // putting the partial tile last (T the tile's rows; g = 1) -- for a sub-request that
+  // recomputes a context's leading tokens, about a third of its keys.
   std::vector<Unit> units;
   std::vector<std::pair<int64_t, int32_t>> fused_runs;  // (first row, rows): key-major seqs
   int64_t n_fused_rows = 0;
@@ -487,18 +492,21 @@ pa_status pa_plan_create(const int32_t* h_context_lens, const int32_t* h_query_l
         fused_runs.push_back({q_row0, q});
         n_fused_rows += q;
       }
+      const bool multi = tc && !(tcd_enabled && rows <= pa::kTcdRows);
+      const int64_t tile = use_pair ? 2 * pa::kTcRows : pa::kTcRows;
+      // rows of the leading partial tile (multiple of g, since tile is)
+      const int64_t lead = multi ? rows % tile : 0;
       for (int32_t kvh = 0; kvh < Hkv; ++kvh) {
         for (int64_t rb = 0; rb < rows;) {
           const int64_t left = rows - rb;
           int path, rt;
           if (!tc) {
             path = kPathDec; rt = pa::kDecRows;
-          } else if (tcd_enabled && rows <= pa::kTcdRows) {
+          } else if (!multi) {
             path = kPathTcDecode; rt = pa::kTcdRows;
-          } else if (use_pair && left > pa::kTcRows) {
-            path = kPathTcPair; rt = 2 * pa::kTcRows;
           } else {
-            path = kPathTc; rt = pa::kTcRows;
+            rt = (rb == 0 && lead > 0) ? (int)lead : (int)tile;
+            path = rt > pa::kTcRows ? kPathTcPair : kPathTc;
           }
           const int32_t rc = (int32_t)std::min<int64_t>(rt, left);
           const int32_t t_last = (int32_t)((rb + rc - 1) / g);

@@ -117,7 +117,7 @@ __device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t b
       : "memory");
 }
 
-template <int D, int RM>
+template <int D, int RM, bool kSW>
 __global__ void __launch_bounds__(kThreads, 1)
     decode_kernel(const __grid_constant__ AttnArgs a, const __grid_constant__ CUtensorMap kmap,
                   const __grid_constant__ CUtensorMap vmap, const Item* __restrict__ items,
@@ -183,7 +183,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (it + 2 * G < n_items) item_after = items[it + 2 * G];
       }
       for (int t0 = cur.kv_begin; t0 < cur.kv_end; t0 += kKeyTile) {
-        ok = mbar_wait_warp(&sm.empty[stage], phase ^ 1u, a.err, a.wait_ns);
+        ok = mbar_wait_warp(&sm.empty[stage], phase ^ 1u, a.err, wait_bound<kSW>(a));
         if (!ok || *(volatile int*)&sm.abort_flag) { ok = false; break; }
         // pieces lane and lane + 32 of this stage (a stage has at most 64 pieces)
         auto locate = [&](int pc, int& tok) -> bool {
@@ -290,7 +290,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int e = 0; e < 8; ++e) acc[r][e] = 0.f;
 
       for (int t0 = item.kv_begin; t0 < kv_end; t0 += kKeyTile) {
-        const bool got = mbar_wait_warp(&sm.full[stage], phase, a.err, a.wait_ns);
+        const bool got = mbar_wait_warp(&sm.full[stage], phase, a.err, wait_bound<kSW>(a));
         if (!got) { alive = false; break; }
         if (warp == 0 && lane == 0) sm.consumed[stage] += 1;
         if (t0 == item.kv_begin) {
@@ -534,10 +534,11 @@ cudaError_t launch_dec_t(const AttnArgs& a, const CUtensorMap& kmap, const CUten
                          const Item* items, int32_t n_items, int box_t, int grid,
                          cudaStream_t s) {
   const int smem = (int)sizeof(DecSmem<D, RM>) + 1024;
-  cudaError_t e = cudaFuncSetAttribute(decode_kernel<D, RM>,
-                                       cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  auto* k = a.wait_ns == kWaitLimitNsHost ? decode_kernel<D, RM, false>
+                                          : decode_kernel<D, RM, true>;
+  cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
-  decode_kernel<D, RM><<<grid, kThreads, smem, s>>>(a, kmap, vmap, items, n_items, box_t);
+  k<<<grid, kThreads, smem, s>>>(a, kmap, vmap, items, n_items, box_t);
   return cudaGetLastError();
 }
 

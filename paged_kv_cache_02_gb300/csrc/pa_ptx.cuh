@@ -106,6 +106,16 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, int* e
   }
 }
 
+// Bound of a kernel's pipeline waits. The kernels are built twice: with kShortWaits
+// false the bound is the compile-time default (the build every normal call runs); with
+// true it is the call's bound (AttnArgs::wait_ns), selected only by a plan whose wait
+// bound differs from the default -- the tests of the timeout path.
+template <bool kShortWaits, class Args>
+__device__ __forceinline__ uint64_t wait_bound(const Args& a) {
+  if constexpr (kShortWaits) return a.wait_ns;
+  else return kWaitLimitNs;
+}
+
 // mbar_wait executed by every lane of a warp, with one verdict for the whole warp:
 // warp-collective instructions that follow (shuffles, ballots, tcgen05.ld / st)
 // then never see a warp split by a wait that ran out in some lanes only.

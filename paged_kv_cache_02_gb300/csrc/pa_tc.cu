@@ -113,7 +113,7 @@ __device__ __forceinline__ int tiles_of(const Item& x) {
 // item k + kQBuf needs q_full(k + kQBuf) from here; the ring's empty barrier of tile
 // n + R (R stages) needs its full barrier of tile n + R from here. So no barrier is
 // ever two phases ahead of the waits below.
-template <bool kIsK>
+template <bool kIsK, bool kSW>
 __device__ __forceinline__ void produce(TcSmem& sm, const AttnArgs& a, const CUtensorMap& map,
                                         const CUtensorMap& qmap, const Item* __restrict__ items,
                                         int n_items, int box_t, int lane) {
@@ -157,7 +157,7 @@ __device__ __forceinline__ void produce(TcSmem& sm, const AttnArgs& a, const CUt
     if (kIsK) {
       // the item's 128 Q rows: tokens x the g heads of its KV head, one box per D half
       const int qb = k % kQBuf;
-      ok = mbar_wait_warp(&sm.q_free[qb], ph(k, kQBuf) ^ 1u, a.err, a.wait_ns);
+      ok = mbar_wait_warp(&sm.q_free[qb], ph(k, kQBuf) ^ 1u, a.err, wait_bound<kSW>(a));
       if (!ok || *(volatile int*)&sm.abort_flag) { ok = false; break; }
       if (lane == 0) {
         mbar_arrive_expect_tx(&sm.q_full[qb], 2u * kHalf);
@@ -190,7 +190,7 @@ __device__ __forceinline__ void produce(TcSmem& sm, const AttnArgs& a, const CUt
       }
       const uint32_t tile_bytes = __popc(__ballot_sync(0xffffffffu, valid)) * piece_bytes * 2u;
       // K_n is free once S of tile n - 2 completed, V_n once both halves' P V of it did
-      ok = mbar_wait_warp(&empty[st], ph(n, kStages) ^ 1u, a.err, a.wait_ns);
+      ok = mbar_wait_warp(&empty[st], ph(n, kStages) ^ 1u, a.err, wait_bound<kSW>(a));
       if (!ok || *(volatile int*)&sm.abort_flag) { ok = false; break; }
       if (lane == 0) mbar_arrive_expect_tx(&full[st], tile_bytes);
       __syncwarp();
@@ -210,6 +210,7 @@ __device__ __forceinline__ void produce(TcSmem& sm, const AttnArgs& a, const CUt
   if (!ok) sm.abort_flag = 1;
 }
 
+template <bool kSW>
 __global__ void __launch_bounds__(kThreadsTc, 1)
     tc_kernel(const __grid_constant__ AttnArgs a, const __grid_constant__ CUtensorMap kmap,
               const __grid_constant__ CUtensorMap vmap, const __grid_constant__ CUtensorMap qmap,
@@ -260,9 +261,9 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
   const uint32_t tmem = sm.tmem_base;
 
   if (warp == 0) {
-    produce<true>(sm, a, kmap, qmap, items, n_items, box_t, lane);
+    produce<true, kSW>(sm, a, kmap, qmap, items, n_items, box_t, lane);
   } else if (warp == 3) {
-    produce<false>(sm, a, vmap, qmap, items, n_items, box_t, lane);
+    produce<false, kSW>(sm, a, vmap, qmap, items, n_items, box_t, lane);
   } else if (warp == 1) {
     // ------------------------------------------------------------ S issuer
     // Phase bounds: q_full of item k + kQBuf needs q_free(k), committed here; k_full of
@@ -276,17 +277,17 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
         const int nt = nt_next;
         if (it + G < n_items) nt_next = tiles_of(items[it + G]);
         const int qb = k % kQBuf;
-        if (!mbar_wait(&sm.q_full[qb], ph(k, kQBuf), a.err, a.wait_ns)) { ok = false; break; }
+        if (!mbar_wait(&sm.q_full[qb], ph(k, kQBuf), a.err, wait_bound<kSW>(a))) { ok = false; break; }
         sm.q_consumed[qb] += 1;
         tc::fence_after_sync();
         const uint64_t qd = tc::smem_desc_sw128(smem_addr(&sm.q[qb][0][0]), 16, 1024);
         for (int j = 0; j < nt; ++j, ++n) {
           const int st = n % kKStages;
           const int b = n & 1;
-          if (!mbar_wait(&sm.k_full[st], ph(n, kKStages), a.err, a.wait_ns)) { ok = false; break; }
+          if (!mbar_wait(&sm.k_full[st], ph(n, kKStages), a.err, wait_bound<kSW>(a))) { ok = false; break; }
           sm.k_consumed[st] += 1;
           // the buffer's last readers, both halves' P V of tile n - 2, are done
-          if (!mbar_wait(&sm.s_free[b], ph(n, 2) ^ 1u, a.err, a.wait_ns)) { ok = false; break; }
+          if (!mbar_wait(&sm.s_free[b], ph(n, 2) ^ 1u, a.err, wait_bound<kSW>(a))) { ok = false; break; }
           tc::fence_after_sync();
           // S = Q K^T: 8 steps of 16 dims; step kk starts (kk / 4) D halves and
           // (kk % 4) 32-byte chunks into both operands
@@ -322,11 +323,11 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
         for (int j = 0; j < nt; ++j, ++n) {
           const int st = n % kVStages;
           const int b = n & 1;
-          if (!mbar_wait(&sm.v_full[st], ph(n, kVStages), a.err, a.wait_ns)) { ok = false; break; }
+          if (!mbar_wait(&sm.v_full[st], ph(n, kVStages), a.err, wait_bound<kSW>(a))) { ok = false; break; }
           sm.v_consumed[st] += 1;
           // at an item's first tile, O_0 and O_1 must have been read out by the previous
           // item's epilogue
-          if (j == 0 && !mbar_wait(&sm.o_free, ((uint32_t)k & 1u) ^ 1u, a.err, a.wait_ns)) {
+          if (j == 0 && !mbar_wait(&sm.o_free, ((uint32_t)k & 1u) ^ 1u, a.err, wait_bound<kSW>(a))) {
             ok = false;
             break;
           }
@@ -353,7 +354,7 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
           // the first 32 columns of that key half's scores.
           const uint64_t vd = tc::smem_desc_sw128(smem_addr(&sm.v[st][0][0]), kHalf, 1024);
           // half 0: keys 0..63 of the tile
-          if (!mbar_wait(&sm.p_full[b][0], ph(n, 2), a.err, a.wait_ns)) { ok = false; break; }
+          if (!mbar_wait(&sm.p_full[b][0], ph(n, 2), a.err, wait_bound<kSW>(a))) { ok = false; break; }
           tc::fence_after_sync();
           {
             const uint32_t pa = tmem + s_col(b);
@@ -370,7 +371,7 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
           }
           tc::commit(&sm.o_done[0][b]);
           // half 1: keys 64..127 of the tile
-          if (!mbar_wait(&sm.p_full[b][1], ph(n, 2), a.err, a.wait_ns)) { ok = false; break; }
+          if (!mbar_wait(&sm.p_full[b][1], ph(n, 2), a.err, wait_bound<kSW>(a))) { ok = false; break; }
           tc::fence_after_sync();
           if (kk_end > 4) {
             const uint32_t pa = tmem + s_col(b) + 64u;
@@ -443,7 +444,7 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
       float m_used = -INFINITY, l = 0.f;
       for (int j = 0; j < nt; ++j, ++n) {
         const int b = n & 1;
-        if (!mbar_wait_warp(&sm.s_full[b], ph(n, 2), a.err, a.wait_ns)) { ok = false; break; }
+        if (!mbar_wait_warp(&sm.s_full[b], ph(n, 2), a.err, wait_bound<kSW>(a))) { ok = false; break; }
         tc::fence_after_sync();
         const int k0 = item.kv_begin + j * kKeys + 64 * h;   // first key of this half
         const uint32_t s_addr = t_lane + s_col(b) + (uint32_t)(64 * h);
@@ -468,7 +469,7 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
           const bool need = m_new > m_used + kRescaleLog2;
           if (__any_sync(0xffffffffu, need)) {
             // O_h must be idle: the previous tile's P V of this half may still run
-            if (!mbar_wait_warp(&sm.o_done[h][(n - 1) & 1], ph(n - 1, 2), a.err, a.wait_ns)) {
+            if (!mbar_wait_warp(&sm.o_done[h][(n - 1) & 1], ph(n - 1, 2), a.err, wait_bound<kSW>(a))) {
               ok = false;
               break;
             }
@@ -533,10 +534,10 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
       sm.xm[xb][h][row] = m_used;
       sm.xl[xb][h][row] = l;
       mbar_arrive(&sm.xbar[quad]);
-      if (!mbar_wait_warp(&sm.xbar[quad], (uint32_t)k & 1u, a.err, a.wait_ns)) { ok = false; break; }
+      if (!mbar_wait_warp(&sm.xbar[quad], (uint32_t)k & 1u, a.err, wait_bound<kSW>(a))) { ok = false; break; }
       // both halves' last P V (each at most one phase ahead of this wait: see above)
-      if (!mbar_wait_warp(&sm.o_done[0][(n - 1) & 1], ph(n - 1, 2), a.err, a.wait_ns) ||
-          !mbar_wait_warp(&sm.o_done[1][(n - 1) & 1], ph(n - 1, 2), a.err, a.wait_ns)) {
+      if (!mbar_wait_warp(&sm.o_done[0][(n - 1) & 1], ph(n - 1, 2), a.err, wait_bound<kSW>(a)) ||
+          !mbar_wait_warp(&sm.o_done[1][(n - 1) & 1], ph(n - 1, 2), a.err, wait_bound<kSW>(a))) {
         ok = false;
         break;
       }
@@ -706,10 +707,10 @@ cudaError_t launch_tc(const AttnArgs& a, const CUtensorMap& kmap, const CUtensor
                       int32_t n_items, int box_t, int grid, cudaStream_t s) {
   if (n_items <= 0) return cudaSuccess;
   const int smem = tc_smem_bytes();
-  cudaError_t e =
-      cudaFuncSetAttribute(tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  auto* k = a.wait_ns == kWaitLimitNsHost ? tc_kernel<false> : tc_kernel<true>;
+  cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
-  tc_kernel<<<grid, kThreadsTc, smem, s>>>(a, kmap, vmap, qmap, omap, items, n_items, box_t);
+  k<<<grid, kThreadsTc, smem, s>>>(a, kmap, vmap, qmap, omap, items, n_items, box_t);
   return cudaGetLastError();
 }
 

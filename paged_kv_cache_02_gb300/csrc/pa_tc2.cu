@@ -109,6 +109,7 @@ __device__ __forceinline__ ItemWalk item_walk(int n_items) {
   return w;
 }
 
+template <bool kSW>
 __global__ void __launch_bounds__(kThreads2, 1)
     tc2_kernel(const __grid_constant__ AttnArgs a, const __grid_constant__ CUtensorMap kmap,
                const __grid_constant__ CUtensorMap vmap, const __grid_constant__ CUtensorMap qmap,
@@ -189,7 +190,7 @@ __global__ void __launch_bounds__(kThreads2, 1)
       // S: q_free then completed phase k - 1. It cannot be further ahead, since phase k
       // needs the Q load below.
       if (k > 0) {
-        ok = mbar_wait_warp(&sm.q_free, (uint32_t)(k - 1) & 1u, a.err, a.wait_ns);
+        ok = mbar_wait_warp(&sm.q_free, (uint32_t)(k - 1) & 1u, a.err, wait_bound<kSW>(a));
         if (!ok || *(volatile int*)&sm.abort_flag) { ok = false; break; }
       }
       if (lane == 0) {
@@ -231,7 +232,7 @@ __global__ void __launch_bounds__(kThreads2, 1)
         const uint32_t tile_bytes = __popc(__ballot_sync(0xffffffffu, valid)) * piece_bytes * 2u;
         const uint32_t row_off = (uint32_t)lane * box_t * 128u;
         // K_n: its stage is free once both chains' S of tile n - 2 completed
-        ok = mbar_wait_warp(&sm.k_empty[st], ph(n, kStages) ^ 1u, a.err, a.wait_ns);
+        ok = mbar_wait_warp(&sm.k_empty[st], ph(n, kStages) ^ 1u, a.err, wait_bound<kSW>(a));
         if (!ok || *(volatile int*)&sm.abort_flag) { ok = false; break; }
         if (lane == 0) mbar_arrive_expect_tx(&sm.k_full[st], tile_bytes);
         __syncwarp();
@@ -241,7 +242,7 @@ __global__ void __launch_bounds__(kThreads2, 1)
         }
         if (lane == 0) sm.k_issued[st] += 1;
         // V_n: free once both chains' P V of tile n - 2 completed
-        ok = mbar_wait_warp(&sm.v_empty[st], ph(n, kStages) ^ 1u, a.err, a.wait_ns);
+        ok = mbar_wait_warp(&sm.v_empty[st], ph(n, kStages) ^ 1u, a.err, wait_bound<kSW>(a));
         if (!ok || *(volatile int*)&sm.abort_flag) { ok = false; break; }
         if (lane == 0) mbar_arrive_expect_tx(&sm.v_full[st], tile_bytes);
         __syncwarp();
@@ -275,13 +276,13 @@ __global__ void __launch_bounds__(kThreads2, 1)
         const int kv_begin = nx.kv_begin, kv_end = nx.kv_end;
         const int nt = tiles_of(nx);
         if (sidx + 1 < W.cnt) nx = items[W.at(sidx + 1)];
-        if (!mbar_wait(&sm.q_full, (uint32_t)k & 1u, a.err, a.wait_ns)) { ok = false; break; }
+        if (!mbar_wait(&sm.q_full, (uint32_t)k & 1u, a.err, wait_bound<kSW>(a))) { ok = false; break; }
         if (t == 0) sm.q_consumed += 1;
         tc::fence_after_sync();
         const uint64_t qd = tc::smem_desc_sw128(smem_addr(&sm.q[t][0][0]), 16, 1024);
         for (int j = 0; j < nt; ++j, ++n) {
           const int st = n % kStages;
-          if (!mbar_wait(&sm.k_full[st], ph(n, kStages), a.err, a.wait_ns)) { ok = false; break; }
+          if (!mbar_wait(&sm.k_full[st], ph(n, kStages), a.err, wait_bound<kSW>(a))) { ok = false; break; }
           if (t == 0) sm.k_consumed[st] += 1;
           tc::fence_after_sync();
           // S_t = Q_t K^T: 8 steps of 16 dims; step kk starts (kk / 4) D halves and
@@ -298,11 +299,11 @@ __global__ void __launch_bounds__(kThreads2, 1)
           if (j + 1 == nt) tc::commit(&sm.q_free);  // this chain's last S of the item
           // at an item's first tile, O_t must have been read out by the previous
           // item's epilogue
-          if (j == 0 && !mbar_wait(&sm.o_free[t], ((uint32_t)k & 1u) ^ 1u, a.err, a.wait_ns)) {
+          if (j == 0 && !mbar_wait(&sm.o_free[t], ((uint32_t)k & 1u) ^ 1u, a.err, wait_bound<kSW>(a))) {
             ok = false;
             break;
           }
-          if (!mbar_wait(&sm.v_full[st], ph(n, kStages), a.err, a.wait_ns)) { ok = false; break; }
+          if (!mbar_wait(&sm.v_full[st], ph(n, kStages), a.err, wait_bound<kSW>(a))) { ok = false; break; }
           if (t == 0) sm.v_consumed[st] += 1;
           // Keys of the tile in the item's range, rounded up to the 16-key step of P V:
           // only those V rows are read. At the item's last tile the rows between the
@@ -331,7 +332,7 @@ __global__ void __launch_bounds__(kThreads2, 1)
           // the first half runs while the second half is computed
 #pragma unroll
           for (int hk = 0; hk < 2; ++hk) {
-            if (!mbar_wait(&sm.p_full[t][hk], (uint32_t)n & 1u, a.err, a.wait_ns)) { ok = false; break; }
+            if (!mbar_wait(&sm.p_full[t][hk], (uint32_t)n & 1u, a.err, wait_bound<kSW>(a))) { ok = false; break; }
             tc::fence_after_sync();
 #pragma unroll
             for (int kk = 4 * hk; kk < 4 * hk + 4; ++kk) {
@@ -351,7 +352,7 @@ __global__ void __launch_bounds__(kThreads2, 1)
           tc::commit(&sm.o_done[t]);
           tc::commit(&sm.v_empty[st]);
           // the next S_t overwrites the columns this P V reads
-          if (!mbar_wait(&sm.o_done[t], (uint32_t)n & 1u, a.err, a.wait_ns)) { ok = false; break; }
+          if (!mbar_wait(&sm.o_done[t], (uint32_t)n & 1u, a.err, wait_bound<kSW>(a))) { ok = false; break; }
         }
       }
       if (!ok) sm.abort_flag = 1;
@@ -381,7 +382,7 @@ __global__ void __launch_bounds__(kThreads2, 1)
       // every S of item k + 2, and the first of those needs this chain's P of item
       // k + 1's last tile: the slot stays valid through this item's epilogue, and the
       // barrier is never two phases ahead of this wait.
-      if (!mbar_wait_warp(&sm.info_full[k % 3], ph(k, 3), a.err, a.wait_ns)) { ok = false; break; }
+      if (!mbar_wait_warp(&sm.info_full[k % 3], ph(k, 3), a.err, wait_bound<kSW>(a))) { ok = false; break; }
       const Item& info = sm.info[k % 3];
       const int kv_begin = info.kv_begin, kv_end = info.kv_end, row_count = info.row_count;
       int lim = -1;                               // causal limit of this row (-1: not a row)
@@ -397,7 +398,7 @@ __global__ void __launch_bounds__(kThreads2, 1)
       const bool warp_live = t * 128 + quad * 32 < row_count;
       float m_used = -INFINITY, l = 0.f;
       for (int j = 0; j < nt; ++j, ++n) {
-        if (!mbar_wait_warp(&sm.s_full[t], (uint32_t)n & 1u, a.err, a.wait_ns)) { ok = false; break; }
+        if (!mbar_wait_warp(&sm.s_full[t], (uint32_t)n & 1u, a.err, wait_bound<kSW>(a))) { ok = false; break; }
         tc::fence_after_sync();
         const int key0 = kv_begin + j * kKeys;
         if (warp_live) {
@@ -489,7 +490,7 @@ __global__ void __launch_bounds__(kThreads2, 1)
       if (!ok) break;
       // ---- epilogue: the chain's last P V (its issuer waited for the one before, so
       // o_done is at most one phase ahead)
-      if (!mbar_wait_warp(&sm.o_done[t], (uint32_t)(n - 1) & 1u, a.err, a.wait_ns)) { ok = false; break; }
+      if (!mbar_wait_warp(&sm.o_done[t], (uint32_t)(n - 1) & 1u, a.err, wait_bound<kSW>(a))) { ok = false; break; }
       tc::fence_after_sync();
       // A warp whose 32 rows all belong to the item (and go to the output, not to
       // split partials) hands O / l to the TMA: it writes 16-column pieces of its rows
@@ -654,10 +655,10 @@ cudaError_t launch_tc2(const AttnArgs& a, const CUtensorMap& kmap, const CUtenso
                        int32_t n_items, int box_t, int grid, cudaStream_t s) {
   if (n_items <= 0) return cudaSuccess;
   const int smem = tc2_smem_bytes();
-  cudaError_t e =
-      cudaFuncSetAttribute(tc2_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  auto* k = a.wait_ns == kWaitLimitNsHost ? tc2_kernel<false> : tc2_kernel<true>;
+  cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
-  tc2_kernel<<<grid, kThreads2, smem, s>>>(a, kmap, vmap, qmap, omap, items, n_items, box_t);
+  k<<<grid, kThreads2, smem, s>>>(a, kmap, vmap, qmap, omap, items, n_items, box_t);
   return cudaGetLastError();
 }
 

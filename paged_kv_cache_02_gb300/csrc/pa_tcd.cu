@@ -178,10 +178,11 @@ struct SoftmaxThread {
 };
 
 // Meets the other softmax warps: red[x % 2][quad][*] written before, read after.
+template <bool kSW>
 __device__ __forceinline__ bool meet(TcdSmem& sm, SoftmaxThread& th, const AttnArgs& a) {
   tc::fence_before_sync();
   mbar_arrive(&sm.xbar);
-  const bool r = mbar_wait_warp(&sm.xbar, th.x & 1u, a.err, a.wait_ns);
+  const bool r = mbar_wait_warp(&sm.xbar, th.x & 1u, a.err, wait_bound<kSW>(a));
   ++th.x;
   tc::fence_after_sync();
   return r;
@@ -190,7 +191,7 @@ __device__ __forceinline__ bool meet(TcdSmem& sm, SoftmaxThread& th, const AttnA
 // One item on the softmax warps, for items of at most NR rows: only the first NR
 // columns of S^T, P^T and O^T are touched (the others feed output rows that are
 // never stored). Returns false if a bounded wait ran out.
-template <int NR>
+template <int NR, bool kSW>
 __device__ bool softmax_item(TcdSmem& sm, const AttnArgs& a, const Item& item, int L, int ql,
                              SoftmaxThread& th) {
   constexpr int H = (NR + 1) / 2;            // P^T rows written by the even lane of a pair
@@ -210,7 +211,7 @@ __device__ bool softmax_item(TcdSmem& sm, const AttnArgs& a, const Item& item, i
     const int key = item.kv_begin + j * kKeys + th.kl;
     // ---- scores of this thread's key for the rows; the buffer is free again after
     float s[NR];
-    if (!mbar_wait_warp(&sm.s_full[b], ph(n, 2), a.err, a.wait_ns)) return false;
+    if (!mbar_wait_warp(&sm.s_full[b], ph(n, 2), a.err, wait_bound<kSW>(a))) return false;
     tc::fence_after_sync();
     tmem_ld_rows<NR>(th.t_lane + (uint32_t)b * kN, s);
     tc::fence_before_sync();
@@ -230,7 +231,7 @@ __device__ bool softmax_item(TcdSmem& sm, const AttnArgs& a, const Item& item, i
         reinterpret_cast<float*>(sm.red[th.x & 1][th.quad])[(th.lane >> sh) & (NR - 1)] = v[0];
     }
     const uint32_t xb = th.x & 1;
-    if (!meet(sm, th, a)) return false;
+    if (!meet<kSW>(sm, th, a)) return false;
     float mt[NR];
     combine4<NR, true>(sm.red[xb], mt);
     float alpha[NR];
@@ -250,7 +251,7 @@ __device__ bool softmax_item(TcdSmem& sm, const AttnArgs& a, const Item& item, i
     // every thread saw the same maxima: the decision is uniform across the warps
     if (any_rescale) {
       // O^T must be idle: wait for the previous tile's P V
-      if (!mbar_wait_warp(&sm.o_tile[(n - 1) & 1], ph(n - 1, 2), a.err, a.wait_ns)) return false;
+      if (!mbar_wait_warp(&sm.o_tile[(n - 1) & 1], ph(n - 1, 2), a.err, wait_bound<kSW>(a))) return false;
       tc::fence_after_sync();
       float o[NR];
       tmem_ld_rows<NR>(th.t_lane + kColO, o);
@@ -270,7 +271,7 @@ __device__ bool softmax_item(TcdSmem& sm, const AttnArgs& a, const Item& item, i
       l_part[r] += p[r];
     }
     // P^T buffer b is free once the P V of tile n - 2 is done
-    if (!mbar_wait_warp(&sm.p_free[b], ph(n, 2) ^ 1u, a.err, a.wait_ns)) return false;
+    if (!mbar_wait_warp(&sm.p_free[b], ph(n, 2) ^ 1u, a.err, wait_bound<kSW>(a))) return false;
     {
       // the even lane of a pair writes rows 0..H-1 for keys (kl, kl + 1), the odd lane
       // rows H..NR-1; K-major, 128-byte swizzle: row r, key k at key half k / 64,
@@ -308,12 +309,12 @@ __device__ bool softmax_item(TcdSmem& sm, const AttnArgs& a, const Item& item, i
       reinterpret_cast<float*>(sm.red[th.x & 1][th.quad])[(th.lane >> sh) & (NR - 1)] = v[0];
   }
   const uint32_t xb = th.x & 1;
-  if (!meet(sm, th, a)) return false;
+  if (!meet<kSW>(sm, th, a)) return false;
   float l_row[NR];
   combine4<NR, false>(sm.red[xb], l_row);
   // the item's last P V (its phase is at most one ahead: see the phase bounds)
   const int n_last = th.n - 1;
-  if (!mbar_wait_warp(&sm.o_tile[n_last & 1], ph(n_last, 2), a.err, a.wait_ns)) return false;
+  if (!mbar_wait_warp(&sm.o_tile[n_last & 1], ph(n_last, 2), a.err, wait_bound<kSW>(a))) return false;
   tc::fence_after_sync();
   float o[NR];
   tmem_ld_rows<NR>(th.t_lane + kColO, o);
@@ -345,6 +346,7 @@ __device__ bool softmax_item(TcdSmem& sm, const AttnArgs& a, const Item& item, i
   return true;
 }
 
+template <bool kSW>
 __global__ void __launch_bounds__(kThreadsD, 1)
     tcd_kernel(const __grid_constant__ AttnArgs a, const __grid_constant__ CUtensorMap kmap,
                const __grid_constant__ CUtensorMap vmap, const __grid_constant__ CUtensorMap qmap,
@@ -425,7 +427,7 @@ __global__ void __launch_bounds__(kThreadsD, 1)
       // half. Buffer k % 2 is free once the issuer issued every S^T of item k - 2.
       {
         const int qb = k & 1;
-        ok = mbar_wait_warp(&sm.q_free[qb], ph(k, 2) ^ 1u, a.err, a.wait_ns);
+        ok = mbar_wait_warp(&sm.q_free[qb], ph(k, 2) ^ 1u, a.err, wait_bound<kSW>(a));
         if (!ok || *(volatile int*)&sm.abort_flag) { ok = false; break; }
         if (lane == 0) {
           mbar_arrive_expect_tx(&sm.q_full[qb], 2u * kQHalf);
@@ -500,7 +502,7 @@ __global__ void __launch_bounds__(kThreadsD, 1)
         const uint32_t tile_bytes = __popc(__ballot_sync(0xffffffffu, valid)) * piece_bytes * 2u;
         const uint32_t piece_off = (uint32_t)lane * box_t * 256u;  // whole groups
         // K_n: its stage is free once S^T of tile n - 3 is done
-        ok = mbar_wait_warp(&sm.k_empty[st], ph(n, kStages) ^ 1u, a.err, a.wait_ns);
+        ok = mbar_wait_warp(&sm.k_empty[st], ph(n, kStages) ^ 1u, a.err, wait_bound<kSW>(a));
         if (!ok || *(volatile int*)&sm.abort_flag) { ok = false; break; }
         if (lane == 0) mbar_arrive_expect_tx(&sm.k_full[st], tile_bytes);
         __syncwarp();
@@ -508,7 +510,7 @@ __global__ void __launch_bounds__(kThreadsD, 1)
           tma_load_5d(&sm.k[st][piece_off], &kmap, &sm.k_full[st], 0, 0, 0, tok >> 3, item.kv_head);
         if (lane == 0) sm.k_issued[st] += 1;
         // V_n: free once P V of tile n - 3 is done
-        ok = mbar_wait_warp(&sm.v_empty[st], ph(n, kStages) ^ 1u, a.err, a.wait_ns);
+        ok = mbar_wait_warp(&sm.v_empty[st], ph(n, kStages) ^ 1u, a.err, wait_bound<kSW>(a));
         if (!ok || *(volatile int*)&sm.abort_flag) { ok = false; break; }
         if (lane == 0) mbar_arrive_expect_tx(&sm.v_full[st], tile_bytes);
         __syncwarp();
@@ -651,7 +653,7 @@ __global__ void __launch_bounds__(kThreadsD, 1)
         }
         if (progress) {
           t_idle = global_timer_ns();
-        } else if (global_timer_ns() - t_idle > a.wait_ns) {
+        } else if (global_timer_ns() - t_idle > wait_bound<kSW>(a)) {
           record_error(a.err, PA_DEVERR_TIMEOUT);
           ok = false;
           break;
@@ -706,15 +708,15 @@ __global__ void __launch_bounds__(kThreadsD, 1)
         record_error(a.err, PA_DEVERR_LENS);
       const int rc = item.row_count;
       if (rc <= 1)
-        ok = softmax_item<1>(sm, a, item, L, ql, th);
+        ok = softmax_item<1, kSW>(sm, a, item, L, ql, th);
       else if (rc <= 2)
-        ok = softmax_item<2>(sm, a, item, L, ql, th);
+        ok = softmax_item<2, kSW>(sm, a, item, L, ql, th);
       else if (rc <= 4)
-        ok = softmax_item<4>(sm, a, item, L, ql, th);
+        ok = softmax_item<4, kSW>(sm, a, item, L, ql, th);
       else if (rc <= 8)
-        ok = softmax_item<8>(sm, a, item, L, ql, th);
+        ok = softmax_item<8, kSW>(sm, a, item, L, ql, th);
       else
-        ok = softmax_item<16>(sm, a, item, L, ql, th);
+        ok = softmax_item<16, kSW>(sm, a, item, L, ql, th);
     }
     if (!ok) sm.abort_flag = 1;
   }
@@ -758,10 +760,10 @@ cudaError_t launch_tcd(const AttnArgs& a, const CUtensorMap& kmap, const CUtenso
                        int grid, cudaStream_t s) {
   if (n_items <= 0) return cudaSuccess;
   const int smem = tcd_smem_bytes();
-  cudaError_t e =
-      cudaFuncSetAttribute(tcd_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  auto* k = a.wait_ns == kWaitLimitNsHost ? tcd_kernel<false> : tcd_kernel<true>;
+  cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
-  tcd_kernel<<<grid, kThreadsD, smem, s>>>(a, kmap, vmap, qmap, items, n_items, box_t);
+  k<<<grid, kThreadsD, smem, s>>>(a, kmap, vmap, qmap, items, n_items, box_t);
   return cudaGetLastError();
 }
 

@@ -150,9 +150,9 @@ def test_plan_covers_every_row_and_key(pa, chunk):
 
 
 def test_plan_pair_tiles(pa):
-    """With tc_pair=1 tensor-core rows go in 256-row items (two 128-row tiles) while more
-    than 128 rows remain, the rest in one 128-row item; tc_pair=-1 keeps 128-row items
-    only."""
+    """With tc_pair=1 tensor-core rows go in 256-row items (two 128-row tiles); rows that
+    do not fill a whole item form the sequence's first item, a 128-row item when at most
+    128 rows are left over; tc_pair=-1 keeps 128-row items only."""
     L = [300, 1000, 700, 129, 2000]
     q = [300, 40, 33, 129, 1]
     g, Hkv = 8, 2
@@ -167,11 +167,38 @@ def test_plan_pair_tiles(pa):
     assert p.stats()["n_tc_pair_items"] == len(rows_by_path[2])
     # 300 tokens x 8 heads = 2400 rows = 9 x 256 + 96
     assert sorted(rc for s, rc in set((s, rc) for s, rc in rows_by_path[2] if s == 0)) == [256]
+    # the leading partial item: rows [0, 96) of sequence 0 (2400 = 96 + 9 x 256), each
+    # KV head, one-tile path, over keys up to the last of its 12 tokens
+    lead = [it for it in items if it[1] == 0 and it[3] == 0]
+    assert len(lead) > 0 and all(it[0] == 1 and it[4] == 96 for it in lead)
+    assert max(it[6] for it in lead) == L[0] - q[0] + 96 // g
     p1 = plan(pa, L, q, Hq=g * Hkv, Hkv=Hkv, D=128, max_chunk_tokens=256, tc_pair=-1)
     items1 = p1.items()
     _coverage(items1, L, q, g, Hkv)
     assert 2 not in set(items1[:, 0].tolist())
     assert p1.stats()["n_tc_pair_items"] == 0
+
+
+def test_plan_partial_tile_first_reads_fewer_keys(pa):
+    """The partial row tile of a sequence comes first: every other tile is whole, and the
+    keys the items read (summed over items) are n (T - r) fewer than with the partial tile
+    last (n whole tiles of T rows, r rows over; g = 1)."""
+    L, q = [800, 2300, 300], [800, 300, 300]      # a recomputed context, a new prompt
+    for pair, T in ((1, 256), (-1, 128)):
+        p = plan(pa, L, q, Hq=4, Hkv=4, D=128, tc_pair=pair)
+        items = p.items()
+        _coverage(items, L, q, 1, 4)
+        for s in range(3):
+            mine = sorted(set((int(it[3]), int(it[4])) for it in items
+                              if it[1] == s and it[2] == 0))
+            r = q[s] % T
+            assert mine[0] == (0, r if r else T)
+            assert all(rc == T for _, rc in mine[1:])
+            keys = sum(int(it[6]) - int(it[5]) for it in items if it[1] == s and it[2] == 0)
+            n = q[s] // T
+            # partial tile last: tiles end at T, 2T, ..., nT, then q
+            last = sum(L[s] - q[s] + T * k for k in range(1, n + 1)) + (L[s] if r else 0)
+            assert keys == last - (n * (T - r) if r else 0)
 
 
 def _tc_intensity(L, q, g, Hkv, D=128):
