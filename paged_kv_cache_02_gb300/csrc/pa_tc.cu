@@ -19,10 +19,8 @@
 //              own barriers, so that a K tile never waits behind a V slot that the
 //              P V products still hold. Block ids come from a shared-memory cache per
 //              producer, filled one item ahead.
-//   warp 1     issues S_j = Q K_j^T into TMEM buffer j % 2 as two key halves (M = 128,
-//              N = 64 each) with their own barriers, so S_{j+1} is computed while the
-//              softmax works on S_j, and half h of S_{j+2} starts as soon as the P V of
-//              half h of tile j is done, without waiting for the other half.
+//   warp 1     issues S_j = Q K_j^T (M = N = 128) into TMEM buffer j % 2, so S_{j+1}
+//              is computed while the softmax works on S_j.
 //   warp 2     issues O_h += P_{j,h} V_{j,h} for the two key halves h of the tile
 //              (keys 64 h .. 64 h + 63) into two accumulators O_0, O_1, each as soon
 //              as its half of P is in TMEM. One thread alone cannot issue both
@@ -66,8 +64,7 @@ constexpr int kStageCols = 16;          // epilogue staging: 32 rows x 16 fp32 p
 constexpr float kRescaleLog2 = 8.f;     // O_h is rescaled once its max grows by > 2^8
 constexpr uint32_t kTmemCols = 512;
 
-constexpr uint32_t kIdescS = tc::idesc_bf16_f32(kRows, kKeys / 2, false);  // Q K^T, one key
-                                                                           // half; K-major
+constexpr uint32_t kIdescS = tc::idesc_bf16_f32(kRows, kKeys, false);  // Q K^T, both K-major
 constexpr uint32_t kIdescO = tc::idesc_bf16_f32(kRows, kD, true);      // P V, V is MN-major
 
 __host__ __device__ constexpr uint32_t s_col(int b) { return (uint32_t)b * 128u; }
@@ -83,7 +80,7 @@ struct TcSmem {
   uint64_t k_full[kKStages], k_empty[kKStages];
   uint64_t v_full[kVStages], v_empty[kVStages];
   uint64_t q_full[kQBuf], q_free[kQBuf];
-  uint64_t s_full[2][2], s_free[2][2];   // [S buffer][key half]
+  uint64_t s_full[2], s_free[2];
   uint64_t p_full[2][2];                // [S buffer][key half]: P of that half written
   uint64_t o_done[2][2];                // [key half][tile parity]: P V of that half done
   uint64_t o_free;                      // the epilogue has read O_0 and O_1
@@ -241,10 +238,8 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
       sm.q_issued[b] = sm.q_consumed[b] = 0;
     }
     for (int b = 0; b < 2; ++b) {
-      mbar_init(&sm.s_full[b][0], 1);
-      mbar_init(&sm.s_full[b][1], 1);
-      mbar_init(&sm.s_free[b][0], 1);
-      mbar_init(&sm.s_free[b][1], 1);
+      mbar_init(&sm.s_full[b], 1);
+      mbar_init(&sm.s_free[b], 1);
       mbar_init(&sm.p_full[b][0], kRows);
       mbar_init(&sm.p_full[b][1], kRows);
       mbar_init(&sm.o_done[0][b], 1);
@@ -271,13 +266,9 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
     produce<false, kSW>(sm, a, vmap, qmap, items, n_items, box_t, lane);
   } else if (warp == 1) {
     // ------------------------------------------------------------ S issuer
-    // S_j = Q K_j^T is issued as two key halves (N = 64 each) with their own barriers:
-    // half h of buffer b is free once the P V of that half of tile j - 2 completed (P_h
-    // lives over half h's columns), and the softmax warps of half h need only their
-    // half, so each half of the chain runs on its own.
     // Phase bounds: q_full of item k + kQBuf needs q_free(k), committed here; k_full of
-    // tile n + 2 needs k_empty(n), committed here; s_free[b][h] of tile n + 2 needs the
-    // P V of half h of tile n + 2, which needs s_full[b][h](n + 2) from here.
+    // tile n + 2 needs k_empty(n), committed here; s_free of tile n + 2 needs the P V
+    // of tile n + 2, which needs s_full(n + 2) from here.
     if (lane == 0) {
       int n = 0, k = 0;
       bool ok = true;
@@ -290,33 +281,24 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
         sm.q_consumed[qb] += 1;
         tc::fence_after_sync();
         const uint64_t qd = tc::smem_desc_sw128(smem_addr(&sm.q[qb][0][0]), 16, 1024);
-        for (int j = 0; j < nt && ok; ++j, ++n) {
+        for (int j = 0; j < nt; ++j, ++n) {
           const int st = n % kKStages;
           const int b = n & 1;
           if (!mbar_wait(&sm.k_full[st], ph(n, kKStages), a.err, wait_bound<kSW>(a))) { ok = false; break; }
           sm.k_consumed[st] += 1;
+          // the buffer's last readers, both halves' P V of tile n - 2, are done
+          if (!mbar_wait(&sm.s_free[b], ph(n, 2) ^ 1u, a.err, wait_bound<kSW>(a))) { ok = false; break; }
+          tc::fence_after_sync();
+          // S = Q K^T: 8 steps of 16 dims; step kk starts (kk / 4) D halves and
+          // (kk % 4) 32-byte chunks into both operands
+          const uint64_t kd = tc::smem_desc_sw128(smem_addr(&sm.k[st][0][0]), 16, 1024);
+          tc::mma_bf16_c<false>(tmem + s_col(b), qd, kd, kIdescS);
 #pragma unroll
-          for (int h = 0; h < 2; ++h) {
-            // half h's last readers, the P V of half h of tile n - 2, are done
-            if (!mbar_wait(&sm.s_free[b][h], ph(n, 2) ^ 1u, a.err, wait_bound<kSW>(a))) {
-              ok = false;
-              break;
-            }
-            tc::fence_after_sync();
-            // 8 steps of 16 dims; step kk starts (kk / 4) D halves and (kk % 4) 32-byte
-            // chunks into both operands; key half h is 64 rows = 8 KB into the K tile
-            const uint64_t kd = tc::smem_desc_sw128(
-                smem_addr(&sm.k[st][0][0]) + 8192u * (uint32_t)h, 16, 1024);
-            const uint32_t d = tmem + s_col(b) + 64u * (uint32_t)h;
-            tc::mma_bf16_c<false>(d, qd, kd, kIdescS);
-#pragma unroll
-            for (int kk = 1; kk < kD / 16; ++kk) {
-              const uint64_t off = (uint64_t)(((kk >> 2) * kHalf + (kk & 3) * 32) >> 4);
-              tc::mma_bf16_c<true>(d, qd + off, kd + off, kIdescS);
-            }
-            tc::commit(&sm.s_full[b][h]);
+          for (int kk = 1; kk < kD / 16; ++kk) {
+            const uint64_t off = (uint64_t)(((kk >> 2) * kHalf + (kk & 3) * 32) >> 4);
+            tc::mma_bf16_c<true>(tmem + s_col(b), qd + off, kd + off, kIdescS);
           }
-          if (!ok) break;
+          tc::commit(&sm.s_full[b]);
           tc::commit(&sm.k_empty[st]);
         }
         if (ok) tc::commit(&sm.q_free[qb]);  // the item's last S issued: Q may be reloaded
@@ -328,10 +310,9 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
     __syncwarp();
   } else if (warp == 2) {
     // ------------------------------------------------------------ P V issuer
-    // Phase bounds: p_full[b][h] of tile n + 2 needs s_full[b][h](n + 2), which needs
-    // s_free[b][h](n), committed here after the P V of half h of tile n; v_full of tile
-    // n + kVStages needs v_empty(n), committed here; o_free of item k + 1 needs the P V
-    // of item k + 1.
+    // Phase bounds: p_full[b][h] of tile n + 2 needs s_full(n + 2), which needs
+    // s_free(n), committed here after the P V of tile n; v_full of tile n + kVStages
+    // needs v_empty(n), committed here; o_free of item k + 1 needs the P V of item k + 1.
     if (lane == 0) {
       int n = 0, k = 0;
       bool ok = true;
@@ -389,7 +370,6 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
                                         vd + (uint64_t)((kq * 16 * 128) >> 4), kIdescO);
           }
           tc::commit(&sm.o_done[0][b]);
-          tc::commit(&sm.s_free[b][0]);
           // half 1: keys 64..127 of the tile
           if (!mbar_wait(&sm.p_full[b][1], ph(n, 2), a.err, wait_bound<kSW>(a))) { ok = false; break; }
           tc::fence_after_sync();
@@ -408,7 +388,7 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
                                         vd1 + (uint64_t)((kq * 16 * 128) >> 4), kIdescO);
           }
           tc::commit(&sm.o_done[1][b]);
-          tc::commit(&sm.s_free[b][1]);
+          tc::commit(&sm.s_free[b]);
           tc::commit(&sm.v_empty[st]);
         }
       }
@@ -420,18 +400,13 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
   } else {
     // ------------------------------------------------------------ softmax / epilogue
     // Warp w: lane quadrant quad = w % 4 (rows 32 quad ..), key half h = (w - 4) / 4.
-    // Phase bounds: s_full[b][h] of tile n + 2 needs s_free[b][h](n), i.e. the P V of
-    // half h of tile n, which needs p_full[b][h](n) from here; o_done[h][b] of tile n + 2
-    // needs p_full[b][h](n + 2) from here, and s_full[b][h](n) implies that the P V of
-    // half h of tile n - 2 and everything the P V issuer issued before it are done, so a
-    // warp's waits for the P V of its own half of tile n - 1 are never two phases off.
-    // At the item's end the waits for the other half's last P V follow the meeting of
-    // the quadrant's two warps (the partner passed s_full of its half of the last tile,
-    // so that P V of tile n - 3 is done), and the next item's first P V needs o_free
-    // from every warp: those waits are never two phases off either. xbar[quad]
-    // completes only with both warps of the quadrant, and the (m, l) exchange buffers
-    // alternate by item: a warp can be at most one item ahead of its partner (the next
-    // item's third tile needs the partner's P of that item).
+    // Phase bounds: s_full of tile n + 2 needs s_free(n), i.e. both halves' P V(n),
+    // which need p_full(n) from here; o_done[h][b] of tile n + 2 needs p_full(n + 2)
+    // from here, and s_full(n) implies that P V(n - 2) and everything before it are
+    // done, so the waits for P V(n - 1) are never two phases off. xbar[quad] completes
+    // only with both warps of the quadrant, and the (m, l) exchange buffers alternate
+    // by item: a warp can be at most one item ahead of its partner (the next item's
+    // third tile needs the partner's P of that item).
     const int quad = warp & 3;
     const int h = (warp - 4) >> 2;
     const int row = quad * 32 + lane;             // tile row = TMEM lane
@@ -469,7 +444,7 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
       float m_used = -INFINITY, l = 0.f;
       for (int j = 0; j < nt; ++j, ++n) {
         const int b = n & 1;
-        if (!mbar_wait_warp(&sm.s_full[b][h], ph(n, 2), a.err, wait_bound<kSW>(a))) { ok = false; break; }
+        if (!mbar_wait_warp(&sm.s_full[b], ph(n, 2), a.err, wait_bound<kSW>(a))) { ok = false; break; }
         tc::fence_after_sync();
         const int k0 = item.kv_begin + j * kKeys + 64 * h;   // first key of this half
         const uint32_t s_addr = t_lane + s_col(b) + (uint32_t)(64 * h);

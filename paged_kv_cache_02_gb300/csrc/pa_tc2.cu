@@ -50,7 +50,6 @@ constexpr float kRescaleLog2 = 8.f;
 constexpr uint32_t kTmemCols = 512;
 
 constexpr uint32_t kIdescS = tc::idesc_bf16_f32(128, kKeys, false);
-constexpr uint32_t kIdescS64 = tc::idesc_bf16_f32(128, kKeys / 2, false);  // one key half
 constexpr uint32_t kIdescO = tc::idesc_bf16_f32(128, kD, true);
 
 __host__ __device__ constexpr uint32_t s_col(int t) { return (uint32_t)t * 128u; }
@@ -281,44 +280,20 @@ __global__ void __launch_bounds__(kThreads2, 1)
         if (t == 0) sm.q_consumed += 1;
         tc::fence_after_sync();
         const uint64_t qd = tc::smem_desc_sw128(smem_addr(&sm.q[t][0][0]), 16, 1024);
-        // S_t = Q_t K^T: 8 steps of 16 dims; step kk starts (kk / 4) D halves and (kk % 4)
-        // 32-byte chunks into both operands. A key half (N = 64) is 64 rows = 8 KB into
-        // the K tile, and its scores are 64 columns into the chain's TMEM region.
-        auto issue_s_half = [&](int st, int h) {
-          const uint64_t kd =
-              tc::smem_desc_sw128(smem_addr(&sm.k[st][0][0]) + 8192u * (uint32_t)h, 16, 1024);
-          const uint32_t d = tmem + s_col(t) + 64u * (uint32_t)h;
-          tc::mma_bf16_c<false>(d, qd, kd, kIdescS64);
+        for (int j = 0; j < nt; ++j, ++n) {
+          const int st = n % kStages;
+          if (!mbar_wait(&sm.k_full[st], ph(n, kStages), a.err, wait_bound<kSW>(a))) { ok = false; break; }
+          if (t == 0) sm.k_consumed[st] += 1;
+          tc::fence_after_sync();
+          // S_t = Q_t K^T: 8 steps of 16 dims; step kk starts (kk / 4) D halves and
+          // (kk % 4) 32-byte chunks into both operands
+          const uint64_t kd = tc::smem_desc_sw128(smem_addr(&sm.k[st][0][0]), 16, 1024);
+          tc::mma_bf16_c<false>(tmem + s_col(t), qd, kd, kIdescS);
 #pragma unroll
           for (int kk = 1; kk < kD / 16; ++kk) {
             const uint64_t off = (uint64_t)(((kk >> 2) * kHalf + (kk & 3) * 32) >> 4);
-            tc::mma_bf16_c<true>(d, qd + off, kd + off, kIdescS64);
+            tc::mma_bf16_c<true>(tmem + s_col(t), qd + off, kd + off, kIdescS);
           }
-        };
-        // whether half 1 of this tile's S was issued during the previous tile (see below)
-        bool early = false;
-        for (int j = 0; j < nt; ++j, ++n) {
-          const int st = n % kStages;
-          if (early) {
-            // K_n already waited for; only the key half whose columns P of the previous
-            // tile occupied is left: its P V completed (o_done waited at the end of the
-            // previous iteration)
-            tc::fence_after_sync();
-            issue_s_half(st, 0);
-          } else {
-            if (!mbar_wait(&sm.k_full[st], ph(n, kStages), a.err, wait_bound<kSW>(a))) { ok = false; break; }
-            if (t == 0) sm.k_consumed[st] += 1;
-            tc::fence_after_sync();
-            const uint64_t kd = tc::smem_desc_sw128(smem_addr(&sm.k[st][0][0]), 16, 1024);
-            tc::mma_bf16_c<false>(tmem + s_col(t), qd, kd, kIdescS);
-#pragma unroll
-            for (int kk = 1; kk < kD / 16; ++kk) {
-              const uint64_t off = (uint64_t)(((kk >> 2) * kHalf + (kk & 3) * 32) >> 4);
-              tc::mma_bf16_c<true>(tmem + s_col(t), qd + off, kd + off, kIdescS);
-            }
-          }
-          early = false;
-          // (the commits track every MMA this thread issued, the early half included)
           tc::commit(&sm.s_full[t]);
           tc::commit(&sm.k_empty[st]);
           if (j + 1 == nt) tc::commit(&sm.q_free);  // this chain's last S of the item
@@ -353,9 +328,8 @@ __global__ void __launch_bounds__(kThreads2, 1)
           // V as the MN-major B operand: step kk covers keys 16 kk .. 16 kk + 15 (rows
           // of 128 bytes), the two D halves are kHalf apart
           const uint64_t vd = tc::smem_desc_sw128(smem_addr(&sm.v[st][0][0]), kHalf, 1024);
-          // P_t(j) is written over S_t(j) by the softmax in two key halves (keys 64 h ..
-          // 64 h + 63 as bf16 pairs in columns 32 h .. 32 h + 31); the P V of the first half
-          // runs while the second half is computed
+          // P_t(j) is written over S_t(j) by the softmax in two key halves; the P V of
+          // the first half runs while the second half is computed
 #pragma unroll
           for (int hk = 0; hk < 2; ++hk) {
             if (!mbar_wait(&sm.p_full[t][hk], (uint32_t)n & 1u, a.err, wait_bound<kSW>(a))) { ok = false; break; }
@@ -371,21 +345,6 @@ __global__ void __launch_bounds__(kThreads2, 1)
                   tc::mma_bf16_ts_c<false>(tmem + o_col(t), pa, vk, kIdescO);
               } else if (kk < kk_end) {
                 tc::mma_bf16_ts_c<true>(tmem + o_col(t), pa, vk, kIdescO);
-              }
-            }
-            if (hk == 0 && j + 1 < nt) {
-              // Half 1 of the next tile's S goes to columns 64..127, which P never
-              // occupies: the softmax read them (its whole score row, with one TMEM load
-              // completed before it wrote P's first half, so p_full[t][0] implies it), so
-              // they may be overwritten now -- if K_{n+1} has landed; else the whole S
-              // of the next tile is issued after this P V, as without this step. Only the
-              // other half (columns 0..63, where P lives) then waits for this P V.
-              const int st1 = (n + 1) % kStages;
-              if (mbar_test_wait(smem_addr(&sm.k_full[st1]), ph(n + 1, kStages))) {
-                if (t == 0) sm.k_consumed[st1] += 1;
-                tc::fence_after_sync();
-                issue_s_half(st1, 1);
-                early = true;
               }
             }
           }
