@@ -74,7 +74,6 @@ struct Tc2Smem {
   int k_issued[kStages], k_consumed[kStages];
   int v_issued[kStages], v_consumed[kStages];
   int q_issued, q_consumed;
-  int a_soft;                           // tiles whose softmax chain A has finished (CTA count)
   int abort_flag;
 };
 
@@ -143,7 +142,6 @@ __global__ void __launch_bounds__(kThreads2, 1)
     }
     sm.q_issued = 0;
     sm.q_consumed = 0;
-    sm.a_soft = 0;
     sm.abort_flag = 0;
     fence_barrier_init();
   }
@@ -284,25 +282,6 @@ __global__ void __launch_bounds__(kThreads2, 1)
         const uint64_t qd = tc::smem_desc_sw128(smem_addr(&sm.q[t][0][0]), 16, 1024);
         for (int j = 0; j < nt; ++j, ++n) {
           const int st = n % kStages;
-          if (t == 1) {
-            // Ping-pong: chain B issues S of tile n once chain A's softmax of tile n is
-            // done, so that one chain's softmax runs while the other chain's products
-            // occupy the tensor core. Left to themselves the chains fall into step
-            // (both wait for the same K/V tile), run their softmaxes at the same time
-            // (sharing the exponential unit) and then queue their products together.
-            // A monotonic count in shared memory, bounded wait: chain A's softmax of tile
-            // n needs nothing of chain B past tile n - 2, which B has issued by now.
-            const uint64_t t0 = global_timer_ns();
-            while (*(volatile int*)&sm.a_soft <= n) {
-              if (*(volatile int*)&sm.abort_flag ||
-                  global_timer_ns() - t0 > wait_bound<kSW>(a)) {
-                record_error(a.err, PA_DEVERR_TIMEOUT);
-                ok = false;
-                break;
-              }
-            }
-            if (!ok) break;
-          }
           if (!mbar_wait(&sm.k_full[st], ph(n, kStages), a.err, wait_bound<kSW>(a))) { ok = false; break; }
           if (t == 0) sm.k_consumed[st] += 1;
           tc::fence_after_sync();
@@ -354,8 +333,6 @@ __global__ void __launch_bounds__(kThreads2, 1)
 #pragma unroll
           for (int hk = 0; hk < 2; ++hk) {
             if (!mbar_wait(&sm.p_full[t][hk], (uint32_t)n & 1u, a.err, wait_bound<kSW>(a))) { ok = false; break; }
-            // chain A's softmax of tile n is done: chain B may issue its S of tile n
-            if (t == 0 && hk == 1) *(volatile int*)&sm.a_soft = n + 1;
             tc::fence_after_sync();
 #pragma unroll
             for (int kk = 4 * hk; kk < 4 * hk + 4; ++kk) {
