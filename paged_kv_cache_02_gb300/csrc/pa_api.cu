@@ -835,6 +835,11 @@ static pa_status attention_impl(pa_plan_t p, void* d_out, pa_dtype out_dtype, co
     }
   }
 
+  // The first attention kernel of the call starts after everything before it in the
+  // stream (the table upload, the write kernel); each later one is launched as a
+  // programmatic dependent of the one before, so that its CTAs start in that kernel's
+  // tail (see launch_kernel).
+  bool pdl = false;
   if (p->n_dec > 0) {
     const int box_t = std::min(p->block_size, pa::kKeyTile);
     CUtensorMap kmap, vmap;
@@ -848,8 +853,9 @@ static pa_status attention_impl(pa_plan_t p, void* d_out, pa_dtype out_dtype, co
     if (sms <= 0) return PA_ERR_CUDA;
     const int grid = std::min(p->n_dec, sms);
     cudaError_t e = pa::launch_decode(a, kmap, vmap, reinterpret_cast<const Item*>(ws + p->off_dec),
-                                      p->n_dec, p->D, p->dec_rows_max, box_t, grid, s);
+                                      p->n_dec, p->D, p->dec_rows_max, box_t, grid, s, pdl);
     if (e != cudaSuccess) return PA_ERR_CUDA;
+    pdl = true;
   }
   if (p->n_tc + p->n_tc2 + p->n_tcd > 0) {
     const int box_t = std::min(p->block_size, 64);
@@ -873,8 +879,9 @@ static pa_status attention_impl(pa_plan_t p, void* d_out, pa_dtype out_dtype, co
       const int grid = std::min(p->n_tcd, sms);
       cudaError_t e = pa::launch_tcd(a, kmap_g, vmap_g, qmap16,
                                      reinterpret_cast<const Item*>(ws + p->off_tcd), p->n_tcd,
-                                     box_t, grid, s);
+                                     box_t, grid, s, pdl);
       if (e != cudaSuccess) return PA_ERR_CUDA;
+      pdl = true;
     }
     CUtensorMap qmap;
     st = pa::make_q_map(&qmap, d_q, p->total_q, p->Hq, p->D, p->g, pa::kTcRows);
@@ -888,20 +895,22 @@ static pa_status attention_impl(pa_plan_t p, void* d_out, pa_dtype out_dtype, co
       const int grid = std::min(p->n_tc2, sms);
       cudaError_t e = pa::launch_tc2(a, kmap, vmap, qmap, omap,
                                      reinterpret_cast<const Item*>(ws + p->off_tc2), p->n_tc2,
-                                     box_t, grid, s);
+                                     box_t, grid, s, pdl);
       if (e != cudaSuccess) return PA_ERR_CUDA;
+      pdl = true;
     }
     if (p->n_tc > 0) {
       const int grid = std::min(p->n_tc, sms);
       cudaError_t e = pa::launch_tc(a, kmap, vmap, qmap, omap,
                                     reinterpret_cast<const Item*>(ws + p->off_tc), p->n_tc, box_t,
-                                    grid, s);
+                                    grid, s, pdl);
       if (e != cudaSuccess) return PA_ERR_CUDA;
+      pdl = true;
     }
   }
   if (p->n_groups > 0) {
     cudaError_t e = pa::launch_combine(
-        a, reinterpret_cast<const SplitGroup*>(ws + p->off_groups), p->n_groups, p->D, s);
+        a, reinterpret_cast<const SplitGroup*>(ws + p->off_groups), p->n_groups, p->D, s, pdl);
     if (e != cudaSuccess) return PA_ERR_CUDA;
   }
   return PA_OK;

@@ -145,6 +145,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     fence_barrier_init();
   }
   __syncthreads();
+  if (threadIdx.x == 0) pdl_launch_dependents();
 
   if (warp == kCWarps) {
     // ------------------------------------------------------------ producer
@@ -484,6 +485,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
     }
   }
+  pdl_wait();  // exit only after the kernel this one may overlap has completed
 }
 
 // Merges the key chunks of split rows: m* = max m_c, l* = sum_c l_c 2^(m_c - m*),
@@ -492,6 +494,9 @@ template <int D>
 __global__ void __launch_bounds__(256) combine_kernel(const __grid_constant__ AttnArgs a,
                                                       const SplitGroup* __restrict__ groups) {
   constexpr int PER = D / 32;
+  // the partials of every attention kernel of the call: each of those waits for its
+  // predecessor before it exits, so the completion of the last implies all of them
+  pdl_wait();
   const SplitGroup gp = groups[blockIdx.x];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   for (int r = warp; r < gp.row_count; r += 8) {
@@ -532,13 +537,14 @@ __global__ void __launch_bounds__(256) combine_kernel(const __grid_constant__ At
 template <int D, int RM>
 cudaError_t launch_dec_t(const AttnArgs& a, const CUtensorMap& kmap, const CUtensorMap& vmap,
                          const Item* items, int32_t n_items, int box_t, int grid,
-                         cudaStream_t s) {
+                         cudaStream_t s, bool pdl) {
   const int smem = (int)sizeof(DecSmem<D, RM>) + 1024;
   auto* k = a.wait_ns == kWaitLimitNsHost ? decode_kernel<D, RM, false>
                                           : decode_kernel<D, RM, true>;
   cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
-  k<<<grid, kThreads, smem, s>>>(a, kmap, vmap, items, n_items, box_t);
+  e = launch_kernel(k, grid, kThreads, smem, s, pdl, a, kmap, vmap, items, n_items, box_t);
+  if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
 
@@ -558,27 +564,26 @@ int decode_smem_bytes(int D, int rows_max) {
 
 cudaError_t launch_decode(const AttnArgs& a, const CUtensorMap& kmap, const CUtensorMap& vmap,
                           const Item* items, int32_t n_items, int D, int rows_max, int box_t,
-                          int grid, cudaStream_t s) {
+                          int grid, cudaStream_t s, bool pdl) {
   if (n_items <= 0) return cudaSuccess;
   if (D == 128) {
-    if (rows_max <= 1) return launch_dec_t<128, 1>(a, kmap, vmap, items, n_items, box_t, grid, s);
-    if (rows_max <= 2) return launch_dec_t<128, 2>(a, kmap, vmap, items, n_items, box_t, grid, s);
-    if (rows_max <= 4) return launch_dec_t<128, 4>(a, kmap, vmap, items, n_items, box_t, grid, s);
-    return launch_dec_t<128, 8>(a, kmap, vmap, items, n_items, box_t, grid, s);
+    if (rows_max <= 1) return launch_dec_t<128, 1>(a, kmap, vmap, items, n_items, box_t, grid, s, pdl);
+    if (rows_max <= 2) return launch_dec_t<128, 2>(a, kmap, vmap, items, n_items, box_t, grid, s, pdl);
+    if (rows_max <= 4) return launch_dec_t<128, 4>(a, kmap, vmap, items, n_items, box_t, grid, s, pdl);
+    return launch_dec_t<128, 8>(a, kmap, vmap, items, n_items, box_t, grid, s, pdl);
   }
-  if (rows_max <= 1) return launch_dec_t<64, 1>(a, kmap, vmap, items, n_items, box_t, grid, s);
-  if (rows_max <= 2) return launch_dec_t<64, 2>(a, kmap, vmap, items, n_items, box_t, grid, s);
-  if (rows_max <= 4) return launch_dec_t<64, 4>(a, kmap, vmap, items, n_items, box_t, grid, s);
-  return launch_dec_t<64, 8>(a, kmap, vmap, items, n_items, box_t, grid, s);
+  if (rows_max <= 1) return launch_dec_t<64, 1>(a, kmap, vmap, items, n_items, box_t, grid, s, pdl);
+  if (rows_max <= 2) return launch_dec_t<64, 2>(a, kmap, vmap, items, n_items, box_t, grid, s, pdl);
+  if (rows_max <= 4) return launch_dec_t<64, 4>(a, kmap, vmap, items, n_items, box_t, grid, s, pdl);
+  return launch_dec_t<64, 8>(a, kmap, vmap, items, n_items, box_t, grid, s, pdl);
 }
 
 cudaError_t launch_combine(const AttnArgs& a, const SplitGroup* groups, int32_t n_groups, int D,
-                           cudaStream_t s) {
+                           cudaStream_t s, bool pdl) {
   if (n_groups <= 0) return cudaSuccess;
-  if (D == 128)
-    combine_kernel<128><<<n_groups, 256, 0, s>>>(a, groups);
-  else
-    combine_kernel<64><<<n_groups, 256, 0, s>>>(a, groups);
+  cudaError_t e = D == 128 ? launch_kernel(combine_kernel<128>, n_groups, 256, 0, s, pdl, a, groups)
+                           : launch_kernel(combine_kernel<64>, n_groups, 256, 0, s, pdl, a, groups);
+  if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
 

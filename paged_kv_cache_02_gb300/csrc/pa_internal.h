@@ -75,6 +75,30 @@ struct AttnArgs {
   uint4* v_pool;
 };
 
+// Launches kernel k on stream s; with pdl, as a programmatic dependent of the
+// previous kernel in the stream: its CTAs may start once every CTA of that kernel has
+// signalled (griddepcontrol.launch_dependents, at its start), i.e. in the tail of
+// that kernel, instead of after its last CTA exits. The attention kernels of one call
+// read nothing another one writes (disjoint outputs and partial rows); each waits for
+// its predecessor to complete before it exits (griddepcontrol.wait), so a kernel's
+// completion still implies that of every kernel before it, and the combine pass waits
+// at its start.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_kernel(void (*k)(KArgs...), int grid, int block, int smem, cudaStream_t s,
+                          bool pdl, Args... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)grid);
+  cfg.blockDim = dim3((unsigned)block);
+  cfg.dynamicSmemBytes = (size_t)smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = pdl ? 1 : 0;
+  return cudaLaunchKernelEx(&cfg, k, args...);
+}
+
 // Device address of the error word of the current device (set up once per device).
 int* device_error_word();
 
@@ -109,13 +133,13 @@ cudaError_t launch_copy_blocks(void* k_pool, void* v_pool, const int32_t* src, c
                                cudaStream_t s);
 cudaError_t launch_decode(const AttnArgs& a, const CUtensorMap& kmap, const CUtensorMap& vmap,
                           const Item* items, int32_t n_items, int D, int rows_max, int box_t,
-                          int grid, cudaStream_t s);
+                          int grid, cudaStream_t s, bool pdl = false);
 cudaError_t launch_combine(const AttnArgs& a, const SplitGroup* groups, int32_t n_groups, int D,
-                           cudaStream_t s);
+                           cudaStream_t s, bool pdl = false);
 int decode_smem_bytes(int D, int rows_max);
 cudaError_t launch_tc(const AttnArgs& a, const CUtensorMap& kmap, const CUtensorMap& vmap,
                       const CUtensorMap& qmap, const CUtensorMap& omap, const Item* items,
-                      int32_t n_items, int box_t, int grid, cudaStream_t s);
+                      int32_t n_items, int box_t, int grid, cudaStream_t s, bool pdl = false);
 // 3-D tiled map over q viewed as [total_q][Hq][D] bf16 with box (64, g, rows / g), 128-byte
 // swizzle: one box is `rows` packed rows (tokens x the g heads of a KV head) of one D half.
 pa_status make_q_map(CUtensorMap* map, const void* q, int64_t total_q, int Hq, int D, int g,
@@ -124,7 +148,7 @@ int tc_smem_bytes();
 // Items of 129..256 rows: two 128-row tiles per CTA that share every K/V tile.
 cudaError_t launch_tc2(const AttnArgs& a, const CUtensorMap& kmap, const CUtensorMap& vmap,
                        const CUtensorMap& qmap, const CUtensorMap& omap, const Item* items,
-                       int32_t n_items, int box_t, int grid, cudaStream_t s);
+                       int32_t n_items, int box_t, int grid, cudaStream_t s, bool pdl = false);
 // 3-D tiled map over the output viewed as [total_q][Hq][D] (fp32 or bf16), box (16,
 // min(g, 32), 32 / min(g, 32)): one box is 16 columns of the 32 packed rows (tokens x
 // heads of one KV head) of a warp. The staging side is swizzled (64-byte rows of fp32
@@ -136,7 +160,7 @@ int tc2_smem_bytes();
 // Items of at most 16 rows: keys on the 128-row side (S^T = K Q^T, O^T = V^T P^T).
 cudaError_t launch_tcd(const AttnArgs& a, const CUtensorMap& kmap, const CUtensorMap& vmap,
                        const CUtensorMap& qmap, const Item* items, int32_t n_items, int box_t,
-                       int grid, cudaStream_t s);
+                       int grid, cudaStream_t s, bool pdl = false);
 int tcd_smem_bytes();
 constexpr int kTcMinRowsDefault = 4;   // without the key-major kernel: rows from which the
                                        // tensor cores take a (sequence, KV head) pair

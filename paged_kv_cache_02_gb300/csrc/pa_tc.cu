@@ -259,6 +259,7 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
   __syncthreads();
   tc::fence_after_sync();
   const uint32_t tmem = sm.tmem_base;
+  if (threadIdx.x == 0) pdl_launch_dependents();
 
   if (warp == 0) {
     produce<true, kSW>(sm, a, kmap, qmap, items, n_items, box_t, lane);
@@ -696,6 +697,7 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
     tc::fence_after_sync();
     tc::tmem_dealloc(tmem, kTmemCols);
   }
+  pdl_wait();  // exit only after the kernel this one may overlap has completed
 }
 
 }  // namespace
@@ -704,13 +706,15 @@ int tc_smem_bytes() { return (int)sizeof(TcSmem) + 1024; }
 
 cudaError_t launch_tc(const AttnArgs& a, const CUtensorMap& kmap, const CUtensorMap& vmap,
                       const CUtensorMap& qmap, const CUtensorMap& omap, const Item* items,
-                      int32_t n_items, int box_t, int grid, cudaStream_t s) {
+                      int32_t n_items, int box_t, int grid, cudaStream_t s, bool pdl) {
   if (n_items <= 0) return cudaSuccess;
   const int smem = tc_smem_bytes();
   auto* k = a.wait_ns == kWaitLimitNsHost ? tc_kernel<false> : tc_kernel<true>;
   cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
-  k<<<grid, kThreadsTc, smem, s>>>(a, kmap, vmap, qmap, omap, items, n_items, box_t);
+  e = launch_kernel(k, grid, kThreadsTc, smem, s, pdl, a, kmap, vmap, qmap, omap, items,
+                    n_items, box_t);
+  if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
 

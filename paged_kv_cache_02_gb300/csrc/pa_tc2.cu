@@ -153,6 +153,7 @@ __global__ void __launch_bounds__(kThreads2, 1)
   __syncthreads();
   tc::fence_after_sync();
   const uint32_t tmem = sm.tmem_base;
+  if (threadIdx.x == 0) pdl_launch_dependents();
 
   if (warp == 0) {
     // ------------------------------------------------------------ TMA producer
@@ -644,6 +645,7 @@ __global__ void __launch_bounds__(kThreads2, 1)
     tc::fence_after_sync();
     tc::tmem_dealloc(tmem, kTmemCols);
   }
+  pdl_wait();  // exit only after the kernel this one may overlap has completed
 }
 
 }  // namespace
@@ -652,13 +654,15 @@ int tc2_smem_bytes() { return (int)sizeof(Tc2Smem) + 1024; }
 
 cudaError_t launch_tc2(const AttnArgs& a, const CUtensorMap& kmap, const CUtensorMap& vmap,
                        const CUtensorMap& qmap, const CUtensorMap& omap, const Item* items,
-                       int32_t n_items, int box_t, int grid, cudaStream_t s) {
+                       int32_t n_items, int box_t, int grid, cudaStream_t s, bool pdl) {
   if (n_items <= 0) return cudaSuccess;
   const int smem = tc2_smem_bytes();
   auto* k = a.wait_ns == kWaitLimitNsHost ? tc2_kernel<false> : tc2_kernel<true>;
   cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
-  k<<<grid, kThreads2, smem, s>>>(a, kmap, vmap, qmap, omap, items, n_items, box_t);
+  e = launch_kernel(k, grid, kThreads2, smem, s, pdl, a, kmap, vmap, qmap, omap, items,
+                    n_items, box_t);
+  if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
 

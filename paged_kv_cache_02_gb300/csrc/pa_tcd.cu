@@ -390,6 +390,7 @@ __global__ void __launch_bounds__(kThreadsD, 1)
   __syncthreads();
   tc::fence_after_sync();
   const uint32_t tmem = sm.tmem_base;
+  if (threadIdx.x == 0) pdl_launch_dependents();
 
   if (warp == 0) {
     // ------------------------------------------------------------ TMA producer
@@ -749,6 +750,7 @@ __global__ void __launch_bounds__(kThreadsD, 1)
     tc::fence_after_sync();
     tc::tmem_dealloc(tmem, kTmemCols);
   }
+  pdl_wait();  // exit only after the kernel this one may overlap has completed
 }
 
 }  // namespace
@@ -757,13 +759,15 @@ int tcd_smem_bytes() { return (int)sizeof(TcdSmem) + 1024; }
 
 cudaError_t launch_tcd(const AttnArgs& a, const CUtensorMap& kmap, const CUtensorMap& vmap,
                        const CUtensorMap& qmap, const Item* items, int32_t n_items, int box_t,
-                       int grid, cudaStream_t s) {
+                       int grid, cudaStream_t s, bool pdl) {
   if (n_items <= 0) return cudaSuccess;
   const int smem = tcd_smem_bytes();
   auto* k = a.wait_ns == kWaitLimitNsHost ? tcd_kernel<false> : tcd_kernel<true>;
   cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
-  k<<<grid, kThreadsD, smem, s>>>(a, kmap, vmap, qmap, items, n_items, box_t);
+  e = launch_kernel(k, grid, kThreadsD, smem, s, pdl, a, kmap, vmap, qmap, items, n_items,
+                    box_t);
+  if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
 
