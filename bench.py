@@ -47,9 +47,13 @@ def log(*a):
     print(*a, file=sys.stderr, flush=True)
 
 
-def kernel_source_hash(kernel: str) -> str:
+def kernel_source_hash(kernels) -> str:
+    """sha256 of the sources of the listed kernels (a name or a list), each file once."""
+    if isinstance(kernels, str):
+        kernels = [kernels]
+    files = sorted({f for k in kernels for f in KERNEL_SOURCES[k]})
     h = hashlib.sha256()
-    for f in KERNEL_SOURCES[kernel]:
+    for f in files:
         with open(os.path.join(ROOT, "paged_kv_cache_02_gb300", "csrc", f), "rb") as fh:
             h.update(fh.read())
     return h.hexdigest()[:16]
@@ -369,13 +373,15 @@ def run_gpu(args, w, cfg_name, rank, local, world):
     n_tc1 = st["n_tc_items"] - n_tcd - n_tc2
     kinds = {k: n for k, n in (("decode", st["n_dec_items"]), ("tc", n_tc1), ("tc2", n_tc2),
                                ("tcd", n_tcd)) if n}
-    kernel = next(iter(kinds)) if len(kinds) == 1 and not st["n_split_groups"] else None
+    # DRAM bytes of the call's attention kernels per call, from the committed capture,
+    # while those kernels' sources hash to the captured ones
     traffic = None
-    if kernel and os.path.exists(PROFILE_TRAFFIC):
+    if kinds and not st["n_split_groups"] and os.path.exists(PROFILE_TRAFFIC):
         with open(PROFILE_TRAFFIC) as f:
             prof = json.load(f)
         entry = prof.get(args.config_key)
-        if entry and entry.get("kernel_hash") == kernel_source_hash(kernel):
+        if entry and sorted(entry.get("kernels", [])) == sorted(kinds) and \
+                entry.get("kernel_hash") == kernel_source_hash(sorted(kinds)):
             traffic = entry.get("dram_bytes_per_launch")
     if bound == "hbm":
         achieved = (kv_b + q_b) / attn_s / 1e9
@@ -764,7 +770,7 @@ def main():
     ap.add_argument("--subset", choices=["prefill", "decode"], default=None,
                     help="run only the prefill or decode sequences of a mixed batch (3, 4)")
     ap.add_argument("--max-seqs", type=int, default=None,
-                    help="keep only the first N sequences (profiler captures of config 2)")
+                    help="keep only the first N sequences (config 2) or N conversations + 2N decodes (config 3), for profiler captures")
     ap.add_argument("--block-size", type=int, default=None,
                     help="block-size sweep: config 2 or 4 with another block size")
     ap.add_argument("--contiguous", action="store_true",

@@ -868,21 +868,6 @@ static pa_status attention_impl(pa_plan_t p, void* d_out, pa_dtype out_dtype, co
     if (st != PA_OK) return st;
     int sms = device_sms();
     if (sms <= 0) return PA_ERR_CUDA;
-    if (p->n_tcd > 0) {
-      CUtensorMap qmap16, kmap_g, vmap_g;
-      st = pa::make_q_map(&qmap16, d_q, p->total_q, p->Hq, p->D, p->g, pa::kTcdRows);
-      if (st != PA_OK) return st;
-      st = pa::make_pool_map_grouped(&kmap_g, d_k_pool, num_blocks, p->block_size, p->Hkv, box_t);
-      if (st != PA_OK) return st;
-      st = pa::make_pool_map_grouped(&vmap_g, d_v_pool, num_blocks, p->block_size, p->Hkv, box_t);
-      if (st != PA_OK) return st;
-      const int grid = std::min(p->n_tcd, sms);
-      cudaError_t e = pa::launch_tcd(a, kmap_g, vmap_g, qmap16,
-                                     reinterpret_cast<const Item*>(ws + p->off_tcd), p->n_tcd,
-                                     box_t, grid, s, pdl);
-      if (e != cudaSuccess) return PA_ERR_CUDA;
-      pdl = true;
-    }
     CUtensorMap qmap;
     st = pa::make_q_map(&qmap, d_q, p->total_q, p->Hq, p->D, p->g, pa::kTcRows);
     if (st != PA_OK) return st;
@@ -904,6 +889,24 @@ static pa_status attention_impl(pa_plan_t p, void* d_out, pa_dtype out_dtype, co
       cudaError_t e = pa::launch_tc(a, kmap, vmap, qmap, omap,
                                     reinterpret_cast<const Item*>(ws + p->off_tc), p->n_tc, box_t,
                                     grid, s, pdl);
+      if (e != cudaSuccess) return PA_ERR_CUDA;
+      pdl = true;
+    }
+    // the key-major (decode) items last: measured 0.5-1.7% faster on the mixed
+    // configurations than first, the memory-bound decode kernel filling the tail
+    // of the multi-token kernels
+    if (p->n_tcd > 0) {
+      CUtensorMap qmap16, kmap_g, vmap_g;
+      st = pa::make_q_map(&qmap16, d_q, p->total_q, p->Hq, p->D, p->g, pa::kTcdRows);
+      if (st != PA_OK) return st;
+      st = pa::make_pool_map_grouped(&kmap_g, d_k_pool, num_blocks, p->block_size, p->Hkv, box_t);
+      if (st != PA_OK) return st;
+      st = pa::make_pool_map_grouped(&vmap_g, d_v_pool, num_blocks, p->block_size, p->Hkv, box_t);
+      if (st != PA_OK) return st;
+      const int grid = std::min(p->n_tcd, sms);
+      cudaError_t e = pa::launch_tcd(a, kmap_g, vmap_g, qmap16,
+                                     reinterpret_cast<const Item*>(ws + p->off_tcd), p->n_tcd,
+                                     box_t, grid, s, pdl);
       if (e != cudaSuccess) return PA_ERR_CUDA;
       pdl = true;
     }

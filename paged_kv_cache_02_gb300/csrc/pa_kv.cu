@@ -52,41 +52,49 @@ __global__ void slot_mapping_kernel(const int32_t* __restrict__ bt, int32_t num_
 constexpr int kCopyThreads = 256;
 constexpr int kCopyUnroll = 4;
 
-// Moves `n_vec` 16-byte vectors of token rows: vector i is chunk i % vec_per_row of
-// row i / vec_per_row. Source rows are contiguous; the destination row comes
-// from the slot list. K and V are moved by the same thread. Rows whose entry in
-// `skip` (optional, one byte per row) is non-zero are left to another kernel.
+// Moves token rows of 16-byte vectors: one warp per row at a time, the row's slot read
+// once, then the row's vectors spread over the lanes (512 contiguous bytes per warp
+// access), kCopyUnroll loads of K and of V in flight per lane before their stores.
+// Source rows are contiguous; the destination row comes from the slot list. Rows whose
+// entry in `skip` (optional, one byte per row) is non-zero are left to another kernel.
 __global__ void __launch_bounds__(kCopyThreads) write_kv_kernel(
     const uint4* __restrict__ k_new, const uint4* __restrict__ v_new,
-    const int64_t* __restrict__ slots, int64_t n_vec, int64_t vec_per_row,
+    const int64_t* __restrict__ slots, int64_t n_rows, int vec_per_row,
     uint4* __restrict__ k_pool, uint4* __restrict__ v_pool, int64_t n_slots,
     const uint8_t* __restrict__ skip, int* err) {
-  const int64_t stride = (int64_t)gridDim.x * kCopyThreads;
-  for (int64_t base = blockIdx.x * (int64_t)kCopyThreads + threadIdx.x; base < n_vec;
-       base += stride * kCopyUnroll) {
-    uint4 kv[kCopyUnroll], vv[kCopyUnroll];
-    int64_t dst[kCopyUnroll];
+  constexpr int kWarps = kCopyThreads / 32;
+  const int lane = threadIdx.x & 31;
+  const int64_t n_warps = (int64_t)gridDim.x * kWarps;
+  for (int64_t row = (int64_t)blockIdx.x * kWarps + (threadIdx.x >> 5); row < n_rows;
+       row += n_warps) {
+    if (skip && __ldg(skip + row)) continue;
+    const int64_t slot = __ldg(slots + row);
+    if (slot < 0) continue;
+    if (slot >= n_slots) {
+      if (lane == 0) record_error(err, PA_DEVERR_SLOT_RANGE);
+      continue;
+    }
+    const uint4* ks = k_new + row * vec_per_row;
+    const uint4* vs = v_new + row * vec_per_row;
+    uint4* kd = k_pool + slot * vec_per_row;
+    uint4* vd = v_pool + slot * vec_per_row;
+    for (int c0 = 0; c0 < vec_per_row; c0 += 32 * kCopyUnroll) {
+      uint4 kv[kCopyUnroll], vv[kCopyUnroll];
 #pragma unroll
-    for (int u = 0; u < kCopyUnroll; ++u) {
-      const int64_t i = base + u * stride;
-      dst[u] = -1;
-      if (i < n_vec) {
-        const int64_t row = i / vec_per_row;
-        const int64_t slot = (skip && __ldg(skip + row)) ? -1 : __ldg(slots + row);
-        if (slot >= n_slots) {
-          record_error(err, PA_DEVERR_SLOT_RANGE);
-        } else if (slot >= 0) {
-          dst[u] = slot * vec_per_row + (i - row * vec_per_row);
-          kv[u] = __ldcs(k_new + i);
-          vv[u] = __ldcs(v_new + i);
+      for (int u = 0; u < kCopyUnroll; ++u) {
+        const int c = c0 + 32 * u + lane;
+        if (c < vec_per_row) {
+          kv[u] = __ldcs(ks + c);
+          vv[u] = __ldcs(vs + c);
         }
       }
-    }
 #pragma unroll
-    for (int u = 0; u < kCopyUnroll; ++u) {
-      if (dst[u] >= 0) {
-        k_pool[dst[u]] = kv[u];
-        v_pool[dst[u]] = vv[u];
+      for (int u = 0; u < kCopyUnroll; ++u) {
+        const int c = c0 + 32 * u + lane;
+        if (c < vec_per_row) {
+          kd[c] = kv[u];
+          vd[c] = vv[u];
+        }
       }
     }
   }
@@ -197,11 +205,17 @@ cudaError_t launch_write_kv(const void* k_new, const void* v_new, const int64_t*
                             int64_t row_bytes, int* err, cudaStream_t s,
                             const uint8_t* skip) {
   const int64_t vec_per_row = row_bytes / 16;
-  const int64_t n_vec = n_new * vec_per_row;
-  if (n_vec == 0) return cudaSuccess;
-  write_kv_kernel<<<copy_grid(n_vec), kCopyThreads, 0, s>>>(
-      static_cast<const uint4*>(k_new), static_cast<const uint4*>(v_new), slots, n_vec,
-      vec_per_row, static_cast<uint4*>(k_pool), static_cast<uint4*>(v_pool), n_slots, skip, err);
+  if (n_new <= 0 || vec_per_row <= 0) return cudaSuccess;
+  if (vec_per_row > INT32_MAX) return cudaErrorInvalidValue;
+  // one warp per row; at most 8 resident 256-thread CTAs per SM
+  int sms = sm_count();
+  if (sms <= 0) sms = 1;
+  const int64_t want = (n_new + kCopyThreads / 32 - 1) / (kCopyThreads / 32);
+  const int grid = (int)(want < (int64_t)sms * 8 ? want : (int64_t)sms * 8);
+  write_kv_kernel<<<grid, kCopyThreads, 0, s>>>(
+      static_cast<const uint4*>(k_new), static_cast<const uint4*>(v_new), slots, n_new,
+      (int)vec_per_row, static_cast<uint4*>(k_pool), static_cast<uint4*>(v_pool), n_slots, skip,
+      err);
   return cudaGetLastError();
 }
 

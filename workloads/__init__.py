@@ -253,7 +253,7 @@ def _cfg2(device, max_seqs=None, block_size=None, contiguous=False):
                    q_scale=1.0 / math.sqrt(D))
 
 
-def _cfg3(device, contiguous=False):
+def _cfg3(device, contiguous=False, max_seqs=None):
     """64 conversations (history + new turn) as two sub-requests each, plus 128 decodes.
 
     Conversation c has ``hist`` cached tokens and ``qn`` new prompt tokens. Its
@@ -276,6 +276,12 @@ def _cfg3(device, contiguous=False):
     kk = np.array([int(_randint(g, 1, int(h) // 64, 1)[0]) for h in hist], dtype=np.int64)
     r = 32 * kk
     Ld = _randint(g, 256, 4096, ND)
+    if max_seqs is not None:
+        # the first max_seqs conversations and 2 * max_seqs decode sequences of the same
+        # length draw (the block placement is drawn for the smaller pool)
+        C, ND = min(C, int(max_seqs)), min(ND, 2 * int(max_seqs))
+        hist, qn, kk, Ld = hist[:C], qn[:C], kk[:C], Ld[:ND]
+        r = 32 * kk
     # block needs per region
     full = hist + qn
     nblk = [_cdiv(int(x), B) for x in full]
@@ -422,8 +428,9 @@ def _cfg5(device, cow: bool):
 def make(config, device="cpu", max_seqs=None, block_size=None, contiguous=False) -> Workload:
     """Workload for config 1..5 or "5cow", values drawn on ``device``.
 
-    ``max_seqs`` keeps only the first sequences of the decode-only batch (config 2): the
-    same draw, smaller, for profiler captures that must stay small. ``block_size``
+    ``max_seqs`` keeps only the first sequences of the decode-only batch (config 2), or
+    the first conversations and twice as many decode sequences of config 3: the same
+    length draw, smaller, for profiler captures that must stay small. ``block_size``
     (configs 2 and 4) and ``contiguous`` (configs 2, 3 and 4) give the block-size sweep's
     and the paged-against-contiguous comparison's variants of the same draw.
     """
@@ -436,7 +443,7 @@ def make(config, device="cpu", max_seqs=None, block_size=None, contiguous=False)
     if config in (2, "2"):
         return _cfg2(device, max_seqs, block_size, contiguous)
     if config in (3, "3"):
-        return _cfg3(device, contiguous)
+        return _cfg3(device, contiguous, max_seqs)
     if config in (4, "4"):
         return _cfg4(device, block_size, contiguous)
     if config in (5, "5"):
