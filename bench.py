@@ -279,7 +279,8 @@ def run_gpu(args, w, cfg_name, rank, local, world):
     ev = {k: [torch.cuda.Event(enable_timing=True) for _ in range(args.steps + 1)]
           for k in ("a", "b", "c", "d", "f", "e")}
 
-    def step(i=None):
+    def step(i=None, fused=None):
+        fused = args.fused if fused is None else fused
         if i is not None:
             ev["a"][i].record(stream)
         pa.pa_slot_mapping(bt, w.num_blocks, w.block_size, sid, pos, out=slots)
@@ -289,7 +290,7 @@ def run_gpu(args, w, cfg_name, rank, local, world):
             pa.pa_copy_blocks(kp, vp, src, dst)
         if i is not None:
             ev["c"][i].record(stream)
-        if args.unfused:
+        if not fused:
             pa.pa_write_kv(kn, vn, slots, kp, vp)
         if i is not None:
             ev["d"][i].record(stream)
@@ -298,7 +299,7 @@ def run_gpu(args, w, cfg_name, rank, local, world):
         pa.pa_plan_upload(plan, ws)
         if i is not None:
             ev["f"][i].record(stream)
-        if args.unfused:
+        if not fused:
             pa.pa_attention_planned(plan, q, kp, vp, bt, cl, ql, ws, out=out)
         else:
             # the KV write of the decode rows inside the key-major kernel, the other rows'
@@ -337,17 +338,38 @@ def run_gpu(args, w, cfg_name, rank, local, world):
            for k, (a, b) in {"slot_mapping": ("a", "b"), "copy_blocks": ("b", "c"),
                              "write_kv": ("c", "d"), "attention": ("d", "e"),
                              "plan_upload": ("d", "f"), "attention_kernels": ("f", "e")}.items()}
-    if not args.unfused:
+    if args.fused:
         per["write_kv"] = "inside the attention call (fused): the decode rows in the " \
                           "key-major kernel, the other rows in one write kernel first"
     err = pa.pa_get_device_error(reset=True)
     if err:
         raise RuntimeError(f"device error {pa.DEVERR.get(err, err)} in the timed region")
 
+    # the other form of the step (fused KV write + attention, or the two calls), timed the
+    # same way for comparison; not part of `value`
+    n_alt = max(3, min(args.steps, 50))
+    a_ev, b_ev = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    for _ in range(3):
+        step(fused=not args.fused)
+    torch.cuda.synchronize(dev)
+    a_ev.record(stream)
+    for _ in range(n_alt):
+        step(fused=not args.fused)
+    b_ev.record(stream)
+    torch.cuda.synchronize(dev)
+    err = pa.pa_get_device_error(reset=True)
+    if err:
+        raise RuntimeError(f"device error {pa.DEVERR.get(err, err)} timing the other step form")
+    alt_ms = a_ev.elapsed_time(b_ev) / n_alt
+    alt_step = {"path": ("pa_write_kv + pa_attention_planned" if args.fused else
+                         "pa_attention_write_planned (fused KV write + attention)"),
+                "ms_per_step": alt_ms, "tokens_per_s": w.total_q / (alt_ms / 1000.0),
+                "steps": n_alt}
+
     T = w.total_q
     value = T * args.steps * world / (elapsed_ms / 1000.0)
     n_tc1 = st["n_tc_items"] - st["n_tc_pair_items"] - st["n_tc_decode_items"]
-    st_write = 1 if (args.unfused or st["n_tc_decode_items"] == 0 or
+    st_write = 1 if (not args.fused or st["n_tc_decode_items"] == 0 or
                      plan_fused_rows(w) < T) else 0
     launches_per_step = 1 + (1 if n_pairs else 0) + st_write + (1 if st["n_dec_items"] else 0) + \
         (1 if n_tc1 else 0) + (1 if st["n_tc_pair_items"] else 0) + \
@@ -481,8 +503,9 @@ def run_gpu(args, w, cfg_name, rank, local, world):
         "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
         "config": cfg_name,
         "out_dtype": args.out,
-        "step_path": ("pa_write_kv + pa_attention_planned" if args.unfused else
-                      "pa_attention_write_planned (fused KV write + attention)"),
+        "step_path": ("pa_attention_write_planned (fused KV write + attention)" if args.fused
+                      else "pa_write_kv + pa_attention_planned"),
+        "other_step_form": alt_step,
         "attention_kernels_ms": attn_ms,
         "roofline": roof,
         "hbm_gbs_attention": (kv_b + q_b) / attn_s / 1e9,
@@ -695,12 +718,13 @@ def block_manager_host(w, steps=32):
     import ctypes as C
     import numpy as np
     import paged_kv_cache_02_gb300 as pa
-    nb, B = int(w.k_pool.shape[0]), int(w.block_size)
+    B = int(w.block_size)
     N = len(w.context_lens)
     L = np.asarray(w.context_lens, np.int64)
     hist = np.maximum(L - np.asarray(w.query_lens, np.int64), 0).astype(np.int32)
-    spare = nb - int(sum(-(-int(x) // B) for x in hist))
-    steps = max(1, min(steps, (spare // max(1, N)) * B // 2))
+    # every history held unshared (the manager's pool, not the workload's, is sized for
+    # that: a shared-prefix workload's pool is smaller), plus room for the timed steps
+    nb = int(sum(-(-int(x) // B) for x in hist)) + N * (-(-steps // B) + 1)
     mb = int(max(-(-(int(x) + steps) // B) for x in hist)) + 1
     bm = pa.BlockManager(nb, B)
     ids = np.arange(N, dtype=np.int64)
@@ -752,8 +776,10 @@ def main():
     ap.add_argument("--impl", choices=["gb300", "reference"], default="gb300")
     ap.add_argument("--config", default="3",
                     help="workload: 1..5 or 5cow (default 3, the Pensieve-style mixed batch)")
-    ap.add_argument("--unfused", action="store_true",
-                    help="the step as pa_write_kv + pa_attention instead of the fused call")
+    ap.add_argument("--fused", action="store_true",
+                    help="time the step as the fused call (pa_attention_write_planned) instead "
+                         "of pa_write_kv + pa_attention_planned; the other form is reported "
+                         "beside it either way")
     ap.add_argument("--no-configs", action="store_true",
                     help="skip the per-config attention sweep (key 'configs')")
     ap.add_argument("--cpu-budget", type=float, default=12.0)
