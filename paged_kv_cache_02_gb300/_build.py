@@ -12,7 +12,7 @@ HERE = os.path.dirname(os.path.abspath(__file__))
 CSRC = os.path.join(HERE, "csrc")
 BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "libpa.so")
-SOURCES = ["pa_api.cu", "pa_kv.cu", "pa_dec.cu", "pa_tc.cu", "pa_tc2.cu", "pa_tc3.cu", "pa_tcd.cu",
+SOURCES = ["pa_api.cu", "pa_kv.cu", "pa_dec.cu", "pa_tc.cu", "pa_tc2.cu", "pa_tcd.cu",
            "pa_bm.cpp"]
 HEADERS = ["pa_internal.h", "pa_ptx.cuh", "pa_tc.cuh", os.path.join("..", "..", "include", "pa.h")]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]

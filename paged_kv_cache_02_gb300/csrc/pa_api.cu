@@ -148,7 +148,6 @@ struct pa_plan_s {
   int32_t num_seqs, Hq, Hkv, D, block_size, max_blocks, g;
   int64_t total_q;
   int32_t n_dec, n_tc, n_tc2, n_tcd, n_groups;
-  bool tc3;                 // the 128-row items run on the three-score-buffer kernel
   int32_t dec_rows_max;
   uint64_t wait_ns;         // bound on each pipeline wait of the kernels
   int64_t n_part_rows;
@@ -456,7 +455,7 @@ pa_status pa_plan_create(const int32_t* h_context_lens, const int32_t* h_query_l
   // buffers and eight softmax warps for one tile). By default pairs are used when the
   // multi-token tensor-core work of the batch is memory-bound: fewer FLOPs per byte of
   // K/V (read once per sequence and KV head), Q and output than the machine balance.
-  bool use_pair = pair_enabled && o.tc_pair > 0 && o.tc_pair != 2;
+  bool use_pair = pair_enabled && o.tc_pair > 0;
   if (pair_enabled && o.tc_pair == 0) {
     double flops = 0.0, bytes = 0.0;
     for (int32_t s = 0; s < num_seqs; ++s) {
@@ -583,7 +582,6 @@ pa_status pa_plan_create(const int32_t* h_context_lens, const int32_t* h_query_l
   p->max_blocks = max_blocks_per_seq; p->g = g; p->total_q = total_q;
   p->n_dec = (int32_t)dec.size(); p->n_tc = (int32_t)tc.size(); p->n_tc2 = (int32_t)tc2.size();
   p->n_tcd = (int32_t)tcd.size();
-  p->tc3 = o.tc_pair == 2;
   p->n_groups = (int32_t)groups.size();
   p->dec_rows_max = dec_rows_max; p->n_part_rows = part_rows;
   p->wait_ns = o.wait_limit_ns > 0 ? (uint64_t)o.wait_limit_ns : pa::kWaitLimitNsHost;
@@ -888,13 +886,9 @@ static pa_status attention_impl(pa_plan_t p, void* d_out, pa_dtype out_dtype, co
     }
     if (p->n_tc > 0) {
       const int grid = std::min(p->n_tc, sms);
-      cudaError_t e =
-          p->tc3 ? pa::launch_tc3(a, kmap, vmap, qmap, omap,
-                                  reinterpret_cast<const Item*>(ws + p->off_tc), p->n_tc, box_t,
-                                  grid, s, pdl)
-                 : pa::launch_tc(a, kmap, vmap, qmap, omap,
-                                 reinterpret_cast<const Item*>(ws + p->off_tc), p->n_tc, box_t,
-                                 grid, s, pdl);
+      cudaError_t e = pa::launch_tc(a, kmap, vmap, qmap, omap,
+                                    reinterpret_cast<const Item*>(ws + p->off_tc), p->n_tc, box_t,
+                                    grid, s, pdl);
       if (e != cudaSuccess) return PA_ERR_CUDA;
       pdl = true;
     }

@@ -157,12 +157,6 @@ cudaError_t launch_tc2(const AttnArgs& a, const CUtensorMap& kmap, const CUtenso
 pa_status make_out_map(CUtensorMap* map, void* out, int64_t total_q, int Hq, int D, int g,
                        bool bf16);
 int tc2_smem_bytes();
-// Items of at most 128 rows on the kernel with three TMEM score buffers and one O
-// accumulator (the score of tile n + 3 overlaps the softmax of tiles n + 1, n + 2).
-cudaError_t launch_tc3(const AttnArgs& a, const CUtensorMap& kmap, const CUtensorMap& vmap,
-                       const CUtensorMap& qmap, const CUtensorMap& omap, const Item* items,
-                       int32_t n_items, int box_t, int grid, cudaStream_t s, bool pdl = false);
-int tc3_smem_bytes();
 // Items of at most 16 rows: keys on the 128-row side (S^T = K Q^T, O^T = V^T P^T).
 cudaError_t launch_tcd(const AttnArgs& a, const CUtensorMap& kmap, const CUtensorMap& vmap,
                        const CUtensorMap& qmap, const Item* items, int32_t n_items, int box_t,

@@ -162,46 +162,6 @@ def test_tensor_core_one_tile_bf16_and_wide_groups(pa, g):
     assert np.all(d <= bound), float((d - bound).max())
 
 
-TC3_CASES = [
-    # (g, block_size, chunk): row counts around the 128-row tile edge, one to many key
-    # tiles (three score buffers wrap around several times), forced splits
-    (1, 16, 0), (1, 32, 128), (8, 32, 0), (8, 8, 256), (4, 256, 0), (16, 64, 192),
-    (64, 32, 0), (128, 32, 0),
-]
-
-
-@pytest.mark.parametrize("g,B,chunk", TC3_CASES)
-def test_tensor_core_three_buffer_tiles(pa, g, B, chunk):
-    """128-row items on the kernel with three TMEM score buffers and one O accumulator
-    (plan option tc_pair = 2): against the oracle on every row, fp32 and bf16 outputs,
-    and against the one-tile kernel."""
-    rows = [129, 200, 256, 257, 384, 511, 64, 1]
-    q = [max(1, -(-r // g)) for r in rows]
-    L = [qq + extra for qq, extra in zip(q, [0, 37, 300, 5, 900, 128, 700, 2000])]
-    w = workloads.make_custom(L, q, Hq=2 * g, Hkv=2, D=128, block_size=B, seed=1300 + g + B)
-    kw = dict(max_chunk_tokens=chunk) if chunk else {}
-    (_, _), run3, want = full_check(pa, w, tc_pair=2, **kw)
-    st = run3["plan"].stats()
-    assert st["n_tc_pair_items"] == 0 and st["n_tc_items"] > st["n_tc_decode_items"]
-    (_, _), run1, _ = full_check(pa, w, tc_pair=-1, **kw)
-    assert torch.allclose(run3["out"], run1["out"], atol=gu.ATOL_MAX, rtol=0)
-    got16 = gu.gpu_step(pa, w, out_dtype=torch.bfloat16, tc_pair=2, **kw)
-    d = np.abs(got16["out"].float().cpu().numpy() - want)
-    bound = np.abs(want) * 2.0 ** -8 + gu.ATOL_MAX
-    assert np.all(d <= bound), float((d - bound).max())
-
-
-def test_tensor_core_three_buffer_many_short_items(pa):
-    """Hundreds of one-key-tile items per CTA on the three-buffer kernel: the score
-    issuer runs ahead across item boundaries (the next item's Q waits for the previous
-    item's scores), every buffer and barrier phase wraps many times."""
-    n = 600
-    w = workloads.make_custom([40 + (i % 5) for i in range(n)], [20 + (i % 7) for i in range(n)],
-                              Hq=8, Hkv=2, D=128, block_size=16, seed=808, write_new=False)
-    (_, _), got, _ = full_check(pa, w, tc_pair=2)
-    assert got["plan"].stats()["n_tc_items"] >= n
-
-
 def test_tensor_core_pair_single_tile_items(pa):
     """Many consecutive two-tile items of one key tile each: every item's last S follows
     its first, so the next item's Q can land while the softmax warps still finish the
@@ -320,7 +280,6 @@ NO_SPLIT = 1 << 14   # a chunk longer than every key range: no split-KV items
 @pytest.mark.parametrize("kw", [{}, {"max_chunk_tokens": NO_SPLIT},
                                 {"tc_pair": 1, "max_chunk_tokens": NO_SPLIT},
                                 {"tc_pair": -1, "max_chunk_tokens": NO_SPLIT},
-                                {"tc_pair": 2, "max_chunk_tokens": NO_SPLIT},
                                 {"tc_min_rows": -1, "max_chunk_tokens": NO_SPLIT},
                                 {"tc_decode": -1}, {"max_chunk_tokens": 192}])
 def test_lazy_rescale_on_growing_scores(pa, kw):
@@ -377,7 +336,7 @@ def test_subrequests_match_single_request(pa):
     two_w.k_pool, two_w.v_pool, two_w.num_blocks = full.k_pool, full.v_pool, full.num_blocks
     two_w.q = torch.cat([full.q[:r], full.q[L - qn:]])
     want = gu.oracle_rows(full, gu.oracle_step(full))
-    for kw in ({}, {"tc_pair": 1}, {"tc_pair": -1}, {"tc_pair": 2}):
+    for kw in ({}, {"tc_pair": 1}, {"tc_pair": -1}):
         one = gu.gpu_step(pa, full, **kw)["out"]
         two = gu.gpu_step(pa, two_w, **kw)["out"]
         gu.assert_attention_close(one.cpu().numpy(), want, "one request")
