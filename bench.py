@@ -422,44 +422,55 @@ def run_gpu(args, w, cfg_name, rank, local, world):
     pin = lambda t: t.cpu().pin_memory()
     h_in = [pin(w.q), pin(w.k_new), pin(w.v_new), pin(bt), pin(cl), pin(ql), pin(sid), pin(pos),
             pin(src), pin(dst)]
-    h_outs = [torch.empty(out.shape, dtype=out.dtype).pin_memory() for _ in range(2)]
+    depth = 3                               # steps in flight
+    h_outs = [torch.empty(out.shape, dtype=out.dtype).pin_memory() for _ in range(depth)]
     h2d = sum(t.numel() * t.element_size() for t in h_in)
     d2h = h_outs[0].numel() * h_outs[0].element_size()
-    # two sets of device buffers: step i uses set i % 2
-    d_sets = [[torch.empty_like(t, device=dev) for t in h_in] for _ in range(2)]
-    d_outs = [out, torch.empty_like(out)]
+    # sets of device buffers: step i uses set i % depth
+    d_sets = [[torch.empty_like(t, device=dev) for t in h_in] for _ in range(depth)]
+    d_outs = [out] + [torch.empty_like(out) for _ in range(depth - 1)]
+    # each buffer set has its own plan workspace (the step's plan tables go up with the
+    # step's inputs)
+    ws_sets = [plan.workspace(dev) for _ in range(depth)]
     s_h2d = torch.cuda.Stream(dev)
     s_d2h = torch.cuda.Stream(dev)
-    free_ev = [None, None]
+    free_ev = [None] * depth
 
-    # Two steps in flight, as a serving loop runs them: the host builds step i's plan and
-    # enqueues its work while the GPU still works on step i - 1, then waits for step
-    # i - 1 to finish (its output is in host memory by then). Step i's inputs go up on a
-    # copy stream and its output comes back on another, so that they overlap the
-    # kernels of the neighbouring steps; events order the reuse of each buffer set (the
-    # copies into set i % 2 wait until step i - 2 has read it and its output is home).
-    # Every step still copies all of its own inputs in and its whole output out.
+    # Several steps in flight, as a serving loop runs them: the host builds step i's plan
+    # and enqueues its work while the GPU still works on the steps before, then waits for
+    # step i - depth + 1 to finish (its output is in host memory by then). Step i's
+    # inputs go up on a copy stream and its output comes back on another, so that they
+    # overlap the kernels of the neighbouring steps; events order the reuse of each
+    # buffer set (the copies into set i % depth wait until step i - depth has read it
+    # and its output is home).
+    # The step's plan tables go up on the copy stream too, ahead of its inputs: uploaded
+    # by the attention call on the compute stream, they would queue on the copy engine
+    # behind the next step's inputs and hold the kernels back. Every step still copies
+    # all of its own inputs in and its whole output out.
     inflight = []
 
     def e2e_step(i):
-        k = i % 2
-        dset, d_out, h_out = d_sets[k], d_outs[k], h_outs[k]
+        k = i % depth
+        dset, d_out, h_out, ws_k = d_sets[k], d_outs[k], h_outs[k], ws_sets[k]
+        p2 = pa.Plan(w.context_lens, w.query_lens, w.Hq, w.Hkv, w.D, w.block_size, w.max_blocks,
+                     **plan_kw)
+        if p2.workspace_bytes > ws_k.numel():
+            raise RuntimeError("plan workspace grew between steps")
         if free_ev[k] is not None:
             s_h2d.wait_event(free_ev[k])
         with torch.cuda.stream(s_h2d):
+            pa.pa_plan_upload(p2, ws_k)
             for hb, db in zip(h_in, dset):
                 db.copy_(hb, non_blocking=True)
         in_ev = torch.cuda.Event()
         in_ev.record(s_h2d)
         dq, dkn, dvn, dbt, dcl, dql, dsid, dpos, dsrc, ddst = dset
-        p2 = pa.Plan(w.context_lens, w.query_lens, w.Hq, w.Hkv, w.D, w.block_size, w.max_blocks,
-                     **plan_kw)
         stream.wait_event(in_ev)
         pa.pa_slot_mapping(dbt, w.num_blocks, w.block_size, dsid, dpos, out=slots)
         if n_pairs:
             pa.pa_copy_blocks(kp, vp, dsrc, ddst)
         pa.pa_write_kv(dkn, dvn, slots, kp, vp)
-        pa.pa_attention(p2, dq, kp, vp, dbt, dcl, dql, out=d_out, workspace=ws)
+        pa.pa_attention_planned(p2, dq, kp, vp, dbt, dcl, dql, ws_k, out=d_out)
         comp_ev = torch.cuda.Event()
         comp_ev.record(stream)
         s_d2h.wait_event(comp_ev)
@@ -469,7 +480,7 @@ def run_gpu(args, w, cfg_name, rank, local, world):
         done.record(s_d2h)
         free_ev[k] = done
         inflight.append((done, p2))
-        if len(inflight) > 1:
+        if len(inflight) > depth - 1:
             ev0, p0 = inflight.pop(0)
             ev0.synchronize()
             p0.close()
@@ -483,7 +494,8 @@ def run_gpu(args, w, cfg_name, rank, local, world):
     for i in range(min(3, args.warmup)):
         e2e_step(i)
     e2e_drain()
-    e2e_steps = max(3, min(args.steps, 200))
+    # at least 40 steps (about 0.3 s): a single host-side hiccup then moves the figure little
+    e2e_steps = max(40, min(args.steps, 200))
     barrier(world)
     torch.cuda.synchronize(dev)
     t0 = time.perf_counter()
@@ -513,10 +525,12 @@ def run_gpu(args, w, cfg_name, rank, local, world):
         "per_call_ms": per,
         "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": int(h2d),
                 "d2h_bytes_per_step": int(d2h), "steps": e2e_steps,
-                "includes": "H2D of the step's inputs from pinned memory, host plan build, "
-                            "slot mapping, copies, KV write, attention, D2H of the output; "
-                            "two steps in flight (the host prepares step i while the GPU "
-                            "runs step i - 1), H2D and D2H on their own streams"},
+                "includes": "H2D of the step's inputs from pinned memory, host plan build "
+                            "and upload of its work tables (not counted in h2d_bytes: under "
+                            "1 MB), slot mapping, copies, KV write, attention, D2H of the "
+                            f"output; {depth} steps in flight (the host prepares step i "
+                            "while the GPU runs the steps before), H2D (tables first) and "
+                            "D2H on their own streams"},
         "gpu_launches": launches_per_step * args.steps,
         "clocks": clocks.summary(h0, h1),
         "plan": {k: st[k] for k in ("n_dec_items", "n_tc_items", "n_split_groups", "chunk_tokens")},
