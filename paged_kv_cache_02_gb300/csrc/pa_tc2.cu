@@ -9,23 +9,32 @@
 //     S_t(j) = Q_t K_j^T  ->  softmax_t(j)  ->  O_t += P_t(j) V_j
 // that keep the tensor core busy while the other chain's softmax runs.
 //
-// Warps (11, one persistent CTA per SM):
+// The scores of a chain come in halves of 64 keys, each into the chain's one score
+// buffer, and P goes to one of two separate P buffers: the score of the next half
+// can then be computed as soon as the softmax has read the current one, while that
+// softmax runs and before its P V is issued, instead of after that P V as when P is
+// written over the scores. Per half h of a chain:
+//     S_t(h) = Q_t K_h^T  ->  softmax_t(h)  ->  O_t += P_t(h) V_h
+// with S_t(h + 1) issued once softmax_t(h) has loaded S_t(h), and P_t(h) written
+// once the P V of half h - 2 (the previous user of its P buffer) is done.
+//
+// Warps (12, one persistent CTA per SM):
 //   0        TMA producer: both tiles' Q rows once per item (single buffer);
 //            K and V tiles of 128 keys gathered per block piece into two
 //            2-stage rings with their own barriers, so that K_{j+2} is loaded
-//            as soon as both chains have multiplied by K_j.
-//   1, 2     MMA issuer of chain A / B: S_t(j); then P_t(j) V_j once the
-//            softmax wrote P_t(j) over S_t(j) in TMEM; then waits for that
-//            P V before the next S_t (P and S share the TMEM columns).
-//   3-6      softmax of chain A, 7-10 softmax of chain B: one thread per row
-//            (its TMEM lane) reads its whole 128-key score row with one TMEM
-//            load; P is written back over S as bf16 pairs, O is rescaled in
-//            TMEM only when the running maximum grows by more than 2^8. The
-//            epilogue stages O through shared memory so that every global
-//            store writes whole 64-byte row pieces.
-// TMEM: S/P of A [0,128), of B [128,256); O of A [256,384), of B [384,512).
-// TMEM loads/stores and whole-warp waits are always warp-uniform; every wait is
-// bounded.
+//            as soon as both chains have multiplied by both halves of K_j.
+//   1        score issuer of both chains (operands in shared memory only).
+//   2, 3     P V issuer of chain A / B (P from TMEM): each issues into its own
+//            chain's accumulator only.
+//   4-7      softmax of chain A, 8-11 softmax of chain B: one thread per row
+//            (its TMEM lane) reads its 64 scores of a half with one TMEM load,
+//            writes P to the half's P buffer as bf16 pairs and rescales O in TMEM
+//            only when the running maximum grows by more than 2^8. The epilogue
+//            stages O through shared memory so that every global store writes
+//            whole 64-byte row pieces.
+// TMEM (chain t at columns 128 t .. 128 t + 127 and 256 + 128 t ..): S_t [0, 64),
+// P_t buffers [64, 96) and [96, 128); O_t in the upper half. TMEM loads/stores and
+// whole-warp waits are always warp-uniform; every wait is bounded.
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
@@ -42,17 +51,21 @@ namespace {
 constexpr int kKeys = 128;              // keys per tile
 constexpr int kD = 128;
 constexpr int kStages = 2;
-constexpr int kThreads2 = 352;          // 11 warps
+constexpr int kThreads2 = 384;          // 12 warps
+constexpr int kHalfKeys = 64;           // keys per score half
 constexpr int kHalf = 128 * 128;        // 128 rows x 64 elements, swizzled (16 KB)
 constexpr int kSoftmaxWarps = 8;
 constexpr int kStageCols = 16;          // epilogue staging: 32 rows x 16 fp32 per warp
 constexpr float kRescaleLog2 = 8.f;
 constexpr uint32_t kTmemCols = 512;
 
-constexpr uint32_t kIdescS = tc::idesc_bf16_f32(128, kKeys, false);
+constexpr uint32_t kIdescS = tc::idesc_bf16_f32(128, kHalfKeys, false);
 constexpr uint32_t kIdescO = tc::idesc_bf16_f32(128, kD, true);
 
 __host__ __device__ constexpr uint32_t s_col(int t) { return (uint32_t)t * 128u; }
+__host__ __device__ constexpr uint32_t p_col(int t, int b) {
+  return (uint32_t)t * 128u + 64u + (uint32_t)b * 32u;
+}
 __host__ __device__ constexpr uint32_t o_col(int t) { return 256u + (uint32_t)t * 128u; }
 
 struct Tc2Smem {
@@ -67,9 +80,11 @@ struct Tc2Smem {
   uint64_t k_full[kStages], k_empty[kStages];
   uint64_t v_full[kStages], v_empty[kStages];
   uint64_t q_full, q_free;
-  uint64_t s_full[2], o_done[2], o_free[2];
-  uint64_t p_full[2][2];                // [chain][key half]: P of keys 64 h .. 64 h + 63 written
-  uint64_t drain[2];
+  uint64_t s_full[2], s_free[2];        // [chain]: score of a half done / read by the softmax
+  uint64_t p_full[2][2];                // [chain][P buffer]: P of a half written
+  uint64_t o_done[2][2];                // [chain][P buffer]: the P V that read it is done
+  uint64_t o_free[2];                   // [chain]: the epilogue read O
+  uint64_t drain[3];
   uint32_t tmem_base;
   int k_issued[kStages], k_consumed[kStages];
   int v_issued[kStages], v_consumed[kStages];
@@ -123,23 +138,25 @@ __global__ void __launch_bounds__(kThreads2, 1)
   if (threadIdx.x == 0) {
     for (int s = 0; s < kStages; ++s) {
       mbar_init(&sm.k_full[s], 1);
-      mbar_init(&sm.k_empty[s], 2);    // both chains' S
+      mbar_init(&sm.k_empty[s], 1);    // the score issuer, after both chains' last half
       mbar_init(&sm.v_full[s], 1);
-      mbar_init(&sm.v_empty[s], 2);    // both chains' P V
+      mbar_init(&sm.v_empty[s], 2);    // both chains' P V issuers
       sm.k_issued[s] = sm.k_consumed[s] = 0;
       sm.v_issued[s] = sm.v_consumed[s] = 0;
     }
     mbar_init(&sm.q_full, 1);
-    mbar_init(&sm.q_free, 2);          // both chains' last S of the item
+    mbar_init(&sm.q_free, 1);          // the score issuer, after the item's last score
     for (int i = 0; i < 3; ++i) mbar_init(&sm.info_full[i], 1);
     for (int t = 0; t < 2; ++t) {
       mbar_init(&sm.s_full[t], 1);
-      mbar_init(&sm.p_full[t][0], 128);
-      mbar_init(&sm.p_full[t][1], 128);
-      mbar_init(&sm.o_done[t], 1);
+      mbar_init(&sm.s_free[t], 128);
+      for (int b = 0; b < 2; ++b) {
+        mbar_init(&sm.p_full[t][b], 128);
+        mbar_init(&sm.o_done[t][b], 1);
+      }
       mbar_init(&sm.o_free[t], 128);
-      mbar_init(&sm.drain[t], 1);
     }
+    for (int i = 0; i < 3; ++i) mbar_init(&sm.drain[i], 1);
     sm.q_issued = 0;
     sm.q_consumed = 0;
     sm.abort_flag = 0;
@@ -260,59 +277,85 @@ __global__ void __launch_bounds__(kThreads2, 1)
       __syncwarp();
     }
     if (!ok) sm.abort_flag = 1;
-  } else if (warp == 1 || warp == 2) {
-    // ------------------------------------------------------------ MMA issuer of chain t
-    // Phase bounds: every barrier this thread waits on is at most one phase ahead of
-    // the wait. k_full / v_full of tile n + 2 need both chains' S / P V of tile n;
-    // p_full(n + 1) needs s_full(n + 1), which this thread commits after the wait
-    // for p_full(n); o_free of item k + 1 needs the P V of item k + 1.
-    const int t = warp - 1;
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ score issuer
+    // Per half h (two per K tile, counted over the CTA's items) and chain t: once
+    // softmax t has loaded S_t(h - 1) (s_free), S_t(h) = Q_t K_h^T into the chain's score
+    // buffer. Both operands are in shared memory.
+    // Phase bounds: s_free[t](h) needs s_full[t](h), committed here after the wait for
+    // s_free[t](h - 1); k_full of tile n + 2 needs k_empty of tile n and q_full of item
+    // k + 1 needs q_free of item k, both committed here after this thread's waits.
     if (lane == 0) {
-      int n = 0, k = 0;   // tile, item of the CTA (each chain sees every tile)
       bool ok = true;
-      // tile counts are read one item ahead, off the critical path
-      Item nx{};
-      if (W.cnt > 0) nx = items[W.at(0)];
-      for (int sidx = 0; sidx < W.cnt && ok; ++sidx, ++k) {
-        const int kv_begin = nx.kv_begin, kv_end = nx.kv_end;
-        const int nt = tiles_of(nx);
-        if (sidx + 1 < W.cnt) nx = items[W.at(sidx + 1)];
-        if (!mbar_wait(&sm.q_full, (uint32_t)k & 1u, a.err, wait_bound<kSW>(a))) { ok = false; break; }
-        if (t == 0) sm.q_consumed += 1;
-        tc::fence_after_sync();
-        const uint64_t qd = tc::smem_desc_sw128(smem_addr(&sm.q[t][0][0]), 16, 1024);
-        for (int j = 0; j < nt; ++j, ++n) {
+      int n = 0, h = 0;                           // tile, half of the CTA
+      for (int sidx = 0; sidx < W.cnt && ok; ++sidx) {
+        const Item it = items[W.at(sidx)];
+        const int nt = tiles_of(it);
+        if (!mbar_wait(&sm.q_full, (uint32_t)sidx & 1u, a.err, wait_bound<kSW>(a))) { ok = false; break; }
+        sm.q_consumed += 1;
+        for (int j = 0; j < nt && ok; ++j, ++n) {
           const int st = n % kStages;
           if (!mbar_wait(&sm.k_full[st], ph(n, kStages), a.err, wait_bound<kSW>(a))) { ok = false; break; }
-          if (t == 0) sm.k_consumed[st] += 1;
-          tc::fence_after_sync();
-          // S_t = Q_t K^T: 8 steps of 16 dims; step kk starts (kk / 4) D halves and
-          // (kk % 4) 32-byte chunks into both operands
-          const uint64_t kd = tc::smem_desc_sw128(smem_addr(&sm.k[st][0][0]), 16, 1024);
-          tc::mma_bf16_c<false>(tmem + s_col(t), qd, kd, kIdescS);
+          sm.k_consumed[st] += 1;
+          const uint64_t kd0 = tc::smem_desc_sw128(smem_addr(&sm.k[st][0][0]), 16, 1024);
+          for (int hk = 0; hk < 2 && ok; ++hk, ++h) {
+            // keys 64 hk .. 64 hk + 63 of the tile: rows 64 hk .. of both D halves
+            const uint64_t kd = kd0 + (uint64_t)((hk * kHalfKeys * 128) >> 4);
+            for (int t = 0; t < 2; ++t) {
+              if (h > 0 &&
+                  !mbar_wait(&sm.s_free[t], (uint32_t)(h - 1) & 1u, a.err, wait_bound<kSW>(a))) {
+                ok = false;
+                break;
+              }
+              tc::fence_after_sync();
+              // 8 steps of 16 dims; step kk starts (kk / 4) D halves and (kk % 4) 32-byte
+              // chunks into both operands
+              const uint64_t qd = tc::smem_desc_sw128(smem_addr(&sm.q[t][0][0]), 16, 1024);
+              tc::mma_bf16_c<false>(tmem + s_col(t), qd, kd, kIdescS);
 #pragma unroll
-          for (int kk = 1; kk < kD / 16; ++kk) {
-            const uint64_t off = (uint64_t)(((kk >> 2) * kHalf + (kk & 3) * 32) >> 4);
-            tc::mma_bf16_c<true>(tmem + s_col(t), qd + off, kd + off, kIdescS);
+              for (int kk = 1; kk < kD / 16; ++kk) {
+                const uint64_t off = (uint64_t)(((kk >> 2) * kHalf + (kk & 3) * 32) >> 4);
+                tc::mma_bf16_c<true>(tmem + s_col(t), qd + off, kd + off, kIdescS);
+              }
+              tc::commit(&sm.s_full[t]);
+            }
           }
-          tc::commit(&sm.s_full[t]);
+          if (!ok) break;
           tc::commit(&sm.k_empty[st]);
-          if (j + 1 == nt) tc::commit(&sm.q_free);  // this chain's last S of the item
-          // at an item's first tile, O_t must have been read out by the previous
-          // item's epilogue
-          if (j == 0 && !mbar_wait(&sm.o_free[t], ((uint32_t)k & 1u) ^ 1u, a.err, wait_bound<kSW>(a))) {
-            ok = false;
-            break;
-          }
+          if (j + 1 == nt) tc::commit(&sm.q_free);  // the item's last score
+        }
+      }
+      if (!ok) sm.abort_flag = 1;
+      tc::commit(&sm.drain[0]);
+      mbar_wait(&sm.drain[0], 0, a.err);
+    }
+    __syncwarp();
+  } else if (warp == 2 || warp == 3) {
+    // ------------------------------------------------------------ P V issuer of chain t
+    // Per half h: O_t += P_t(h) V_h once softmax t wrote P_t(h) into P buffer h % 2;
+    // P from TMEM, V from shared memory. This thread issues into O_t only.
+    // Phase bounds: p_full[t][b] of the next use of buffer b needs o_done[t][b] of this
+    // use, committed here after the wait for this use; v_full of tile n + 2 needs
+    // v_empty of tile n from both chains' issuers; o_free[t] of item k + 1 needs the
+    // first P V of item k + 1.
+    const int t = warp - 2;
+    if (lane == 0) {
+      bool ok = true;
+      int n = 0, h = 0;                           // tile, half of the CTA
+      for (int sidx = 0; sidx < W.cnt && ok; ++sidx) {
+        const Item it = items[W.at(sidx)];
+        const int nt = tiles_of(it);
+        for (int j = 0; j < nt && ok; ++j, ++n) {
+          const int st = n % kStages;
           if (!mbar_wait(&sm.v_full[st], ph(n, kStages), a.err, wait_bound<kSW>(a))) { ok = false; break; }
           if (t == 0) sm.v_consumed[st] += 1;
           // Keys of the tile in the item's range, rounded up to the 16-key step of P V:
           // only those V rows are read. At the item's last tile the rows between the
-          // range's end and that step hold whatever the block tail holds: zero them
-          // (at most 15 rows) so that 0 * (non-finite) never reaches O. Both chains
-          // write the same zeros, each before its own P V.
-          const int key0 = kv_begin + j * kKeys;
-          const int valid = min(kKeys, kv_end - key0);
+          // range's end and that step hold whatever the block tail holds: zero them (at
+          // most 15 rows) so that 0 * (non-finite) never reaches O. Both chains write
+          // the same zeros, each before its own P V.
+          const int key0 = it.kv_begin + j * kKeys;
+          const int valid = min(kKeys, it.kv_end - key0);
           const int kk_end = (valid + 15) >> 4;
           if (valid < kk_end * 16) {
             for (int r = valid; r < kk_end * 16; ++r) {
@@ -326,18 +369,27 @@ __global__ void __launch_bounds__(kThreads2, 1)
             }
             tc::fence_async_shared();
           }
+          // at an item's first tile, O_t must have been read out by the previous item's
+          // epilogue
+          if (j == 0 &&
+              !mbar_wait(&sm.o_free[t], ((uint32_t)sidx & 1u) ^ 1u, a.err, wait_bound<kSW>(a))) {
+            ok = false;
+            break;
+          }
           // V as the MN-major B operand: step kk covers keys 16 kk .. 16 kk + 15 (rows
           // of 128 bytes), the two D halves are kHalf apart
           const uint64_t vd = tc::smem_desc_sw128(smem_addr(&sm.v[st][0][0]), kHalf, 1024);
-          // P_t(j) is written over S_t(j) by the softmax in two key halves; the P V of
-          // the first half runs while the second half is computed
-#pragma unroll
-          for (int hk = 0; hk < 2; ++hk) {
-            if (!mbar_wait(&sm.p_full[t][hk], (uint32_t)n & 1u, a.err, wait_bound<kSW>(a))) { ok = false; break; }
+          for (int hk = 0; hk < 2 && ok; ++hk, ++h) {
+            const int b = h & 1;
+            if (!mbar_wait(&sm.p_full[t][b], (uint32_t)(h >> 1) & 1u, a.err, wait_bound<kSW>(a))) {
+              ok = false;
+              break;
+            }
             tc::fence_after_sync();
 #pragma unroll
-            for (int kk = 4 * hk; kk < 4 * hk + 4; ++kk) {
-              const uint32_t pa = tmem + s_col(t) + (uint32_t)kk * 8u;
+            for (int kq = 0; kq < 4; ++kq) {
+              const int kk = 4 * hk + kq;           // 16-key step of the tile
+              const uint32_t pa = tmem + p_col(t, b) + (uint32_t)kq * 8u;
               const uint64_t vk = vd + (uint64_t)((kk * 16 * 128) >> 4);
               if (kk == 0) {
                 if (j > 0)
@@ -348,41 +400,40 @@ __global__ void __launch_bounds__(kThreads2, 1)
                 tc::mma_bf16_ts_c<true>(tmem + o_col(t), pa, vk, kIdescO);
               }
             }
+            tc::commit(&sm.o_done[t][b]);
           }
           if (!ok) break;
-          tc::commit(&sm.o_done[t]);
           tc::commit(&sm.v_empty[st]);
-          // the next S_t overwrites the columns this P V reads
-          if (!mbar_wait(&sm.o_done[t], (uint32_t)n & 1u, a.err, wait_bound<kSW>(a))) { ok = false; break; }
         }
       }
       if (!ok) sm.abort_flag = 1;
-      tc::commit(&sm.drain[t]);
-      mbar_wait(&sm.drain[t], 0, a.err);
+      tc::commit(&sm.drain[1 + t]);
+      mbar_wait(&sm.drain[1 + t], 0, a.err);
     }
     __syncwarp();
   } else {
     // ------------------------------------------------------------ softmax of chain t
-    // One thread per row (its TMEM lane): the whole 128-key score row is read from
-    // TMEM with one load, so S is never re-read and no other thread needs the row's
-    // maximum or sum. P goes back over S 16 columns at a time and is handed to the
-    // issuer in two key halves.
-    // Phase bounds: s_full[t](n + 1) needs p_full[t](n), which these threads arrive
-    // on; o_done[t](n + 1) needs p_full[t](n + 1); v_full of tile n + 2 needs this
-    // chain's P V of tile n. So no barrier is ever two phases ahead of a wait here.
-    const int t = (warp - 3) >> 2;                // 0 = tile A (warps 3-6), 1 = tile B
+    // One thread per row (its TMEM lane): the 64 scores of a half are read from TMEM
+    // with one load, so no other thread needs the row's maximum or sum. The score
+    // buffer is released right after that load; P goes to the half's P buffer.
+    // Phase bounds: s_full[t](h + 1) needs s_free[t](h), on which these threads arrive
+    // after their wait for s_full[t](h); o_done[t][b] of the next use of buffer b needs
+    // p_full[t][b] of that use, written here after the wait for this use; v_full of tile
+    // n + 2 needs this chain's P V of tile n. So no barrier is ever two phases ahead of
+    // a wait here.
+    const int t = (warp - 4) >> 2;                // 0 = tile A (warps 4-7), 1 = tile B
     const int quad = warp & 3;
     const int row = quad * 32 + lane;             // row within the tile = TMEM lane
     const uint32_t t_lane = tmem + ((uint32_t)(quad * 32) << 16);
-    float* stg = sm.stage[warp - 3];
-    int n = 0;                                    // tile of the CTA
+    float* stg = sm.stage[warp - 4];
+    int h = 0;                                    // half of the CTA
     bool ok = true;
     for (int sidx = 0, k = 0; sidx < W.cnt && ok; ++sidx, ++k) {
       // The producer published the item's description in slot k % 3 before its Q load.
       // The slot (and its barrier's next phase) is rewritten for item k + 3 only after
-      // every S of item k + 2, and the first of those needs this chain's P of item
-      // k + 1's last tile: the slot stays valid through this item's epilogue, and the
-      // barrier is never two phases ahead of this wait.
+      // every score of item k + 2, and the first of those needs this chain's load of
+      // item k + 1's last score: the slot stays valid through this item's epilogue, and
+      // the barrier is never two phases ahead of this wait.
       if (!mbar_wait_warp(&sm.info_full[k % 3], ph(k, 3), a.err, wait_bound<kSW>(a))) { ok = false; break; }
       const Item& info = sm.info[k % 3];
       const int kv_begin = info.kv_begin, kv_end = info.kv_end, row_count = info.row_count;
@@ -398,23 +449,27 @@ __global__ void __launch_bounds__(kThreads2, 1)
       const int trow = t * 128 + row;             // row within the item
       const bool warp_live = t * 128 + quad * 32 < row_count;
       float m_used = -INFINITY, l = 0.f;
-      for (int j = 0; j < nt; ++j, ++n) {
-        if (!mbar_wait_warp(&sm.s_full[t], (uint32_t)n & 1u, a.err, wait_bound<kSW>(a))) { ok = false; break; }
+      for (int hs = 0; hs < 2 * nt; ++hs, ++h) {
+        const int b = h & 1;
+        if (!mbar_wait_warp(&sm.s_full[t], (uint32_t)h & 1u, a.err, wait_bound<kSW>(a))) { ok = false; break; }
         tc::fence_after_sync();
-        const int key0 = kv_begin + j * kKeys;
+        const int key0 = kv_begin + hs * kHalfKeys;
+        float s[kHalfKeys];
+        if (warp_live) tc::tmem_ld64(t_lane + s_col(t), s);
+        // the score buffer may take the next half's score
+        tc::fence_before_sync();
+        mbar_arrive(&sm.s_free[t]);
+        float pk[4][8];                           // P as bf16 pairs, 8 columns per 16 keys
         if (warp_live) {
-          const bool masked = key0 + kKeys - 1 > lim;
-          float s[128];
-          tc::tmem_ld128(t_lane + s_col(t), s);
-          if (masked) {
+          if (key0 + kHalfKeys - 1 > lim) {
 #pragma unroll
-            for (int i = 0; i < 128; ++i)
+            for (int i = 0; i < kHalfKeys; ++i)
               if (key0 + i > lim) s[i] = -INFINITY;
           }
           // running maximum of the raw scores (the scale is positive)
           float m4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
 #pragma unroll
-          for (int i = 0; i < 64; ++i) m4[i & 3] = fmax3(m4[i & 3], s[2 * i], s[2 * i + 1]);
+          for (int i = 0; i < kHalfKeys / 2; ++i) m4[i & 3] = fmax3(m4[i & 3], s[2 * i], s[2 * i + 1]);
           const float m_new =
               fmaxf(m_used, fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3])) * a.scale_log2);
           if (m_used == -INFINITY) m_used = m_new;
@@ -427,16 +482,34 @@ __global__ void __launch_bounds__(kThreads2, 1)
             l *= alpha;
             m_used = m_new;
           }
-          // P = 2^(scale * s - m) as bf16 pairs: keys 16 c .. 16 c + 15 go to
-          // columns 8 c .. 8 c + 7; a masked score is -inf and gives exactly 0
+          if (warp_rescale) {
+            // O_t must be idle: the P V of half h - 1 (of this item: the first half of an
+            // item never rescales) is done. tcgen05.ld / st are warp-collective, so the
+            // warp rescales together (factor 1 for rows that need none).
+            if (!mbar_wait_warp(&sm.o_done[t][(h - 1) & 1], (uint32_t)((h - 1) >> 1) & 1u, a.err,
+                                wait_bound<kSW>(a))) {
+              ok = false;
+              break;
+            }
+            tc::fence_after_sync();
+#pragma unroll 1
+            for (int c8 = 0; c8 < kD / 16; ++c8) {
+              float o[16];
+              const uint32_t addr = t_lane + o_col(t) + (uint32_t)c8 * 16u;
+              tc::tmem_ld16(addr, o);
+#pragma unroll
+              for (int i = 0; i < 16; ++i) o[i] *= alpha;
+              tc::tmem_st16(addr, o);
+            }
+          }
+          // P = 2^(scale * s - m) as bf16 pairs: keys 16 c .. 16 c + 15 go to columns
+          // 8 c .. 8 c + 7 of the P buffer; a masked score is -inf and gives exactly 0
           const float neg_m = (m_used == -INFINITY) ? 0.f : -m_used;
           const uint64_t sc2 = f2_pack(a.scale_log2, a.scale_log2);
           const uint64_t nm2 = f2_pack(neg_m, neg_m);
           uint64_t sum2[2] = {0ull, 0ull};
-          __syncwarp();  // tcgen05.st is .sync.aligned: reconverge after the per-row update
 #pragma unroll
-          for (int c = 0; c < 8; ++c) {
-            float pk[8];
+          for (int c = 0; c < 4; ++c) {
 #pragma unroll
             for (int i2 = 0; i2 < 8; ++i2) {
               const int i = c * 8 + i2;
@@ -444,29 +517,7 @@ __global__ void __launch_bounds__(kThreads2, 1)
               f2_unpack(f2_fma(f2_pack(s[2 * i], s[2 * i + 1]), sc2, nm2), x0, x1);
               const float p0 = fast_exp2(x0), p1 = fast_exp2(x1);
               sum2[i & 1] = f2_add(sum2[i & 1], f2_pack(p0, p1));
-              pk[i2] = __uint_as_float(pack_bf16(p0, p1));
-            }
-            tc::tmem_st8(t_lane + s_col(t) + (uint32_t)c * 8u, pk);
-            if (c == 3 && warp_rescale) {
-              // O_t is idle until the first half's P V: its issuer waited for the
-              // previous P V before this S. Done here, once half the score row is dead,
-              // 16 columns at a time; tcgen05.ld / st are warp-collective, so the warp
-              // rescales together (factor 1 for rows that need none).
-#pragma unroll 1
-              for (int c8 = 0; c8 < kD / 16; ++c8) {
-                float o[16];
-                const uint32_t addr = t_lane + o_col(t) + (uint32_t)c8 * 16u;
-                tc::tmem_ld16(addr, o);
-#pragma unroll
-                for (int i = 0; i < 16; ++i) o[i] *= alpha;
-                tc::tmem_st16(addr, o);
-              }
-            }
-            if ((c & 3) == 3) {
-              // keys 64 (c / 4) .. + 63 are in TMEM: that half's P V may start
-              tc::tmem_wait_st();
-              tc::fence_before_sync();
-              mbar_arrive(&sm.p_full[t][c >> 2]);
+              pk[c][i2] = __uint_as_float(pack_bf16(p0, p1));
             }
           }
           float sa, sb;
@@ -474,24 +525,32 @@ __global__ void __launch_bounds__(kThreads2, 1)
           l += sa + sb;
         } else {
           // rows past the item: zero P, so that no stale bits reach the tensor core
-          float z[16];
 #pragma unroll
-          for (int i = 0; i < 16; ++i) z[i] = 0.f;
+          for (int c = 0; c < 4; ++c)
 #pragma unroll
-          for (int c = 0; c < 4; ++c) {
-            tc::tmem_st16(t_lane + s_col(t) + (uint32_t)c * 16u, z);
-            if (c & 1) {
-              tc::tmem_wait_st();
-              tc::fence_before_sync();
-              mbar_arrive(&sm.p_full[t][c >> 1]);
-            }
-          }
+            for (int i2 = 0; i2 < 8; ++i2) pk[c][i2] = 0.f;
         }
+        // the P buffer is free once the P V of half h - 2 is done
+        if (!mbar_wait_warp(&sm.o_done[t][b], ((uint32_t)(h >> 1) & 1u) ^ 1u, a.err, wait_bound<kSW>(a))) {
+          ok = false;
+          break;
+        }
+        tc::fence_after_sync();
+        __syncwarp();  // tcgen05.st is .sync.aligned: reconverge after the per-row work
+#pragma unroll
+        for (int c = 0; c < 4; ++c) tc::tmem_st8(t_lane + p_col(t, b) + (uint32_t)c * 8u, pk[c]);
+        tc::tmem_wait_st();
+        tc::fence_before_sync();
+        mbar_arrive(&sm.p_full[t][b]);
       }
       if (!ok) break;
-      // ---- epilogue: the chain's last P V (its issuer waited for the one before, so
-      // o_done is at most one phase ahead)
-      if (!mbar_wait_warp(&sm.o_done[t], (uint32_t)(n - 1) & 1u, a.err, wait_bound<kSW>(a))) { ok = false; break; }
+      // ---- epilogue: the chain's last P V (o_done of its buffer is at most one phase
+      // ahead: the next use of that buffer needs this chain's P of the next item)
+      if (!mbar_wait_warp(&sm.o_done[t][(h - 1) & 1], (uint32_t)((h - 1) >> 1) & 1u, a.err,
+                          wait_bound<kSW>(a))) {
+        ok = false;
+        break;
+      }
       tc::fence_after_sync();
       // A warp whose 32 rows all belong to the item (and go to the output, not to
       // split partials) hands O / l to the TMA: it writes 16-column pieces of its rows
