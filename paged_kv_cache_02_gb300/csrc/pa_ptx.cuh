@@ -106,24 +106,6 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, int* e
   }
 }
 
-// mbar_wait without suspending, for a wait that should end within a few hundred cycles
-// (the other arrivals are already on their way): a suspended thread would only be
-// woken later. Same bound as mbar_wait.
-__device__ __forceinline__ bool mbar_wait_poll(uint64_t* bar, uint32_t parity, int* err,
-                                               uint64_t limit_ns = kWaitLimitNs) {
-  const uint32_t a = smem_addr(bar);
-  for (int i = 0; i < 64; ++i)
-    if (mbar_test_wait(a, parity)) return true;
-  const uint64_t t0 = global_timer_ns();
-  while (!mbar_test_wait(a, parity)) {
-    if (global_timer_ns() - t0 > limit_ns) {
-      record_error(err, PA_DEVERR_TIMEOUT);
-      return false;
-    }
-  }
-  return true;
-}
-
 // Bound of a kernel's pipeline waits. The kernels are built twice: with kShortWaits
 // false the bound is the compile-time default (the build every normal call runs); with
 // true it is the call's bound (AttnArgs::wait_ns), selected only by a plan whose wait
