@@ -494,8 +494,9 @@ def run_gpu(args, w, cfg_name, rank, local, world):
     for i in range(min(3, args.warmup)):
         e2e_step(i)
     e2e_drain()
-    # at least 40 steps (about 0.3 s): a single host-side hiccup then moves the figure little
-    e2e_steps = max(40, min(args.steps, 200))
+    # at least 120 steps (about 1 s): the host link's occasional 20-50 ms stalls then
+    # move the figure little
+    e2e_steps = max(120, min(args.steps, 200))
     barrier(world)
     torch.cuda.synchronize(dev)
     t0 = time.perf_counter()
