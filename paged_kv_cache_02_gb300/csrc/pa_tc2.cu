@@ -32,8 +32,8 @@
 //            only when the running maximum grows by more than 2^8. The epilogue
 //            stages O through shared memory so that every global store writes
 //            whole 64-byte row pieces.
-// TMEM (chain t at columns 128 t .. 128 t + 127 and 256 + 128 t ..): S_t [0, 64),
-// P_t buffers [64, 96) and [96, 128); O_t in the upper half. TMEM loads/stores and
+// TMEM columns of chain t: S_t at 128 t + [0, 64), its P buffers at 128 t + [64, 96)
+// and 128 t + [96, 128), O_t at 256 + 128 t + [0, 128). TMEM loads/stores and
 // whole-warp waits are always warp-uniform; every wait is bounded.
 #include <cuda.h>
 #include <cuda_bf16.h>
