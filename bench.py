@@ -47,15 +47,42 @@ def log(*a):
     print(*a, file=sys.stderr, flush=True)
 
 
+def _code_only(text: str) -> str:
+    """C/C++ source without its comments and with whitespace runs collapsed: what the
+    compiler sees, so that editing a comment does not change a kernel's hash."""
+    out, i, n = [], 0, len(text)
+    while i < n:
+        c = text[i]
+        if c in "\"'":                                  # string or character literal
+            j = i + 1
+            while j < n and text[j] != c:
+                j += 2 if text[j] == "\\" else 1
+            out.append(text[i:j + 1])
+            i = j + 1
+        elif text.startswith("//", i):
+            j = text.find("\n", i)
+            i = n if j < 0 else j
+        elif text.startswith("/*", i):
+            j = text.find("*/", i + 2)
+            i = n if j < 0 else j + 2
+            out.append(" ")
+        else:
+            out.append(c)
+            i += 1
+    return " ".join("".join(out).split())
+
+
 def kernel_source_hash(kernels) -> str:
-    """sha256 of the sources of the listed kernels (a name or a list), each file once."""
+    """sha256 of the code (comments and whitespace aside) of the sources of the listed
+    kernels (a name or a list), each file once."""
     if isinstance(kernels, str):
         kernels = [kernels]
     files = sorted({f for k in kernels for f in KERNEL_SOURCES[k]})
     h = hashlib.sha256()
     for f in files:
-        with open(os.path.join(ROOT, "paged_kv_cache_02_gb300", "csrc", f), "rb") as fh:
-            h.update(fh.read())
+        with open(os.path.join(ROOT, "paged_kv_cache_02_gb300", "csrc", f),
+                  encoding="utf-8") as fh:
+            h.update(_code_only(fh.read()).encode())
     return h.hexdigest()[:16]
 
 
