@@ -196,7 +196,7 @@ def max_over_ranks(x: float, world: int) -> float:
 
 # ------------------------------------------------------------------ oracle (CPU) arm
 
-def oracle_step_sample(w, orc, host, n_threads, budget_s=10.0, max_passes=30):
+def oracle_step_sample(w, orc, host, n_threads, budget_s=10.0, max_passes=1000):
     """Times the oracle on bounded passes over the same workload: slot mapping, copies,
     KV write and attention for a contiguous block of query rows. Returns (rows/s, sample)."""
     import numpy as np
