@@ -248,7 +248,10 @@ def run_reference(args, w, cfg_name):
     host = {"q": u16(w.q), "k_pool": u16(w.k_pool), "v_pool": u16(w.v_pool),
             "k_new": u16(w.k_new), "v_new": u16(w.v_new)}
     n_threads = os.cpu_count() or 1
-    budget = max(1.0, min(20.0, 150.0 / max(1, args.steps + args.warmup)))
+    # about 150 s for the whole run whatever --steps and --warmup are: each step is at
+    # least one pass (about 0.1 s on the GPU machine's 16 cores), so with the default 1,000
+    # steps a step is one pass
+    budget = max(0.01, min(20.0, 150.0 / max(1, args.steps + args.warmup)))
     for _ in range(args.warmup):
         oracle_step_sample(w, orc, host, n_threads, budget_s=min(budget, 2.0), max_passes=1)
     vals, samples, total = [], [], 0.0
