@@ -198,44 +198,52 @@ def max_over_ranks(x: float, world: int) -> float:
 
 def oracle_step_sample(w, orc, host, n_threads, budget_s=10.0, max_passes=1000):
     """Times the oracle on bounded passes over the same workload: slot mapping, copies,
-    KV write and attention for a contiguous block of query rows. Returns (rows/s, sample)."""
+    KV write and attention for R query rows spread evenly over the whole batch (so the
+    sample has the batch's mix of context lengths). Returns (rows/s, sample, seconds)."""
     import numpy as np
-    from workloads import host_bits as u16
     T = w.total_q
-    rows_per_pass = T
-    # estimated cost per row (visible keys * heads) to bound one pass to ~budget/3
+    # cost of each row (visible keys x heads) for sizing a pass to about budget / 3
     pref = np.concatenate([[0], np.cumsum(w.query_lens)])
     seq_of_row = np.repeat(np.arange(w.num_seqs), w.query_lens)
     pos = w.context_lens[seq_of_row] - w.query_lens[seq_of_row] + (np.arange(T) - pref[seq_of_row])
     cost = (pos + 1).astype(np.float64) * w.Hq * w.D * 2  # MACs per row
-    t_probe = time.perf_counter()
-    probe_rows = np.arange(min(T, 8), dtype=np.int64)
-    orc.attention(host["q"], host["k_pool"], host["v_pool"], w.block_table, w.context_lens,
-                  w.query_lens, rows=probe_rows, n_threads=n_threads)
-    dt_probe = max(1e-6, time.perf_counter() - t_probe)
-    macs_per_s = max(1e6, cost[:len(probe_rows)].sum() / dt_probe)
-    cum = np.cumsum(cost)
-    limit = macs_per_s * budget_s / 3.0
-    rows_per_pass = int(max(1, min(T, np.searchsorted(cum, limit) + 1)))
-    rows = np.arange(rows_per_pass, dtype=np.int64)
-    kp, vp = host["k_pool"].copy(), host["v_pool"].copy()
+    spread = lambda r: np.unique(np.linspace(0, T - 1, max(1, min(T, r))).astype(np.int64))
+    key = ("_macs_per_s", n_threads)                      # measured once per process
+    if key not in host:
+        probe_rows = spread(16)
+        t_probe = time.perf_counter()
+        orc.attention(host["q"], host["k_pool"], host["v_pool"], w.block_table,
+                      w.context_lens, w.query_lens, rows=probe_rows, n_threads=n_threads)
+        dt_probe = max(1e-6, time.perf_counter() - t_probe)
+        host[key] = max(1e6, cost[probe_rows].sum() / dt_probe)
+    macs_per_s = host[key]
+    rows = spread(int(macs_per_s * budget_s / 3.0 / cost.mean()) + 1)
+    R = len(rows)
+    # working copies of the pools, made once per process (a pass writes into them)
+    if "_kp" not in host:
+        host["_kp"], host["_vp"] = host["k_pool"].copy(), host["v_pool"].copy()
+    kp, vp = host["_kp"], host["_vp"]
+    # the write in proportion: when the new tokens are the query rows (one new token per
+    # query token, in the same order), a pass writes the new tokens of its rows only
+    tok = rows if len(w.new_seq) == T else np.arange(len(w.new_seq))
     done_rows = 0
     passes = 0
     t0 = time.perf_counter()
     while True:
-        slots = orc.slot_mapping(w.block_table, w.num_blocks, w.block_size, w.new_seq, w.new_pos)
+        slots = orc.slot_mapping(w.block_table, w.num_blocks, w.block_size, w.new_seq[tok],
+                                 w.new_pos[tok])
         if len(w.cow_src):
             orc.copy_blocks(kp, vp, w.cow_src, w.cow_dst)
-        orc.write_kv(host["k_new"], host["v_new"], slots, kp, vp)
+        orc.write_kv(host["k_new"][tok], host["v_new"][tok], slots, kp, vp)
         orc.attention(host["q"], kp, vp, w.block_table, w.context_lens, w.query_lens,
-                      rows=None if rows_per_pass == T else rows, n_threads=n_threads)
-        done_rows += rows_per_pass
+                      rows=None if R == T else rows, n_threads=n_threads)
+        done_rows += R
         passes += 1
         el = time.perf_counter() - t0
         if el >= budget_s or passes >= max_passes:
             break
-    sample = (f"{passes} pass(es) of slot mapping + KV write of all {len(w.new_seq)} new tokens "
-              f"+ attention of query rows [0, {rows_per_pass}) of {T} ({w.name}), "
+    sample = (f"{passes} pass(es) of slot mapping + KV write + attention of {R} query rows "
+              f"spread evenly over all {T} (and their {len(tok)} new tokens) of {w.name}, "
               f"{el:.1f} s on {n_threads} threads")
     return done_rows / el, sample, el
 
