@@ -125,6 +125,20 @@ def test_tensor_core_pair_tiles(pa, g, B, chunk):
     assert torch.allclose(pair_run["out"], one_run["out"], atol=gu.ATOL_MAX, rtol=0)
 
 
+@pytest.mark.parametrize("chunk", [0, 64])
+def test_tensor_core_pair_half_tile_tails(pa, chunk):
+    """The two-tile kernel takes each 128-key tile as two 64-key score halves: key ranges
+    ending at 64 and 65 keys into the last tile (its second half has no key, or one), and
+    with 64-key split chunks every item's only tile has an empty second half."""
+    w = workloads.make_custom([320, 321, 448, 257], [256, 256, 256, 200], Hq=2, Hkv=2, D=128,
+                              block_size=16, seed=77)
+    kw = dict(max_chunk_tokens=chunk) if chunk else {}
+    (_, _), got, _ = full_check(pa, w, tc_pair=1, **kw)
+    assert got["plan"].stats()["n_tc_pair_items"] > 0
+    if chunk:
+        assert got["plan"].stats()["n_split_groups"] > 0
+
+
 @pytest.mark.parametrize("g", [8, 64, 128])
 def test_tensor_core_pair_bf16_and_wide_groups(pa, g):
     """Two-tile items with bf16 output (the epilogue's tensor stores in bf16) and with
